@@ -1,0 +1,74 @@
+"""Plants plausible mistakes in the CPU oracle and checks that a pin catches
+each one.  Mistakes are planted in the oracle only, on the CPU, by patching
+module attributes for the duration of one test."""
+import numpy as np
+import pytest
+
+import oracle.oracle as OO
+import tests.test_oracle_pins as P
+
+
+def _swapped_nibbles(codes, scale_of_element):
+    lo, hi = codes & 0x0F, codes >> 4
+    nib = np.empty((codes.shape[0], codes.shape[1] * 2), np.uint8)
+    nib[:, 0::2], nib[:, 1::2] = hi, lo                    # wrong nibble order
+    return OO._E2M1_TABLE[nib] * scale_of_element
+
+
+def _topk_high_index_ties(logits, k):
+    rev = np.asarray(logits)[:, ::-1]
+    E = rev.shape[1]
+    return (E - 1 - OO.__dict__["_orig_topk"](rev, k)).astype(np.int32)
+
+
+class _MruEvictLRU(OO.ExpertSlotLRU):
+    def lookup(self, layer, experts):                      # evicts the MRU key instead
+        self.recency.reverse()
+        try:
+            return super().lookup(layer, experts)
+        finally:
+            self.recency.reverse()
+
+
+def _ffn_without_up(x_rows, Wg, Wu, Wd, h_bf16=True):
+    g = x_rows @ Wg.T
+    h = OO.silu(g)
+    return (OO.round_to_bf16(h) if h_bf16 else h) @ Wd.T
+
+
+def _gates_no_max_shift_wrong(logits, idx):
+    sel = np.take_along_axis(np.asarray(logits, np.float64), idx.astype(np.int64), axis=1)
+    z = np.exp(sel)
+    return (z / z.sum(axis=1, keepdims=True) * 0.999).astype(np.float32)   # dropped normalisation
+
+
+def _e4m3_bias8(byte):
+    v = OO.__dict__["_orig_e4m3"](byte)
+    return v / 2.0                                           # off-by-one exponent bias
+
+
+MUTATIONS = [
+    ("nibble order", "_fp4_matrix", _swapped_nibbles,
+     [P.test_nvfp4_dequant_all_codes_times_all_scales, P.test_mxfp4_dequant_all_codes_times_all_scales]),
+    ("top-k ties to the higher id", "topk_experts", _topk_high_index_ties,
+     [P.test_topk_exhaustive_tiny]),
+    ("LRU evicts the MRU", "ExpertSlotLRU", _MruEvictLRU,
+     [lambda: [P.test_lru_hand_worked_traces(t) for t in P._parse_traces()]]),
+    ("up projection dropped", "expert_ffn", _ffn_without_up,
+     [lambda: P.test_layer_equals_dense_masked_mixture("bf16", 2)]),
+    ("gates not normalised", "gates_of", _gates_no_max_shift_wrong,
+     [P.test_gates_closed_forms]),
+    ("E4M3 exponent bias", "e4m3_value", _e4m3_bias8,
+     [P.test_e4m3_matches_torch_for_all_bytes]),
+]
+
+
+@pytest.mark.parametrize("name,attr,bad,pins", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pin_catches_planted_mistake(monkeypatch, name, attr, bad, pins):
+    monkeypatch.setitem(OO.__dict__, "_orig_topk", OO.topk_experts)
+    monkeypatch.setitem(OO.__dict__, "_orig_e4m3", OO.e4m3_value)
+    monkeypatch.setattr(OO, attr, bad)
+    monkeypatch.setattr(P.O, attr, bad, raising=False)
+    for pin in pins:
+        with pytest.raises(AssertionError):
+            pin()

@@ -1,0 +1,456 @@
+"""Pins of the CPU oracle to things other than itself: the pages' own figures,
+closed forms, library routines, brute force and hand-worked traces.
+
+Each test is chosen so that a plausible slip in the oracle (a wrong table
+entry, a swapped nibble, a transposed section, a dropped term, a wrong tie
+rule) fails it.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import ftgen
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- formats
+
+def test_e2m1_from_bit_fields():
+    # e2m1: 1 sign, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 is subnormal
+    for c in range(16):
+        s = -1.0 if c & 8 else 1.0
+        e = (c >> 1) & 3
+        m = c & 1
+        want = s * (m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1 + m / 2))
+        assert O.e2m1_value(c) == want, c
+
+
+def test_e4m3_matches_torch_for_all_bytes():
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([O.e4m3_value(b) for b in range(256)])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+
+
+def test_e8m0_matches_torch_for_all_bytes():
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = np.array([O.e8m0_value(b) for b in range(256)])
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ref[ok], got[ok])
+
+
+def test_bf16_decode_and_rounding_match_torch():
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 1 << 16, 4096, dtype=np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]           # drop inf/nan patterns
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_bits_to_f64(bits), ref)
+    assert O.bf16_value(0x3F80) == 1.0 and O.bf16_value(0xC000) == -2.0
+    # rounding: fp32-representable values (one rounding step on both sides)
+    v = (rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000)).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.round_to_bf16(v.astype(np.float64)), ref)
+
+
+def _hand_blob_nvfp4(I, H, scale_of_row, g):
+    """Builds an NVFP4 blob by hand: in every 16-block, element i carries code
+    i; row r's block scales are all scale_of_row(r)."""
+    HI = H * I
+    nib = np.tile(np.arange(16, dtype=np.uint8), H // 16)           # one row of codes
+    row_codes = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)
+    gu_c = np.tile(row_codes, (2 * I, 1))
+    gu_s = np.array([[scale_of_row(r)] * (H // 16) for r in range(2 * I)], np.uint8)
+    nib_d = np.tile(np.arange(16, dtype=np.uint8), I // 16)
+    d_c = np.tile((nib_d[0::2] | (nib_d[1::2] << 4)).astype(np.uint8), (H, 1))
+    d_s = np.array([[scale_of_row(r)] * (I // 16) for r in range(H)], np.uint8)
+    gs = np.array(g + [0.0], np.float32).view(np.uint8)
+    blob = np.concatenate([gu_c.ravel(), gu_s.ravel(), d_c.ravel(), d_s.ravel(), gs])
+    assert blob.size == O.blob_bytes(O.FMT_NVFP4, H, I) == 27 * HI // 16 + 16
+    return blob
+
+
+def test_nvfp4_dequant_all_codes_times_all_scales():
+    # 2I = 256 rows -> row r uses E4M3 byte r: every (code, scale) pair appears
+    I, H = 128, 32
+    g = [0.75, 1.5, 2.0]
+    blob = _hand_blob_nvfp4(I, H, lambda r: r % 256, g)
+    Wg, Wu, Wd = O.dequant_expert(blob, O.FMT_NVFP4, H, I)
+    e4m3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    code = np.arange(H) % 16
+    e2m1 = np.array([(-1.0 if c & 8 else 1.0) * [0, .5, 1, 1.5, 2, 3, 4, 6][c & 7] for c in range(16)])
+    for r in range(2 * I):
+        W, rr, gg = (Wg, r, g[0]) if r < I else (Wu, r - I, g[1])
+        want = e2m1[code] * e4m3[r] * gg
+        np.testing.assert_array_equal(np.isnan(W[rr]), np.isnan(want))
+        ok = ~np.isnan(want)
+        np.testing.assert_array_equal(W[rr][ok], want[ok])
+    code_d = np.arange(I) % 16
+    for r in range(H):
+        np.testing.assert_array_equal(Wd[r], e2m1[code_d] * e4m3[r] * g[2])
+
+
+def test_mxfp4_dequant_all_codes_times_all_scales():
+    I, H = 128, 64
+    HI = H * I
+    nib = np.tile(np.arange(16, dtype=np.uint8), H // 16)
+    gu_c = np.tile((nib[0::2] | (nib[1::2] << 4)).astype(np.uint8), (2 * I, 1))
+    gu_s = np.array([[r % 255] * (H // 32) for r in range(2 * I)], np.uint8)   # bytes 0..254
+    nib_d = np.tile(np.arange(16, dtype=np.uint8), I // 16)
+    d_c = np.tile((nib_d[0::2] | (nib_d[1::2] << 4)).astype(np.uint8), (H, 1))
+    d_s = np.array([[(3 * r) % 255] * (I // 32) for r in range(H)], np.uint8)
+    blob = np.concatenate([gu_c.ravel(), gu_s.ravel(), d_c.ravel(), d_s.ravel()])
+    assert blob.size == O.blob_bytes(O.FMT_MXFP4, H, I) == 51 * HI // 32
+    Wg, Wu, Wd = O.dequant_expert(blob, O.FMT_MXFP4, H, I)
+    e8m0 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    e2m1 = np.array([(-1.0 if c & 8 else 1.0) * [0, .5, 1, 1.5, 2, 3, 4, 6][c & 7] for c in range(16)])
+    code = np.arange(H) % 16
+    for r in range(2 * I):
+        W, rr = (Wg, r) if r < I else (Wu, r - I)
+        np.testing.assert_array_equal(W[rr], e2m1[code] * e8m0[r % 255])
+    for r in range(H):
+        np.testing.assert_array_equal(Wd[r], e2m1[np.arange(I) % 16] * e8m0[(3 * r) % 255])
+
+
+def test_dequant_bf16_is_within_half_ulp_of_master_weights():
+    # pins the blob section order and orientation (gate, up, down) against the
+    # fp32 master weights the generator quantised
+    H, I = 64, 96
+    blob = ftgen.expert_blob("bf16", H, I, key=7, seed=99)
+    Wg, Wu, Wd = O.dequant_expert(blob, O.FMT_BF16, H, I)
+    g, u, d = ftgen.master_weights(H, I, key=7, seed=99)
+    for W, M in ((Wg, g), (Wu, u), (Wd, d)):
+        assert W.shape == M.shape
+        half_ulp = np.ldexp(1.0, np.floor(np.log2(np.abs(M).astype(np.float64))).astype(int) - 8)
+        assert np.all(np.abs(W - M) <= half_ulp)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_dequant_fp4_tracks_master_weights(fmt):
+    H, I = 256, 128
+    blob = ftgen.expert_blob(fmt, H, I, key=3, seed=5)
+    Ws = O.dequant_expert(blob, O.FMT_NVFP4 if fmt == "nvfp4" else O.FMT_MXFP4, H, I)
+    Ms = ftgen.master_weights(H, I, key=3, seed=5)
+    for W, M in zip(Ws, Ms):
+        rel = np.linalg.norm(W - M) / np.linalg.norm(M)
+        assert rel < 0.2, rel                       # 4-bit grid: ~10 % rms error
+        corr = np.corrcoef(W.ravel(), M.ravel())[0, 1]
+        assert corr > 0.97, corr                     # a misplaced section would decorrelate
+
+
+def _golden_numbers():
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "pages_arithmetic.txt")):
+        if line.strip() and not line.startswith("#"):
+            name, v = line.split()[:2]
+            vals[name] = float(v)
+    return vals
+
+
+def test_packed_size_matches_pages():
+    gv = _golden_numbers()
+    for H, I in ((2048, 768), (7168, 2048), (6144, 2048), (256, 512)):
+        n = 3 * H * I
+        bits = (O.blob_bytes(O.FMT_NVFP4, H, I) - 16) * 8 / n
+        assert bits == gv["nvfp4_bits_per_weight"]
+        assert O.blob_bytes(O.FMT_BF16, H, I) * 8 / n == 16
+        assert O.blob_bytes(O.FMT_MXFP4, H, I) * 8 / n == 4.25
+    # the pages' estimates: 284B at 4 bits ~142 GB, at 4.5 bits ~160 GB; 35B at 4.5 ~20 GB
+    assert round(284e9 * 4 / 8 / 1e9) == gv["fp4_params_284b_gb"]
+    assert abs(284e9 * gv["nvfp4_bits_per_weight"] / 8 / 1e9 - gv["nvfp4_params_284b_gb"]) < 1.0
+    assert abs(35e9 * gv["nvfp4_bits_per_weight"] / 8 / 1e9 - gv["nvfp4_params_35b_gb"]) < 0.5
+
+
+def test_stream_copy_time_formula_matches_pages():
+    gv = _golden_numbers()
+    t = gv["expert_bytes_284b_gb"] / gv["pcie5_h2d_gbps"]
+    assert abs(t - gv["chunk_copy_s"]) < 0.05
+    assert abs(gv["chunk_tokens"] / t - gv["prefill_tokens_per_s"]) < 50
+    chunks = math.ceil(gv["context_tokens"] / gv["chunk_tokens"])
+    assert chunks == gv["context_chunks"]
+    assert abs(chunks * t - gv["context_copy_s"]) < 0.5
+
+
+# ---------------------------------------------------------------- router
+
+def _stable_sort_topk(logits, k):
+    out = []
+    for row in np.asarray(logits, np.float64):
+        order = np.lexsort((np.arange(row.size), -row))    # by -logit, then by id
+        out.append(order[:k])
+    return np.array(out, np.int32)
+
+
+def test_topk_equals_full_stable_sort_random_and_tied():
+    rng = np.random.default_rng(1)
+    for E, k in ((8, 2), (128, 8), (256, 8), (5, 5), (1, 1)):
+        lg = rng.standard_normal((64, E)).astype(np.float32)
+        assert np.array_equal(O.topk_experts(lg, k), _stable_sort_topk(lg, k))
+        tied = rng.integers(-2, 3, (64, E)).astype(np.float32)  # many equal logits
+        assert np.array_equal(O.topk_experts(tied, k), _stable_sort_topk(tied, k))
+
+
+def test_topk_exhaustive_tiny():
+    vals = (0.0, 1.0, 2.0)
+    rows = np.array(list(itertools.product(vals, repeat=4)), np.float32)
+    for k in range(1, 5):
+        assert np.array_equal(O.topk_experts(rows, k), _stable_sort_topk(rows, k))
+
+
+def test_gates_closed_forms():
+    rng = np.random.default_rng(2)
+    lg = rng.standard_normal((50, 16)).astype(np.float32)
+    idx = O.topk_experts(lg, 4)
+    g = O.gates_of(lg, idx)
+    assert np.allclose(g.sum(axis=1), 1.0, atol=1e-6)
+    assert np.all(np.diff(g, axis=1) <= 0)                 # descending logits -> descending gates
+    # full softmax over all E, then renormalised over the selected k
+    p = scipy.special.softmax(lg.astype(np.float64), axis=1)
+    sel = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    np.testing.assert_allclose(g, sel / sel.sum(axis=1, keepdims=True), rtol=1e-6)
+    # shift invariance and k = 1
+    np.testing.assert_allclose(O.gates_of(lg + 3.0, idx), g, rtol=1e-6)
+    assert np.all(O.gates_of(lg, O.topk_experts(lg, 1)) == 1.0)
+
+
+# ---------------------------------------------------------------- cache
+
+def _parse_traces():
+    traces, cur = [], None
+    for line in open(os.path.join(GOLDEN, "lru_traces.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        f = line.split()
+        if f[0] == "trace":
+            kv = dict(x.split("=") for x in f[2:])
+            cur = dict(name=f[1], S=int(kv["S"]), L=int(kv["L"]), E=int(kv["E"]), warm=kv["warm"] == "1", calls=[])
+            traces.append(cur)
+        elif f[0] == "call":
+            arrow = f.index("->")
+            layer, experts = int(f[1]), [int(v) for v in f[2:arrow]]
+            plan = []
+            for item in f[arrow + 1:]:
+                e, s, hm, ev = item.split(":")
+                plan.append((int(e), int(s), hm == "hit", -1 if ev == "-" else int(ev)))
+            cur["calls"].append((layer, experts, plan))
+        elif f[0] == "stats":
+            cur["stats"] = tuple(int(v) for v in f[1:])
+    return traces
+
+
+@pytest.mark.parametrize("trace", _parse_traces(), ids=lambda t: t["name"])
+def test_lru_hand_worked_traces(trace):
+    lru = O.ExpertSlotLRU(trace["S"], trace["L"], trace["E"])
+    if trace["warm"]:
+        lru.warm_fill()
+    look = hits = misses = ev = 0
+    for layer, experts, want in trace["calls"]:
+        got = lru.lookup(layer, experts)
+        assert got == want
+        look += len(got)
+        hits += sum(p[2] for p in got)
+        misses += sum(not p[2] for p in got)
+        ev += sum(p[3] >= 0 for p in got)
+    assert (look, hits, misses, ev) == trace["stats"]
+
+
+def _random_calls(rng, L, E, n, umax):
+    calls = []
+    for _ in range(n):
+        layer = int(rng.integers(0, L))
+        u = sorted(set(int(v) for v in rng.integers(0, E, int(rng.integers(1, umax + 1)))))
+        calls.append((layer, u))
+    return calls
+
+
+@pytest.mark.parametrize("warm", [True, False])
+def test_lru_matches_most_recent_distinct_keys_characterisation(warm):
+    """An LRU cache of S entries holds exactly the S most recently touched
+    distinct keys (the inclusion property behind Mattson's stack distances).
+    Checked with a serial touch history kept independently of the oracle."""
+    rng = np.random.default_rng(3)
+    for trial in range(300):
+        L, E = int(rng.integers(1, 4)), int(rng.integers(1, 7))
+        umax = min(E, 3)
+        S = int(rng.integers(2 * umax, 2 * umax + 4))
+        lru = O.ExpertSlotLRU(S, L, E)
+        history = []
+        if warm:
+            history = list(range(min(S, L * E)))
+            lru.warm_fill()
+        for layer, u in _random_calls(rng, L, E, 30, umax):
+            # the S most recent distinct keys before this call
+            resident, seen = set(), set()
+            for key in reversed(history):
+                if key not in seen:
+                    seen.add(key)
+                    if len(resident) < S:
+                        resident.add(key)
+            plan = lru.lookup(layer, u)
+            keys = [layer * E + e for e in u]
+            assert [p[2] for p in plan] == [k in resident for k in keys]
+            # serial order of touches: hits ascending, then misses ascending
+            history += [k for k, p in zip(keys, plan) if p[2]] + [k for k, p in zip(keys, plan) if not p[2]]
+            # victims are the least recent resident keys not touched by this call
+            victims = [p[3] for p in plan if p[3] >= 0]
+            if victims:
+                order = []
+                for key in reversed(history[: -len(keys)]):
+                    if key in resident and key not in order:
+                        order.append(key)
+                oldest_first = [k for k in reversed(order) if k not in keys]
+                assert victims == oldest_first[: len(victims)]
+            # slot table is a bijection between resident keys and slots
+            assert sorted(lru.key_slot.values()) == sorted(set(lru.key_slot.values()))
+            for key, slot in lru.key_slot.items():
+                assert lru.slot_key[slot] == key
+
+
+def test_lru_invariants_and_capacity_cases():
+    rng = np.random.default_rng(4)
+    L, E = 3, 6
+    # S >= L*E with warm fill: never a miss
+    lru = O.ExpertSlotLRU(L * E, L, E)
+    lru.warm_fill()
+    for layer, u in _random_calls(rng, L, E, 200, 4):
+        assert all(p[2] for p in lru.lookup(layer, u))
+    # S = infinity (>= keys), cold: misses == distinct keys seen
+    lru = O.ExpertSlotLRU(L * E + 5, L, E)
+    seen, misses, free_used, evictions = set(), 0, 0, 0
+    for layer, u in _random_calls(rng, L, E, 200, 4):
+        plan = lru.lookup(layer, u)
+        misses += sum(not p[2] for p in plan)
+        evictions += sum(p[3] >= 0 for p in plan)
+        seen |= {layer * E + e for e in u}
+    assert misses == len(seen) and evictions == 0
+    # evictions = misses - free slots consumed
+    lru = O.ExpertSlotLRU(8, L, E)
+    misses = evictions = 0
+    for layer, u in _random_calls(rng, L, E, 300, 4):
+        plan = lru.lookup(layer, u)
+        misses += sum(not p[2] for p in plan)
+        evictions += sum(p[3] >= 0 for p in plan)
+    assert evictions == misses - 8
+
+
+# ---------------------------------------------------------------- permute
+
+def test_permute_equals_stable_argsort():
+    rng = np.random.default_rng(5)
+    for T, E, k in ((1, 128, 8), (64, 8, 2), (37, 16, 4), (0, 8, 2)):
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else np.zeros((0, k), np.int32)
+        off, perm, inv = O.permute_by_expert(idx, E)
+        flat = idx.reshape(-1)
+        assert np.array_equal(perm, np.argsort(flat, kind="stable"))
+        assert np.array_equal(off, np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+        assert np.array_equal(inv[perm], np.arange(flat.size))
+
+
+# ---------------------------------------------------------------- FFN / layer
+
+def test_silu_matches_library_sigmoid():
+    a = np.linspace(-30, 30, 1001)
+    np.testing.assert_allclose(O.silu(a), a * scipy.special.expit(a), rtol=1e-14, atol=1e-300)
+
+
+def _dense_reference(x, logits, k, weights, h_bf16=True):
+    """All E experts on all tokens, masked by the top-k gates."""
+    T, E = logits.shape
+    p = scipy.special.softmax(logits.astype(np.float64), axis=1)
+    order = np.lexsort((np.tile(np.arange(E), (T, 1)), -logits.astype(np.float64)), axis=1)[:, :k]
+    G = np.zeros((T, E))
+    for t in range(T):
+        sel = order[t]
+        G[t, sel] = p[t, sel] / p[t, sel].sum()
+    out = np.zeros((T, x.shape[1]))
+    for e in range(E):
+        Wg, Wu, Wd = weights[e]
+        a = x @ Wg.T
+        h = a * scipy.special.expit(a) * (x @ Wu.T)
+        if h_bf16:
+            h = O.round_to_bf16(h)
+        out += G[:, [e]] * (h @ Wd.T)
+    return out
+
+
+@pytest.mark.parametrize("fmt,k", [("bf16", 2), ("nvfp4", 3), ("mxfp4", 2), ("bf16", 6)])
+def test_layer_equals_dense_masked_mixture(fmt, k):
+    H, I, E, T, seed = 64, 96, 6, 9, 11
+    f = ftgen.FMT_NAMES[fmt]
+    pool = ftgen.pool(fmt, H, I, list(range(E)), seed)
+    orc = O.MoELayerOracle(H, E, k, I, f, n_slots=E, n_layers=1, blob_of=lambda key: pool[key])
+    x = ftgen.x_bf16(seed, T, H, 0, 0)
+    lg = ftgen.router_logits(seed, T, E, 0, 0)
+    res = orc.forward(0, x, lg)
+    weights = [O.dequant_expert(pool[e], f, H, I) for e in range(E)]
+    ref = _dense_reference(O.bf16_bits_to_f64(x), lg, k, weights)
+    # both sides round h to bf16; a last-bit difference in an fp64 sum can flip
+    # one rounding, which moves an output by ~1e-7 of the largest output
+    np.testing.assert_allclose(res["out"], ref, rtol=0, atol=1e-6 * np.abs(ref).max())
+
+
+def test_single_expert_is_plain_swiglu_mlp():
+    H, I = 32, 64
+    pool = ftgen.pool("bf16", H, I, [0], 1)
+    orc = O.MoELayerOracle(H, 1, 1, I, O.FMT_BF16, 1, 1, lambda key: pool[key], h_bf16=False)
+    x = ftgen.x_bf16(1, 5, H, 0, 0)
+    res = orc.forward(0, x, ftgen.router_logits(1, 5, 1, 0, 0))
+    xf = torch.from_numpy(O.bf16_bits_to_f64(x))
+    g, u, d = (torch.from_numpy(np.ascontiguousarray(w)) for w in O.dequant_expert(pool[0], O.FMT_BF16, H, I))
+    ref = torch.nn.functional.silu(xf @ g.T) * (xf @ u.T) @ d.T
+    np.testing.assert_allclose(res["out"], ref.numpy(), rtol=1e-12, atol=1e-15)
+    assert np.all(res["gates"] == 1.0)
+
+
+def test_k_equals_E_is_softmax_mixture():
+    H, I, E, T = 32, 32, 4, 6
+    pool = ftgen.pool("bf16", H, I, list(range(E)), 2)
+    orc = O.MoELayerOracle(H, E, E, I, O.FMT_BF16, E, 1, lambda key: pool[key], h_bf16=False)
+    x = ftgen.x_bf16(2, T, H, 0, 0)
+    lg = ftgen.router_logits(2, T, E, 0, 0)
+    res = orc.forward(0, x, lg)
+    p = scipy.special.softmax(lg.astype(np.float64), axis=1)
+    xf = O.bf16_bits_to_f64(x)
+    ref = 0
+    for e in range(E):
+        Wg, Wu, Wd = O.dequant_expert(pool[e], O.FMT_BF16, H, I)
+        a = xf @ Wg.T
+        ref = ref + p[:, [e]] * ((a * scipy.special.expit(a) * (xf @ Wu.T)) @ Wd.T)
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-6, atol=1e-12)
+
+
+def test_token_sample_equals_full_rows():
+    H, I, E, k, T = 64, 64, 8, 2, 12
+    pool = ftgen.pool("nvfp4", H, I, list(range(E)), 3)
+    mk = lambda: O.MoELayerOracle(H, E, k, I, O.FMT_NVFP4, E, 1, lambda key: pool[key])
+    x = ftgen.x_bf16(3, T, H, 0, 0)
+    lg = ftgen.router_logits(3, T, E, 0, 0)
+    full = mk().forward(0, x, lg)["out"]
+    part = mk().forward(0, x, lg, tokens=[1, 5, 11])
+    np.testing.assert_array_equal(part["out"], full[[1, 5, 11]])
+
+
+def test_stream_mode_equals_resident_lru_and_counts_copies():
+    H, I, E, k, T, L = 64, 64, 4, 2, 5, 4
+    pool = ftgen.pool("mxfp4", H, I, list(range(L * E)), 4)
+    mk = lambda mode, S: O.MoELayerOracle(H, E, k, I, O.FMT_MXFP4, S, L, lambda key: pool[key], mode=mode)
+    st, lr = mk(O.MODE_STREAM, 2 * E), mk(O.MODE_LRU, L * E)
+    for step in range(2):
+        for layer in range(L):
+            x = ftgen.x_bf16(4, T, H, step, layer)
+            lg = ftgen.router_logits(4, T, E, step, layer)
+            a, b = st.forward(layer, x, lg), lr.forward(layer, x, lg)
+            np.testing.assert_array_equal(a["out"], b["out"])
+            assert b["last"]["misses"] == 0
+    # first pass: each layer once plus the wrap-around prefetch of layer 0;
+    # second pass: layer 0 already staged, so L-1 layers + the wrap prefetch
+    assert st.stats["streamed"] == E * (L + 1) + E * L
