@@ -1,0 +1,104 @@
+// ft_internal.cuh -- shared declarations of the sm_103a MoE-offload library.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ftmoe {
+
+enum { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_MXFP4 = 2 };
+enum { MODE_LRU = 0, MODE_STREAM = 1 };
+
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 32;
+constexpr int kRouteThreads = 1024;       // single-CTA routing / plan kernels
+constexpr int kChunkTokens = 32;          // tokens per CTA in the multi-CTA routing path
+
+// Byte offsets of the sections of one expert blob (see include/ft_moe.h).
+struct BlobLayout {
+  int64_t gu_codes, gu_sf, d_codes, d_sf, gscale, bytes;
+};
+
+__host__ __device__ inline BlobLayout blob_layout(int fmt, int64_t H, int64_t I) {
+  const int64_t HI = H * I;
+  BlobLayout b{};
+  if (fmt == FMT_BF16) {
+    b.gu_codes = 0; b.gu_sf = 0; b.d_codes = 4 * HI; b.d_sf = 0; b.gscale = -1; b.bytes = 6 * HI;
+  } else if (fmt == FMT_NVFP4) {
+    b.gu_codes = 0; b.gu_sf = HI; b.d_codes = HI + HI / 8; b.d_sf = b.d_codes + HI / 2;
+    b.gscale = b.d_sf + HI / 16; b.bytes = b.gscale + 16;
+  } else {
+    b.gu_codes = 0; b.gu_sf = HI; b.d_codes = HI + HI / 16; b.d_sf = b.d_codes + HI / 2;
+    b.gscale = -1; b.bytes = b.d_sf + HI / 32;
+  }
+  return b;
+}
+
+// Device buffers describing one call's routing and cache plan.
+struct PlanBufs {
+  int32_t *topk_idx;   // [T*k]
+  float *gates;        // [T*k]
+  int32_t *offsets;    // [E+1]
+  int32_t *perm;       // [T*k]
+  int32_t *inv;        // [T*k]
+  int32_t *u_expert;   // [Umax]  distinct experts, ascending
+  int32_t *u_slot;     // [Umax]
+  int32_t *u_hit;      // [Umax]
+  int32_t *u_evicted;  // [Umax]
+  int32_t *n;          // [4]: n_unique, n_hit, n_miss, n_evicted
+};
+
+// Cache tables (device).
+struct CacheBufs {
+  int32_t *key_slot;        // [L*E]  slot of key, -1 if not resident
+  int32_t *slot_key;        // [S]    key in slot, -1 if free
+  const int32_t *order_in;  // [S]    slots, least recent first (free slots first, by index)
+  int32_t *order_out;       // [S]
+  unsigned long long *stats;  // [16]: cumulative {lookups,hits,misses,evictions,bytes} at 0..4, last call at 8..12
+};
+
+struct RouteArgs {
+  const float *logits;
+  int T, E, k, layer, mode, bank, S;
+  long long blob_bytes;
+  PlanBufs plan;
+  CacheBufs cache;
+  int32_t *mirror;          // mapped host memory: [0]=seq [1]=n_miss [2..2+Umax) keys [..) slots; may be null
+  int umax;
+  uint32_t seq;
+  // multi-CTA path scratch
+  int32_t *chunk_counts;    // [n_chunks][E]
+  int32_t *chunk_base;      // [n_chunks][E]
+  int n_chunks;
+};
+
+// Launchers (route.cu)
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
+cudaError_t launch_topk_only(const float *logits, int T, int E, int k, int32_t *idx, float *gates,
+                             cudaStream_t s);
+cudaError_t launch_permute_only(const int32_t *idx, int T, int k, int E, int32_t *offsets,
+                                int32_t *perm, int32_t *inv, int32_t *chunk_counts,
+                                int32_t *chunk_base, cudaStream_t s);
+size_t permute_scratch_ints(int T, int k, int E);
+void route_init_attributes();
+
+// Expert FFN (ffn_gemv.cu)
+struct FfnArgs {
+  const uint8_t *slot_bank;
+  long long slot_stride;
+  int H, I, E, k, fmt;
+  const __nv_bfloat16 *x;     // [T][H]
+  __nv_bfloat16 *h;           // [T*k][I]   permuted order
+  float *y;                   // [T*k][H]   permuted order
+  PlanBufs plan;
+  int umax;
+  int only;                   // 0 all, 1 hits only, 2 misses only
+};
+cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_down(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_combine(const float *y, const float *gates, const int32_t *inv, int T, int k, int H,
+                           __nv_bfloat16 *out, cudaStream_t s);
+void ffn_init_attributes();
+
+}  // namespace ftmoe

@@ -1,0 +1,497 @@
+// ft_moe.cu -- handle, C ABI and per-call orchestration.
+//
+// LRU mode, one forward call on the caller's stream:
+//   route (GPU: top-k, gates, permute, slot lookup, LRU update, miss list
+//          written to mapped host memory)
+//   gate/up FFN over the hits               -- starts right after route
+//   host: bounded wait for the miss list; one cudaMemcpyAsync per miss on
+//         the copy stream, ordered after route, so every earlier reader of
+//         an evicted slot has finished
+//   gate/up FFN over the misses             -- after the copies
+//   down FFN, combine
+// The misses' PCIe copies overlap the hits' FFN ("Why a Huge MoE Model Fits
+// on One Consumer GPU": a cached expert runs at GPU speed; a miss is
+// streamed over PCIe).
+//
+// STREAM mode ("Long Prompts Are the Bottleneck": each MoE layer copies all of
+// its experts for a prefill chunk, and the copy of layer N+1 overlaps the
+// compute of layer N): bank (layer mod 2) holds the layer's E experts.
+// Each call also issues the next layer's copies into the other bank, after
+// the FFN that last read that bank.
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/ft_moe.h"
+#include "ft_internal.cuh"
+
+using namespace ftmoe;
+
+struct ft_moe {
+  int H = 0, E = 0, k = 0, I = 0, fmt = 0, S = 0, L = 0, Tmax = 0, umax = 0, mode = MODE_LRU;
+  int64_t blob_bytes = 0, slot_stride = 0;
+  int device = 0;
+  uint8_t *slots = nullptr;
+  int32_t *key_slot = nullptr, *slot_key = nullptr, *order[2] = {nullptr, nullptr};
+  int order_cur = 0;
+  unsigned long long *stats_dev = nullptr;
+  PlanBufs plan{};
+  int32_t *chunk_counts = nullptr, *chunk_base = nullptr;
+  __nv_bfloat16 *hbuf = nullptr;
+  float *ybuf = nullptr;
+  int32_t *mirror_host = nullptr, *mirror_dev = nullptr;
+  std::vector<const void *> pool;
+  bool pool_loaded = false;
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_copy = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_bank_ready[2] = {nullptr, nullptr}, ev_bank_free[2] = {nullptr, nullptr};
+  int bank_layer[2] = {-1, -1};
+  uint32_t seq = 0;
+  int last_T = 0;
+  bool any_call = false;
+  uint64_t host_warm = 0, host_streamed = 0, host_bytes = 0;
+  uint64_t last_streamed = 0, last_stream_bytes = 0;
+  std::string err;
+};
+
+namespace {
+
+thread_local std::string g_create_err;
+
+int fail(ft_moe *h, int code, const std::string &msg) {
+  if (h) h->err = msg;
+  else g_create_err = msg;
+  return code;
+}
+
+int cuda_fail(ft_moe *h, cudaError_t e, const char *what) {
+  return fail(h, FT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define FT_CUDA(h, call)                              \
+  do {                                                \
+    cudaError_t e_ = (call);                          \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, #call); \
+  } while (0)
+
+bool fault(const char *what) {
+  const char *f = std::getenv("FT_FAULT");
+  return f && std::strcmp(f, what) == 0;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t blob_bytes_of(int fmt, int H, int I) {
+  if (fmt < 0 || fmt > 2 || H <= 0 || I <= 0 || H % 256 || I % 256) return -1;
+  return blob_layout(fmt, H, I).bytes;
+}
+
+template <class T>
+cudaError_t dev_alloc(T **p, size_t n) {
+  return cudaMalloc(reinterpret_cast<void **>(p), n * sizeof(T) + 16);
+}
+
+void free_all(ft_moe *h) {
+  cudaFree(h->slots);
+  cudaFree(h->key_slot);
+  cudaFree(h->slot_key);
+  cudaFree(h->order[0]);
+  cudaFree(h->order[1]);
+  cudaFree(h->stats_dev);
+  cudaFree(h->plan.topk_idx);
+  cudaFree(h->plan.gates);
+  cudaFree(h->plan.offsets);
+  cudaFree(h->plan.perm);
+  cudaFree(h->plan.inv);
+  cudaFree(h->plan.u_expert);
+  cudaFree(h->plan.u_slot);
+  cudaFree(h->plan.u_hit);
+  cudaFree(h->plan.u_evicted);
+  cudaFree(h->plan.n);
+  cudaFree(h->chunk_counts);
+  cudaFree(h->chunk_base);
+  cudaFree(h->hbuf);
+  cudaFree(h->ybuf);
+  if (h->mirror_host) cudaFreeHost(h->mirror_host);
+  if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+  for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
+                         h->ev_bank_free[0], h->ev_bank_free[1]})
+    if (ev) cudaEventDestroy(ev);
+}
+
+// Waits for everything the handle has issued.
+int sync_handle(ft_moe *h) {
+  if (h->any_call) FT_CUDA(h, cudaEventSynchronize(h->ev_done));
+  FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+  return FT_OK;
+}
+
+// Initial cache state of the current mode; clears the counters.
+int reset_tables(ft_moe *h, bool warm) {
+  FT_CUDA(h, cudaSetDevice(h->device));
+  if (int rc = sync_handle(h)) return rc;
+  std::vector<int32_t> key_slot((size_t)h->L * h->E, -1), slot_key(h->S, -1), order(h->S);
+  int n = 0;
+  if (h->mode == MODE_LRU && warm) n = (int)std::min<int64_t>(h->S, (int64_t)h->L * h->E);
+  for (int s = 0; s < n; ++s) {
+    slot_key[s] = s;
+    key_slot[s] = s;
+  }
+  // free slots first (ascending index), then the warm keys, least recent first
+  int pos = 0;
+  for (int s = n; s < h->S; ++s) order[pos++] = s;
+  for (int s = 0; s < n; ++s) order[pos++] = s;
+  FT_CUDA(h, cudaMemcpy(h->key_slot, key_slot.data(), key_slot.size() * 4, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(h->slot_key, slot_key.data(), slot_key.size() * 4, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(h->order[0], order.data(), order.size() * 4, cudaMemcpyHostToDevice));
+  h->order_cur = 0;
+  FT_CUDA(h, cudaMemset(h->stats_dev, 0, 16 * sizeof(unsigned long long)));
+  h->host_warm = h->host_streamed = h->host_bytes = 0;
+  h->last_streamed = h->last_stream_bytes = 0;
+  h->bank_layer[0] = h->bank_layer[1] = -1;
+  h->last_T = 0;
+  if (h->pool_loaded) {
+    for (int s = 0; s < n; ++s)
+      FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)s * h->slot_stride, h->pool[s], h->blob_bytes,
+                                 cudaMemcpyHostToDevice, h->copy_stream));
+    FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+    h->host_warm = n;
+    h->host_bytes = (uint64_t)n * h->blob_bytes;
+  }
+  return FT_OK;
+}
+
+// STREAM mode: make bank (layer mod 2) receive all experts of `layer`, after
+// the FFN that last read that bank.
+int stage_layer(ft_moe *h, int layer) {
+  const int b = layer & 1;
+  if (h->bank_layer[b] == layer) return FT_OK;
+  FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_bank_free[b], 0));
+  for (int e = 0; e < h->E; ++e)
+    FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)(b * h->E + e) * h->slot_stride,
+                               h->pool[(size_t)layer * h->E + e], h->blob_bytes, cudaMemcpyHostToDevice,
+                               h->copy_stream));
+  FT_CUDA(h, cudaEventRecord(h->ev_bank_ready[b], h->copy_stream));
+  h->bank_layer[b] = layer;
+  h->last_streamed += h->E;
+  h->last_stream_bytes += (uint64_t)h->E * h->blob_bytes;
+  return FT_OK;
+}
+
+int64_t wait_timeout_ms() {
+  const char *v = std::getenv("FT_WAIT_TIMEOUT_MS");
+  return v ? std::max<int64_t>(1, std::atoll(v)) : 20000;
+}
+
+// Bounded host wait for the route kernel's miss list (mapped host memory).
+int wait_plan(ft_moe *h) {
+  if (fault("timeout")) return fail(h, FT_ERR_TIMEOUT, "injected wait timeout (FT_FAULT=timeout)");
+  const auto t0 = std::chrono::steady_clock::now();
+  const int64_t limit = wait_timeout_ms();
+  volatile int32_t *flag = h->mirror_host;
+  for (uint64_t spin = 0; *flag != (int32_t)h->seq; ++spin) {
+    if ((spin & 1023) == 1023) {
+      cudaError_t q = cudaEventQuery(h->ev_route);
+      if (q != cudaSuccess && q != cudaErrorNotReady) return cuda_fail(h, q, "route kernel");
+      if (q == cudaSuccess && *flag != (int32_t)h->seq)
+        return fail(h, FT_ERR_DEVICE, "route kernel finished without publishing its miss list");
+      const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+      if (ms > limit) return fail(h, FT_ERR_TIMEOUT, "timed out waiting for the miss list");
+    }
+    __builtin_ia32_pause();
+  }
+  std::atomic_thread_fence(std::memory_order_acquire);
+  return FT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t ft_moe_blob_bytes(int weight_fmt, int hidden, int inter) { return blob_bytes_of(weight_fmt, hidden, inter); }
+
+int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fmt, int n_slots, int n_layers,
+                  int max_tokens, ft_moe **out) {
+  if (!out) return fail(nullptr, FT_ERR_ARG, "out is NULL");
+  if (blob_bytes_of(weight_fmt, hidden, inter) < 0 || hidden > 8192 || inter > 8192)
+    return fail(nullptr, FT_ERR_ARG, "hidden/inter must be multiples of 256 in 256..8192 and weight_fmt 0..2");
+  if (n_experts < 1 || n_experts > kMaxExperts) return fail(nullptr, FT_ERR_ARG, "n_experts must be in 1..512");
+  if (top_k < 1 || top_k > std::min(n_experts, kMaxTopK)) return fail(nullptr, FT_ERR_ARG, "top_k must be in 1..min(E,32)");
+  if (n_layers < 1 || n_slots < 1 || max_tokens < 1 || n_slots > (1 << 16) ||
+      (int64_t)n_layers * n_experts > (1LL << 30) || (int64_t)max_tokens * top_k > (1LL << 30))
+    return fail(nullptr, FT_ERR_ARG, "n_layers, max_tokens must be positive; n_slots in 1..65536");
+  const int umax = (int)std::min<int64_t>(n_experts, (int64_t)max_tokens * top_k);
+  if (n_slots < umax)
+    return fail(nullptr, FT_ERR_CACHE_TOO_SMALL,
+                "n_slots < min(E, max_tokens*top_k): one call's experts would not fit in the cache");
+  if (fault("alloc")) return fail(nullptr, FT_ERR_OOM, "injected allocation failure (FT_FAULT=alloc)");
+
+  ft_moe *h = new ft_moe();
+  h->H = hidden; h->E = n_experts; h->k = top_k; h->I = inter; h->fmt = weight_fmt;
+  h->S = n_slots; h->L = n_layers; h->Tmax = max_tokens; h->umax = umax;
+  h->blob_bytes = blob_bytes_of(weight_fmt, hidden, inter);
+  h->slot_stride = (h->blob_bytes + 255) / 256 * 256;
+  auto bail = [&](int rc) { free_all(h); delete h; return rc; };
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) { cuda_fail(nullptr, e, "cudaGetDevice"); return bail(FT_ERR_CUDA); }
+  const size_t TK = (size_t)max_tokens * top_k;
+  const size_t chunk_ints = permute_scratch_ints(max_tokens, top_k, n_experts) / 2;
+  bool ok = cudaMalloc(&h->slots, (size_t)n_slots * h->slot_stride) == cudaSuccess &&
+            dev_alloc(&h->key_slot, (size_t)n_layers * n_experts) == cudaSuccess &&
+            dev_alloc(&h->slot_key, n_slots) == cudaSuccess && dev_alloc(&h->order[0], n_slots) == cudaSuccess &&
+            dev_alloc(&h->order[1], n_slots) == cudaSuccess && dev_alloc(&h->stats_dev, 16) == cudaSuccess &&
+            dev_alloc(&h->plan.topk_idx, TK) == cudaSuccess && dev_alloc(&h->plan.gates, TK) == cudaSuccess &&
+            dev_alloc(&h->plan.offsets, n_experts + 1) == cudaSuccess && dev_alloc(&h->plan.perm, TK) == cudaSuccess &&
+            dev_alloc(&h->plan.inv, TK) == cudaSuccess && dev_alloc(&h->plan.u_expert, umax) == cudaSuccess &&
+            dev_alloc(&h->plan.u_slot, umax) == cudaSuccess && dev_alloc(&h->plan.u_hit, umax) == cudaSuccess &&
+            dev_alloc(&h->plan.u_evicted, umax) == cudaSuccess && dev_alloc(&h->plan.n, 4) == cudaSuccess &&
+            dev_alloc(&h->chunk_counts, chunk_ints) == cudaSuccess &&
+            dev_alloc(&h->chunk_base, chunk_ints) == cudaSuccess &&
+            dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess;
+  if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
+  if (cudaHostAlloc(&h->mirror_host, sizeof(int32_t) * (2 + 2 * (size_t)umax), cudaHostAllocMapped) != cudaSuccess ||
+      cudaHostGetDevicePointer(reinterpret_cast<void **>(&h->mirror_dev), h->mirror_host, 0) != cudaSuccess) {
+    cudaGetLastError();
+    fail(nullptr, FT_ERR_OOM, "mapped pinned allocation failed");
+    return bail(FT_ERR_OOM);
+  }
+  std::memset(h->mirror_host, 0, sizeof(int32_t) * (2 + 2 * (size_t)umax));
+  ok = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_route, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_copy, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_bank_ready[0], cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_bank_ready[1], cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_bank_free[0], cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_bank_free[1], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) { cuda_fail(nullptr, cudaGetLastError(), "stream/event creation"); return bail(FT_ERR_CUDA); }
+  route_init_attributes();
+  ffn_init_attributes();
+  if (int rc = reset_tables(h, false)) { g_create_err = h->err; return bail(rc); }
+  *out = h;
+  return FT_OK;
+}
+
+int ft_moe_load_pool(ft_moe *h, const void *const *host_experts) {
+  if (!h || !host_experts) return fail(h, FT_ERR_ARG, "NULL handle or pool table");
+  if (fault("pin")) return fail(h, FT_ERR_NOT_PINNED, "injected unpinned pool (FT_FAULT=pin)");
+  const size_t n = (size_t)h->L * h->E;
+  for (size_t i = 0; i < n; ++i) {
+    if (!host_experts[i]) return fail(h, FT_ERR_ARG, "NULL expert pointer at " + std::to_string(i));
+    cudaPointerAttributes at{};
+    cudaError_t e = cudaPointerGetAttributes(&at, host_experts[i]);
+    if (e != cudaSuccess || at.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      return fail(h, FT_ERR_NOT_PINNED, "expert " + std::to_string(i) + " is not in page-locked host memory");
+    }
+  }
+  h->pool.assign(host_experts, host_experts + n);
+  h->pool_loaded = true;
+  return reset_tables(h, true);
+}
+
+int ft_moe_set_mode(ft_moe *h, int mode) {
+  if (!h || (mode != MODE_LRU && mode != MODE_STREAM)) return fail(h, FT_ERR_ARG, "bad mode");
+  if (mode == MODE_STREAM && h->S < 2 * h->E)
+    return fail(h, FT_ERR_CACHE_TOO_SMALL, "STREAM mode needs n_slots >= 2*E (two staging layers)");
+  if (int rc = sync_handle(h)) return rc;
+  h->mode = mode;
+  return reset_tables(h, true);
+}
+
+int ft_cache_reset(ft_moe *h, int warm) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  return reset_tables(h, warm != 0);
+}
+
+int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const float *router_logits, void *out,
+                   void *stream_) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (!h->pool_loaded) return fail(h, FT_ERR_STATE, "no expert pool loaded");
+  if (layer < 0 || layer >= h->L) return fail(h, FT_ERR_ARG, "layer out of range");
+  if (n_tokens < 0 || n_tokens > h->Tmax) return fail(h, FT_ERR_ARG, "n_tokens out of range");
+  h->last_streamed = h->last_stream_bytes = 0;
+  h->last_T = n_tokens;
+  if (n_tokens == 0) return FT_OK;
+  if (!x || !router_logits || !out) return fail(h, FT_ERR_ARG, "NULL x, router_logits or out");
+  if (!aligned16(x) || !aligned16(router_logits) || !aligned16(out))
+    return fail(h, FT_ERR_ARG, "x, router_logits and out must be 16-byte aligned");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  FT_CUDA(h, cudaSetDevice(h->device));
+  if (h->mode == MODE_LRU) {
+    cudaStreamCaptureStatus cs;
+    FT_CUDA(h, cudaStreamIsCapturing(stream, &cs));
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(h, FT_ERR_STATE, "LRU-mode forward waits on the host and cannot be captured");
+  }
+  const int bank = layer & 1;
+  if (h->mode == MODE_STREAM) {
+    if (int rc = stage_layer(h, layer)) return rc;
+    const int nxt = layer + 1 < h->L ? layer + 1 : 0;
+    if ((nxt & 1) != bank)
+      if (int rc = stage_layer(h, nxt)) return rc;
+    FT_CUDA(h, cudaStreamWaitEvent(stream, h->ev_bank_ready[bank], 0));
+  }
+  h->any_call = true;
+  ++h->seq;
+  RouteArgs ra{};
+  ra.logits = router_logits;
+  ra.T = n_tokens; ra.E = h->E; ra.k = h->k; ra.layer = layer; ra.mode = h->mode; ra.bank = bank; ra.S = h->S;
+  ra.blob_bytes = h->blob_bytes;
+  ra.plan = h->plan;
+  ra.cache.key_slot = h->key_slot;
+  ra.cache.slot_key = h->slot_key;
+  ra.cache.order_in = h->order[h->order_cur];
+  ra.cache.order_out = h->order[h->order_cur ^ 1];
+  ra.cache.stats = h->stats_dev;
+  ra.mirror = h->mode == MODE_LRU ? h->mirror_dev : nullptr;
+  ra.umax = h->umax;
+  ra.seq = h->seq;
+  ra.chunk_counts = h->chunk_counts;
+  ra.chunk_base = h->chunk_base;
+  FT_CUDA(h, launch_route(ra, stream));
+  if (h->mode == MODE_LRU) h->order_cur ^= 1;
+  FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
+
+  FfnArgs fa{};
+  fa.slot_bank = h->slots;
+  fa.slot_stride = h->slot_stride;
+  fa.H = h->H; fa.I = h->I; fa.E = h->E; fa.k = h->k; fa.fmt = h->fmt;
+  fa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+  fa.h = h->hbuf;
+  fa.y = h->ybuf;
+  fa.plan = h->plan;
+  fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
+  if (h->mode == MODE_LRU) {
+    fa.only = 1;
+    FT_CUDA(h, launch_gateup(fa, stream));
+    if (int rc = wait_plan(h)) return rc;
+    const int n_miss = h->mirror_host[1];
+    if (n_miss > 0) {
+      FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_route, 0));
+      for (int i = 0; i < n_miss; ++i) {
+        const int key = h->mirror_host[2 + i], slot = h->mirror_host[2 + h->umax + i];
+        if (key < 0 || key >= h->L * h->E || slot < 0 || slot >= h->S)
+          return fail(h, FT_ERR_DEVICE, "miss list entry out of range");
+        FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)slot * h->slot_stride, h->pool[key], h->blob_bytes,
+                                   cudaMemcpyHostToDevice, h->copy_stream));
+      }
+      FT_CUDA(h, cudaEventRecord(h->ev_copy, h->copy_stream));
+      FT_CUDA(h, cudaStreamWaitEvent(stream, h->ev_copy, 0));
+      fa.only = 2;
+      FT_CUDA(h, launch_gateup(fa, stream));
+    }
+  } else {
+    fa.only = 0;
+    FT_CUDA(h, launch_gateup(fa, stream));
+  }
+  fa.only = 0;
+  FT_CUDA(h, launch_down(fa, stream));
+  FT_CUDA(h, launch_combine(h->ybuf, h->plan.gates, h->plan.inv, n_tokens, h->k, h->H,
+                            reinterpret_cast<__nv_bfloat16 *>(out), stream));
+  if (h->mode == MODE_STREAM) FT_CUDA(h, cudaEventRecord(h->ev_bank_free[bank], stream));
+  FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
+  h->host_streamed += h->last_streamed;
+  h->host_bytes += h->last_stream_bytes;
+  return FT_OK;
+}
+
+int ft_cache_stats(ft_moe *h, ft_stats *cum, ft_stats *last) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  unsigned long long d[16];
+  FT_CUDA(h, cudaMemcpy(d, h->stats_dev, sizeof d, cudaMemcpyDeviceToHost));
+  if (cum) *cum = ft_stats{d[0], d[1], d[2], d[3], h->host_warm, h->host_streamed, d[4] + h->host_bytes};
+  if (last) {
+    if (h->last_T == 0) *last = ft_stats{0, 0, 0, 0, 0, 0, 0};
+    else *last = ft_stats{d[8], d[9], d[10], d[11], 0, h->last_streamed, d[12] + h->last_stream_bytes};
+  }
+  return FT_OK;
+}
+
+int ft_cache_trace(ft_moe *h, int32_t *experts, int32_t *slots, int32_t *hit, int32_t *evicted, int cap, int *n) {
+  if (!h || cap < 0) return fail(h, FT_ERR_ARG, "NULL handle or negative cap");
+  if (int rc = sync_handle(h)) return rc;
+  int cnt[4] = {0, 0, 0, 0};
+  if (h->last_T > 0) FT_CUDA(h, cudaMemcpy(cnt, h->plan.n, sizeof cnt, cudaMemcpyDeviceToHost));
+  const int m = std::min(cap, cnt[0]);
+  if (m > 0) {
+    if (experts) FT_CUDA(h, cudaMemcpy(experts, h->plan.u_expert, 4 * (size_t)m, cudaMemcpyDeviceToHost));
+    if (slots) FT_CUDA(h, cudaMemcpy(slots, h->plan.u_slot, 4 * (size_t)m, cudaMemcpyDeviceToHost));
+    if (hit) FT_CUDA(h, cudaMemcpy(hit, h->plan.u_hit, 4 * (size_t)m, cudaMemcpyDeviceToHost));
+    if (evicted) FT_CUDA(h, cudaMemcpy(evicted, h->plan.u_evicted, 4 * (size_t)m, cudaMemcpyDeviceToHost));
+  }
+  if (n) *n = cnt[0];
+  return FT_OK;
+}
+
+int ft_moe_last_routing(ft_moe *h, int32_t *topk_idx, float *gates, int32_t *offsets, int32_t *perm, int32_t *inv,
+                        int *n_tokens) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  const size_t TK = (size_t)h->last_T * h->k;
+  if (TK) {
+    if (topk_idx) FT_CUDA(h, cudaMemcpy(topk_idx, h->plan.topk_idx, 4 * TK, cudaMemcpyDeviceToHost));
+    if (gates) FT_CUDA(h, cudaMemcpy(gates, h->plan.gates, 4 * TK, cudaMemcpyDeviceToHost));
+    if (offsets) FT_CUDA(h, cudaMemcpy(offsets, h->plan.offsets, 4 * (size_t)(h->E + 1), cudaMemcpyDeviceToHost));
+    if (perm) FT_CUDA(h, cudaMemcpy(perm, h->plan.perm, 4 * TK, cudaMemcpyDeviceToHost));
+    if (inv) FT_CUDA(h, cudaMemcpy(inv, h->plan.inv, 4 * TK, cudaMemcpyDeviceToHost));
+  }
+  if (n_tokens) *n_tokens = h->last_T;
+  return FT_OK;
+}
+
+int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  const size_t TK = (size_t)h->last_T * h->k;
+  if (TK && h_act) FT_CUDA(h, cudaMemcpy(h_act, h->hbuf, 2 * TK * h->I, cudaMemcpyDeviceToHost));
+  if (TK && y) FT_CUDA(h, cudaMemcpy(y, h->ybuf, 4 * TK * h->H, cudaMemcpyDeviceToHost));
+  return FT_OK;
+}
+
+int64_t ft_moe_slot_stride(const ft_moe *h) { return h ? h->slot_stride : -1; }
+
+const char *ft_last_error(const ft_moe *h) { return h ? h->err.c_str() : g_create_err.c_str(); }
+
+int ft_moe_destroy(ft_moe *h) {
+  if (!h) return FT_OK;
+  cudaSetDevice(h->device);
+  sync_handle(h);
+  free_all(h);
+  delete h;
+  return FT_OK;
+}
+
+int ft_topk_softmax(const float *router_logits, int T, int E, int k, int32_t *topk_idx, float *gates, void *stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > std::min(E, kMaxTopK))
+    return fail(nullptr, FT_ERR_ARG, "bad T/E/k");
+  if (T > 0 && (!router_logits || !topk_idx || !gates)) return fail(nullptr, FT_ERR_ARG, "NULL pointer");
+  cudaError_t e = launch_topk_only(router_logits, T, E, k, topk_idx, gates, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FT_OK : cuda_fail(nullptr, e, "topk kernel");
+}
+
+size_t ft_permute_workspace_bytes(int T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return sizeof(int32_t) * permute_scratch_ints(T, k, E);
+}
+
+int ft_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *offsets, int32_t *perm, int32_t *inv,
+               void *workspace, size_t workspace_bytes, void *stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > kMaxTopK) return fail(nullptr, FT_ERR_ARG, "bad T/E/k");
+  if (!offsets || (T > 0 && (!topk_idx || !perm || !inv))) return fail(nullptr, FT_ERR_ARG, "NULL pointer");
+  const size_t need = ft_permute_workspace_bytes(T, k, E);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return fail(nullptr, FT_ERR_ARG, "workspace too small");
+  int32_t *ws = reinterpret_cast<int32_t *>(workspace);
+  const size_t half = permute_scratch_ints(T, k, E) / 2;
+  cudaError_t e = launch_permute_only(topk_idx, T, k, E, offsets, perm, inv, ws, ws ? ws + half : nullptr,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FT_OK : cuda_fail(nullptr, e, "permute kernels");
+}
+
+}  // extern "C"

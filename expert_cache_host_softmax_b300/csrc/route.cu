@@ -1,0 +1,439 @@
+// route.cu -- router top-k + softmax, permute-by-expert, and the on-device
+// LRU slot plan.
+//
+// "FreeToken: Run Frontier MoE Models on Your Own GPU, and the RAM It Takes",
+// section "Why a Huge MoE Model Fits on One Consumer GPU": a router sends each
+// token to a few experts.  The GPU keeps an LRU cache of expert slots, one
+// global pool shared across layers.  A hit runs at GPU speed; a miss is
+// streamed over PCIe.
+//
+// Readings where the page is silent: top-k on the raw logits, ties to the
+// lower expert id; gates = softmax over the k selected logits.  A lookup is
+// one distinct (layer, expert) per call.  Hits become most recent in
+// ascending expert id.  Then misses, in ascending id, take the lowest free
+// slot or the least recent slot.
+//
+// The recency list lives on the device as an array of slot ids, least recent
+// first.  Free slots sit at the front in index order.  One call rewrites it
+// in a single block-wide compaction:
+//   [untouched non-victims in old order] [hits, ascending id] [misses, ascending id]
+// The victims are the first n_miss non-hit entries of the old order.  So the
+// whole LRU update is O(S / blockDim) per thread, plus two block scans.
+#include <math.h>
+
+#include "ft_internal.cuh"
+
+namespace ftmoe {
+
+namespace {
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Exclusive block-wide prefix sum of v; *total receives the block sum.
+// All threads of the block must call it.  s_warp holds >= 32 ints.
+__device__ int block_excl_scan(int v, int *s_warp, int *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    s_warp[lane] = t;
+  }
+  __syncthreads();
+  const int base = w ? s_warp[w - 1] : 0;
+  *total = s_warp[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// One warp selects the k largest logits of one token (ties to the lower id,
+// NaN treated as -inf) and writes their ids and softmax gates.  Returns, in
+// lanes 0..k-1, the selected expert of rank `lane` (else -1).
+__device__ int warp_topk_softmax(const float *__restrict__ row, int E, int k, int32_t *out_idx,
+                                 float *out_gate) {
+  const int lane = threadIdx.x & 31;
+  float v[kMaxExperts / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    const int e = lane + 32 * i;
+    float x = e < E ? __ldg(row + e) : -INFINITY;
+    v[i] = isnan(x) ? -INFINITY : x;
+  }
+  unsigned taken = 0;
+  float my_v = -INFINITY;
+  int my_i = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
+  }
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  float z = lane < k ? expf(my_v - m) : 0.0f;
+  float sum = z;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    out_idx[lane] = my_i;
+    out_gate[lane] = z / sum;
+  }
+  return lane < k ? my_i : -1;
+}
+
+// Stable scatter of pairs [p0, p1) by expert.  s_base[e] is the next free
+// permuted position of expert e and is advanced.  s_wcnt holds nwarps*E ints.
+__device__ void block_rank_scatter(const int32_t *__restrict__ idx, int p0, int p1, int E, int *s_base,
+                                   int *s_wcnt, int32_t *__restrict__ perm, int32_t *__restrict__ inv) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
+  for (int r0 = p0; r0 < p1; r0 += blockDim.x) {
+    for (int i = tid; i < nw * E; i += blockDim.x) s_wcnt[i] = 0;
+    __syncthreads();
+    const int p = r0 + tid;
+    int e = p < p1 ? idx[p] : -1;
+    const bool valid = e >= 0 && e < E;   // out-of-range ids are not placed
+    if (!valid) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(peers & lanemask_lt());
+    if (valid && lane == __ffs(peers) - 1) s_wcnt[w * E + e] = __popc(peers);
+    __syncthreads();
+    for (int e2 = tid; e2 < E; e2 += blockDim.x) {
+      int run = s_base[e2];
+      for (int ww = 0; ww < nw; ++ww) {
+        const int c = s_wcnt[ww * E + e2];
+        s_wcnt[ww * E + e2] = run;
+        run += c;
+      }
+      s_base[e2] = run;
+    }
+    __syncthreads();
+    if (valid) {
+      const int pos = s_wcnt[w * E + e] + rank_w;
+      perm[pos] = p;
+      inv[p] = pos;
+    }
+    __syncthreads();
+  }
+}
+
+struct PlanSmem {
+  int *s_count;   // [E] tokens per expert in this call
+  int *s_uexp;    // [E]
+  int *s_victim;  // [E]
+  unsigned *s_bits;  // [(S+31)/32]
+  int *s_warp;    // [32]
+};
+
+// Distinct experts of the call, slot lookup, LRU update, plan and stats.
+// One CTA.  Needs blockDim.x >= E.
+__device__ void block_plan(const RouteArgs &a, const PlanSmem &sm) {
+  const int tid = threadIdx.x, NT = blockDim.x, E = a.E, S = a.S;
+  const int flag = (tid < E) && sm.s_count[tid] > 0;
+  int nU;
+  const int u = block_excl_scan(flag, sm.s_warp, &nU);
+  if (flag) sm.s_uexp[u] = tid;
+  __syncthreads();
+
+  int key = -1, slot = -1, hit = 0;
+  if (tid < nU) {
+    const int e = sm.s_uexp[tid];
+    key = a.layer * E + e;
+    if (a.mode == MODE_LRU) {
+      slot = a.cache.key_slot[key];
+      hit = slot >= 0;
+    } else {
+      slot = a.bank * E + e;
+      hit = 1;
+    }
+  }
+  int nH;
+  const int hrank = block_excl_scan(tid < nU && hit, sm.s_warp, &nH);
+  const int nM = nU - nH;
+  const int mrank = tid - hrank;
+  int evicted = -1;
+
+  if (a.mode == MODE_LRU) {
+    const int nwords = (S + 31) >> 5;
+    for (int i = tid; i < nwords; i += NT) sm.s_bits[i] = 0u;
+    __syncthreads();
+    if (tid < nU && hit) atomicOr(&sm.s_bits[slot >> 5], 1u << (slot & 31));
+    __syncthreads();
+    const int per = (S + NT - 1) / NT;
+    const int i0 = min(S, tid * per), i1 = min(S, i0 + per);
+    int cnt = 0;
+    for (int i = i0; i < i1; ++i) {
+      const int s = a.cache.order_in[i];
+      cnt += !((sm.s_bits[s >> 5] >> (s & 31)) & 1u);
+    }
+    int nonhit;
+    int r = block_excl_scan(cnt, sm.s_warp, &nonhit);
+    for (int i = i0; i < i1; ++i) {
+      const int s = a.cache.order_in[i];
+      if ((sm.s_bits[s >> 5] >> (s & 31)) & 1u) continue;
+      if (r < nM) sm.s_victim[r] = s;
+      else a.cache.order_out[r - nM] = s;
+      ++r;
+    }
+    __syncthreads();
+    if (tid < nU) {
+      if (hit) {
+        a.cache.order_out[S - nH - nM + hrank] = slot;
+      } else {
+        const int v = sm.s_victim[mrank];
+        a.cache.order_out[S - nM + mrank] = v;
+        const int ek = a.cache.slot_key[v];
+        if (ek >= 0) {
+          a.cache.key_slot[ek] = -1;
+          evicted = ek;
+        }
+        a.cache.slot_key[v] = key;
+        a.cache.key_slot[key] = v;
+        slot = v;
+      }
+    }
+  }
+  int nEv;
+  block_excl_scan(evicted >= 0, sm.s_warp, &nEv);
+  if (tid < nU) {
+    a.plan.u_expert[tid] = sm.s_uexp[tid];
+    a.plan.u_slot[tid] = slot;
+    a.plan.u_hit[tid] = hit;
+    a.plan.u_evicted[tid] = evicted;
+    if (a.mirror && !hit) {
+      a.mirror[2 + mrank] = key;
+      a.mirror[2 + a.umax + mrank] = slot;
+      __threadfence_system();
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    a.plan.n[0] = nU;
+    a.plan.n[1] = nH;
+    a.plan.n[2] = nM;
+    a.plan.n[3] = nEv;
+    unsigned long long *st = a.cache.stats;
+    const unsigned long long bytes = a.mode == MODE_LRU ? (unsigned long long)nM * a.blob_bytes : 0ull;
+    const unsigned long long hits_ = a.mode == MODE_LRU ? nH : 0, miss_ = a.mode == MODE_LRU ? nM : 0;
+    st[0] += nU; st[1] += hits_; st[2] += miss_; st[3] += nEv; st[4] += bytes;
+    st[8] = nU; st[9] = hits_; st[10] = miss_; st[11] = nEv; st[12] = bytes;
+    if (a.mirror) {
+      a.mirror[1] = nM;
+      __threadfence_system();
+      *(volatile int32_t *)&a.mirror[0] = (int32_t)a.seq;
+      __threadfence_system();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernels
+
+// Whole routing of a small call in one CTA: top-k + gates, histogram,
+// offsets, plan, stable scatter.
+__global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
+  extern __shared__ int smem[];
+  const int E = a.E;
+  int *s_count = smem;                 // E
+  int *s_base = s_count + E;           // E
+  int *s_uexp = s_base + E;            // E
+  int *s_victim = s_uexp + E;          // E
+  int *s_warp = s_victim + E;          // 32
+  int *s_wcnt = s_warp + 32;           // 32*E
+  unsigned *s_bits = (unsigned *)(s_wcnt + 32 * E);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < E; i += blockDim.x) s_count[i] = 0;
+  __syncthreads();
+  for (int t = w; t < a.T; t += blockDim.x >> 5) {
+    const int e = warp_topk_softmax(a.logits + (size_t)t * E, E, a.k, a.plan.topk_idx + (size_t)t * a.k,
+                                    a.plan.gates + (size_t)t * a.k);
+    if (lane < a.k) atomicAdd(&s_count[e], 1);
+  }
+  __syncthreads();
+  int total;
+  const int off = block_excl_scan(tid < E ? s_count[tid] : 0, s_warp, &total);
+  if (tid < E) {
+    a.plan.offsets[tid] = off;
+    s_base[tid] = off;
+  }
+  if (tid == 0) a.plan.offsets[E] = total;
+  PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp};
+  block_plan(a, sm);
+  __syncthreads();
+  block_rank_scatter(a.plan.topk_idx, 0, a.T * a.k, E, s_base, s_wcnt, a.plan.perm, a.plan.inv);
+}
+
+// Multi-CTA path, step 1: top-k + gates for kChunkTokens tokens per CTA
+// (one warp per token), and the CTA's expert histogram.
+__global__ void __launch_bounds__(256) topk_chunk_kernel(const float *__restrict__ logits, int T, int E, int k,
+                                                         int32_t *idx, float *gates, int32_t *chunk_counts) {
+  __shared__ int s_count[kMaxExperts];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < E; i += blockDim.x) s_count[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
+  for (int t = t0 + w; t < t1; t += blockDim.x >> 5) {
+    const int e = warp_topk_softmax(logits + (size_t)t * E, E, k, idx + (size_t)t * k, gates + (size_t)t * k);
+    if (lane < k) atomicAdd(&s_count[e], 1);
+  }
+  __syncthreads();
+  if (chunk_counts)
+    for (int i = tid; i < E; i += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + i] = s_count[i];
+}
+
+// Histogram of given expert ids per chunk (stateless permute).
+__global__ void __launch_bounds__(256) hist_chunk_kernel(const int32_t *__restrict__ idx, int T, int k, int E,
+                                                         int32_t *chunk_counts) {
+  __shared__ int s_count[kMaxExperts];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E; i += blockDim.x) s_count[i] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kChunkTokens * k, p1 = min(T, (blockIdx.x + 1) * kChunkTokens) * k;
+  for (int p = p0 + tid; p < p1; p += blockDim.x) {
+    const int e = idx[p];
+    if (e >= 0 && e < E) atomicAdd(&s_count[e], 1);   // out-of-range ids are not counted
+  }
+  __syncthreads();
+  for (int i = tid; i < E; i += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + i] = s_count[i];
+}
+
+// Multi-CTA path, step 2 (one CTA): per-expert totals and offsets, each
+// chunk's starting position per expert, then (with_plan) the cache plan.
+__global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int with_plan) {
+  extern __shared__ int smem[];
+  const int E = a.E;
+  int *s_count = smem;
+  int *s_uexp = s_count + E;
+  int *s_victim = s_uexp + E;
+  int *s_warp = s_victim + E;
+  unsigned *s_bits = (unsigned *)(s_warp + 32);
+  const int tid = threadIdx.x;
+  int cnt = 0;
+  if (tid < E)
+    for (int c = 0; c < a.n_chunks; ++c) cnt += a.chunk_counts[(size_t)c * E + tid];
+  int total;
+  const int off = block_excl_scan(tid < E ? cnt : 0, s_warp, &total);
+  if (tid < E) {
+    s_count[tid] = cnt;
+    a.plan.offsets[tid] = off;
+    int run = off;
+    for (int c = 0; c < a.n_chunks; ++c) {
+      a.chunk_base[(size_t)c * E + tid] = run;
+      run += a.chunk_counts[(size_t)c * E + tid];
+    }
+  }
+  if (tid == 0) a.plan.offsets[E] = total;
+  __syncthreads();
+  if (with_plan) {
+    PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp};
+    block_plan(a, sm);
+  }
+}
+
+// Multi-CTA path, step 3: stable scatter of each chunk's pairs.
+__global__ void __launch_bounds__(256) scatter_chunk_kernel(const int32_t *__restrict__ idx, int T, int k, int E,
+                                                            const int32_t *__restrict__ chunk_base, int32_t *perm,
+                                                            int32_t *inv) {
+  extern __shared__ int smem[];
+  int *s_base = smem;         // E
+  int *s_wcnt = smem + E;     // 8*E
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_base[i] = chunk_base[(size_t)blockIdx.x * E + i];
+  __syncthreads();
+  const int p0 = blockIdx.x * kChunkTokens * k, p1 = min(T, (blockIdx.x + 1) * kChunkTokens) * k;
+  block_rank_scatter(idx, p0, p1, E, s_base, s_wcnt, perm, inv);
+}
+
+size_t small_smem_bytes(int E, int S) {
+  return sizeof(int) * (4 * (size_t)E + 32 + 32 * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
+}
+size_t plan_smem_bytes(int E, int S) {
+  return sizeof(int) * (3 * (size_t)E + 32) + sizeof(unsigned) * (((size_t)S + 31) / 32);
+}
+
+}  // namespace
+
+void route_init_attributes() {
+  cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaFuncSetAttribute(scatter_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+}
+
+static int n_chunks_of(int T) { return (T + kChunkTokens - 1) / kChunkTokens; }
+
+size_t permute_scratch_ints(int T, int k, int E) {
+  (void)k;
+  return 2 * (size_t)n_chunks_of(T) * (size_t)E;
+}
+
+// Small calls (T*k <= 2048 pairs) route in one CTA; larger ones in three
+// kernels over kChunkTokens-token chunks.
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t s) {
+  if (a.T * a.k <= 2048 || a.chunk_counts == nullptr) {
+    route_small_kernel<<<1, kRouteThreads, small_smem_bytes(a.E, a.S), s>>>(a);
+    return cudaGetLastError();
+  }
+  RouteArgs b = a;
+  b.n_chunks = n_chunks_of(a.T);
+  topk_chunk_kernel<<<b.n_chunks, 256, 0, s>>>(a.logits, a.T, a.E, a.k, a.plan.topk_idx, a.plan.gates,
+                                               b.chunk_counts);
+  plan_kernel<<<1, kRouteThreads, plan_smem_bytes(a.E, a.S), s>>>(b, 1);
+  scatter_chunk_kernel<<<b.n_chunks, 256, sizeof(int) * 9 * (size_t)a.E, s>>>(
+      a.plan.topk_idx, a.T, a.k, a.E, b.chunk_base, a.plan.perm, a.plan.inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_only(const float *logits, int T, int E, int k, int32_t *idx, float *gates,
+                             cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  topk_chunk_kernel<<<n_chunks_of(T), 256, 0, s>>>(logits, T, E, k, idx, gates, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_only(const int32_t *idx, int T, int k, int E, int32_t *offsets, int32_t *perm,
+                                int32_t *inv, int32_t *chunk_counts, int32_t *chunk_base, cudaStream_t s) {
+  RouteArgs a{};
+  a.T = T; a.k = k; a.E = E; a.S = 1;
+  a.plan.offsets = offsets;
+  a.chunk_counts = chunk_counts;
+  a.chunk_base = chunk_base;
+  a.n_chunks = n_chunks_of(T);
+  if (T > 0) hist_chunk_kernel<<<a.n_chunks, 256, 0, s>>>(idx, T, k, E, chunk_counts);
+  plan_kernel<<<1, kRouteThreads, plan_smem_bytes(E, 1), s>>>(a, 0);
+  if (T > 0)
+    scatter_chunk_kernel<<<a.n_chunks, 256, sizeof(int) * 9 * (size_t)E, s>>>(idx, T, k, E, chunk_base, perm, inv);
+  return cudaGetLastError();
+}
+
+}  // namespace ftmoe

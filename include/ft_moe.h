@@ -1,0 +1,214 @@
+/*
+ * ft_moe.h -- C ABI of the host-resident-expert MoE layer for B300 (sm_103a).
+ *
+ * One Mixture-of-Experts layer forward.  The full expert pool sits in pinned
+ * host RAM.  A fixed number of GPU expert slots act as one least-recently-used
+ * cache, shared by all layers.  Sources:
+ *   "FreeToken: Run Frontier MoE Models on Your Own GPU, and the RAM It Takes"
+ *   (devpik.com):
+ *     section "Why a Huge MoE Model Fits on One Consumer GPU" -- the router
+ *       sends each token to a few experts.  The GPU keeps an LRU cache of
+ *       expert slots.  A cached expert runs at GPU speed; a miss is streamed
+ *       over PCIe.  One global LRU pool is shared across layers.
+ *     section "The Real Requirement Is System RAM" -- NVFP4 is 4-bit values
+ *       plus an 8-bit scale for every 16 weights.
+ *     section "Long Prompts Are the Bottleneck" -- prefill copies all experts
+ *       of a layer for each chunk.  The copy of layer N+1 overlaps the compute
+ *       of layer N, and the cache must hold the two staging layers.
+ *   "FreeToken: Run a 290B MoE Model on One Gaming GPU" (wpnews.pro), section
+ *     "VRAM Is Not the Bottleneck You Think It Is" -- the complete pool lives in
+ *     system RAM, and VRAM is an LRU cache of recently activated experts.
+ *
+ * Conventions.
+ *   - Every call returns an ft_status code.  On error it changes no state that
+ *     a later call depends on, except where a call's own text says otherwise.
+ *     ft_last_error() gives a one-line reason.
+ *   - "device" pointers are CUDA device memory of the handle's device;
+ *     "host" pointers are CPU memory.  The caller owns all pointers it passes.
+ *     The library owns every device buffer it allocates, and frees it in
+ *     ft_moe_destroy.
+ *   - stream arguments are cudaStream_t values passed as void* (0 = legacy
+ *     default stream).
+ *   - Calls on one handle are not thread-safe; serialise them.
+ *   - Layouts are row-major.  bf16 is stored as uint16 bit patterns.
+ *
+ * Expert blob (the unit the pool holds and a slot caches).  Per expert there
+ * are three matrices: gate [I][H], up [I][H] and down [H][I], with K
+ * contiguous.  Gate and up are stacked as W_gu [2I][H].
+ *   FT_FMT_BF16 : W_gu bf16[2I][H] | W_d bf16[H][I]                (6HI bytes)
+ *   FT_FMT_NVFP4: gu codes u8[2I][H/2] | gu scales e4m3[2I][H/16]
+ *               | d codes u8[H][I/2]   | d scales e4m3[H][I/16]
+ *               | f32 global scale {gate, up, down, 0}          (27HI/16 + 16)
+ *   FT_FMT_MXFP4: gu codes u8[2I][H/2] | gu scales e8m0[2I][H/32]
+ *               | d codes u8[H][I/2]   | d scales e8m0[H][I/32]         (51HI/32)
+ * FP4 code bytes hold element 2j in the low nibble and 2j+1 in the high
+ * nibble.  An NVFP4 weight is e2m1(code) * e4m3(block scale) * global scale.
+ * An MXFP4 weight is e2m1(code) * 2^(e8m0 - 127) (OCP Microscaling v1.0).
+ */
+#ifndef FT_MOE_H_
+#define FT_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ft_moe ft_moe; /* opaque handle: slot bank, cache tables, streams, events */
+
+enum ft_fmt { FT_FMT_BF16 = 0, FT_FMT_NVFP4 = 1, FT_FMT_MXFP4 = 2 };
+
+enum ft_mode {
+  FT_MODE_LRU = 0,    /* decode: per-call slot lookup, LRU update, miss streaming */
+  FT_MODE_STREAM = 1  /* prefill: whole layers streamed into two slot banks (double buffer) */
+};
+
+enum ft_status {
+  FT_OK = 0,
+  FT_ERR_ARG = -1,             /* an argument is out of range or a pointer is NULL */
+  FT_ERR_CUDA = -2,            /* a CUDA runtime call failed */
+  FT_ERR_OOM = -3,             /* device or pinned allocation failed */
+  FT_ERR_NOT_PINNED = -4,      /* a pool pointer is not page-locked host memory */
+  FT_ERR_CACHE_TOO_SMALL = -5, /* too few slots for one call (LRU) or two staging layers (STREAM) */
+  FT_ERR_STATE = -6,           /* call not valid in the handle's state */
+  FT_ERR_TIMEOUT = -7,         /* a bounded host wait for the device expired */
+  FT_ERR_DEVICE = -8           /* a kernel reported an error word */
+};
+
+/* Cache counters.  A lookup is one distinct (layer, expert) of a forward call;
+ * hits + misses = lookups.  evictions counts misses that displaced a resident
+ * expert.  warm_loads counts experts copied by load_pool/reset.  streamed
+ * counts experts copied by STREAM-mode layer staging.  bytes_h2d counts all
+ * expert bytes copied host->device. */
+typedef struct {
+  uint64_t lookups, hits, misses, evictions, warm_loads, streamed, bytes_h2d;
+} ft_stats;
+
+/* Packed bytes of one expert blob in weight_fmt (layouts above), or -1 for a
+ * bad format or shape. */
+int64_t ft_moe_blob_bytes(int weight_fmt, int hidden, int inter);
+
+/* Creates a layer stack of n_layers MoE layers that share one slot cache.
+ *   hidden H, inter I: multiples of 256; n_experts E in 1..512; top_k in
+ *   1..min(E, 32); weight_fmt an ft_fmt; n_slots S in 1..65536; max_tokens >= 1
+ *   bounds n_tokens of every forward.
+ * Allocates on the current CUDA device: S slots of ft_moe_blob_bytes each
+ * (rounded up to 256 B), the cache tables, and scratch sized by max_tokens.
+ * Errors: FT_ERR_ARG (shape), FT_ERR_CACHE_TOO_SMALL when
+ * S < min(E, max_tokens*top_k) (the distinct experts of one call must fit, so
+ * a call never evicts one of its own experts), FT_ERR_OOM, FT_ERR_CUDA.
+ * *out is set only on FT_OK.
+ * Env FT_FAULT=alloc makes it return FT_ERR_OOM before touching the device
+ * (host-side fault injection for tests). */
+int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fmt,
+                  int n_slots, int n_layers, int max_tokens, ft_moe **out);
+
+/* Registers the host expert pool: host_experts[layer * E + e] points to the
+ * blob of expert e of that layer, in page-locked host memory
+ * (cudaHostAlloc/cudaHostRegister).  The pointers are not copied.  The memory
+ * must outlive the handle.  A contiguous pool is the case
+ * ptr[i] = base + i * blob_bytes.  Then warm-fills the cache: keys
+ * 0..min(S, L*E)-1 go to slots 0.., with slot 0 the least recently used.
+ * Synchronous.  Errors: FT_ERR_ARG (NULL), FT_ERR_NOT_PINNED, FT_ERR_CUDA.
+ * Env FT_FAULT=pin returns FT_ERR_NOT_PINNED before touching the device. */
+int ft_moe_load_pool(ft_moe *h, const void *const *host_experts);
+
+/* Selects FT_MODE_LRU or FT_MODE_STREAM and resets the cache to that mode's
+ * initial state (LRU: warm fill; STREAM: both banks empty).  STREAM needs
+ * S >= 2*E, room for the two staging layers ("Long Prompts Are the
+ * Bottleneck"); FT_ERR_CACHE_TOO_SMALL otherwise.  Synchronous. */
+int ft_moe_set_mode(ft_moe *h, int mode);
+
+/* One MoE layer forward for n_tokens tokens (0 <= n_tokens <= max_tokens):
+ *   x             device bf16 [n_tokens][H]
+ *   router_logits device f32  [n_tokens][E]
+ *   out           device bf16 [n_tokens][H]   (written; may not alias x)
+ * For each token, experts = the top_k largest logits (ties to the lower id),
+ * gates = softmax over those top_k logits, and
+ * out = sum_j gate_j * W_d (silu(W_g x) * (W_u x)) over the token's experts,
+ * with h rounded to bf16 and fp32 accumulation.
+ * LRU mode: the distinct experts of the call are looked up in the slot
+ * table.  Hits move to MRU in ascending expert id.  Then misses, in ascending
+ * id, take the lowest free slot or evict the LRU expert.  All of this is
+ * decided on the GPU.  Miss blobs are copied by cudaMemcpyAsync on the
+ * handle's copy stream, overlapping the FFN of the hits.  The call blocks the
+ * host until the GPU's miss list is known: a bounded wait, FT_ERR_TIMEOUT
+ * after FT_WAIT_TIMEOUT_MS (default 20000).  It cannot run under stream
+ * capture (FT_ERR_STATE).
+ * STREAM mode: bank (layer mod 2) receives all E experts of `layer` before
+ * its FFN.  The copy of the next layer starts in this call and overlaps this
+ * layer's compute.
+ * Work is ordered after earlier work on `stream`.  out is ready when `stream`
+ * reaches the end of this call's work.  Errors: FT_ERR_ARG, FT_ERR_STATE (no
+ * pool loaded), FT_ERR_TIMEOUT, FT_ERR_CUDA.  After FT_ERR_TIMEOUT or
+ * FT_ERR_CUDA the cache state is undefined until ft_cache_reset. */
+int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x,
+                   const float *router_logits, void *out, void *stream);
+
+/* Cumulative counters since the last reset/mode change, and those of the
+ * last forward call.  Waits for the handle's outstanding work.  Either
+ * pointer may be NULL. */
+int ft_cache_stats(ft_moe *h, ft_stats *cumulative, ft_stats *last_call);
+
+/* Restores the initial cache state (warm != 0: warm fill as in load_pool;
+ * warm == 0: every slot free) and clears the counters.  Synchronous. */
+int ft_cache_reset(ft_moe *h, int warm);
+
+/* The last forward call's cache plan, one entry per distinct expert in
+ * ascending id: experts[i], slots[i], hit[i] (1/0), evicted[i] (the displaced
+ * key layer*E+e, or -1).  Writes min(count, cap) entries into host arrays
+ * (any may be NULL) and sets *n = count.  Waits for the handle's work. */
+int ft_cache_trace(ft_moe *h, int32_t *experts, int32_t *slots, int32_t *hit,
+                   int32_t *evicted, int cap, int *n);
+
+/* The last forward call's routing, copied to host arrays (any may be NULL):
+ * topk_idx i32 [T][k], gates f32 [T][k], offsets i32 [E+1] (start of each
+ * expert's group in permuted order), perm i32 [T*k] (pair t*k+j in each
+ * permuted position: grouped by expert ascending, stable in pair order) and
+ * inv i32 [T*k] (permuted position of each pair).  *n_tokens = T.
+ * Waits for the handle's work. */
+int ft_moe_last_routing(ft_moe *h, int32_t *topk_idx, float *gates, int32_t *offsets,
+                        int32_t *perm, int32_t *inv, int *n_tokens);
+
+/* Diagnostics: the last forward call's intermediate activations, copied to
+ * host arrays (either may be NULL), in permuted order:
+ * h_act bf16 [T*k][I] (silu(gate) * up, rounded to bf16) and y f32 [T*k][H]
+ * (the down projection of h_act before the gate-weighted combine).
+ * Waits for the handle's work. */
+int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y);
+
+/* Bytes between consecutive slots in the device slot bank. */
+int64_t ft_moe_slot_stride(const ft_moe *h);
+
+/* One-line reason for the last failure on h (or of the last failed create
+ * when h is NULL).  Never NULL. */
+const char *ft_last_error(const ft_moe *h);
+
+/* Waits for outstanding work, frees every device and pinned buffer the
+ * handle owns, and frees the handle.  NULL is a no-op. */
+int ft_moe_destroy(ft_moe *h);
+
+/* ---- stateless steps (device pointers, asynchronous on `stream`) ---- */
+
+/* Router step: for each of T tokens, the top_k largest of E logits (ties to
+ * the lower id, descending) into topk_idx i32 [T][k], and their softmax into
+ * gates f32 [T][k].  E in 1..512, k in 1..min(E, 32).  Errors: FT_ERR_ARG,
+ * FT_ERR_CUDA. */
+int ft_topk_softmax(const float *router_logits, int T, int E, int k, int32_t *topk_idx,
+                    float *gates, void *stream);
+
+/* Permute step: stable counting sort of the T*k (token, rank) pairs by
+ * expert.  Outputs offsets i32 [E+1], perm i32 [T*k] and inv i32 [T*k], as
+ * in ft_moe_last_routing.  Ids outside [0, E) are neither counted nor placed
+ * (their inv entries are left unwritten and offsets[E] falls short of T*k).  workspace: device scratch of at least
+ * ft_permute_workspace_bytes(T, k, E) bytes, owned by the caller, contents
+ * ignored on entry.  Errors: FT_ERR_ARG, FT_ERR_CUDA. */
+size_t ft_permute_workspace_bytes(int T, int k, int E);
+int ft_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *offsets, int32_t *perm,
+               int32_t *inv, void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FT_MOE_H_ */

@@ -1,0 +1,224 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing indices, permutations, slot plans and cache counters must match
+bit-exactly.  Gates must agree to 1e-6.  Layer outputs must be within the
+stated max relative error of 2e-2: max|out - ref| / max|ref| per call, with
+bf16 activations.  The down projection must be within 1e-3 of a float64
+product on the kernel's own operands (its bf16 h and the dequantised
+weights).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import ftgen
+import oracle as O
+from ftgen.configs import CONFIGS
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import expert_cache_host_softmax_b300 as F  # noqa: E402
+
+OUT_TOL = 2e-2
+GEMM_TOL = 1e-3
+GATE_TOL = 1e-6
+
+
+# ------------------------------------------------------------ stateless steps
+
+@pytest.mark.parametrize("T,E,k", [(1, 128, 8), (64, 8, 2), (37, 256, 8), (1000, 512, 32), (5, 1, 1),
+                                   (3, 33, 33), (0, 8, 2)])
+def test_topk_softmax_matches_oracle(T, E, k):
+    rng = np.random.default_rng(T * 1000 + E)
+    for tied in (False, True):
+        lg = (rng.integers(-3, 4, (T, E)) if tied else rng.standard_normal((T, E))).astype(np.float32)
+        idx, gates = F.topk_softmax(torch.from_numpy(lg).cuda(), k)
+        torch.cuda.synchronize()
+        ref_idx = O.topk_experts(lg, k) if T else np.zeros((0, k), np.int32)
+        assert np.array_equal(idx.cpu().numpy(), ref_idx)
+        if T:
+            np.testing.assert_allclose(gates.cpu().numpy(), O.gates_of(lg, ref_idx), rtol=0, atol=GATE_TOL)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 128, 8), (64, 8, 2), (33, 16, 4), (4096, 128, 8), (8192, 256, 8),
+                                   (1, 1, 1), (0, 8, 2), (777, 512, 3)])
+def test_permute_matches_oracle(T, E, k):
+    rng = np.random.default_rng(T + 7 * E)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    idx = O.topk_experts(lg, k) if T else np.zeros((0, k), np.int32)
+    off, perm, inv = F.permute(torch.from_numpy(idx).cuda(), E)
+    torch.cuda.synchronize()
+    r_off, r_perm, r_inv = O.permute_by_expert(idx, E)
+    assert np.array_equal(off.cpu().numpy(), r_off)
+    assert np.array_equal(perm.cpu().numpy(), r_perm)
+    assert np.array_equal(inv.cpu().numpy(), r_inv)
+
+
+# ------------------------------------------------------------ whole layer
+
+def _check_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=False, fmt=None):
+    xd, lgd = Hn.to_dev(x, lg)
+    out = gpu.forward(layer, xd, lgd)
+    torch.cuda.synchronize()
+    ref = orc.forward(layer, x, lg, tokens=tokens)
+    r = gpu.last_routing()
+    assert np.array_equal(r["idx"], ref["idx"])
+    np.testing.assert_allclose(r["gates"], ref["gates"], rtol=0, atol=GATE_TOL)
+    assert np.array_equal(r["offsets"], ref["offsets"])
+    assert np.array_equal(r["perm"], ref["perm"])
+    assert np.array_equal(r["inv"], ref["inv"])
+    assert gpu.trace() == [tuple(p) for p in ref["plan"]]
+    _, last = gpu.stats()
+    for key_ in ("lookups", "hits", "misses", "evictions", "streamed", "bytes_h2d"):
+        assert last[key_] == ref["last"][key_], key_
+    got = Hn.out_to_f64(out)[ref["out_tokens"]]
+    err = Hn.rel_err(got, ref["out"])
+    assert err <= OUT_TOL, err
+    if gemm_check:
+        T = x.shape[0]
+        hb, y = gpu.last_activations(T)
+        hf = O.bf16_bits_to_f64(hb)
+        for e in ref["experts"]:
+            lo, hi = int(ref["offsets"][e]), int(ref["offsets"][e + 1])
+            _, _, Wd = orc.weights(layer * orc.E + e)
+            y_ref = hf[lo:hi] @ Wd.T
+            assert Hn.rel_err(y[lo:hi].astype(np.float64), y_ref) <= GEMM_TOL
+    return err
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4", "mxfp4"])
+def test_tiny_config_all_formats(fmt):
+    c = CONFIGS["tiny"]
+    gpu, orc, _ = Hn.make_pair(c["H"], c["E"], c["k"], c["I"], fmt, c["S"], c["L"], c["T"], c["seed"])
+    x, lg = Hn.inputs(c["seed"], c["T"], c["H"], c["E"], 0, 0)
+    _check_call(gpu, orc, 0, x, lg, gemm_check=True)
+    cum, _ = gpu.stats()
+    assert cum["misses"] == 0 and cum["warm_loads"] == c["E"]
+    gpu.close()
+
+
+@pytest.mark.parametrize("fmt,T", [("nvfp4", 1), ("bf16", 3), ("mxfp4", 2), ("nvfp4", 9)])
+def test_lru_trace_with_misses_matches_oracle(fmt, T):
+    H, I, E, k, L, S = 256, 256, 16, 2, 3, min(16, 8 + 2 * T)
+    seed = 77 + T
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed)
+    errs = []
+    for step in range(25):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, T, H, E, step, layer, zipf=0.7)
+            errs.append(_check_call(gpu, orc, layer, x, lg, gemm_check=(step % 10 == 0)))
+    cum, _ = gpu.stats()
+    for key_ in ("lookups", "hits", "misses", "evictions", "warm_loads", "bytes_h2d"):
+        assert cum[key_] == orc.stats[key_], key_
+    assert cum["misses"] > 0 and cum["evictions"] > 0
+    gpu.close()
+
+
+def _golden_traces():
+    from tests.test_oracle_pins import _parse_traces
+    return _parse_traces()
+
+
+@pytest.mark.parametrize("trace", _golden_traces(), ids=lambda t: t["name"])
+def test_hand_worked_lru_traces_on_gpu(trace):
+    H = I = 256
+    E, L, S = trace["E"], trace["L"], trace["S"]
+    gpu, _, _ = Hn.make_pair(H, E, 1, I, "bf16", S, L, 2, 5, warm=trace["warm"])
+    look = hits = misses = ev = 0
+    for layer, experts, want in trace["calls"]:
+        T = len(experts)
+        lg = np.full((T, E), -5.0, np.float32)
+        for t, e in enumerate(experts):
+            lg[t, e] = 5.0                       # token t routes to expert e (k = 1)
+        x = ftgen.x_bf16(5, T, H, 0, layer)
+        xd, lgd = Hn.to_dev(x, lg)
+        gpu.forward(layer, xd, lgd)
+        assert gpu.trace() == want
+        _, last = gpu.stats()
+        look += last["lookups"]; hits += last["hits"]; misses += last["misses"]; ev += last["evictions"]
+    assert (look, hits, misses, ev) == trace["stats"]
+    gpu.close()
+
+
+def test_stream_mode_matches_oracle():
+    H, I, E, k, L, T = 256, 512, 8, 2, 4, 40
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "mxfp4", 2 * E, L, T, 21, mode="stream")
+    for step in range(2):
+        for layer in range(L):
+            x, lg = Hn.inputs(21, T, H, E, step, layer, zipf=0.8)
+            _check_call(gpu, orc, layer, x, lg)
+    cum, _ = gpu.stats()
+    assert cum["streamed"] == orc.stats["streamed"] == E * (2 * L + 1)
+    gpu.close()
+
+
+@pytest.mark.parametrize("E,k,T", [(1, 1, 5), (8, 8, 7), (64, 8, 300)])
+def test_edge_shapes(E, k, T):
+    # E = 1 (plain MLP), k = E (dense mixture), T*k > 2048 (multi-CTA routing)
+    H, I = 256, 256
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, 1, T, 31)
+    x, lg = Hn.inputs(31, T, H, E, 0, 0)
+    _check_call(gpu, orc, 0, x, lg, gemm_check=True)
+    # an empty call changes nothing
+    xd, lgd = Hn.to_dev(x[:0], lg[:0])
+    out = gpu.forward(0, xd, lgd)
+    assert out.shape == (0, H)
+    _, last = gpu.stats()
+    assert last["lookups"] == 0
+    gpu.close()
+
+
+def test_unit_global_scale_nvfp4():
+    # g = 1 puts N(0, 0.02) block scales in E4M3's subnormal range
+    H, I, E, k, T = 256, 256, 4, 2, 6
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, 1, T, 41, flags=ftgen.FLAG_NVFP4_UNIT_GSCALE)
+    x, lg = Hn.inputs(41, T, H, E, 0, 0)
+    _check_call(gpu, orc, 0, x, lg, gemm_check=True)
+    gpu.close()
+
+
+# ------------------------------------------------------------ failure paths
+
+def test_wait_timeout_is_reported_and_reset_recovers(monkeypatch):
+    H, I, E, k, T = 256, 256, 8, 2, 4
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "bf16", 8, 2, T, 51)
+    x, lg = Hn.inputs(51, T, H, E, 0, 0)
+    xd, lgd = Hn.to_dev(x, lg)
+    monkeypatch.setenv("FT_FAULT", "timeout")
+    with pytest.raises(F.FtError) as ei:
+        gpu.forward(1, xd, lgd)
+    assert ei.value.code == F.FT_ERR_TIMEOUT
+    monkeypatch.delenv("FT_FAULT")
+    gpu.reset(warm=True)
+    _check_call(gpu, orc, 1, x, lg)
+    gpu.close()
+
+
+def test_unpinned_pool_is_rejected(monkeypatch):
+    H, I, E = 256, 256, 4
+    gpu = F.MoELayerStack(H, E, 1, I, "bf16", 4, 1, 1)
+    plain = np.zeros(E * ftgen.blob_bytes("bf16", H, I), np.uint8)
+    with pytest.raises(F.FtError) as ei:
+        gpu.load_pool([plain.ctypes.data + i * ftgen.blob_bytes("bf16", H, I) for i in range(E)])
+    assert ei.value.code == F.FT_ERR_NOT_PINNED
+    monkeypatch.setenv("FT_FAULT", "pin")
+    with pytest.raises(F.FtError) as ei:
+        gpu.load_pool([0x1000] * E)
+    assert ei.value.code == F.FT_ERR_NOT_PINNED
+    gpu.close()
+
+
+def test_forward_before_pool_and_bad_layer():
+    gpu = F.MoELayerStack(256, 4, 1, 256, "bf16", 4, 2, 1)
+    x = torch.zeros((1, 256), dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros((1, 4), dtype=torch.float32, device="cuda")
+    with pytest.raises(F.FtError) as ei:
+        gpu.forward(0, x, lg)
+    assert ei.value.code == F.FT_ERR_STATE
+    gpu.close()
