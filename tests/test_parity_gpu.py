@@ -33,7 +33,7 @@ GATE_TOL = 1e-6
 # ------------------------------------------------------------ stateless steps
 
 @pytest.mark.parametrize("T,E,k", [(1, 128, 8), (64, 8, 2), (37, 256, 8), (1000, 512, 32), (5, 1, 1),
-                                   (3, 33, 33), (0, 8, 2)])
+                                   (3, 32, 32), (0, 8, 2)])
 def test_topk_softmax_matches_oracle(T, E, k):
     rng = np.random.default_rng(T * 1000 + E)
     for tied in (False, True):
