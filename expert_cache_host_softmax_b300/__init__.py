@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "FT_OK", -1: "FT_ERR_ARG", -2: "FT_ERR_CUDA", -3: "FT_ERR_OOM
 #: every symbol include/ft_moe.h declares
 EXPORTED = ("ft_moe_blob_bytes", "ft_moe_create", "ft_moe_load_pool", "ft_moe_set_mode", "ft_moe_forward",
             "ft_cache_stats", "ft_cache_reset", "ft_cache_trace", "ft_moe_last_routing", "ft_moe_last_activations",
-            "ft_moe_slot_stride",
+            "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_slot_stride", "ft_moe_kernel_launches",
             "ft_last_error", "ft_moe_destroy", "ft_topk_softmax", "ft_permute_workspace_bytes", "ft_permute")
 
 
@@ -70,6 +70,10 @@ def lib():
         L.ft_cache_trace.argtypes = [vp, vp, vp, vp, vp, i32, P(i32)]
         L.ft_moe_last_routing.argtypes = [vp, vp, vp, vp, vp, vp, P(i32)]
         L.ft_moe_last_activations.argtypes = [vp, vp, vp]
+        L.ft_moe_set_profiling.argtypes = [vp, i32]
+        L.ft_moe_profile_read.argtypes = [vp, vp, vp, i32]
+        L.ft_moe_kernel_launches.restype = i64
+        L.ft_moe_kernel_launches.argtypes = [vp]
         L.ft_moe_slot_stride.restype = i64
         L.ft_moe_slot_stride.argtypes = [vp]
         L.ft_last_error.restype = ctypes.c_char_p
@@ -188,6 +192,23 @@ class MoELayerStack:
         y = np.zeros((T * self.k, self.H), np.float32)
         _check(lib().ft_moe_last_activations(self._h, hb.ctypes.data, y.ctypes.data), self._h)
         return hb, y
+
+    PROF_CLASSES = ("route", "gateup_hit", "gateup_miss", "down", "combine", "miss_copy", "stream_copy")
+
+    def set_profiling(self, on=True):
+        _check(lib().ft_moe_set_profiling(self._h, 1 if on else 0), self._h)
+
+    def profile(self):
+        """{class: (total ms, occurrences)} since profiling was enabled."""
+        n = len(self.PROF_CLASSES)
+        ms = np.zeros(n, np.float64)
+        cnt = np.zeros(n, np.int64)
+        _check(lib().ft_moe_profile_read(self._h, ms.ctypes.data, cnt.ctypes.data, n), self._h)
+        return {c: (float(ms[i]), int(cnt[i])) for i, c in enumerate(self.PROF_CLASSES)}
+
+    @property
+    def kernel_launches(self):
+        return int(lib().ft_moe_kernel_launches(self._h))
 
     @property
     def slot_stride(self):

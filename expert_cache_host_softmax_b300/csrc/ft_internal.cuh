@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/ft_moe.h"
+
 namespace ftmoe {
 
 enum { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_MXFP4 = 2 };
@@ -14,6 +16,7 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 constexpr int kRouteThreads = 1024;       // single-CTA routing / plan kernels
 constexpr int kChunkTokens = 32;          // tokens per CTA in the multi-CTA routing path
+constexpr int kSmallRoutePairs = 2048;    // calls with T*k up to this route in one CTA
 
 // Byte offsets of the sections of one expert blob (see include/ft_moe.h).
 struct BlobLayout {
@@ -75,6 +78,7 @@ struct RouteArgs {
 
 // Launchers (route.cu)
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s);
+int route_kernel_count(int T, int k);
 cudaError_t launch_topk_only(const float *logits, int T, int E, int k, int32_t *idx, float *gates,
                              cudaStream_t s);
 cudaError_t launch_permute_only(const int32_t *idx, int T, int k, int E, int32_t *offsets,

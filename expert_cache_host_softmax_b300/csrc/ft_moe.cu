@@ -56,6 +56,13 @@ struct ft_moe {
   bool any_call = false;
   uint64_t host_warm = 0, host_streamed = 0, host_bytes = 0;
   uint64_t last_streamed = 0, last_stream_bytes = 0;
+  // optional per-step timing (ft_moe_set_profiling)
+  bool prof = false;
+  cudaEvent_t prof_ev[2 * FT_PROF_CLASSES] = {};
+  bool prof_pending[FT_PROF_CLASSES] = {};
+  double prof_ms[FT_PROF_CLASSES] = {};
+  int64_t prof_launches[FT_PROF_CLASSES] = {};
+  int64_t kernel_launches = 0;
   std::string err;
 };
 
@@ -122,6 +129,31 @@ void free_all(ft_moe *h) {
   for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
                          h->ev_bank_free[0], h->ev_bank_free[1]})
     if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : h->prof_ev)
+    if (ev) cudaEventDestroy(ev);
+}
+
+// Profiling: events around one step class on the stream it runs on.
+void prof_begin(ft_moe *h, int cls, cudaStream_t s) {
+  if (h->prof) cudaEventRecord(h->prof_ev[2 * cls], s);
+}
+void prof_end(ft_moe *h, int cls, cudaStream_t s) {
+  if (!h->prof) return;
+  cudaEventRecord(h->prof_ev[2 * cls + 1], s);
+  h->prof_pending[cls] = true;
+}
+// Folds the recorded pairs into the totals (waits for them).
+void prof_collect(ft_moe *h) {
+  for (int c = 0; c < FT_PROF_CLASSES; ++c) {
+    if (!h->prof_pending[c]) continue;
+    float ms = 0.f;
+    if (cudaEventSynchronize(h->prof_ev[2 * c + 1]) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, h->prof_ev[2 * c], h->prof_ev[2 * c + 1]) == cudaSuccess) {
+      h->prof_ms[c] += ms;
+      h->prof_launches[c] += 1;
+    }
+    h->prof_pending[c] = false;
+  }
 }
 
 // Waits for everything the handle has issued.
@@ -172,10 +204,13 @@ int stage_layer(ft_moe *h, int layer) {
   const int b = layer & 1;
   if (h->bank_layer[b] == layer) return FT_OK;
   FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_bank_free[b], 0));
+  if (h->prof && h->prof_pending[FT_PROF_STREAM_COPY]) prof_collect(h);
+  prof_begin(h, FT_PROF_STREAM_COPY, h->copy_stream);
   for (int e = 0; e < h->E; ++e)
     FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)(b * h->E + e) * h->slot_stride,
                                h->pool[(size_t)layer * h->E + e], h->blob_bytes, cudaMemcpyHostToDevice,
                                h->copy_stream));
+  prof_end(h, FT_PROF_STREAM_COPY, h->copy_stream);
   FT_CUDA(h, cudaEventRecord(h->ev_bank_ready[b], h->copy_stream));
   h->bank_layer[b] = layer;
   h->last_streamed += h->E;
@@ -354,7 +389,10 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   ra.seq = h->seq;
   ra.chunk_counts = h->chunk_counts;
   ra.chunk_base = h->chunk_base;
+  prof_begin(h, FT_PROF_ROUTE, stream);
   FT_CUDA(h, launch_route(ra, stream));
+  prof_end(h, FT_PROF_ROUTE, stream);
+  h->kernel_launches += route_kernel_count(n_tokens, h->k) + 3;  // + gate/up, down, combine
   if (h->mode == MODE_LRU) h->order_cur ^= 1;
   FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
 
@@ -369,11 +407,14 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
   if (h->mode == MODE_LRU) {
     fa.only = 1;
+    prof_begin(h, FT_PROF_GATEUP_HIT, stream);
     FT_CUDA(h, launch_gateup(fa, stream));
+    prof_end(h, FT_PROF_GATEUP_HIT, stream);
     if (int rc = wait_plan(h)) return rc;
     const int n_miss = h->mirror_host[1];
     if (n_miss > 0) {
       FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_route, 0));
+      prof_begin(h, FT_PROF_MISS_COPY, h->copy_stream);
       for (int i = 0; i < n_miss; ++i) {
         const int key = h->mirror_host[2 + i], slot = h->mirror_host[2 + h->umax + i];
         if (key < 0 || key >= h->L * h->E || slot < 0 || slot >= h->S)
@@ -381,23 +422,59 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
         FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)slot * h->slot_stride, h->pool[key], h->blob_bytes,
                                    cudaMemcpyHostToDevice, h->copy_stream));
       }
+      prof_end(h, FT_PROF_MISS_COPY, h->copy_stream);
       FT_CUDA(h, cudaEventRecord(h->ev_copy, h->copy_stream));
       FT_CUDA(h, cudaStreamWaitEvent(stream, h->ev_copy, 0));
       fa.only = 2;
+      h->kernel_launches += 1;
+      prof_begin(h, FT_PROF_GATEUP_MISS, stream);
       FT_CUDA(h, launch_gateup(fa, stream));
+      prof_end(h, FT_PROF_GATEUP_MISS, stream);
     }
   } else {
     fa.only = 0;
+    prof_begin(h, FT_PROF_GATEUP_HIT, stream);
     FT_CUDA(h, launch_gateup(fa, stream));
+    prof_end(h, FT_PROF_GATEUP_HIT, stream);
   }
   fa.only = 0;
+  prof_begin(h, FT_PROF_DOWN, stream);
   FT_CUDA(h, launch_down(fa, stream));
+  prof_end(h, FT_PROF_DOWN, stream);
+  prof_begin(h, FT_PROF_COMBINE, stream);
   FT_CUDA(h, launch_combine(h->ybuf, h->plan.gates, h->plan.inv, n_tokens, h->k, h->H,
                             reinterpret_cast<__nv_bfloat16 *>(out), stream));
+  prof_end(h, FT_PROF_COMBINE, stream);
   if (h->mode == MODE_STREAM) FT_CUDA(h, cudaEventRecord(h->ev_bank_free[bank], stream));
   FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
   h->host_streamed += h->last_streamed;
   h->host_bytes += h->last_stream_bytes;
+  if (h->prof) prof_collect(h);
+  return FT_OK;
+}
+
+int ft_moe_set_profiling(ft_moe *h, int enable) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  for (int i = 0; i < 2 * FT_PROF_CLASSES; ++i)
+    if (!h->prof_ev[i]) FT_CUDA(h, cudaEventCreate(&h->prof_ev[i]));
+  for (int c = 0; c < FT_PROF_CLASSES; ++c) {
+    h->prof_ms[c] = 0.0;
+    h->prof_launches[c] = 0;
+    h->prof_pending[c] = false;
+  }
+  h->prof = enable != 0;
+  return FT_OK;
+}
+
+int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches, int n) {
+  if (!h || n < 0) return fail(h, FT_ERR_ARG, "NULL handle or negative n");
+  if (int rc = sync_handle(h)) return rc;
+  prof_collect(h);
+  for (int c = 0; c < std::min(n, (int)FT_PROF_CLASSES); ++c) {
+    if (ms) ms[c] = h->prof_ms[c];
+    if (launches) launches[c] = h->prof_launches[c];
+  }
   return FT_OK;
 }
 
@@ -456,6 +533,8 @@ int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y) {
 }
 
 int64_t ft_moe_slot_stride(const ft_moe *h) { return h ? h->slot_stride : -1; }
+
+int64_t ft_moe_kernel_launches(const ft_moe *h) { return h ? h->kernel_launches : -1; }
 
 const char *ft_last_error(const ft_moe *h) { return h ? h->err.c_str() : g_create_err.c_str(); }
 

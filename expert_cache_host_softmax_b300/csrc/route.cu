@@ -397,10 +397,12 @@ size_t permute_scratch_ints(int T, int k, int E) {
   return 2 * (size_t)n_chunks_of(T) * (size_t)E;
 }
 
-// Small calls (T*k <= 2048 pairs) route in one CTA; larger ones in three
-// kernels over kChunkTokens-token chunks.
+int route_kernel_count(int T, int k) { return T * k <= kSmallRoutePairs ? 1 : 3; }
+
+// Small calls (T*k <= kSmallRoutePairs) route in one CTA; larger ones in
+// three kernels over kChunkTokens-token chunks.
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s) {
-  if (a.T * a.k <= 2048 || a.chunk_counts == nullptr) {
+  if (a.T * a.k <= kSmallRoutePairs || a.chunk_counts == nullptr) {
     route_small_kernel<<<1, kRouteThreads, small_smem_bytes(a.E, a.S), s>>>(a);
     return cudaGetLastError();
   }

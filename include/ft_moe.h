@@ -178,8 +178,32 @@ int ft_moe_last_routing(ft_moe *h, int32_t *topk_idx, float *gates, int32_t *off
  * Waits for the handle's work. */
 int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y);
 
+/* Step classes timed by the profiling facility. */
+enum ft_prof_class {
+  FT_PROF_ROUTE = 0,       /* top-k, permute and cache plan kernels */
+  FT_PROF_GATEUP_HIT = 1,  /* gate/up FFN over hits (LRU) or over all experts (STREAM) */
+  FT_PROF_GATEUP_MISS = 2, /* gate/up FFN over misses (LRU) */
+  FT_PROF_DOWN = 3,        /* down FFN */
+  FT_PROF_COMBINE = 4,     /* gate-weighted combine */
+  FT_PROF_MISS_COPY = 5,   /* the misses' host->device copies of one call (copy stream) */
+  FT_PROF_STREAM_COPY = 6, /* one layer's staging copies in STREAM mode (copy stream) */
+  FT_PROF_CLASSES = 7
+};
+
+/* Profiling: while enabled, every forward brackets each step class with CUDA
+ * events on the stream that runs it, and waits at its end for them (so the
+ * forward becomes host-synchronous).  Enabling or disabling clears the
+ * totals.  ft_moe_profile_read returns, per class (first n classes), the
+ * summed milliseconds and the number of timed occurrences. */
+int ft_moe_set_profiling(ft_moe *h, int enable);
+int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches, int n);
+
 /* Bytes between consecutive slots in the device slot bank. */
 int64_t ft_moe_slot_stride(const ft_moe *h);
+
+/* Number of CUDA kernels the handle has launched since creation (-1 for
+ * NULL). */
+int64_t ft_moe_kernel_launches(const ft_moe *h);
 
 /* One-line reason for the last failure on h (or of the last failed create
  * when h is NULL).  Never NULL. */

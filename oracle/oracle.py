@@ -361,12 +361,16 @@ class MoELayerOracle:
         if nxt % 2 != layer % 2:
             fill(nxt)
 
-    def forward(self, layer: int, x_bits: np.ndarray, logits: np.ndarray, tokens=None):
+    def forward(self, layer: int, x_bits: np.ndarray, logits: np.ndarray, tokens=None, ffn_experts=None):
         """x_bits: bf16 bits [T, H]; logits: float32 [T, E].
 
         Returns a dict with routing (idx, gates), permutation, the cache plan
         for this call, the per-call statistics, and out (float64 [T, H], or only
-        the rows in `tokens` when a token sample is given)."""
+        the rows in `tokens` when a token sample is given).
+
+        ffn_experts (timing samples only): evaluate the FFN of just these
+        experts of the call; routing and the cache update still run in full,
+        and out then holds no meaningful values."""
         T = x_bits.shape[0]
         idx = topk_experts(logits, self.k)
         gates = gates_of(logits, idx)
@@ -393,6 +397,16 @@ class MoELayerOracle:
         want = set(range(T)) if tokens is None else set(int(t) for t in tokens)
         x = bf16_bits_to_f64(x_bits)
         y = {}
+        if ffn_experts is not None:
+            res["out"] = None
+            res["out_tokens"] = np.array(sorted(want), np.int64)
+            for e in ffn_experts:
+                lo, hi = int(offsets[e]), int(offsets[e + 1])
+                pairs = [int(p) for p in perm[lo:hi] if int(p) // self.k in want]
+                if pairs:
+                    Wg, Wu, Wd = self.weights(layer * self.E + e)
+                    expert_ffn(np.stack([x[p // self.k] for p in pairs]), Wg, Wu, Wd, self.h_bf16)
+            return res
         for e in experts:
             lo, hi = int(offsets[e]), int(offsets[e + 1])
             pairs = [int(p) for p in perm[lo:hi] if int(p) // self.k in want]
