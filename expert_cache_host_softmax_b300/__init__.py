@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "FT_OK", -1: "FT_ERR_ARG", -2: "FT_ERR_CUDA", -3: "FT_ERR_OOM
 EXPORTED = ("ft_moe_blob_bytes", "ft_moe_create", "ft_moe_load_pool", "ft_moe_set_mode", "ft_moe_forward",
             "ft_cache_stats", "ft_cache_reset", "ft_cache_trace", "ft_moe_last_routing", "ft_moe_last_activations",
             "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_slot_stride", "ft_moe_kernel_launches",
-            "ft_last_error", "ft_moe_destroy", "ft_topk_softmax", "ft_permute_workspace_bytes", "ft_permute")
+            "ft_last_error", "ft_moe_destroy", "ft_topk_softmax", "ft_permute_workspace_bytes", "ft_permute", "ft_permute_noalloc")
 
 
 class FtStats(ctypes.Structure):
@@ -83,6 +83,7 @@ def lib():
         L.ft_permute_workspace_bytes.restype = sz
         L.ft_permute_workspace_bytes.argtypes = [i32, i32, i32]
         L.ft_permute.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        L.ft_permute_noalloc.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -237,4 +238,22 @@ def permute(topk_idx, n_experts, stream=None):
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     _check(lib().ft_permute(_ptr(topk_idx), T, k, n_experts, _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(ws),
                             ws_bytes, _stream_ptr(stream)))
+    return offsets, perm, inv
+
+
+#: scratch bytes of ft_permute_noalloc's fixed device array
+PERMUTE_NOALLOC_MAX_SCRATCH_BYTES = 2 << 20
+
+
+def permute_noalloc(topk_idx, n_experts, stream=None):
+    """ft_permute_noalloc: like permute() but the library allocates nothing
+    and takes no workspace (its scratch is a fixed device array)."""
+    import torch
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    offsets = torch.empty(n_experts + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    _check(lib().ft_permute_noalloc(_ptr(topk_idx), T, k, n_experts, _ptr(offsets), _ptr(perm), _ptr(inv),
+                                    _stream_ptr(stream)))
     return offsets, perm, inv

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "../../include/ft_moe.h"
 
 namespace ftmoe {
@@ -104,5 +106,8 @@ cudaError_t launch_down(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *gates, const int32_t *inv, int T, int k, int H,
                            __nv_bfloat16 *out, cudaStream_t s);
 void ffn_init_attributes();
+
+// Sets the message ft_last_error(NULL) returns on this thread.
+void set_stateless_error(const std::string &msg);
 
 }  // namespace ftmoe

@@ -246,6 +246,8 @@ int wait_plan(ft_moe *h) {
 
 }  // namespace
 
+void ftmoe::set_stateless_error(const std::string &msg) { g_create_err = msg; }
+
 extern "C" {
 
 int64_t ft_moe_blob_bytes(int weight_fmt, int hidden, int inter) { return blob_bytes_of(weight_fmt, hidden, inter); }

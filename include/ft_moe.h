@@ -232,6 +232,32 @@ size_t ft_permute_workspace_bytes(int T, int k, int E);
 int ft_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *offsets, int32_t *perm,
                int32_t *inv, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- permute without allocation ----
+ * The pages have no counterpart to this entry point.  It exists for callers
+ * that cannot allocate device memory when they run the permute step.  Examples:
+ * a serving loop that keeps cudaMalloc/cudaFree off its hot path, because those
+ * calls can synchronise the whole device; or a framework whose device memory is
+ * all owned by its own pool allocator, with no way to lend scratch to a library.
+ *
+ * Same inputs, outputs and result as ft_permute, but with no workspace
+ * argument.  Its scratch is one file-scope device array of
+ * FT_PERMUTE_NOALLOC_MAX_SCRATCH_BYTES bytes.  Every GPU that loads the library
+ * holds that array until the process exits.  The call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *   - Limit: needs 2 * ceil(T/32) * E * 4 bytes of scratch; larger requests
+ *     return FT_ERR_ARG (e.g. E = 256 allows T <= 32768).
+ *   - The first call made with a given device current looks up the array's
+ *     device address (cudaGetSymbolAddress) once for that device.  Make that
+ *     first call before any stream capture.
+ *   - Every call shares the one array and overwrites it.  Calls whose work
+ *     overlaps on the GPU (other streams, other threads) race on it; serialise
+ *     them, e.g. on one stream.  Nothing in the array needs to start at zero:
+ *     each call writes every entry before reading it.
+ * Errors: FT_ERR_ARG, FT_ERR_CUDA (ft_last_error(NULL) says which). */
+#define FT_PERMUTE_NOALLOC_MAX_SCRATCH_BYTES (2u << 20)
+int ft_permute_noalloc(const int32_t *topk_idx, int T, int k, int E, int32_t *offsets, int32_t *perm,
+                       int32_t *inv, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
