@@ -107,6 +107,13 @@ cudaError_t launch_combine(const float *y, const float *gates, const int32_t *in
                            __nv_bfloat16 *out, cudaStream_t s);
 void ffn_init_attributes();
 
+// Expert FFN on the tensor cores (grouped_gemm.cu)
+void gemm_init_attributes();
+int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, int H, int I, void *map_gu,
+                     void *map_d);
+cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_gu, const void *map_d, int *err,
+                          int64_t max_rows, cudaStream_t s);
+
 // Sets the message ft_last_error(NULL) returns on this thread.
 void set_stateless_error(const std::string &msg);
 

@@ -54,6 +54,7 @@ struct ft_moe {
   uint32_t seq = 0;
   int last_T = 0;
   bool any_call = false;
+  bool last_tc = false;
   uint64_t host_warm = 0, host_streamed = 0, host_bytes = 0;
   uint64_t last_streamed = 0, last_stream_bytes = 0;
   // optional per-step timing (ft_moe_set_profiling)
@@ -63,6 +64,12 @@ struct ft_moe {
   double prof_ms[FT_PROF_CLASSES] = {};
   int64_t prof_launches[FT_PROF_CLASSES] = {};
   int64_t kernel_launches = 0;
+  // tensor-core FFN: TMA descriptors over the slot bank, the kernel choice,
+  // and a device error word that bounded waits write when they give up
+  alignas(64) unsigned char tmap[2][128] = {};
+  bool tmaps_ok = false;
+  int ffn_kernel = FT_FFN_AUTO;
+  int *err_dev = nullptr;
   std::string err;
 };
 
@@ -124,6 +131,7 @@ void free_all(ft_moe *h) {
   cudaFree(h->chunk_base);
   cudaFree(h->hbuf);
   cudaFree(h->ybuf);
+  cudaFree(h->err_dev);
   if (h->mirror_host) cudaFreeHost(h->mirror_host);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
@@ -156,11 +164,34 @@ void prof_collect(ft_moe *h) {
   }
 }
 
-// Waits for everything the handle has issued.
+// Waits for everything the handle has issued, then checks the device error
+// word (set by a kernel whose bounded wait gave up).
 int sync_handle(ft_moe *h) {
   if (h->any_call) FT_CUDA(h, cudaEventSynchronize(h->ev_done));
   FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+  int code = 0;
+  FT_CUDA(h, cudaMemcpy(&code, h->err_dev, sizeof code, cudaMemcpyDeviceToHost));
+  if (code != 0) {
+    FT_CUDA(h, cudaMemset(h->err_dev, 0, sizeof(int)));
+    return fail(h, FT_ERR_DEVICE, "a tensor-core FFN kernel gave up waiting (site " + std::to_string(code) + ")");
+  }
   return FT_OK;
+}
+
+// Whether this call's FFN runs on the tensor cores: forced by
+// ft_moe_set_ffn_kernel, else when the call's experts average at least 64
+// token rows each (below that the weight-streaming GEMV wins).
+bool use_tc(const ft_moe *h, int T) {
+  if (!h->tmaps_ok) return false;
+  if (h->ffn_kernel == FT_FFN_GEMV) return false;
+  if (h->ffn_kernel == FT_FFN_TC) return true;
+  const int64_t rows = (int64_t)T * h->k, distinct = std::min<int64_t>(h->E, rows);
+  return rows >= 64 * distinct;
+}
+
+cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cudaStream_t s) {
+  if (tc) return launch_tc_ffn(fa, down, h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
+  return down ? launch_down(fa, s) : launch_gateup(fa, s);
 }
 
 // Initial cache state of the current mode; clears the counters.
@@ -289,7 +320,8 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->plan.u_evicted, umax) == cudaSuccess && dev_alloc(&h->plan.n, 4) == cudaSuccess &&
             dev_alloc(&h->chunk_counts, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->chunk_base, chunk_ints) == cudaSuccess &&
-            dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess;
+            dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
+            dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess;
   if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
   if (cudaHostAlloc(&h->mirror_host, sizeof(int32_t) * (2 + 2 * (size_t)umax), cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer(reinterpret_cast<void **>(&h->mirror_dev), h->mirror_host, 0) != cudaSuccess) {
@@ -309,6 +341,8 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
   if (!ok) { cuda_fail(nullptr, cudaGetLastError(), "stream/event creation"); return bail(FT_ERR_CUDA); }
   route_init_attributes();
   ffn_init_attributes();
+  gemm_init_attributes();
+  h->tmaps_ok = make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0;
   if (int rc = reset_tables(h, false)) { g_create_err = h->err; return bail(rc); }
   *out = h;
   return FT_OK;
@@ -407,10 +441,12 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.y = h->ybuf;
   fa.plan = h->plan;
   fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
+  const bool tc = use_tc(h, n_tokens);
+  h->last_tc = tc;
   if (h->mode == MODE_LRU) {
     fa.only = 1;
     prof_begin(h, FT_PROF_GATEUP_HIT, stream);
-    FT_CUDA(h, launch_gateup(fa, stream));
+    FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
     prof_end(h, FT_PROF_GATEUP_HIT, stream);
     if (int rc = wait_plan(h)) return rc;
     const int n_miss = h->mirror_host[1];
@@ -430,18 +466,18 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
       fa.only = 2;
       h->kernel_launches += 1;
       prof_begin(h, FT_PROF_GATEUP_MISS, stream);
-      FT_CUDA(h, launch_gateup(fa, stream));
+      FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
       prof_end(h, FT_PROF_GATEUP_MISS, stream);
     }
   } else {
     fa.only = 0;
     prof_begin(h, FT_PROF_GATEUP_HIT, stream);
-    FT_CUDA(h, launch_gateup(fa, stream));
+    FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
     prof_end(h, FT_PROF_GATEUP_HIT, stream);
   }
   fa.only = 0;
   prof_begin(h, FT_PROF_DOWN, stream);
-  FT_CUDA(h, launch_down(fa, stream));
+  FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream));
   prof_end(h, FT_PROF_DOWN, stream);
   prof_begin(h, FT_PROF_COMBINE, stream);
   FT_CUDA(h, launch_combine(h->ybuf, h->plan.gates, h->plan.inv, n_tokens, h->k, h->H,
@@ -533,6 +569,16 @@ int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y) {
   if (TK && y) FT_CUDA(h, cudaMemcpy(y, h->ybuf, 4 * TK * h->H, cudaMemcpyDeviceToHost));
   return FT_OK;
 }
+
+int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
+  if (!h || which < FT_FFN_AUTO || which > FT_FFN_TC) return fail(h, FT_ERR_ARG, "bad FFN kernel choice");
+  if (which == FT_FFN_TC && !h->tmaps_ok)
+    return fail(h, FT_ERR_CUDA, "tensor-core FFN unavailable: the TMA descriptors could not be encoded");
+  h->ffn_kernel = which;
+  return FT_OK;
+}
+
+int ft_moe_last_ffn_kernel(const ft_moe *h) { return h ? (h->last_tc ? FT_FFN_TC : FT_FFN_GEMV) : -1; }
 
 int64_t ft_moe_slot_stride(const ft_moe *h) { return h ? h->slot_stride : -1; }
 

@@ -1,0 +1,736 @@
+// grouped_gemm.cu -- grouped SwiGLU expert FFN on the 5th-generation tensor
+// cores (tcgen05 + TMEM), for calls whose experts see many tokens (prefill).
+//
+// Per distinct expert u of a call (blob in slot u_slot[u]; its tokens sit at
+// permuted positions offsets[e] .. offsets[e+1]):
+//   gate/up:  [g | u] = x_rows . W_gu^T   (fp32 accumulators in TMEM)
+//             h = bf16( silu(g) * u )     (epilogue)
+//   down:     y = h . W_d^T               (fp32)
+// The pages say only that cached experts run "at GPU speed" ("Why a Huge MoE
+// Model Fits on One Consumer GPU"); SwiGLU and this kernel design are ours.
+//
+// One persistent CTA per SM walks the call's output tiles.  A tile is 128
+// token rows x 256 weight rows (gate/up: 128 gate rows + the 128 matching up
+// rows, so the SiLU*mul epilogue sees both halves; down: 256 rows of H).
+// K advances in blocks of 64 through a ring of shared-memory stages:
+//   - A (token rows, bf16) is gathered row by row with cp.async into the
+//     128-byte-swizzled K-major layout (gate/up rows come from x through the
+//     permutation; down rows are the contiguous h rows of the group);
+//   - B (weights) comes by TMA from the slot bank.  BF16 weights land directly
+//     in the swizzled layout.  NVFP4 / MXFP4 codes land raw; the loader warps
+//     dequantise them to bf16 (e2m1 x block scale, exact in bf16) into the
+//     swizzled B tile.  The NVFP4 per-matrix global scale is applied to the
+//     fp32 accumulator in the epilogue.
+//   - one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> f32)
+//     into one of two TMEM accumulators (2 x 256 columns), so the epilogue of
+//     a tile overlaps the MMAs of the next;
+//   - four epilogue warps read the accumulator with tcgen05.ld (one TMEM lane
+//     = one token row per thread) and write h (bf16) or y (f32).
+// Every mbarrier wait is bounded in time.  A wait that runs out records an
+// error code, raises the CTA's abort flag, and every role drains its own
+// in-flight copies before the CTA frees its TMEM and exits.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "ft_internal.cuh"
+
+namespace ftmoe {
+
+namespace {
+
+constexpr int BM = 128;          // token rows per tile (one TMEM lane each)
+constexpr int BN = 256;          // weight rows per tile (MMA N)
+constexpr int BK = 64;           // K per stage: 128 bytes of bf16 (one swizzle atom)
+constexpr int NS = 4;            // stages in the ring
+constexpr int LAG = 3;           // stages between issuing a load and publishing it
+constexpr int kEpiWarps = 4;
+constexpr int A_STAGE = BM * BK * 2;          // 16 KB
+constexpr int B_STAGE = BN * BK * 2;          // 32 KB
+constexpr int RAW_STAGE = BN * BK / 2;        // 8 KB of e2m1 codes
+constexpr uint32_t kTmemCols = 512;           // two accumulators of BN fp32 columns
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxU = kMaxExperts;
+
+template <int FMT>
+struct Cfg {
+  static constexpr bool kFp4 = FMT != FMT_BF16;
+  static constexpr int kLoadWarps = kFp4 ? 8 : 4;
+  static constexpr int kLoadThreads = kLoadWarps * 32;
+  static constexpr int kEpiWarp0 = kLoadWarps;               // multiple of 4: TMEM lane quarter = warp % 4
+  static constexpr int kMmaWarp = kLoadWarps + kEpiWarps;
+  static constexpr int kThreads = (kMmaWarp + 1) * 32;
+  static constexpr int kNB = kFp4 ? 2 : NS;                  // bf16 B stages
+  static constexpr int kChunksA = 8 * BM / kLoadThreads;    // 16-byte chunks of A per loader thread
+  // shared memory: [A x NS][B x kNB][RAW x NS (fp4)] then barriers and tables
+  static constexpr int kOffB = NS * A_STAGE;
+  static constexpr int kOffRaw = kOffB + kNB * B_STAGE;
+  static constexpr int kOffBar = kOffRaw + (kFp4 ? NS * RAW_STAGE : 0);
+  static constexpr int kBars = 4 * NS + 4 + 1;   // full, bfull, empty, (unused), tmem_full x2, tmem_empty x2, drain
+  static constexpr int kOffTab = kOffBar + kBars * 8 + 16;
+  static constexpr int kSmem = kOffTab + 4 * (2 * (kMaxU + 1)) + 64;
+  static constexpr int kSmemAlloc = kSmem + 1024;             // room to align the base to 1024
+};
+
+struct GemmArgs {
+  const uint8_t *slot_bank;
+  long long slot_stride;
+  int H, I, k;
+  const __nv_bfloat16 *x;   // [T][H]
+  __nv_bfloat16 *h;         // [T*k][I]
+  float *y;                 // [T*k][H]
+  PlanBufs plan;
+  int only;                 // 0 all, 1 hits, 2 misses
+  long long gscale_off;     // byte offset of the NVFP4 global scales in a blob, else -1
+  int *err;                 // device error word (first failure code)
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete.  Gives up
+// after kWaitLimitNs, or as soon as the CTA's abort flag is up: returns false,
+// and on a timeout records `where` in the error word and raises the flag.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err,
+                                       int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicCAS(err, 0, where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] . B[smem]^T, both K-major bf16, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05.mma this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), descriptor version 1 (sm_100 family).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;             // LBO (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // SBO
+  d |= static_cast<uint64_t>(1) << 46;             // version
+  d |= static_cast<uint64_t>(2) << 61;             // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = f32, K-major A and B,
+// N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+// Two e2m1 codes (one byte) -> two halves.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+      : "=r"(out)
+      : "r"(byte));
+  return __half22float2(*reinterpret_cast<__half2 *>(&out));
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(out)
+      : "r"(byte & 0xFFu));
+  return __low2float(*reinterpret_cast<__half2 *>(&out));
+}
+
+__device__ __forceinline__ float e8m0_to_float(uint32_t b) {
+  if (b == 0xFFu) return __int_as_float(0x7fc00000);
+  return __uint_as_float(b ? (b << 23) : 0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Eight e2m1 codes (one 32-bit word, element 2j in the low nibble of byte j)
+// times one block scale -> eight bf16 values (exact: at most 6 significant bits).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, float s) {
+  uint4 o;
+  float2 a = e2m1x2_to_float2(w), b = e2m1x2_to_float2(w >> 8), c = e2m1x2_to_float2(w >> 16),
+         d = e2m1x2_to_float2(w >> 24);
+  o.x = pack_bf16x2(a.x * s, a.y * s);
+  o.y = pack_bf16x2(b.x * s, b.y * s);
+  o.z = pack_bf16x2(c.x * s, c.y * s);
+  o.w = pack_bf16x2(d.x * s, d.y * s);
+  return o;
+}
+
+// ------------------------------------------------------------------ tiles
+
+struct TileInfo {
+  int u, n, mt;     // distinct expert, N tile, M tile
+  int row0, rows;   // first permuted row of the tile, valid rows (<= BM)
+  int slot;
+};
+
+// Tile t -> (u, n, m): experts in order, then N tiles, then M tiles (M fastest,
+// so the CTAs that share a weight tile run side by side).
+__device__ __forceinline__ TileInfo decode_tile(int t, const int *s_start, const int *s_mt, int nU, int NTN,
+                                                const GemmArgs &a) {
+  int lo = 0, hi = nU;  // last u with s_start[u]*NTN <= t
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_start[mid] * NTN <= t) lo = mid;
+    else hi = mid;
+  }
+  TileInfo ti;
+  ti.u = lo;
+  const int mt = s_mt[lo];
+  const int rem = t - s_start[lo] * NTN;
+  ti.n = rem / mt;
+  ti.mt = rem - ti.n * mt;
+  const int e = a.plan.u_expert[lo];
+  const int off = a.plan.offsets[e], cnt = a.plan.offsets[e + 1] - off;
+  ti.row0 = off + ti.mt * BM;
+  ti.rows = min(BM, cnt - ti.mt * BM);
+  ti.slot = a.plan.u_slot[lo];
+  return ti;
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int FMT, bool DOWN>
+__global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
+    gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmB) {
+  using C = Cfg<FMT>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  unsigned char *sm = smem_raw + (base - raw_base);
+  const uint32_t sA = base, sB = base + C::kOffB, sRaw = base + C::kOffRaw;
+  const uint32_t bar0 = base + C::kOffBar;
+  auto FULL = [&](int s) { return bar0 + 8u * s; };              // A (and converted B) published
+  auto BFULL = [&](int s) { return bar0 + 8u * (NS + s); };      // B / raw B by TMA
+  auto EMPTY = [&](int s) { return bar0 + 8u * (2 * NS + s); };  // stage consumed by the MMAs
+  auto TFULL = [&](int b) { return bar0 + 8u * (4 * NS + b); };
+  auto TEMPTY = [&](int b) { return bar0 + 8u * (4 * NS + 2 + b); };
+  const uint32_t DRAIN = bar0 + 8u * (4 * NS + 4);
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + C::kOffBar + C::kBars * 8);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(sm + C::kOffBar + C::kBars * 8 + 4);
+  int *s_start = reinterpret_cast<int *>(sm + C::kOffTab);
+  int *s_mt = s_start + (kMaxU + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = DOWN ? a.I : a.H;
+  const int nk = K / BK;
+  const int NTN = DOWN ? a.H / BN : a.I / (BN / 2);
+
+  // ---- prologue: barriers, TMEM, tile table
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(FULL(s), C::kLoadThreads);
+      mbar_init(BFULL(s), 1);
+      mbar_init(EMPTY(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(TFULL(b), 1);
+      mbar_init(TEMPTY(b), kEpiWarps * 32);
+    }
+    mbar_init(DRAIN, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == C::kMmaWarp) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  const int nU = a.plan.n[0];
+  if (warp == 0) {
+    // per distinct expert: M tiles (0 when filtered out); exclusive prefix in s_start
+    int run = 0;
+    for (int u0 = 0; u0 < nU; u0 += 32) {
+      const int u = u0 + lane;
+      int mt = 0;
+      if (u < nU) {
+        const int e = a.plan.u_expert[u];
+        const int cnt = a.plan.offsets[e + 1] - a.plan.offsets[e];
+        const int hit = a.plan.u_hit[u];
+        const bool sel = a.only == 0 || (a.only == 1 && hit) || (a.only == 2 && !hit);
+        mt = sel ? (cnt + BM - 1) / BM : 0;
+        s_mt[u] = mt;
+      }
+      int x = mt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (u < nU) s_start[u] = run + x - mt;
+      run += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) s_start[nU] = run;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int n_tiles = s_start[nU] * NTN;
+
+  if (warp < C::kLoadWarps) {
+    // ================================================================ loaders
+    const int t = tid;
+    const int arow = t % BM;                 // A row loaded by this thread
+    const int achunk0 = (t / BM) * C::kChunksA;
+    // FP4: B row converted by this thread (0..255) and its scale registers
+    uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_nxt = make_uint4(0, 0, 0, 0);
+    const BlobLayout L = blob_layout(FMT, a.H, a.I);
+    int j = 0;  // stage counter across tiles
+    bool ok = true;
+    auto finish = [&](int jj) -> bool {
+      // publish stage jj (issued LAG stages ago): A rows landed; FP4: dequantise B
+      const int s = jj % NS;
+      if constexpr (C::kFp4) {
+        if (!mbar_wait(BFULL(s), (jj / NS) & 1, s_abort, a.err, 11)) return false;
+        const uint32_t raw = sRaw + s * RAW_STAGE + t * 32;
+        uint4 q0, q1;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(q0.x), "=r"(q0.y), "=r"(q0.z), "=r"(q0.w)
+                     : "r"(raw));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(q1.x), "=r"(q1.y), "=r"(q1.z), "=r"(q1.w)
+                     : "r"(raw + 16));
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        // scales of this stage: NVFP4 4 bytes (one per 16), MXFP4 2 bytes (one per 32)
+        const int sub = jj & 3;
+        float sc[4];
+        if constexpr (FMT == FMT_NVFP4) {
+          const uint32_t word = sub == 0 ? sc_cur.x : sub == 1 ? sc_cur.y : sub == 2 ? sc_cur.z : sc_cur.w;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[i] = e4m3_to_float((word >> (8 * i)) & 0xFFu);
+        } else {
+          const uint32_t word = (sub >> 1) == 0 ? sc_cur.x : sc_cur.y;
+          const uint32_t pair = (word >> (16 * (sub & 1))) & 0xFFFFu;
+          sc[0] = sc[1] = e8m0_to_float(pair & 0xFFu);
+          sc[2] = sc[3] = e8m0_to_float(pair >> 8);
+        }
+        const uint32_t bdst = sB + (jj % C::kNB) * B_STAGE + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = dequant8(w[c], sc[c >> 1]);
+          const uint32_t d = bdst + ((c ^ (t & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v.x), "r"(v.y), "r"(v.z),
+                       "r"(v.w)
+                       : "memory");
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(FULL(s));
+      return true;
+    };
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
+      // this thread's A source row (rows past the group repeat its last row;
+      // their results are never stored)
+      const int r = ti.row0 + min(arow, ti.rows - 1);
+      const __nv_bfloat16 *asrc;
+      if constexpr (DOWN) asrc = a.h + (size_t)r * a.I;
+      else asrc = a.x + (size_t)(a.plan.perm[r] / a.k) * a.H;
+      const uint8_t *blob = a.slot_bank + (size_t)ti.slot * a.slot_stride;
+      // FP4: this thread's B row inside the blob (gate/up: 128 gate rows then 128 up rows)
+      int brow = 0;
+      const uint8_t *sf_row = nullptr;
+      if constexpr (C::kFp4) {
+        brow = DOWN ? ti.n * BN + t : (t < BN / 2 ? ti.n * (BN / 2) + t : a.I + ti.n * (BN / 2) + (t - BN / 2));
+        const int sf_per_row = K / (FMT == FMT_NVFP4 ? 16 : 32);
+        sf_row = blob + (DOWN ? L.d_sf : L.gu_sf) + (size_t)brow * sf_per_row;
+      }
+      for (int kb = 0; kb < nk; ++kb, ++j) {
+        const int s = j % NS;
+        if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 10)) { ok = false; break; }
+        if (t == 0) {
+          if constexpr (C::kFp4) {
+            mbar_arrive_expect_tx(BFULL(s), RAW_STAGE);
+            const uint32_t dst = sRaw + s * RAW_STAGE;
+            if (DOWN) {
+              tma_load_3d(dst, &tmB, BFULL(s), kb * (BK / 2), ti.n * BN, ti.slot);
+              tma_load_3d(dst + RAW_STAGE / 2, &tmB, BFULL(s), kb * (BK / 2), ti.n * BN + BN / 2, ti.slot);
+            } else {
+              tma_load_3d(dst, &tmB, BFULL(s), kb * (BK / 2), ti.n * (BN / 2), ti.slot);
+              tma_load_3d(dst + RAW_STAGE / 2, &tmB, BFULL(s), kb * (BK / 2), a.I + ti.n * (BN / 2), ti.slot);
+            }
+          } else {
+            mbar_arrive_expect_tx(BFULL(s), B_STAGE);
+            const uint32_t dst = sB + s * B_STAGE;
+            if (DOWN) {
+              tma_load_3d(dst, &tmB, BFULL(s), kb * BK, ti.n * BN, ti.slot);
+              tma_load_3d(dst + B_STAGE / 2, &tmB, BFULL(s), kb * BK, ti.n * BN + BN / 2, ti.slot);
+            } else {
+              tma_load_3d(dst, &tmB, BFULL(s), kb * BK, ti.n * (BN / 2), ti.slot);
+              tma_load_3d(dst + B_STAGE / 2, &tmB, BFULL(s), kb * BK, a.I + ti.n * (BN / 2), ti.slot);
+            }
+          }
+        }
+        // A: this thread's chunks of its row, swizzled (chunk c of row r at c ^ (r & 7))
+        const uint32_t adst = sA + s * A_STAGE + arow * 128;
+        const char *src = reinterpret_cast<const char *>(asrc + (size_t)kb * BK);
+#pragma unroll
+        for (int c = 0; c < C::kChunksA; ++c) {
+          const int cc = achunk0 + c;
+          cp_async16(adst + ((cc ^ (arow & 7)) << 4), src + cc * 16);
+        }
+        cp_async_commit();
+        if constexpr (C::kFp4) {
+          // scales for the 4 stages kb..kb+3 (NVFP4: 16 bytes, MXFP4: 8 bytes), one group ahead
+          if ((kb & 3) == 0) {
+            const int per = FMT == FMT_NVFP4 ? 4 : 2;   // scale bytes per stage
+            if (FMT == FMT_NVFP4) sc_nxt = __ldg(reinterpret_cast<const uint4 *>(sf_row + kb * per));
+            else {
+              const uint2 v = __ldg(reinterpret_cast<const uint2 *>(sf_row + kb * per));
+              sc_nxt = make_uint4(v.x, v.y, 0, 0);
+            }
+          }
+        }
+        if (j >= LAG) {
+          cp_async_wait<LAG>();
+          if constexpr (C::kFp4) {
+            if (((j - LAG) & 3) == 0) sc_cur = sc_nxt;
+          }
+          if (!finish(j - LAG)) { ok = false; ++j; break; }   // stage j was issued
+        }
+      }
+    }
+    // publish the last LAG stages
+    cp_async_wait<0>();
+    if (ok) {
+      for (int jj = max(0, j - LAG); jj < j; ++jj) {
+        if constexpr (C::kFp4) {
+          if ((jj & 3) == 0) sc_cur = sc_nxt;
+          // B stage jj % 2 was last read by stage jj - 2: in the main loop the
+          // EMPTY wait of the stage issued alongside covers that; here, wait for it
+          const int p = jj - 2;
+          if (p >= 0 && !mbar_wait(EMPTY(p % NS), (p / NS) & 1, s_abort, a.err, 12)) break;
+        }
+        if (!finish(jj)) break;
+      }
+    }
+    // drain: every TMA this CTA issued must land before the CTA exits
+    if (t == 0) {
+      for (int jj = max(0, j - NS); jj < j; ++jj) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(BFULL(jj % NS), (jj / NS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      int j = 0, tl = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tl) {
+        const int b = tl & 1;
+        if (!mbar_wait(TEMPTY(b), ((tl >> 1) & 1) ^ 1, s_abort, a.err, 20)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + b * BN;
+        for (int kb = 0; kb < nk; ++kb, ++j) {
+          const int s = j % NS;
+          if (!mbar_wait(FULL(s), (j / NS) & 1, s_abort, a.err, 21) ||
+              (!C::kFp4 && !mbar_wait(BFULL(s), (j / NS) & 1, s_abort, a.err, 22))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sA + s * A_STAGE, b0 = sB + (j % C::kNB) * B_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), kIdesc, (kb | kk) != 0);
+          mma_commit(EMPTY(s));
+        }
+        if (ok) mma_commit(TFULL(b));
+      }
+      // every MMA issued must complete before TMEM is freed
+      mma_commit(DRAIN);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(DRAIN, 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + kEpiWarps) {
+    // ================================================================ epilogue
+    const int q = warp & 3;            // TMEM lane quarter
+    const int row = q * 32 + lane;     // tile row of this thread
+    int tl = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
+      if (!mbar_wait(TFULL(b), (tl >> 1) & 1, s_abort, a.err, 30)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+      float g0 = 1.0f, g1 = 1.0f;
+      if (a.gscale_off >= 0) {
+        const float *gs = reinterpret_cast<const float *>(a.slot_bank + (size_t)ti.slot * a.slot_stride +
+                                                         a.gscale_off);
+        g0 = DOWN ? gs[2] : gs[0];
+        g1 = gs[1];
+      }
+      const bool valid = row < ti.rows;
+      if constexpr (!DOWN) {
+        __nv_bfloat16 *dst = a.h + (size_t)(ti.row0 + row) * a.I + ti.n * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 16) {
+          float gv[16], uv[16];
+          tmem_ld16(tb + c, gv);
+          tmem_ld16(tb + BN / 2 + c, uv);
+          if (valid) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float h2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float g = gv[2 * i + e] * g0, u = uv[2 * i + e] * g1;
+                h2[e] = g / (1.0f + expf(-g)) * u;
+              }
+              pk[i] = pack_bf16x2(h2[0], h2[1]);
+            }
+            uint4 *o = reinterpret_cast<uint4 *>(dst + c);
+            o[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            o[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else {
+        float *dst = a.y + (size_t)(ti.row0 + row) * a.H + ti.n * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tb + c, v);
+          if (valid) {
+            float4 *o = reinterpret_cast<float4 *>(dst + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(TEMPTY(b));
+    }
+  }
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+template <int FMT, bool DOWN>
+void set_attr() {
+  cudaFuncSetAttribute(gemm_kernel<FMT, DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<FMT>::kSmemAlloc);
+}
+
+template <int FMT, bool DOWN>
+cudaError_t launch(const GemmArgs &a, const CUtensorMap &map, int grid, cudaStream_t s) {
+  gemm_kernel<FMT, DOWN><<<grid, Cfg<FMT>::kThreads, Cfg<FMT>::kSmemAlloc, s>>>(a, map);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+static_assert(Cfg<FMT_BF16>::kSmemAlloc <= 227 * 1024, "bf16 smem");
+static_assert(Cfg<FMT_NVFP4>::kSmemAlloc <= 227 * 1024, "fp4 smem");
+
+int tc_num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+void gemm_init_attributes() {
+  set_attr<FMT_BF16, false>();
+  set_attr<FMT_BF16, true>();
+  set_attr<FMT_NVFP4, false>();
+  set_attr<FMT_NVFP4, true>();
+  set_attr<FMT_MXFP4, false>();
+  set_attr<FMT_MXFP4, true>();
+}
+
+// Tensor maps over the slot bank: 3-D (K, rows, slot).  BF16: box 64 x 128
+// elements with the 128-byte swizzle.  FP4: raw code bytes, box 32 x 128.
+int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, int H, int I, void *map_gu,
+                     void *map_d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return -1;
+  const BlobLayout L = blob_layout(fmt, H, I);
+  for (int which = 0; which < 2; ++which) {
+    const bool down = which == 1;
+    const int64_t K = down ? I : H, rows = down ? H : 2 * I;
+    CUtensorMap *m = reinterpret_cast<CUtensorMap *>(down ? map_d : map_gu);
+    void *gaddr = const_cast<uint8_t *>(slots) + (down ? L.d_codes : L.gu_codes);
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    CUtensorMapDataType dt;
+    CUtensorMapSwizzle sw;
+    if (fmt == FMT_BF16) {
+      dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      dims[0] = K; strides[0] = K * 2;
+      box[0] = BK;
+      sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    } else {
+      dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+      dims[0] = K / 2; strides[0] = K / 2;
+      box[0] = BK / 2;
+      sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+    }
+    dims[1] = rows; dims[2] = S;
+    strides[1] = slot_stride;
+    box[1] = BN / 2; box[2] = 1;
+    CUresult r = enc(m, dt, 3, gaddr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return (int)r;
+  }
+  return 0;
+}
+
+// Grouped gate/up (down=false) or down (down=true) FFN of the call's experts on
+// the tensor cores.  `max_tiles` bounds the CTAs launched.
+cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_gu, const void *map_d, int *err,
+                          int64_t max_rows, cudaStream_t s) {
+  GemmArgs a{};
+  a.slot_bank = f.slot_bank;
+  a.slot_stride = f.slot_stride;
+  a.H = f.H; a.I = f.I; a.k = f.k;
+  a.x = f.x; a.h = f.h; a.y = f.y;
+  a.plan = f.plan;
+  a.only = f.only;
+  a.gscale_off = f.fmt == FMT_NVFP4 ? blob_layout(FMT_NVFP4, f.H, f.I).gscale : -1;
+  a.err = err;
+  const int NTN = down ? f.H / BN : f.I / (BN / 2);
+  // M tiles <= ceil(rows / BM) + distinct experts
+  const int64_t mtiles = (max_rows + BM - 1) / BM + f.umax;
+  const int grid = (int)std::min<int64_t>(tc_num_sms(), std::max<int64_t>(1, mtiles * NTN));
+  const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(down ? map_d : map_gu);
+  switch (f.fmt) {
+    case FMT_BF16: return down ? launch<FMT_BF16, true>(a, m, grid, s) : launch<FMT_BF16, false>(a, m, grid, s);
+    case FMT_NVFP4: return down ? launch<FMT_NVFP4, true>(a, m, grid, s) : launch<FMT_NVFP4, false>(a, m, grid, s);
+    default: return down ? launch<FMT_MXFP4, true>(a, m, grid, s) : launch<FMT_MXFP4, false>(a, m, grid, s);
+  }
+}
+
+}  // namespace ftmoe

@@ -198,6 +198,25 @@ enum ft_prof_class {
 int ft_moe_set_profiling(ft_moe *h, int enable);
 int ft_moe_profile_read(ft_moe *h, double *ms, int64_t *launches, int n);
 
+/* Which kernel computes the expert FFN (gate/up + SiLU*mul, then down). */
+enum ft_ffn_kernel {
+  FT_FFN_AUTO = 0, /* tensor cores when the call's distinct experts average >= 64 token rows each */
+  FT_FFN_GEMV = 1, /* dequant-fused CUDA-core GEMV: streams each weight once per 8 tokens (decode) */
+  FT_FFN_TC = 2    /* tcgen05 grouped GEMM: TMA-fed weight tiles, TMEM accumulators (prefill) */
+};
+
+/* Selects the FFN kernel for later forward calls (default FT_FFN_AUTO).  Both
+ * compute the same function with fp32 accumulation; they differ in the order
+ * of the K-dimension sums only.  FT_FFN_TC: 128-row token tiles times 256
+ * weight rows; FP4 weights are dequantised exactly to bf16 in shared memory.
+ * Errors: FT_ERR_ARG; FT_ERR_CUDA when the TMA descriptors of the slot bank
+ * could not be encoded at create time (then only the GEMV is available). */
+int ft_moe_set_ffn_kernel(ft_moe *h, int which);
+
+/* The FFN kernel the last forward call used: FT_FFN_GEMV or FT_FFN_TC
+ * (-1 for NULL). */
+int ft_moe_last_ffn_kernel(const ft_moe *h);
+
 /* Bytes between consecutive slots in the device slot bank. */
 int64_t ft_moe_slot_stride(const ft_moe *h);
 

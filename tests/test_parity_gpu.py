@@ -183,6 +183,98 @@ def test_unit_global_scale_nvfp4():
     gpu.close()
 
 
+# ------------------------------------------------------------ tensor-core FFN
+
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("H,I,E,k,T", [(256, 256, 8, 2, 300), (512, 768, 4, 2, 333), (1024, 512, 16, 4, 97)])
+def test_tc_ffn_matches_oracle(fmt, H, I, E, k, T):
+    # several M tiles per expert with ragged tails, several N tiles, K of 4..16 stages
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, fmt, E, 1, T, 61 + H + T)
+    gpu.set_ffn_kernel("tc")
+    x, lg = Hn.inputs(61, T, H, E, 0, 0)
+    _check_call(gpu, orc, 0, x, lg, gemm_check=True)
+    assert gpu.last_ffn_kernel == "tc"
+    gpu.close()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4", "mxfp4"])
+def test_tc_and_gemv_agree(fmt):
+    # the two kernels differ only in the order of the K sums
+    H, I, E, k, T = 512, 512, 8, 2, 200
+    gpu, _, _ = Hn.make_pair(H, E, k, I, fmt, E, 1, T, 71)
+    x, lg = Hn.inputs(71, T, H, E, 0, 0)
+    xd, lgd = Hn.to_dev(x, lg)
+    outs, acts = [], []
+    for which in ("gemv", "tc"):
+        gpu.set_ffn_kernel(which)
+        outs.append(Hn.out_to_f64(gpu.forward(0, xd, lgd)))
+        acts.append(gpu.last_activations(T))
+        assert gpu.last_ffn_kernel == which
+    assert Hn.rel_err(outs[1], outs[0]) <= 1e-2
+    h0, h1 = (O.bf16_bits_to_f64(a[0]) for a in acts)
+    assert Hn.rel_err(h1, h0) <= 1e-2
+    assert Hn.rel_err(acts[1][1].astype(np.float64), acts[0][1].astype(np.float64)) <= 1e-2
+    gpu.close()
+
+
+def test_tc_ffn_unit_global_scale_and_lru_misses():
+    # NVFP4 with g = 1 (subnormal E4M3 block scales); misses copied mid-call,
+    # so the hit and miss halves of the gate/up run as separate launches
+    H, I, E, k, T, L = 256, 256, 8, 2, 200, 3
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, L, T, 81, flags=ftgen.FLAG_NVFP4_UNIT_GSCALE)
+    gpu.set_ffn_kernel("tc")
+    for step in range(2):
+        for layer in range(L):
+            x, lg = Hn.inputs(81, T, H, E, step, layer, zipf=0.5)
+            _check_call(gpu, orc, layer, x, lg, gemm_check=(layer == 1))
+    cum, _ = gpu.stats()
+    assert cum["misses"] > 0 and cum["misses"] == orc.stats["misses"]
+    gpu.close()
+
+
+def test_tc_stream_mode_matches_oracle():
+    H, I, E, k, L, T = 256, 512, 8, 2, 4, 300
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "mxfp4", 2 * E, L, T, 91, mode="stream")
+    gpu.set_ffn_kernel("tc")
+    for layer in range(L):
+        x, lg = Hn.inputs(91, T, H, E, 0, layer, zipf=0.8)
+        _check_call(gpu, orc, layer, x, lg)
+    gpu.close()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
+def test_prefill35b_full_size_sampled(fmt):
+    # the prefill layer at full size (4096 tokens, H 2048, 128 experts, top-8,
+    # I 768); FFN kernel chosen automatically; the oracle checks 64 sampled tokens
+    c = CONFIGS["prefill35b"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, fmt, c["S"], 1, T, c["seed"])
+    x, lg = Hn.inputs(c["seed"], T, H, E, 0, 0)
+    tokens = list(range(0, T, 64))
+    _check_call(gpu, orc, 0, x, lg, tokens=tokens)
+    assert gpu.last_ffn_kernel == "tc"
+    # GEMM accumulation of the down projection on sampled rows
+    hb, y = gpu.last_activations(T)
+    hf = O.bf16_bits_to_f64(hb)
+    r = gpu.last_routing()
+    for e in (0, 57, 127):
+        lo, hi = int(r["offsets"][e]), int(r["offsets"][e + 1])
+        _, _, Wd = orc.weights(e)
+        assert Hn.rel_err(y[lo:hi].astype(np.float64), hf[lo:hi] @ Wd.T) <= GEMM_TOL
+    gpu.close()
+
+
+def test_auto_picks_gemv_for_decode():
+    H, I, E, k = 256, 256, 16, 4
+    gpu, _, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, 1, 64, 3)
+    for T, want in ((1, "gemv"), (8, "gemv"), (64, "gemv")):
+        x, lg = Hn.inputs(3, T, H, E, 0, 0)
+        xd, lgd = Hn.to_dev(x, lg)
+        gpu.forward(0, xd, lgd)
+        assert gpu.last_ffn_kernel == want
+    gpu.close()
+
+
 # ------------------------------------------------------------ failure paths
 
 def test_wait_timeout_is_reported_and_reset_recovers(monkeypatch):
