@@ -145,30 +145,44 @@ def _gen_inputs(cfg, seed, n_steps):
 
 class _OracleRunner:
     """The CPU oracle over the workload's calls, in order (step-major, then
-    layer).  Blobs are generated before any call is timed."""
+    layer).  Blobs are generated before any call is timed.  Prefill workloads
+    (one chunk per step) reuse the step-0 inputs, as the GPU bench does."""
 
-    def __init__(self, cfg, seed, n_phys, max_calls):
+    def __init__(self, cfg, seed, n_phys, max_calls, fmt=None):
         import oracle as O
         self.cfg, self.seed = cfg, seed
+        self.fmt = fmt or cfg["fmt"]
+        self.prefill = cfg["steps"] == 1
         H, E, k, I, L = cfg["H"], cfg["E"], cfg["k"], cfg["I"], cfg["L"]
+        # sampled token rows per call: every token of a decode call; for a
+        # prefill chunk a strided sample, smaller for the large expert shapes
+        # (the oracle dequantises every expert a sampled token touches)
+        self.n_sample = 256 if H * I <= 2048 * 768 else 4
         self.calls = []
         step = 0
         while len(self.calls) < max_calls:
             for l in range(L):
                 if len(self.calls) < max_calls:
-                    self.calls.append((step, l, tokens_at(cfg, step)))
+                    self.calls.append((0 if self.prefill else step, l, tokens_at(cfg, step)))
             step += 1
         need = set()
         for step, l, T in self.calls:
             lg = ftgen.router_logits(seed, T, E, step, l, cfg["zipf"], epoch_at(cfg, step))
-            need |= {(l * E + int(e)) % n_phys for e in O.topk_experts(lg, k).reshape(-1)}
+            idx = O.topk_experts(lg, k)
+            rows = self._sample(T)
+            if rows is not None:
+                idx = idx[rows]
+            need |= {(l * E + int(e)) % n_phys for e in idx.reshape(-1)}
         need = sorted(need)
-        blobs = ftgen.pool(cfg["fmt"], H, I, need, seed)
+        blobs = ftgen.pool(self.fmt, H, I, need, seed)
         self.blobs = {p: blobs[i] for i, p in enumerate(need)}
-        self.orc = O.MoELayerOracle(H, E, k, I, ftgen.FMT_NAMES[cfg["fmt"]], cfg["S"], L,
+        self.orc = O.MoELayerOracle(H, E, k, I, ftgen.FMT_NAMES[self.fmt], cfg["S"], L,
                                     lambda key: self.blobs[key % n_phys],
                                     mode=O.MODE_STREAM if cfg["mode"] == "stream" else O.MODE_LRU)
         self.pos = 0
+
+    def _sample(self, T):
+        return None if T <= 64 else list(range(0, T, max(1, T // self.n_sample)))[: self.n_sample]
 
     def next_call(self, one_expert=False):
         """Runs the next call; returns (seconds, token rows, distinct experts).
@@ -180,7 +194,7 @@ class _OracleRunner:
         self.pos += 1
         x = ftgen.x_bf16(self.seed, T, cfg["H"], step, l)
         lg = ftgen.router_logits(self.seed, T, cfg["E"], step, l, cfg["zipf"], epoch_at(cfg, step))
-        sample = None if T <= 64 else list(range(0, T, max(1, T // 256)))
+        sample = self._sample(T)
         experts = sorted(set(int(e) for e in O.topk_experts(lg, cfg["k"]).reshape(-1)))
         sub = [experts[self.pos % len(experts)]] if one_expert else None
         t0 = time.perf_counter()
@@ -197,11 +211,13 @@ def _single_thread():
         return contextlib.nullcontext()
 
 
-def _cpu_baseline(cfg, seed, n_phys, budget_s=15.0, max_calls=192):
+def _cpu_baseline(cfg, seed, n_phys, budget_s=15.0, max_calls=192, fmt=None):
     """Times the CPU oracle, as it stands, single-threaded, on the workload's
     first layer calls until `budget_s` seconds of oracle time.
     Returns (tokens/s through the L-layer stack, description, calls, seconds)."""
-    run = _OracleRunner(cfg, seed, n_phys, max_calls)
+    if cfg["steps"] == 1:
+        max_calls = min(max_calls, 2)
+    run = _OracleRunner(cfg, seed, n_phys, max_calls, fmt)
     calls, rows, used = 0, 0, 0.0
     with _single_thread():
         while used < budget_s and run.pos < len(run.calls):
@@ -210,8 +226,9 @@ def _cpu_baseline(cfg, seed, n_phys, budget_s=15.0, max_calls=192):
             rows += r
             calls += 1
     L = cfg["L"]
-    desc = (f"oracle on the first {calls} layer calls of {cfg['name']} in order ({rows} token rows, "
-            f"FFN included), float64 numpy, 1 thread; tokens/s = rows / {L} layers / seconds")
+    desc = (f"oracle on the first {calls} layer calls of {cfg['name']} in order ({rows} token rows"
+            f"{' sampled from each chunk' if cfg['steps'] == 1 else ''}, routing of every token, FFN of the "
+            f"sampled rows), float64 numpy, 1 thread; tokens/s = rows / {L} layers / seconds")
     return rows / L / used, desc, calls, used
 
 
@@ -245,6 +262,16 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def _ffn_bytes(fmt, H, I):
+    """Weight bytes of one expert's gate/up and down matrices."""
+    HI = H * I
+    if fmt == "nvfp4":
+        return 2 * HI // 2 + 2 * HI // 16, HI // 2 + HI // 16
+    if fmt == "mxfp4":
+        return 2 * HI // 2 + 2 * HI // 32, HI // 2 + HI // 32
+    return 4 * HI, 2 * HI
+
+
 def run_ours(args, cfg):
     import torch
     import expert_cache_host_softmax_b300 as F
@@ -259,23 +286,34 @@ def run_ours(args, cfg):
     peaks = _peaks()
     seed = cfg["seed"] + rank
     T, H, E, k, I, L, S = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["I"], cfg["L"], cfg["S"]
-    nb = ftgen.blob_bytes(cfg["fmt"], H, I)
+    fmt = args.fmt or cfg["fmt"]
+    # prefill workloads: one chunk through the stack per step, same inputs each
+    # step; with resident experts, L2 is flushed before every timed step (the
+    # streaming workload copies every expert from host memory each step, and
+    # is timed as one window so that the copy of the next step's first layer,
+    # which overlaps the last layer, stays inside it); decode: fresh inputs per step
+    reuse_inputs = cfg["steps"] == 1
+    prefill = reuse_inputs and cfg["mode"] != "stream"
+    nb = ftgen.blob_bytes(fmt, H, I)
     n_keys = L * E
     n_phys = min(args.n_phys, n_keys)
 
     # pinned host pool: n_phys distinct blobs, logical key -> key % n_phys
     pool = torch.empty(n_phys * nb, dtype=torch.uint8, pin_memory=True)
-    ftgen.pool(cfg["fmt"], H, I, list(range(n_phys)), seed, out=pool.numpy().reshape(n_phys, nb))
+    ftgen.pool(fmt, H, I, list(range(n_phys)), seed, out=pool.numpy().reshape(n_phys, nb))
     ptrs = [pool.data_ptr() + (key % n_phys) * nb for key in range(n_keys)]
-    stack = F.MoELayerStack(H, E, k, I, cfg["fmt"], S, L, T)
+    stack = F.MoELayerStack(H, E, k, I, fmt, S, L, T)
     stack.load_pool(ptrs, keepalive=pool)
     if cfg["mode"] == "stream":
         stack.set_mode(F.FT_MODE_STREAM)
+    if args.ffn != "auto":
+        stack.set_ffn_kernel(args.ffn)
 
     W, K = args.warmup, args.steps
     n_prof = min(args.profile_steps, K)
     n_steps = W + K
-    X, G = _gen_inputs(cfg, seed, n_steps)
+    n_in = 1 if reuse_inputs else n_steps
+    X, G = _gen_inputs(cfg, seed, n_in)
     Xd = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).to(dev)
     Gd = torch.from_numpy(G).to(dev)
     outd = torch.empty((L, T, H), dtype=torch.bfloat16, device=dev)
@@ -285,12 +323,14 @@ def run_ours(args, cfg):
     h = stack._h
     x_ptr0, g_ptr0, o_ptr0 = Xd.data_ptr(), Gd.data_ptr(), outd.data_ptr()
     xs, gs, os_ = T * H * 2, T * E * 4, T * H * 2
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if prefill else None
 
     def step(s, xb=None, gb=None):
         t = tokens_at(cfg, s)
+        si = 0 if reuse_inputs else s
         for l in range(L):
-            xo = (xb + l * xs) if xb is not None else x_ptr0 + (s * L + l) * xs
-            go = (gb + l * gs) if gb is not None else g_ptr0 + (s * L + l) * gs
+            xo = (xb + l * xs) if xb is not None else x_ptr0 + (si * L + l) * xs
+            go = (gb + l * gs) if gb is not None else g_ptr0 + (si * L + l) * gs
             rc = Lb.ft_moe_forward(h, l, t, xo, go, o_ptr0 + l * os_, sp)
             if rc != 0:
                 raise F.FtError(rc, Lb.ft_last_error(h).decode())
@@ -300,8 +340,37 @@ def run_ours(args, cfg):
             import torch.distributed as dist
             dist.barrier()
 
+    def flush_l2():
+        # write a buffer twice the size of L2 on the bench stream, outside the timed events
+        with torch.cuda.stream(stream):
+            flush_buf.zero_()
+
+    def timed_steps(steps, body):
+        """Device time (ms) of `body(s)` over `steps`: one event pair around all
+        of them (decode), or per step after an L2 flush (prefill)."""
+        if not prefill:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for s in steps:
+                body(s)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1)
+        total = 0.0
+        for s in steps:
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            body(s)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            total += e0.elapsed_time(e1)
+        return total
+
     with torch.cuda.stream(stream):
         for s in range(W):
+            if prefill:
+                flush_l2()
             step(s)
     torch.cuda.synchronize(dev)
     pcie_gbs = _pcie_h2d_gbs(torch, dev, pool)
@@ -314,17 +383,11 @@ def run_ours(args, cfg):
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
-    e0.record(stream)
-    for s in range(W, W + K):
-        step(s)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    ms = timed_steps(range(W, W + K), step)
     wall = time.perf_counter() - wall0
     barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
     cum1, _ = stack.stats()
     launches = stack.kernel_launches - launches0
     d = {key_: cum1[key_] - cum0[key_] for key_ in cum1}
@@ -346,17 +409,16 @@ def run_ours(args, cfg):
     gin = torch.empty((L, T, E), dtype=torch.float32, device=dev)
     barrier()
     torch.cuda.synchronize(dev)
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step(s):
+        si = 0 if reuse_inputs else s
+        xin.copy_(Xh[si], non_blocking=True)
+        gin.copy_(Gh[si], non_blocking=True)
+        step(s, xin.data_ptr(), gin.data_ptr())
+        outh.copy_(outd, non_blocking=True)
+
     with torch.cuda.stream(stream):
-        f0.record(stream)
-        for s in range(W, W + K):
-            xin.copy_(Xh[s], non_blocking=True)
-            gin.copy_(Gh[s], non_blocking=True)
-            step(s, xin.data_ptr(), gin.data_ptr())
-            outh.copy_(outd, non_blocking=True)
-        f1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = f0.elapsed_time(f1)
+        e2e_ms = timed_steps(range(W, W + K), e2e_step)
     if ws > 1:
         import torch.distributed as dist
         tt = torch.tensor([e2e_ms], device=dev)
@@ -369,68 +431,83 @@ def run_ours(args, cfg):
     c0, _ = stack.stats()
     with torch.cuda.stream(stream):
         for s in range(W, W + n_prof):
+            if prefill:
+                flush_l2()
             step(s)
     torch.cuda.synchronize(dev)
     prof = stack.profile()
     c1, _ = stack.stats()
     stack.set_profiling(False)
+    ffn_kernel = stack.last_ffn_kernel
     pd = {key_: c1[key_] - c0[key_] for key_ in c1}
 
-    # algorithmic bytes of the FFN kernels (weights of each distinct expert once
-    # per call, plus activations)
-    HI = H * I
-    if cfg["fmt"] == "nvfp4":
-        gu_bytes, d_bytes = 2 * HI // 2 + 2 * HI // 16, HI // 2 + HI // 16
-    elif cfg["fmt"] == "mxfp4":
-        gu_bytes, d_bytes = 2 * HI // 2 + 2 * HI // 32, HI // 2 + HI // 32
-    else:
-        gu_bytes, d_bytes = 4 * HI, 2 * HI
+    # algorithmic bytes and FLOPs of the FFN kernels: each distinct expert's
+    # weights once per call, plus activations; FLOPs 2 per multiply-add
+    gu_bytes, d_bytes = _ffn_bytes(fmt, H, I)
     calls_p = n_prof * L
-    toks_p = sum(tokens_at(cfg, s) for s in range(W, W + n_prof))
+    toks_p = sum(tokens_at(cfg, s) for s in range(W, W + n_prof)) * L
     act_gu = toks_p * k * (H * 2 + I * 2)          # x rows read per (token, expert) + h written
     act_dn = toks_p * k * (I * 2 + H * 4)          # h read + y written
+    fl_gu, fl_dn = 2 * toks_p * k * 2 * I * H, 2 * toks_p * k * H * I
     kern = {
-        "gateup": (pd["lookups"] * gu_bytes + act_gu, prof["gateup_hit"][0] + prof["gateup_miss"][0],
-                   prof["gateup_hit"][1] + prof["gateup_miss"][1]),
-        "down": (pd["lookups"] * d_bytes + act_dn, prof["down"][0], prof["down"][1]),
-        "route": (toks_p * E * 4, prof["route"][0], prof["route"][1]),
-        "combine": (toks_p * (k * H * 4 + H * 2), prof["combine"][0], prof["combine"][1]),
+        "gateup": (pd["lookups"] * gu_bytes + act_gu, prof["gateup_hit"][0] + prof["gateup_miss"][0], fl_gu),
+        "down": (pd["lookups"] * d_bytes + act_dn, prof["down"][0], fl_dn),
+        "route": (toks_p * E * 4, prof["route"][0], 0),
+        "combine": (toks_p * (k * H * 4 + H * 2), prof["combine"][0], 0),
     }
     dom = max(kern, key=lambda n: kern[n][1])
-    b_dom, ms_dom, n_dom = kern[dom]
-    achieved = b_dom / (ms_dom * 1e-3) / 1e9 if ms_dom > 0 else 0.0
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_src": peaks["src"],
-                "bytes_per_call": b_dom / calls_p, "ms_per_call": ms_dom / calls_p,
-                "kernel_ms_share": {n: round(kern[n][1] / max(1e-9, sum(v[1] for v in kern.values())), 4)
-                                    for n in kern}}
+    b_dom, ms_dom, f_dom = kern[dom]
+    share = {n: round(kern[n][1] / max(1e-9, sum(v[1] for v in kern.values())), 4) for n in kern}
+    if ffn_kernel == "tc" and f_dom > 0:
+        achieved = f_dom / (ms_dom * 1e-3) / 1e12 if ms_dom > 0 else 0.0
+        roofline = {"bound": "tensor", "kernel": f"{dom} (tcgen05 grouped GEMM, bf16 operands)", "achieved": achieved,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                    "traffic": None, "peak_src": peaks["src"] + " bf16 burst",
+                    "flops_per_call": f_dom / calls_p, "ms_per_call": ms_dom / calls_p,
+                    "hbm_gbs_achieved": b_dom / (ms_dom * 1e-3) / 1e9 if ms_dom > 0 else 0.0,
+                    "kernel_ms_share": share}
+    else:
+        achieved = b_dom / (ms_dom * 1e-3) / 1e9 if ms_dom > 0 else 0.0
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_src": peaks["src"],
+                    "bytes_per_call": b_dom / calls_p, "ms_per_call": ms_dom / calls_p, "kernel_ms_share": share}
     copy_ms = prof["miss_copy"][0]
     copy_gbs = pd["misses"] * nb / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None
+    stream_ms = prof["stream_copy"][0]
+    stream_gbs = pd["streamed"] * nb / (stream_ms * 1e-3) / 1e9 if stream_ms > 0 else None
 
-    # ---- path roofline: the slowest of HBM weight bytes, PCIe miss bytes, FLOPs
+    # ---- path roofline: the slowest of HBM weight bytes, PCIe expert bytes, FLOPs
     t_step = ms_max * 1e-3 / K
     w_hbm = d["lookups"] * nb / K
-    m_pcie = d["misses"] * nb / K
-    flops = 2 * 3 * HI * k * tokens / K * L
+    m_pcie = (d["misses"] + d["streamed"]) * nb / K
+    flops = 2 * 3 * H * I * k * tokens / K * L
     t_hbm = w_hbm / (peaks["hbm_gbs"] * 1e9)
     t_pcie = m_pcie / (pcie_gbs * 1e9)
-    t_flop = flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_flop = flops / (peaks["bf16_tflops"] * 1e12)
     t_roof = max(t_hbm, t_pcie, t_flop)
     path = {"t_step_ms": t_step * 1e3, "t_roof_ms": t_roof * 1e3, "frac": t_roof / t_step,
             "bound": ("hbm", "pcie", "tensor")[int(np.argmax([t_hbm, t_pcie, t_flop]))],
             "hbm_bytes_per_step": w_hbm, "pcie_bytes_per_step": m_pcie, "flops_per_step": flops,
+            "tensor_peak": "bf16 burst (measured)", "ffn_kernel": ffn_kernel,
             "pcie_h2d_gbs_measured": pcie_gbs, "miss_copy_gbs_achieved": copy_gbs,
+            "stream_copy_gbs_achieved": stream_gbs,
             "hits_per_step": d["hits"] / K, "misses_per_step": d["misses"] / K,
-            "hit_rate": d["hits"] / max(1, d["lookups"])}
+            "streamed_per_step": d["streamed"] / K, "hit_rate": d["hits"] / max(1, d["lookups"])}
 
+    if prefill:
+        l2 = f"L2 flushed (256 MiB write) before each timed step; weights {E * nb / 1e9:.2f} GB per layer"
+    elif cfg["mode"] == "stream":
+        l2 = f"every expert streamed from pinned host memory each step ({L * E * nb / 1e9:.1f} GB per step)"
+    else:
+        l2 = f"working set > L2: {S} slots x {nb} B = {S * nb / 1e9:.2f} GB slot bank"
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4-w/bf16-act/f32-acc" if cfg["fmt"] == "nvfp4" else cfg["fmt"], "data": "synthetic",
+        "dtype": {"nvfp4": "nvfp4-w/bf16-act/f32-acc", "mxfp4": "mxfp4-w/bf16-act/f32-acc"}.get(fmt, "bf16/f32-acc"),
+        "data": "synthetic",
         "config": {"workload": cfg["name"], "layers": L, "hidden": H, "experts": E, "top_k": k, "inter": I,
-                   "weight_fmt": cfg["fmt"], "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": f"working set > L2: {S} slots x {nb} B = {S * nb / 1e9:.2f} GB slot bank",
+                   "weight_fmt": fmt, "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
+                   "mode": cfg["mode"], "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
                    "pool": f"{n_keys} logical experts over {n_phys} distinct pinned blobs ({n_phys * nb / 1e9:.2f} GB)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": L * T * (H * 2 + E * 4),
                 "d2h_bytes_per_step": L * T * H * 2},
@@ -441,7 +518,7 @@ def run_ours(args, cfg):
         "wall_s_timed": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        tps, desc, calls, secs = _cpu_baseline(cfg, cfg["seed"], n_phys, budget_s=args.cpu_budget)
+        tps, desc, calls, secs = _cpu_baseline(cfg, cfg["seed"], n_phys, budget_s=args.cpu_budget, fmt=fmt)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
                                 "seconds": secs}
     if rank == 0:
@@ -463,6 +540,9 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=32)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fmt", choices=("bf16", "nvfp4", "mxfp4"), default=None,
+                    help="weight format (default: the workload's)")
+    ap.add_argument("--ffn", choices=("auto", "gemv", "tc"), default="auto", help="FFN kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1,5 +1,5 @@
 // ffn_gemv.cu -- grouped SwiGLU expert FFN for small token groups (decode),
-// with the weight dequantisation fused into the dot products.  Also the
+// with the weight dequantisation fused into the dot products, and the
 // gate-weighted combine.
 //
 // Per distinct expert u of a call (its blob sits in slot u_slot[u]) and its
@@ -7,10 +7,18 @@
 //   gate/up:  h[p][r] = bf16( silu(g) * u ),  g = W_g[r] . x_t,  u = W_u[r] . x_t
 //   down:     y[p][n] = W_d[n] . h[p]                       (fp32)
 //   combine:  out[t][n] = sum_j gates[t][j] * y[inv[t*k+j]][n], j ascending
-// Weight bytes are read once per token chunk of up to 8 tokens.  Decode
-// (1..8 tokens per expert) is bound by HBM bytes, not by the contraction, so
-// this path uses CUDA cores.  Each warp streams whole weight rows with 16-byte
-// loads.  The matching activations are staged once per CTA in shared memory.
+// Decode (1..4 tokens per expert) reads each weight once per call and does
+// 1..4 multiply-adds with it: bound by HBM bytes and by latency, not by the
+// contraction, so this path uses CUDA cores.  What matters is bytes in
+// flight: eight lanes share one weight row, every lane issues all of its
+// 16-byte loads for a batch of chunks before it computes, and the grid has
+// one CTA per 16 output features per expert.  Activations are staged once per
+// CTA in shared memory.
+//
+// For small calls the combine is fused into the down projection: each CTA
+// counts itself done on a per-feature-tile counter, and the last CTA of a tile
+// sums that tile's outputs over the call's tokens (in rank order) and resets
+// the counter for the next call.
 //
 // Formats: NVFP4 (e2m1 codes, E4M3 scale per 16, fp32 global scale per
 // matrix), MXFP4 (e2m1 codes, E8M0 scale per 32; OCP Microscaling v1.0),
@@ -21,10 +29,10 @@ namespace ftmoe {
 
 namespace {
 
-constexpr int kFfnThreads = 256;
-constexpr int kRowsPerWarp = 2;
-constexpr int kRowsPerCta = (kFfnThreads / 32) * kRowsPerWarp;
-constexpr int kTokChunk = 8;
+constexpr int kWarps = 4;                       // per CTA
+constexpr int kTokChunk = 4;                    // tokens per pass over the weights
+constexpr int kMinFeatPerCta = kWarps;          // LPR = 32: one feature per warp
+constexpr int kFusedCombineMaxT = 16;
 
 // Two e2m1 codes (one byte) -> two halves, via the sm_100-family conversion.
 __device__ __forceinline__ __half2 e2m1x2_to_half2(uint32_t byte) {
@@ -63,79 +71,96 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float *f) {
   }
 }
 
-// Decodes one 32-element chunk c of a weight row into w[32] (without the
-// NVFP4 global scale, which is applied to the finished dot product).
+// Raw bytes of one 32-element chunk of a weight row: FP4 = 16 code bytes +
+// scale bits; BF16 = 64 bytes.
 template <int FMT>
-__device__ __forceinline__ void load_chunk(const uint8_t *__restrict__ codes_row, const uint8_t *__restrict__ sf_row,
-                                           int c, float *w) {
+struct Chunk {
+  uint4 q[FMT == FMT_BF16 ? 4 : 1];
+  uint32_t sf;
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_chunk(const uint8_t *__restrict__ codes_row,
+                                           const uint8_t *__restrict__ sf_row, int c, Chunk<FMT> &ch) {
   if constexpr (FMT == FMT_BF16) {
     const uint4 *p = reinterpret_cast<const uint4 *>(codes_row) + 4 * c;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) bf16x8_to_float(__ldg(p + i), w + 8 * i);
+    for (int i = 0; i < 4; ++i) ch.q[i] = __ldg(p + i);
+    ch.sf = 0;
   } else {
-    const uint4 q = __ldg(reinterpret_cast<const uint4 *>(codes_row) + c);
-    float s0, s1;
-    if constexpr (FMT == FMT_NVFP4) {
-      const uint32_t sb = __ldg(reinterpret_cast<const uint16_t *>(sf_row) + c);
-      const float2 s = __half22float2(e4m3x2_to_half2(sb));
-      s0 = s.x;
-      s1 = s.y;
-    } else {
-      s0 = s1 = e8m0_to_float(__ldg(sf_row + c));
-    }
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+    ch.q[0] = __ldg(reinterpret_cast<const uint4 *>(codes_row) + c);
+    if constexpr (FMT == FMT_NVFP4) ch.sf = __ldg(reinterpret_cast<const uint16_t *>(sf_row) + c);
+    else ch.sf = __ldg(sf_row + c);
+  }
+}
+
+// Decodes 8 weights (elements 8i .. 8i+7) of a chunk into w[8]: BF16 values,
+// or the bare e2m1 values of FP4 codes (block scales are applied per 8-element
+// partial sum, see chunk_fma).
+template <int FMT>
+__device__ __forceinline__ void decode8(const Chunk<FMT> &ch, int i, float *w) {
+  if constexpr (FMT == FMT_BF16) {
+    bf16x8_to_float(ch.q[i], w);
+  } else {
+    const uint32_t word = i == 0 ? ch.q[0].x : i == 1 ? ch.q[0].y : i == 2 ? ch.q[0].z : ch.q[0].w;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const float2 v = __half22float2(e2m1x2_to_half2(words[i] >> (8 * b)));
-        const float s = i < 2 ? s0 : s1;  // bytes 0..7 -> elements 0..15 (first block of 16)
-        w[8 * i + 2 * b] = v.x * s;
-        w[8 * i + 2 * b + 1] = v.y * s;
-      }
+    for (int b = 0; b < 4; ++b) {
+      const float2 v = __half22float2(e2m1x2_to_half2(word >> (8 * b)));
+      w[2 * b] = v.x;
+      w[2 * b + 1] = v.y;
     }
   }
 }
 
-// acc[t] += row . xs[t] over K for NT tokens (lane-partial; caller reduces).
+// acc[t] += chunk . xs[t][32c .. 32c+31].  FP4: each 8-element partial sum of
+// e2m1 value x activation (every product exact in fp32) is multiplied by its
+// block scale once (NVFP4: elements 0..15 and 16..31 have one E4M3 scale
+// each; MXFP4: one E8M0 scale for all 32); the NVFP4 global scale is applied
+// to the finished dot product.
 template <int FMT, int NT>
-__device__ __forceinline__ void row_dot(const uint8_t *__restrict__ codes_row, const uint8_t *__restrict__ sf_row,
-                                        int K, const __nv_bfloat16 *xs, float *acc) {
-  const int lane = threadIdx.x & 31;
-  for (int c = lane; c < K / 32; c += 32) {
-    float w[32];
-    load_chunk<FMT>(codes_row, sf_row, c, w);
+__device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloat16 *xs, int K, int c, float *acc) {
+  float s0 = 1.0f, s1 = 1.0f;
+  if constexpr (FMT == FMT_NVFP4) {
+    const float2 s = __half22float2(e4m3x2_to_half2(ch.sf));
+    s0 = s.x;
+    s1 = s.y;
+  } else if constexpr (FMT == FMT_MXFP4) {
+    s0 = s1 = e8m0_to_float(ch.sf);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float w[8];
+    decode8<FMT>(ch, i, w);
+    const float s = i < 2 ? s0 : s1;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)t * K + 32 * c);
-      float a = acc[t];
+      const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)t * K + 32 * c)[i];
+      float xf[8];
+      bf16x8_to_float(xv, xf);
+      float p = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float xf[8];
-        bf16x8_to_float(xp[i], xf);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) a = fmaf(w[8 * i + q], xf[q], a);
-      }
-      acc[t] = a;
+      for (int q = 0; q < 8; ++q) p = fmaf(w[q], xf[q], p);
+      acc[t] = FMT == FMT_BF16 ? acc[t] + p : fmaf(s, p, acc[t]);
     }
   }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sum over the LPR lanes of this lane's row group (xor stays inside the group).
+template <int LPR>
+__device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-template <int FMT>
 struct RowPtrs {
   const uint8_t *codes, *sf;
 };
 
 // Row r of W_gu (r < 2I) or of W_d, inside one blob.
 template <int FMT>
-__device__ __forceinline__ RowPtrs<FMT> row_ptrs(const uint8_t *blob, const BlobLayout &L, bool down, int r, int K) {
-  RowPtrs<FMT> p;
+__device__ __forceinline__ RowPtrs row_ptrs(const uint8_t *blob, const BlobLayout &L, bool down, int r, int K) {
+  RowPtrs p;
   if constexpr (FMT == FMT_BF16) {
     p.codes = blob + (down ? L.d_codes : L.gu_codes) + (size_t)r * K * 2;
     p.sf = nullptr;
@@ -149,112 +174,140 @@ __device__ __forceinline__ RowPtrs<FMT> row_ptrs(const uint8_t *blob, const Blob
   return p;
 }
 
-template <int FMT, int NT>
-__device__ void gateup_rows(const uint8_t *blob, const BlobLayout &L, int H, int I, int row0,
-                            const __nv_bfloat16 *xs, int nt, __nv_bfloat16 *h_out /* row p0 of h */,
-                            float gs_g, float gs_u) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Dot products of NROWS weight rows (gate/up: 2, down: 1) with NT staged
+// activation rows, over this lane's chunks l, l+LPR, l+2 LPR, ... of K.  Loads
+// of a batch of chunks are all issued before any of them is used.
+template <int FMT, int NT, int NROWS, int LPR>
+__device__ __forceinline__ void rows_dot(const RowPtrs *rp, int K, const __nv_bfloat16 *xs, int l8,
+                                         float (&acc)[NROWS][NT]) {
+  constexpr int kBatch = FMT == FMT_BF16 ? 2 : 4;
+  const int cpl = K / (32 * LPR);  // chunks per lane
 #pragma unroll 1
-  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-    const int r = row0 + warp * kRowsPerWarp + rr;
-    if (r >= I) break;
-    float ag[NT], au[NT];
+  for (int i0 = 0; i0 < cpl; i0 += kBatch) {
+    Chunk<FMT> ch[NROWS][kBatch];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.0f;
-    const RowPtrs<FMT> pg = row_ptrs<FMT>(blob, L, false, r, H);
-    const RowPtrs<FMT> pu = row_ptrs<FMT>(blob, L, false, I + r, H);
-    row_dot<FMT, NT>(pg.codes, pg.sf, H, xs, ag);
-    row_dot<FMT, NT>(pu.codes, pu.sf, H, xs, au);
+    for (int b = 0; b < kBatch; ++b)
+      if (i0 + b < cpl)
+#pragma unroll
+        for (int r = 0; r < NROWS; ++r) load_chunk<FMT>(rp[r].codes, rp[r].sf, l8 + LPR * (i0 + b), ch[r][b]);
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+      if (i0 + b < cpl)
+#pragma unroll
+        for (int r = 0; r < NROWS; ++r) chunk_fma<FMT, NT>(ch[r][b], xs, K, l8 + LPR * (i0 + b), acc[r]);
+  }
+}
+
+template <int FMT, bool DOWN, int NT, int LPR>
+__device__ __forceinline__ void ffn_rows(const uint8_t *blob, const BlobLayout &L, const FfnArgs &a, int feat,
+                                         const __nv_bfloat16 *xs, int nt, int p0, float gs0, float gs1, int l8) {
+  if constexpr (!DOWN) {
+    if (feat >= a.I) return;
+    const RowPtrs rp[2] = {row_ptrs<FMT>(blob, L, false, feat, a.H), row_ptrs<FMT>(blob, L, false, a.I + feat, a.H)};
+    float acc[2][NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.0f;
+    rows_dot<FMT, NT, 2, LPR>(rp, a.H, xs, l8, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      const float g = warp_sum(ag[t]) * gs_g;
-      const float u = warp_sum(au[t]) * gs_u;
-      if (lane == t && t < nt) {
-        const float hv = g / (1.0f + expf(-g)) * u;
-        h_out[(size_t)t * I + r] = __float2bfloat16_rn(hv);
-      }
+      const float g = group_sum<LPR>(acc[0][t]) * gs0;
+      const float u = group_sum<LPR>(acc[1][t]) * gs1;
+      if (l8 == t && t < nt) a.h[(size_t)(p0 + t) * a.I + feat] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+    }
+  } else {
+    if (feat >= a.H) return;
+    const RowPtrs rp[1] = {row_ptrs<FMT>(blob, L, true, feat, a.I)};
+    float acc[1][NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[0][t] = 0.0f;
+    rows_dot<FMT, NT, 1, LPR>(rp, a.I, xs, l8, acc);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float v = group_sum<LPR>(acc[0][t]) * gs0;
+      if (l8 == t && t < nt) a.y[(size_t)(p0 + t) * a.H + feat] = v;
     }
   }
 }
 
-template <int FMT, int NT>
-__device__ void down_rows(const uint8_t *blob, const BlobLayout &L, int H, int I, int row0,
-                          const __nv_bfloat16 *xs, int nt, float *y_out /* row p0 of y */, float gs_d) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll 1
-  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-    const int n = row0 + warp * kRowsPerWarp + rr;
-    if (n >= H) break;
-    float a[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) a[t] = 0.0f;
-    const RowPtrs<FMT> pd = row_ptrs<FMT>(blob, L, true, n, I);
-    row_dot<FMT, NT>(pd.codes, pd.sf, I, xs, a);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const float v = warp_sum(a[t]) * gs_d;
-      if (lane == t && t < nt) y_out[(size_t)t * H + n] = v;
-    }
-  }
-}
-
-// One CTA: kRowsPerCta rows of one distinct expert, all of its tokens.
-template <int FMT, bool DOWN>
-__global__ void __launch_bounds__(kFfnThreads) ffn_gemv_kernel(FfnArgs a) {
+// One CTA: kWarps * 32 / LPR output features of one distinct expert, all of
+// its tokens, NT (>= the tokens any expert of the call has, up to kTokChunk)
+// token rows per pass.  With combine counters (down only), the last CTA of
+// each feature tile also writes that tile of the combined output.
+template <int FMT, bool DOWN, int NT, int LPR>
+__global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, CombineArgs cb) {
+  constexpr int kFeatPerCta = kWarps * (32 / LPR);
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
   const int u = blockIdx.y;
-  if (u >= a.plan.n[0]) return;
-  const int hit = a.plan.u_hit[u];
-  if ((a.only == 1 && !hit) || (a.only == 2 && hit)) return;
-  const int e = a.plan.u_expert[u];
-  const int off = a.plan.offsets[e];
-  const int n = a.plan.offsets[e + 1] - off;
-  const uint8_t *blob = a.slot_bank + (size_t)a.plan.u_slot[u] * a.slot_stride;
-  const BlobLayout L = blob_layout(FMT, a.H, a.I);
-  const int K = DOWN ? a.I : a.H;
-  float gs0 = 1.0f, gs1 = 1.0f;
-  if constexpr (FMT == FMT_NVFP4) {
-    const float *gs = reinterpret_cast<const float *>(blob + L.gscale);
-    gs0 = DOWN ? gs[2] : gs[0];
-    gs1 = gs[1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l8 = lane & (LPR - 1);
+  bool work = u < a.plan.n[0];
+  int hit = 0;
+  if (work) {
+    hit = a.plan.u_hit[u];
+    if ((a.only == 1 && !hit) || (a.only == 2 && hit)) work = false;
   }
-  const int row0 = blockIdx.x * kRowsPerCta;
-  for (int c0 = 0; c0 < n; c0 += kTokChunk) {
-    const int nt = min(kTokChunk, n - c0);
-    // stage the chunk's activations (bf16 rows of K) in shared memory
-    const int vec_per_row = K / 8;
-    for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) {
-      const int t = i / vec_per_row, v = i - t * vec_per_row;
-      const __nv_bfloat16 *src;
-      if (DOWN) {
-        src = a.h + (size_t)(off + c0 + t) * a.I;
-      } else {
-        const int pair = a.plan.perm[off + c0 + t];
-        src = a.x + (size_t)(pair / a.k) * a.H;
+  if (work) {
+    const int e = a.plan.u_expert[u];
+    const int off = a.plan.offsets[e];
+    const int n = a.plan.offsets[e + 1] - off;
+    const uint8_t *blob = a.slot_bank + (size_t)a.plan.u_slot[u] * a.slot_stride;
+    const BlobLayout L = blob_layout(FMT, a.H, a.I);
+    const int K = DOWN ? a.I : a.H;
+    float gs0 = 1.0f, gs1 = 1.0f;
+    if constexpr (FMT == FMT_NVFP4) {
+      const float *gs = reinterpret_cast<const float *>(blob + L.gscale);
+      gs0 = DOWN ? gs[2] : gs[0];
+      gs1 = gs[1];
+    }
+    const int feat = blockIdx.x * kFeatPerCta + warp * (32 / LPR) + lane / LPR;
+    for (int c0 = 0; c0 < n; c0 += kTokChunk) {
+      const int nt = min(kTokChunk, n - c0);
+      // stage the chunk's activations (bf16 rows of K) in shared memory
+      const int vec_per_row = K / 8;
+      for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) {
+        const int t = i / vec_per_row, v = i - t * vec_per_row;
+        const __nv_bfloat16 *src;
+        if (DOWN) {
+          src = a.h + (size_t)(off + c0 + t) * a.I;
+        } else {
+          const int pair = a.plan.perm[off + c0 + t];
+          src = a.x + (size_t)(pair / a.k) * a.H;
+        }
+        reinterpret_cast<uint4 *>(xs + (size_t)t * K)[v] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
       }
-      reinterpret_cast<uint4 *>(xs + (size_t)t * K)[v] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+      __syncthreads();
+      // rows nt..NT-1 of xs may hold stale data: their dot products are computed and dropped
+      ffn_rows<FMT, DOWN, NT, LPR>(blob, L, a, feat, xs, nt, off + c0, gs0, gs1, l8);
+      __syncthreads();
+    }
+  }
+  if constexpr (DOWN) {
+    if (cb.counters == nullptr) return;
+    // fused combine: the last of the gridDim.y CTAs of this feature tile sums it
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int prev = atomicAdd(cb.counters + blockIdx.x, 1);
+      s_last = prev == (int)gridDim.y - 1;
     }
     __syncthreads();
-    if constexpr (!DOWN) {
-      __nv_bfloat16 *hp = a.h + (size_t)(off + c0) * a.I;
-      if (nt == 1) gateup_rows<FMT, 1>(blob, L, a.H, a.I, row0, xs, nt, hp, gs0, gs1);
-      else if (nt == 2) gateup_rows<FMT, 2>(blob, L, a.H, a.I, row0, xs, nt, hp, gs0, gs1);
-      else if (nt <= 4) gateup_rows<FMT, 4>(blob, L, a.H, a.I, row0, xs, nt, hp, gs0, gs1);
-      else gateup_rows<FMT, 8>(blob, L, a.H, a.I, row0, xs, nt, hp, gs0, gs1);
-    } else {
-      float *yp = a.y + (size_t)(off + c0) * a.H;
-      if (nt == 1) down_rows<FMT, 1>(blob, L, a.H, a.I, row0, xs, nt, yp, gs0);
-      else if (nt == 2) down_rows<FMT, 2>(blob, L, a.H, a.I, row0, xs, nt, yp, gs0);
-      else if (nt <= 4) down_rows<FMT, 4>(blob, L, a.H, a.I, row0, xs, nt, yp, gs0);
-      else down_rows<FMT, 8>(blob, L, a.H, a.I, row0, xs, nt, yp, gs0);
+    if (!s_last) return;
+    __threadfence();
+    const int f0 = blockIdx.x * kFeatPerCta;
+    for (int i = threadIdx.x; i < cb.T * kFeatPerCta; i += blockDim.x) {
+      const int t = i / kFeatPerCta, f = f0 + (i - t * kFeatPerCta);
+      if (f >= a.H) continue;
+      float acc = 0.0f;
+      for (int j = 0; j < a.k; ++j) {
+        const float g = cb.gates[(size_t)t * a.k + j];
+        acc = fmaf(g, __ldcg(a.y + (size_t)cb.inv[(size_t)t * a.k + j] * a.H + f), acc);
+      }
+      cb.out[(size_t)t * a.H + f] = __float2bfloat16_rn(acc);
     }
-    __syncthreads();
+    if (threadIdx.x == 0) cb.counters[blockIdx.x] = 0;
   }
 }
-
-// Tokens with fewer than 8 rows staged leave rows nt..NT-1 of xs stale; the
-// dot products of those rows are computed and dropped (lane == t < nt).
 
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, const float *__restrict__ gates,
                                                       const int32_t *__restrict__ inv, int k, int H,
@@ -278,34 +331,82 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
   reinterpret_cast<uint2 *>(out + (size_t)t * H)[n4] = pk;
 }
 
-template <bool DOWN>
-cudaError_t launch_ffn(const FfnArgs &a, cudaStream_t s) {
-  const int rows = DOWN ? a.H : a.I;
+// Lanes per weight row: a power of two dividing the row's 32-element chunks,
+// as large as leaves each lane >= 4 chunks (fewer lanes per row for short rows).
+int lanes_per_row(int K) {
+  const int chunks = K / 32;
+  for (int l : {32, 16, 8})
+    if (chunks % l == 0 && chunks / l >= 4) return l;
+  for (int l : {32, 16, 8})
+    if (chunks % l == 0) return l;
+  return 8;
+}
+
+template <int FMT, bool DOWN, int NT, int LPR>
+cudaError_t launch_t(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
+  const int feats = DOWN ? a.H : a.I;
   const int K = DOWN ? a.I : a.H;
-  dim3 grid((rows + kRowsPerCta - 1) / kRowsPerCta, a.umax);
-  const size_t smem = (size_t)kTokChunk * K * sizeof(__nv_bfloat16);
-  switch (a.fmt) {
-    case FMT_BF16: ffn_gemv_kernel<FMT_BF16, DOWN><<<grid, kFfnThreads, smem, s>>>(a); break;
-    case FMT_NVFP4: ffn_gemv_kernel<FMT_NVFP4, DOWN><<<grid, kFfnThreads, smem, s>>>(a); break;
-    default: ffn_gemv_kernel<FMT_MXFP4, DOWN><<<grid, kFfnThreads, smem, s>>>(a); break;
-  }
+  constexpr int fpc = kWarps * (32 / LPR);
+  dim3 grid((feats + fpc - 1) / fpc, a.umax);
+  const size_t smem = (size_t)NT * K * sizeof(__nv_bfloat16);
+  ffn_gemv_kernel<FMT, DOWN, NT, LPR><<<grid, kWarps * 32, smem, s>>>(a, cb);
   return cudaGetLastError();
+}
+
+template <int FMT, bool DOWN, int NT>
+cudaError_t launch_l(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
+  const int l = lanes_per_row(DOWN ? a.I : a.H);
+  if (l == 32) return launch_t<FMT, DOWN, NT, 32>(a, cb, s);
+  if (l == 16) return launch_t<FMT, DOWN, NT, 16>(a, cb, s);
+  return launch_t<FMT, DOWN, NT, 8>(a, cb, s);
+}
+
+template <int FMT, bool DOWN>
+cudaError_t launch_n(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
+  // no expert of a call sees more tokens than the call has
+  if (a.max_tokens <= 1) return launch_l<FMT, DOWN, 1>(a, cb, s);
+  if (a.max_tokens == 2) return launch_l<FMT, DOWN, 2>(a, cb, s);
+  return launch_l<FMT, DOWN, 4>(a, cb, s);
+}
+
+template <bool DOWN>
+cudaError_t launch_ffn(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
+  switch (a.fmt) {
+    case FMT_BF16: return launch_n<FMT_BF16, DOWN>(a, cb, s);
+    case FMT_NVFP4: return launch_n<FMT_NVFP4, DOWN>(a, cb, s);
+    default: return launch_n<FMT_MXFP4, DOWN>(a, cb, s);
+  }
+}
+
+template <int FMT, bool DOWN, int NT>
+void attr_l() {
+  const int max_smem = NT * 8192 * 2;
+  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+}
+
+template <int FMT>
+void attr_f() {
+  attr_l<FMT, false, 1>(); attr_l<FMT, false, 2>(); attr_l<FMT, false, 4>();
+  attr_l<FMT, true, 1>(); attr_l<FMT, true, 2>(); attr_l<FMT, true, 4>();
 }
 
 }  // namespace
 
 void ffn_init_attributes() {
-  const int max_smem = kTokChunk * 8192 * 2;
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT_BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT_NVFP4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT_MXFP4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT_BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT_NVFP4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT_MXFP4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  attr_f<FMT_BF16>();
+  attr_f<FMT_NVFP4>();
+  attr_f<FMT_MXFP4>();
 }
 
-cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t s) { return launch_ffn<false>(a, s); }
-cudaError_t launch_down(const FfnArgs &a, cudaStream_t s) { return launch_ffn<true>(a, s); }
+int combine_tiles(int H) { return (H + kMinFeatPerCta - 1) / kMinFeatPerCta; }
+
+bool gemv_fuses_combine(int T) { return T <= kFusedCombineMaxT; }
+
+cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t s) { return launch_ffn<false>(a, CombineArgs{}, s); }
+
+cudaError_t launch_down(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) { return launch_ffn<true>(a, cb, s); }
 
 cudaError_t launch_combine(const float *y, const float *gates, const int32_t *inv, int T, int k, int H,
                            __nv_bfloat16 *out, cudaStream_t s) {

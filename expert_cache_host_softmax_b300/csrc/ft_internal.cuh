@@ -100,9 +100,23 @@ struct FfnArgs {
   PlanBufs plan;
   int umax;
   int only;                   // 0 all, 1 hits only, 2 misses only
+  int max_tokens;             // tokens of the call (no expert sees more)
 };
+// Combine fused into the down GEMV (small calls): out[t] = sum_j gates[t][j] *
+// y[inv[t*k+j]], written by the last CTA of each feature tile.  counters: one
+// int per tile (combine_tiles(H)), zero between calls.  counters == nullptr
+// disables the fusion.
+struct CombineArgs {
+  const float *gates;
+  const int32_t *inv;
+  __nv_bfloat16 *out;
+  int *counters;
+  int T;
+};
+int combine_tiles(int H);
+bool gemv_fuses_combine(int T);
 cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t s);
-cudaError_t launch_down(const FfnArgs &a, cudaStream_t s);
+cudaError_t launch_down(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *gates, const int32_t *inv, int T, int k, int H,
                            __nv_bfloat16 *out, cudaStream_t s);
 void ffn_init_attributes();

@@ -70,6 +70,7 @@ struct ft_moe {
   bool tmaps_ok = false;
   int ffn_kernel = FT_FFN_AUTO;
   int *err_dev = nullptr;
+  int *combine_counters = nullptr;   // per feature tile, for the combine fused into the down GEMV
   std::string err;
 };
 
@@ -132,6 +133,7 @@ void free_all(ft_moe *h) {
   cudaFree(h->hbuf);
   cudaFree(h->ybuf);
   cudaFree(h->err_dev);
+  cudaFree(h->combine_counters);
   if (h->mirror_host) cudaFreeHost(h->mirror_host);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
@@ -189,9 +191,10 @@ bool use_tc(const ft_moe *h, int T) {
   return rows >= 64 * distinct;
 }
 
-cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cudaStream_t s) {
+cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cudaStream_t s,
+                    const CombineArgs &cb = CombineArgs{}) {
   if (tc) return launch_tc_ffn(fa, down, h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
-  return down ? launch_down(fa, s) : launch_gateup(fa, s);
+  return down ? launch_down(fa, cb, s) : launch_gateup(fa, s);
 }
 
 // Initial cache state of the current mode; clears the counters.
@@ -321,7 +324,9 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->chunk_counts, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->chunk_base, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
-            dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess;
+            dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
+            dev_alloc(&h->combine_counters, combine_tiles(hidden)) == cudaSuccess &&
+            cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(hidden)) == cudaSuccess;
   if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
   if (cudaHostAlloc(&h->mirror_host, sizeof(int32_t) * (2 + 2 * (size_t)umax), cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer(reinterpret_cast<void **>(&h->mirror_dev), h->mirror_host, 0) != cudaSuccess) {
@@ -428,7 +433,7 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   prof_begin(h, FT_PROF_ROUTE, stream);
   FT_CUDA(h, launch_route(ra, stream));
   prof_end(h, FT_PROF_ROUTE, stream);
-  h->kernel_launches += route_kernel_count(n_tokens, h->k) + 3;  // + gate/up, down, combine
+  h->kernel_launches += route_kernel_count(n_tokens, h->k) + 2;  // + gate/up, down (+ combine below)
   if (h->mode == MODE_LRU) h->order_cur ^= 1;
   FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
 
@@ -441,6 +446,7 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.y = h->ybuf;
   fa.plan = h->plan;
   fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
+  fa.max_tokens = n_tokens;
   const bool tc = use_tc(h, n_tokens);
   h->last_tc = tc;
   if (h->mode == MODE_LRU) {
@@ -476,13 +482,26 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
     prof_end(h, FT_PROF_GATEUP_HIT, stream);
   }
   fa.only = 0;
+  // small calls on the GEMV: the combine runs inside the down kernel
+  const bool fused = !tc && gemv_fuses_combine(n_tokens);
+  CombineArgs cb{};
+  if (fused) {
+    cb.gates = h->plan.gates;
+    cb.inv = h->plan.inv;
+    cb.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    cb.counters = h->combine_counters;
+    cb.T = n_tokens;
+  }
   prof_begin(h, FT_PROF_DOWN, stream);
-  FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream));
+  FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream, cb));
   prof_end(h, FT_PROF_DOWN, stream);
-  prof_begin(h, FT_PROF_COMBINE, stream);
-  FT_CUDA(h, launch_combine(h->ybuf, h->plan.gates, h->plan.inv, n_tokens, h->k, h->H,
-                            reinterpret_cast<__nv_bfloat16 *>(out), stream));
-  prof_end(h, FT_PROF_COMBINE, stream);
+  if (!fused) {
+    h->kernel_launches += 1;
+    prof_begin(h, FT_PROF_COMBINE, stream);
+    FT_CUDA(h, launch_combine(h->ybuf, h->plan.gates, h->plan.inv, n_tokens, h->k, h->H,
+                              reinterpret_cast<__nv_bfloat16 *>(out), stream));
+    prof_end(h, FT_PROF_COMBINE, stream);
+  }
   if (h->mode == MODE_STREAM) FT_CUDA(h, cudaEventRecord(h->ev_bank_free[bank], stream));
   FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
   h->host_streamed += h->last_streamed;

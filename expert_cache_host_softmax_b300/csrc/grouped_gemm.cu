@@ -42,8 +42,6 @@ namespace {
 constexpr int BM = 128;          // token rows per tile (one TMEM lane each)
 constexpr int BN = 256;          // weight rows per tile (MMA N)
 constexpr int BK = 64;           // K per stage: 128 bytes of bf16 (one swizzle atom)
-constexpr int NS = 4;            // stages in the ring
-constexpr int LAG = 3;           // stages between issuing a load and publishing it
 constexpr int kEpiWarps = 4;
 constexpr int A_STAGE = BM * BK * 2;          // 16 KB
 constexpr int B_STAGE = BN * BK * 2;          // 32 KB
@@ -55,18 +53,28 @@ constexpr int kMaxU = kMaxExperts;
 template <int FMT>
 struct Cfg {
   static constexpr bool kFp4 = FMT != FMT_BF16;
+  // stages of A + (bf16) B; FP4 also has a ring of raw-code stages
+  static constexpr int kNS = kFp4 ? 3 : 4;
+  static constexpr int kNR = kFp4 ? 4 : 0;
   static constexpr int kLoadWarps = kFp4 ? 8 : 4;
   static constexpr int kLoadThreads = kLoadWarps * 32;
   static constexpr int kEpiWarp0 = kLoadWarps;               // multiple of 4: TMEM lane quarter = warp % 4
   static constexpr int kMmaWarp = kLoadWarps + kEpiWarps;
-  static constexpr int kThreads = (kMmaWarp + 1) * 32;
-  static constexpr int kNB = kFp4 ? 2 : NS;                  // bf16 B stages
+  static constexpr int kTmaWarp = kFp4 ? kMmaWarp + 1 : -1;  // FP4: raw-code TMA producer
+  static constexpr int kThreads = (kMmaWarp + 1 + (kFp4 ? 1 : 0)) * 32;
   static constexpr int kChunksA = 8 * BM / kLoadThreads;    // 16-byte chunks of A per loader thread
-  // shared memory: [A x NS][B x kNB][RAW x NS (fp4)] then barriers and tables
-  static constexpr int kOffB = NS * A_STAGE;
-  static constexpr int kOffRaw = kOffB + kNB * B_STAGE;
-  static constexpr int kOffBar = kOffRaw + (kFp4 ? NS * RAW_STAGE : 0);
-  static constexpr int kBars = 4 * NS + 4 + 1;   // full, bfull, empty, (unused), tmem_full x2, tmem_empty x2, drain
+  // A stage is published (one FULL arrival per loader thread) kLag stages
+  // after its loads were issued, once the thread's own cp.async group has
+  // landed and been fenced for the tensor core's (async-proxy) reads.
+  static constexpr int kLag = kNS - 1;
+  static constexpr int kFullCount = kLoadThreads;
+  // shared memory: [A x kNS][B x kNS][RAW x kNR] then barriers and tables
+  static constexpr int kOffB = kNS * A_STAGE;
+  static constexpr int kOffRaw = kOffB + kNS * B_STAGE;
+  static constexpr int kOffBar = kOffRaw + kNR * RAW_STAGE;
+  // barriers: FULL, BFULL, EMPTY (kNS each), RAWFULL, RAWEMPTY (kNR each),
+  // TFULL x2, TEMPTY x2, DRAIN
+  static constexpr int kBars = 3 * kNS + 2 * kNR + 5;
   static constexpr int kOffTab = kOffBar + kBars * 8 + 16;
   static constexpr int kSmem = kOffTab + 4 * (2 * (kMaxU + 1)) + 64;
   static constexpr int kSmemAlloc = kSmem + 1024;             // room to align the base to 1024
@@ -149,6 +157,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
@@ -300,18 +309,21 @@ template <int FMT, bool DOWN>
 __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
     gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmB) {
   using C = Cfg<FMT>;
+  constexpr int NS = C::kNS, NR = C::kNR;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   unsigned char *sm = smem_raw + (base - raw_base);
   const uint32_t sA = base, sB = base + C::kOffB, sRaw = base + C::kOffRaw;
   const uint32_t bar0 = base + C::kOffBar;
-  auto FULL = [&](int s) { return bar0 + 8u * s; };              // A (and converted B) published
-  auto BFULL = [&](int s) { return bar0 + 8u * (NS + s); };      // B / raw B by TMA
-  auto EMPTY = [&](int s) { return bar0 + 8u * (2 * NS + s); };  // stage consumed by the MMAs
-  auto TFULL = [&](int b) { return bar0 + 8u * (4 * NS + b); };
-  auto TEMPTY = [&](int b) { return bar0 + 8u * (4 * NS + 2 + b); };
-  const uint32_t DRAIN = bar0 + 8u * (4 * NS + 4);
+  auto FULL = [&](int s) { return bar0 + 8u * s; };                    // A (and converted B) landed
+  auto BFULL = [&](int s) { return bar0 + 8u * (NS + s); };            // bf16 B landed (TMA)
+  auto EMPTY = [&](int s) { return bar0 + 8u * (2 * NS + s); };        // stage consumed by the MMAs
+  auto RAWFULL = [&](int r) { return bar0 + 8u * (3 * NS + r); };      // FP4 codes landed (TMA)
+  auto RAWEMPTY = [&](int r) { return bar0 + 8u * (3 * NS + NR + r); };  // FP4 codes converted
+  auto TFULL = [&](int b) { return bar0 + 8u * (3 * NS + 2 * NR + b); };
+  auto TEMPTY = [&](int b) { return bar0 + 8u * (3 * NS + 2 * NR + 2 + b); };
+  const uint32_t DRAIN = bar0 + 8u * (3 * NS + 2 * NR + 4);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + C::kOffBar + C::kBars * 8);
   volatile int *s_abort = reinterpret_cast<volatile int *>(sm + C::kOffBar + C::kBars * 8 + 4);
   int *s_start = reinterpret_cast<int *>(sm + C::kOffTab);
@@ -325,9 +337,13 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
   // ---- prologue: barriers, TMEM, tile table
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(FULL(s), C::kLoadThreads);
+      mbar_init(FULL(s), C::kFullCount);
       mbar_init(BFULL(s), 1);
       mbar_init(EMPTY(s), 1);
+    }
+    for (int r = 0; r < NR; ++r) {
+      mbar_init(RAWFULL(r), 1);
+      mbar_init(RAWEMPTY(r), C::kLoadThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(TFULL(b), 1);
@@ -372,54 +388,24 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
 
   if (warp < C::kLoadWarps) {
     // ================================================================ loaders
+    // Stage j: publish stage j - kLag (this thread's A chunks for it have
+    // landed: cp.async.wait_group; fence for the async proxy; arrive on FULL),
+    // then wait for slot j, issue its A row chunks by cp.async, and (BF16)
+    // thread 0 issues its B tile by TMA, or (FP4) every thread dequantises one
+    // B row from the raw codes into the swizzled bf16 tile right away.
+    // Publishing before the slot wait keeps the MMA fed: slot j frees when the
+    // MMA finishes stage j - kNS, which was published kNS - kLag >= 1 stages ago.
+    constexpr int LAG = C::kLag;
     const int t = tid;
-    const int arow = t % BM;                 // A row loaded by this thread
+    const int arow = t % BM;
     const int achunk0 = (t / BM) * C::kChunksA;
-    // FP4: B row converted by this thread (0..255) and its scale registers
-    uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_nxt = make_uint4(0, 0, 0, 0);
     const BlobLayout L = blob_layout(FMT, a.H, a.I);
+    uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_nxt = make_uint4(0, 0, 0, 0);
     int j = 0;  // stage counter across tiles
     bool ok = true;
-    auto finish = [&](int jj) -> bool {
-      // publish stage jj (issued LAG stages ago): A rows landed; FP4: dequantise B
-      const int s = jj % NS;
-      if constexpr (C::kFp4) {
-        if (!mbar_wait(BFULL(s), (jj / NS) & 1, s_abort, a.err, 11)) return false;
-        const uint32_t raw = sRaw + s * RAW_STAGE + t * 32;
-        uint4 q0, q1;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(q0.x), "=r"(q0.y), "=r"(q0.z), "=r"(q0.w)
-                     : "r"(raw));
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(q1.x), "=r"(q1.y), "=r"(q1.z), "=r"(q1.w)
-                     : "r"(raw + 16));
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        // scales of this stage: NVFP4 4 bytes (one per 16), MXFP4 2 bytes (one per 32)
-        const int sub = jj & 3;
-        float sc[4];
-        if constexpr (FMT == FMT_NVFP4) {
-          const uint32_t word = sub == 0 ? sc_cur.x : sub == 1 ? sc_cur.y : sub == 2 ? sc_cur.z : sc_cur.w;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sc[i] = e4m3_to_float((word >> (8 * i)) & 0xFFu);
-        } else {
-          const uint32_t word = (sub >> 1) == 0 ? sc_cur.x : sc_cur.y;
-          const uint32_t pair = (word >> (16 * (sub & 1))) & 0xFFFFu;
-          sc[0] = sc[1] = e8m0_to_float(pair & 0xFFu);
-          sc[2] = sc[3] = e8m0_to_float(pair >> 8);
-        }
-        const uint32_t bdst = sB + (jj % C::kNB) * B_STAGE + t * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = dequant8(w[c], sc[c >> 1]);
-          const uint32_t d = bdst + ((c ^ (t & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v.x), "r"(v.y), "r"(v.z),
-                       "r"(v.w)
-                       : "memory");
-        }
-      }
+    auto publish = [&](int jj) {
       fence_proxy_async();
-      mbar_arrive(FULL(s));
-      return true;
+      mbar_arrive(FULL(jj % NS));
     };
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
@@ -429,30 +415,24 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
       const __nv_bfloat16 *asrc;
       if constexpr (DOWN) asrc = a.h + (size_t)r * a.I;
       else asrc = a.x + (size_t)(a.plan.perm[r] / a.k) * a.H;
-      const uint8_t *blob = a.slot_bank + (size_t)ti.slot * a.slot_stride;
-      // FP4: this thread's B row inside the blob (gate/up: 128 gate rows then 128 up rows)
-      int brow = 0;
+      // FP4: this thread's B row in the blob (gate/up: 128 gate rows, then the 128 matching up rows)
       const uint8_t *sf_row = nullptr;
       if constexpr (C::kFp4) {
-        brow = DOWN ? ti.n * BN + t : (t < BN / 2 ? ti.n * (BN / 2) + t : a.I + ti.n * (BN / 2) + (t - BN / 2));
+        const int brow =
+            DOWN ? ti.n * BN + t : (t < BN / 2 ? ti.n * (BN / 2) + t : a.I + ti.n * (BN / 2) + (t - BN / 2));
         const int sf_per_row = K / (FMT == FMT_NVFP4 ? 16 : 32);
-        sf_row = blob + (DOWN ? L.d_sf : L.gu_sf) + (size_t)brow * sf_per_row;
+        sf_row = a.slot_bank + (size_t)ti.slot * a.slot_stride + (DOWN ? L.d_sf : L.gu_sf) +
+                 (size_t)brow * sf_per_row;
       }
       for (int kb = 0; kb < nk; ++kb, ++j) {
+        if (j >= LAG) {
+          cp_async_wait<LAG - 1>();   // groups j-LAG+1 .. j-1 may still be in flight
+          publish(j - LAG);
+        }
         const int s = j % NS;
         if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 10)) { ok = false; break; }
-        if (t == 0) {
-          if constexpr (C::kFp4) {
-            mbar_arrive_expect_tx(BFULL(s), RAW_STAGE);
-            const uint32_t dst = sRaw + s * RAW_STAGE;
-            if (DOWN) {
-              tma_load_3d(dst, &tmB, BFULL(s), kb * (BK / 2), ti.n * BN, ti.slot);
-              tma_load_3d(dst + RAW_STAGE / 2, &tmB, BFULL(s), kb * (BK / 2), ti.n * BN + BN / 2, ti.slot);
-            } else {
-              tma_load_3d(dst, &tmB, BFULL(s), kb * (BK / 2), ti.n * (BN / 2), ti.slot);
-              tma_load_3d(dst + RAW_STAGE / 2, &tmB, BFULL(s), kb * (BK / 2), a.I + ti.n * (BN / 2), ti.slot);
-            }
-          } else {
+        if constexpr (!C::kFp4) {
+          if (t == 0) {
             mbar_arrive_expect_tx(BFULL(s), B_STAGE);
             const uint32_t dst = sB + s * B_STAGE;
             if (DOWN) {
@@ -474,47 +454,100 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         }
         cp_async_commit();
         if constexpr (C::kFp4) {
-          // scales for the 4 stages kb..kb+3 (NVFP4: 16 bytes, MXFP4: 8 bytes), one group ahead
+          // block scales of the 4 stages of group kb/4 (NVFP4: 16 bytes, MXFP4:
+          // 8 bytes), loaded one group ahead
+          constexpr int per = FMT == FMT_NVFP4 ? 4 : 2;   // scale bytes per stage
+          auto load_group = [&](int g) -> uint4 {
+            if (FMT == FMT_NVFP4) return __ldg(reinterpret_cast<const uint4 *>(sf_row + g * 4 * per));
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(sf_row + g * 4 * per));
+            return make_uint4(v.x, v.y, 0, 0);
+          };
+          if (kb == 0) sc_nxt = load_group(0);
           if ((kb & 3) == 0) {
-            const int per = FMT == FMT_NVFP4 ? 4 : 2;   // scale bytes per stage
-            if (FMT == FMT_NVFP4) sc_nxt = __ldg(reinterpret_cast<const uint4 *>(sf_row + kb * per));
-            else {
-              const uint2 v = __ldg(reinterpret_cast<const uint2 *>(sf_row + kb * per));
-              sc_nxt = make_uint4(v.x, v.y, 0, 0);
-            }
+            sc_cur = sc_nxt;
+            if (kb + 4 < nk) sc_nxt = load_group(kb / 4 + 1);
           }
-        }
-        if (j >= LAG) {
-          cp_async_wait<LAG>();
-          if constexpr (C::kFp4) {
-            if (((j - LAG) & 3) == 0) sc_cur = sc_nxt;
+          const int sub = kb & 3;
+          float sc[4];
+          if constexpr (FMT == FMT_NVFP4) {
+            const uint32_t word = sub == 0 ? sc_cur.x : sub == 1 ? sc_cur.y : sub == 2 ? sc_cur.z : sc_cur.w;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[i] = e4m3_to_float((word >> (8 * i)) & 0xFFu);
+          } else {
+            const uint32_t word = (sub >> 1) == 0 ? sc_cur.x : sc_cur.y;
+            const uint32_t pair = (word >> (16 * (sub & 1))) & 0xFFFFu;
+            sc[0] = sc[1] = e8m0_to_float(pair & 0xFFu);
+            sc[2] = sc[3] = e8m0_to_float(pair >> 8);
           }
-          if (!finish(j - LAG)) { ok = false; ++j; break; }   // stage j was issued
+          const int rs = j % NR;
+          if (!mbar_wait(RAWFULL(rs), (j / NR) & 1, s_abort, a.err, 11)) { ok = false; ++j; break; }
+          const uint32_t raw = sRaw + rs * RAW_STAGE + t * 32;
+          uint4 q0, q1;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(q0.x), "=r"(q0.y), "=r"(q0.z), "=r"(q0.w)
+                       : "r"(raw)
+                       : "memory");
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(q1.x), "=r"(q1.y), "=r"(q1.z), "=r"(q1.w)
+                       : "r"(raw + 16)
+                       : "memory");
+          const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          const uint32_t bdst = sB + s * B_STAGE + t * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = dequant8(w[c], sc[c >> 1]);
+            const uint32_t d = bdst + ((c ^ (t & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v.x), "r"(v.y), "r"(v.z),
+                         "r"(v.w)
+                         : "memory");
+          }
+          // the raw codes have been consumed (the stores above depend on them):
+          // the producer may now refill this raw slot
+          mbar_arrive(RAWEMPTY(rs));
         }
       }
     }
-    // publish the last LAG stages
-    cp_async_wait<0>();
-    if (ok) {
-      for (int jj = max(0, j - LAG); jj < j; ++jj) {
-        if constexpr (C::kFp4) {
-          if ((jj & 3) == 0) sc_cur = sc_nxt;
-          // B stage jj % 2 was last read by stage jj - 2: in the main loop the
-          // EMPTY wait of the stage issued alongside covers that; here, wait for it
-          const int p = jj - 2;
-          if (p >= 0 && !mbar_wait(EMPTY(p % NS), (p / NS) & 1, s_abort, a.err, 12)) break;
-        }
-        if (!finish(jj)) break;
-      }
-    }
-    // drain: every TMA this CTA issued must land before the CTA exits
-    if (t == 0) {
+    // publish the stages still pending, and exit with no copy of ours in flight
+    cp_async_wait_all();
+    if (ok)
+      for (int jj = max(0, j - LAG); jj < j; ++jj) publish(jj);
+    if (!C::kFp4 && t == 0) {
       for (int jj = max(0, j - NS); jj < j; ++jj) {
         const unsigned long long t0 = globaltimer();
         while (!mbar_try_wait(BFULL(jj % NS), (jj / NS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
     }
+  } else if (C::kFp4 && warp == C::kTmaWarp) {
+    // ================================================================ FP4 code producer
+    if (lane == 0) {
+      int j = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
+        for (int kb = 0; kb < nk; ++kb, ++j) {
+          const int rs = j % NR;
+          if (!mbar_wait(RAWEMPTY(rs), ((j / NR) & 1) ^ 1, s_abort, a.err, 40)) { ok = false; break; }
+          fence_proxy_async();   // the converters' reads of this slot precede the TMA's writes
+          mbar_arrive_expect_tx(RAWFULL(rs), RAW_STAGE);
+          const uint32_t dst = sRaw + rs * RAW_STAGE;
+          if (DOWN) {
+            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * (BK / 2), ti.n * BN, ti.slot);
+            tma_load_3d(dst + RAW_STAGE / 2, &tmB, RAWFULL(rs), kb * (BK / 2), ti.n * BN + BN / 2, ti.slot);
+          } else {
+            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * (BK / 2), ti.n * (BN / 2), ti.slot);
+            tma_load_3d(dst + RAW_STAGE / 2, &tmB, RAWFULL(rs), kb * (BK / 2), a.I + ti.n * (BN / 2), ti.slot);
+          }
+        }
+      }
+      // every TMA this CTA issued must land before the CTA exits
+      for (int jj = max(0, j - NR); jj < j; ++jj) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(RAWFULL(jj % NR), (jj / NR) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp == C::kMmaWarp) {
     // ================================================================ MMA issuer
     if (lane == 0) {
@@ -533,7 +566,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sA + s * A_STAGE, b0 = sB + (j % C::kNB) * B_STAGE;
+          const uint32_t a0 = sA + s * A_STAGE, b0 = sB + s * B_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             mma_bf16(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), kIdesc, (kb | kk) != 0);
@@ -650,6 +683,7 @@ cudaError_t launch(const GemmArgs &a, const CUtensorMap &map, int grid, cudaStre
 
 static_assert(Cfg<FMT_BF16>::kSmemAlloc <= 227 * 1024, "bf16 smem");
 static_assert(Cfg<FMT_NVFP4>::kSmemAlloc <= 227 * 1024, "fp4 smem");
+static_assert(Cfg<FMT_NVFP4>::kThreads == 448 && Cfg<FMT_BF16>::kThreads == 288, "warp roles");
 
 int tc_num_sms() {
   static int n = 0;

@@ -21,6 +21,8 @@
 // whole LRU update is O(S / blockDim) per thread, plus two block scans.
 #include <math.h>
 
+#include <algorithm>
+
 #include "ft_internal.cuh"
 
 namespace ftmoe {
@@ -156,11 +158,41 @@ struct PlanSmem {
   int *s_victim;  // [E]
   unsigned *s_bits;  // [(S+31)/32]
   int *s_warp;    // [32]
+  int *s_keyslot;    // [E] this layer's key -> slot, loaded up front (or null)
+  int *s_victim_key; // [E] key held by each victim slot (with s_keyslot)
 };
 
+// The cache-table entries a thread needs, loaded at kernel start so that the
+// plan itself waits on no global memory: its range of the recency list and the
+// key held by each of those slots.
+constexpr int kPre = 8;
+struct Prefetch {
+  int n;              // entries held, or -1 (range longer than kPre: read in place)
+  int ord[kPre], key[kPre];
+};
+
+__device__ __forceinline__ void prefetch_tables(const RouteArgs &a, int *s_keyslot, Prefetch &pf) {
+  const int tid = threadIdx.x, NT = blockDim.x;
+  pf.n = -1;
+  if (a.mode != MODE_LRU) return;
+  for (int e = tid; e < a.E; e += NT) s_keyslot[e] = a.cache.key_slot[a.layer * a.E + e];
+  const int per = (a.S + NT - 1) / NT;
+  if (per > kPre) return;
+  const int i0 = min(a.S, tid * per), i1 = min(a.S, i0 + per);
+  pf.n = i1 - i0;
+#pragma unroll
+  for (int q = 0; q < kPre; ++q)
+    if (q < pf.n) pf.ord[q] = a.cache.order_in[i0 + q];
+#pragma unroll
+  for (int q = 0; q < kPre; ++q)
+    if (q < pf.n) pf.key[q] = a.cache.slot_key[pf.ord[q]];
+}
+
 // Distinct experts of the call, slot lookup, LRU update, plan and stats.
-// One CTA.  Needs blockDim.x >= E.
-__device__ void block_plan(const RouteArgs &a, const PlanSmem &sm) {
+// One CTA.  Needs blockDim.x >= E.  With a prefetch (pf.n >= 0 and
+// sm.s_keyslot set), the tables are read from what prefetch_tables loaded.
+// The miss list is published to the host before the statistics are updated.
+__device__ void block_plan(const RouteArgs &a, const PlanSmem &sm, const Prefetch &pf) {
   const int tid = threadIdx.x, NT = blockDim.x, E = a.E, S = a.S;
   const int flag = (tid < E) && sm.s_count[tid] > 0;
   int nU;
@@ -173,7 +205,7 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm) {
     const int e = sm.s_uexp[tid];
     key = a.layer * E + e;
     if (a.mode == MODE_LRU) {
-      slot = a.cache.key_slot[key];
+      slot = sm.s_keyslot ? sm.s_keyslot[e] : a.cache.key_slot[key];
       hit = slot >= 0;
     } else {
       slot = a.bank * E + e;
@@ -194,19 +226,40 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm) {
     __syncthreads();
     const int per = (S + NT - 1) / NT;
     const int i0 = min(S, tid * per), i1 = min(S, i0 + per);
-    int cnt = 0;
-    for (int i = i0; i < i1; ++i) {
-      const int s = a.cache.order_in[i];
-      cnt += !((sm.s_bits[s >> 5] >> (s & 31)) & 1u);
-    }
-    int nonhit;
-    int r = block_excl_scan(cnt, sm.s_warp, &nonhit);
-    for (int i = i0; i < i1; ++i) {
-      const int s = a.cache.order_in[i];
-      if ((sm.s_bits[s >> 5] >> (s & 31)) & 1u) continue;
-      if (r < nM) sm.s_victim[r] = s;
-      else a.cache.order_out[r - nM] = s;
-      ++r;
+    int cnt = 0, r;
+    if (pf.n >= 0) {
+#pragma unroll
+      for (int q = 0; q < kPre; ++q)
+        if (q < pf.n) cnt += !((sm.s_bits[pf.ord[q] >> 5] >> (pf.ord[q] & 31)) & 1u);
+      int nonhit;
+      r = block_excl_scan(cnt, sm.s_warp, &nonhit);
+#pragma unroll
+      for (int q = 0; q < kPre; ++q) {
+        if (q >= pf.n) continue;
+        const int s = pf.ord[q];
+        if ((sm.s_bits[s >> 5] >> (s & 31)) & 1u) continue;
+        if (r < nM) {
+          sm.s_victim[r] = s;
+          sm.s_victim_key[r] = pf.key[q];
+        } else {
+          a.cache.order_out[r - nM] = s;
+        }
+        ++r;
+      }
+    } else {
+      for (int i = i0; i < i1; ++i) {
+        const int s = a.cache.order_in[i];
+        cnt += !((sm.s_bits[s >> 5] >> (s & 31)) & 1u);
+      }
+      int nonhit;
+      r = block_excl_scan(cnt, sm.s_warp, &nonhit);
+      for (int i = i0; i < i1; ++i) {
+        const int s = a.cache.order_in[i];
+        if ((sm.s_bits[s >> 5] >> (s & 31)) & 1u) continue;
+        if (r < nM) sm.s_victim[r] = s;
+        else a.cache.order_out[r - nM] = s;
+        ++r;
+      }
     }
     __syncthreads();
     if (tid < nU) {
@@ -215,7 +268,7 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm) {
       } else {
         const int v = sm.s_victim[mrank];
         a.cache.order_out[S - nM + mrank] = v;
-        const int ek = a.cache.slot_key[v];
+        const int ek = pf.n >= 0 ? sm.s_victim_key[mrank] : a.cache.slot_key[v];
         if (ek >= 0) {
           a.cache.key_slot[ek] = -1;
           evicted = ek;
@@ -236,11 +289,18 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm) {
     if (a.mirror && !hit) {
       a.mirror[2 + mrank] = key;
       a.mirror[2 + a.umax + mrank] = slot;
-      __threadfence_system();
     }
   }
   __syncthreads();
   if (tid == 0) {
+    if (a.mirror) {
+      // the block's miss-list writes precede this fence (barrier above), and
+      // the host reads the list only after it sees the new sequence number
+      a.mirror[1] = nM;
+      __threadfence_system();
+      *(volatile int32_t *)&a.mirror[0] = (int32_t)a.seq;
+      __threadfence_system();
+    }
     a.plan.n[0] = nU;
     a.plan.n[1] = nH;
     a.plan.n[2] = nM;
@@ -250,33 +310,32 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm) {
     const unsigned long long hits_ = a.mode == MODE_LRU ? nH : 0, miss_ = a.mode == MODE_LRU ? nM : 0;
     st[0] += nU; st[1] += hits_; st[2] += miss_; st[3] += nEv; st[4] += bytes;
     st[8] = nU; st[9] = hits_; st[10] = miss_; st[11] = nEv; st[12] = bytes;
-    if (a.mirror) {
-      a.mirror[1] = nM;
-      __threadfence_system();
-      *(volatile int32_t *)&a.mirror[0] = (int32_t)a.seq;
-      __threadfence_system();
-    }
   }
 }
 
 // ---------------------------------------------------------------- kernels
 
 // Whole routing of a small call in one CTA: top-k + gates, histogram,
-// offsets, plan, stable scatter.
+// offsets, plan, stable scatter.  The cache tables are read at the start,
+// alongside the logits, so the plan waits on no further global loads.
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
   extern __shared__ int smem[];
-  const int E = a.E;
+  const int E = a.E, nw = blockDim.x >> 5;
   int *s_count = smem;                 // E
   int *s_base = s_count + E;           // E
   int *s_uexp = s_base + E;            // E
   int *s_victim = s_uexp + E;          // E
-  int *s_warp = s_victim + E;          // 32
-  int *s_wcnt = s_warp + 32;           // 32*E
-  unsigned *s_bits = (unsigned *)(s_wcnt + 32 * E);
+  int *s_keyslot = s_victim + E;       // E
+  int *s_victim_key = s_keyslot + E;   // E
+  int *s_warp = s_victim_key + E;      // 32
+  int *s_wcnt = s_warp + 32;           // nw*E
+  unsigned *s_bits = (unsigned *)(s_wcnt + nw * E);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  Prefetch pf;
+  prefetch_tables(a, s_keyslot, pf);
   for (int i = tid; i < E; i += blockDim.x) s_count[i] = 0;
   __syncthreads();
-  for (int t = w; t < a.T; t += blockDim.x >> 5) {
+  for (int t = w; t < a.T; t += nw) {
     const int e = warp_topk_softmax(a.logits + (size_t)t * E, E, a.k, a.plan.topk_idx + (size_t)t * a.k,
                                     a.plan.gates + (size_t)t * a.k);
     if (lane < a.k) atomicAdd(&s_count[e], 1);
@@ -289,8 +348,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
     s_base[tid] = off;
   }
   if (tid == 0) a.plan.offsets[E] = total;
-  PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp};
-  block_plan(a, sm);
+  PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, a.mode == MODE_LRU ? s_keyslot : nullptr, s_victim_key};
+  block_plan(a, sm, pf);
   __syncthreads();
   block_rank_scatter(a.plan.topk_idx, 0, a.T * a.k, E, s_base, s_wcnt, a.plan.perm, a.plan.inv);
 }
@@ -357,8 +416,10 @@ __global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int wi
   if (tid == 0) a.plan.offsets[E] = total;
   __syncthreads();
   if (with_plan) {
-    PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp};
-    block_plan(a, sm);
+    PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, nullptr, nullptr};
+    Prefetch pf;
+    pf.n = -1;
+    block_plan(a, sm, pf);
   }
 }
 
@@ -375,8 +436,13 @@ __global__ void __launch_bounds__(256) scatter_chunk_kernel(const int32_t *__res
   block_rank_scatter(idx, p0, p1, E, s_base, s_wcnt, perm, inv);
 }
 
+// Threads of the single-CTA routing kernel: at least E (one per expert in
+// the plan), at least 256, a whole number of warps.
+int small_threads(int E) { return std::min(kRouteThreads, std::max(256, (E + 31) / 32 * 32)); }
+
 size_t small_smem_bytes(int E, int S) {
-  return sizeof(int) * (4 * (size_t)E + 32 + 32 * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
+  const size_t nw = small_threads(E) / 32;
+  return sizeof(int) * (6 * (size_t)E + 32 + nw * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
 }
 size_t plan_smem_bytes(int E, int S) {
   return sizeof(int) * (3 * (size_t)E + 32) + sizeof(unsigned) * (((size_t)S + 31) / 32);
@@ -403,7 +469,7 @@ int route_kernel_count(int T, int k) { return T * k <= kSmallRoutePairs ? 1 : 3;
 // three kernels over kChunkTokens-token chunks.
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s) {
   if (a.T * a.k <= kSmallRoutePairs || a.chunk_counts == nullptr) {
-    route_small_kernel<<<1, kRouteThreads, small_smem_bytes(a.E, a.S), s>>>(a);
+    route_small_kernel<<<1, small_threads(a.E), small_smem_bytes(a.E, a.S), s>>>(a);
     return cudaGetLastError();
   }
   RouteArgs b = a;
