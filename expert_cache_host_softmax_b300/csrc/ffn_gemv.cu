@@ -234,8 +234,10 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, const BlobLayout &
 // token rows per pass.  With combine counters (down only), the last CTA of
 // each feature tile also writes that tile of the combined output.
 template <int FMT, bool DOWN, int NT, int LPR>
-__global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, CombineArgs cb) {
-  constexpr int kFeatPerCta = kWarps * (32 / LPR);
+__global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, CombineArgs cb, int fpw) {
+  // fpw passes per warp over feature groups: long rows (large K) give each CTA
+  // more features, so that the staged activations serve more weight bytes
+  const int kFeatPerCta = kWarps * (32 / LPR) * fpw;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
   const int u = blockIdx.y;
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
       gs0 = DOWN ? gs[2] : gs[0];
       gs1 = gs[1];
     }
-    const int feat = blockIdx.x * kFeatPerCta + warp * (32 / LPR) + lane / LPR;
+    const int feat0 = blockIdx.x * kFeatPerCta + warp * (32 / LPR) + lane / LPR;
     for (int c0 = 0; c0 < n; c0 += kTokChunk) {
       const int nt = min(kTokChunk, n - c0);
       // stage the chunk's activations (bf16 rows of K) in shared memory
@@ -277,7 +279,8 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
       }
       __syncthreads();
       // rows nt..NT-1 of xs may hold stale data: their dot products are computed and dropped
-      ffn_rows<FMT, DOWN, NT, LPR>(blob, L, a, feat, xs, nt, off + c0, gs0, gs1, l8);
+      for (int fp = 0; fp < fpw; ++fp)
+        ffn_rows<FMT, DOWN, NT, LPR>(blob, L, a, feat0 + fp * kWarps * (32 / LPR), xs, nt, off + c0, gs0, gs1, l8);
       __syncthreads();
     }
   }
@@ -346,10 +349,11 @@ template <int FMT, bool DOWN, int NT, int LPR>
 cudaError_t launch_t(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
   const int feats = DOWN ? a.H : a.I;
   const int K = DOWN ? a.I : a.H;
-  constexpr int fpc = kWarps * (32 / LPR);
+  const int fpw = K >= 4096 ? 4 : 1;
+  const int fpc = kWarps * (32 / LPR) * fpw;
   dim3 grid((feats + fpc - 1) / fpc, a.umax);
   const size_t smem = (size_t)NT * K * sizeof(__nv_bfloat16);
-  ffn_gemv_kernel<FMT, DOWN, NT, LPR><<<grid, kWarps * 32, smem, s>>>(a, cb);
+  ffn_gemv_kernel<FMT, DOWN, NT, LPR><<<grid, kWarps * 32, smem, s>>>(a, cb, fpw);
   return cudaGetLastError();
 }
 
@@ -380,7 +384,7 @@ cudaError_t launch_ffn(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) 
 
 template <int FMT, bool DOWN, int NT>
 void attr_l() {
-  const int max_smem = NT * 8192 * 2;
+  const int max_smem = NT * 8192 * 2;   // activations of NT token rows, K <= 8192
   cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);

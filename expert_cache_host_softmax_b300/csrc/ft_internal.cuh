@@ -101,6 +101,7 @@ struct FfnArgs {
   int umax;
   int only;                   // 0 all, 1 hits only, 2 misses only
   int max_tokens;             // tokens of the call (no expert sees more)
+  int *err;                   // device error word: a bounded wait that gave up records its site
 };
 // Combine fused into the down GEMV (small calls): out[t] = sum_j gates[t][j] *
 // y[inv[t*k+j]], written by the last CTA of each feature tile.  counters: one
@@ -125,8 +126,11 @@ void ffn_init_attributes();
 void gemm_init_attributes();
 int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, int H, int I, void *map_gu,
                      void *map_d);
-cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_gu, const void *map_d, int *err,
-                          int64_t max_rows, cudaStream_t s);
+int make_act_map(const void *base, int64_t rows, int K, void *map);
+cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, int k, int H, int n, __nv_bfloat16 *xp,
+                               cudaStream_t s);
+cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const void *map_h, const void *map_gu,
+                          const void *map_d, int *err, int64_t max_rows, cudaStream_t s);
 
 // Sets the message ft_last_error(NULL) returns on this thread.
 void set_stateless_error(const std::string &msg);

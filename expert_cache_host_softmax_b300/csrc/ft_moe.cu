@@ -47,8 +47,10 @@ struct ft_moe {
   int32_t *mirror_host = nullptr, *mirror_dev = nullptr;
   std::vector<const void *> pool;
   bool pool_loaded = false;
-  cudaStream_t copy_stream = nullptr;
-  cudaEvent_t ev_route = nullptr, ev_copy = nullptr, ev_done = nullptr;
+  // miss copies alternate between two copy streams, so that one copy's
+  // set-up overlaps the previous copy's transfer; copy_stream joins both
+  cudaStream_t copy_stream = nullptr, copy_stream2 = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_copy = nullptr, ev_copy2 = nullptr, ev_done = nullptr;
   cudaEvent_t ev_bank_ready[2] = {nullptr, nullptr}, ev_bank_free[2] = {nullptr, nullptr};
   int bank_layer[2] = {-1, -1};
   uint32_t seq = 0;
@@ -66,7 +68,9 @@ struct ft_moe {
   int64_t kernel_launches = 0;
   // tensor-core FFN: TMA descriptors over the slot bank, the kernel choice,
   // and a device error word that bounded waits write when they give up
-  alignas(64) unsigned char tmap[2][128] = {};
+  alignas(64) unsigned char tmap[2][128] = {};     // weights: gate/up, down
+  alignas(64) unsigned char amap[2][128] = {};     // activations: permuted x rows, h
+  __nv_bfloat16 *xpbuf = nullptr;                  // x gathered into permuted order [Tmax*k][H]
   bool tmaps_ok = false;
   int ffn_kernel = FT_FFN_AUTO;
   int *err_dev = nullptr;
@@ -133,10 +137,12 @@ void free_all(ft_moe *h) {
   cudaFree(h->hbuf);
   cudaFree(h->ybuf);
   cudaFree(h->err_dev);
+  cudaFree(h->xpbuf);
   cudaFree(h->combine_counters);
   if (h->mirror_host) cudaFreeHost(h->mirror_host);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
-  for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
+  if (h->copy_stream2) cudaStreamDestroy(h->copy_stream2);
+  for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_copy2, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
                          h->ev_bank_free[0], h->ev_bank_free[1]})
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : h->prof_ev)
@@ -171,6 +177,7 @@ void prof_collect(ft_moe *h) {
 int sync_handle(ft_moe *h) {
   if (h->any_call) FT_CUDA(h, cudaEventSynchronize(h->ev_done));
   FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+  FT_CUDA(h, cudaStreamSynchronize(h->copy_stream2));
   int code = 0;
   FT_CUDA(h, cudaMemcpy(&code, h->err_dev, sizeof code, cudaMemcpyDeviceToHost));
   if (code != 0) {
@@ -193,7 +200,15 @@ bool use_tc(const ft_moe *h, int T) {
 
 cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cudaStream_t s,
                     const CombineArgs &cb = CombineArgs{}) {
-  if (tc) return launch_tc_ffn(fa, down, h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
+  if (tc) {
+    if (!down && fa.only != 2) {
+      // the permuted x rows, once per call (before the first gate/up launch)
+      cudaError_t e = launch_gather_rows(fa.x, fa.plan.perm, h->k, h->H, T * h->k, h->xpbuf, s);
+      if (e != cudaSuccess) return e;
+      h->kernel_launches += 1;
+    }
+    return launch_tc_ffn(fa, down, h->amap[0], h->amap[1], h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
+  }
   return down ? launch_down(fa, cb, s) : launch_gateup(fa, s);
 }
 
@@ -325,6 +340,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->chunk_base, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
+            dev_alloc(&h->xpbuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->combine_counters, combine_tiles(hidden)) == cudaSuccess &&
             cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(hidden)) == cudaSuccess;
   if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
@@ -336,8 +352,10 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
   }
   std::memset(h->mirror_host, 0, sizeof(int32_t) * (2 + 2 * (size_t)umax));
   ok = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) == cudaSuccess &&
+       cudaStreamCreateWithFlags(&h->copy_stream2, cudaStreamNonBlocking) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_route, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_copy, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_copy2, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_bank_ready[0], cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_bank_ready[1], cudaEventDisableTiming) == cudaSuccess &&
@@ -347,7 +365,9 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
   route_init_attributes();
   ffn_init_attributes();
   gemm_init_attributes();
-  h->tmaps_ok = make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0;
+  h->tmaps_ok = make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
+                make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
+                make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
   if (int rc = reset_tables(h, false)) { g_create_err = h->err; return bail(rc); }
   *out = h;
   return FT_OK;
@@ -447,6 +467,7 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.plan = h->plan;
   fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
   fa.max_tokens = n_tokens;
+  fa.err = h->err_dev;
   const bool tc = use_tc(h, n_tokens);
   h->last_tc = tc;
   if (h->mode == MODE_LRU) {
@@ -457,14 +478,21 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
     if (int rc = wait_plan(h)) return rc;
     const int n_miss = h->mirror_host[1];
     if (n_miss > 0) {
+      // both copy streams start after the route kernel (every earlier reader
+      // of an evicted slot has finished by then); misses alternate between them
       FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_route, 0));
+      if (n_miss > 1) FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream2, h->ev_route, 0));
       prof_begin(h, FT_PROF_MISS_COPY, h->copy_stream);
       for (int i = 0; i < n_miss; ++i) {
         const int key = h->mirror_host[2 + i], slot = h->mirror_host[2 + h->umax + i];
         if (key < 0 || key >= h->L * h->E || slot < 0 || slot >= h->S)
           return fail(h, FT_ERR_DEVICE, "miss list entry out of range");
         FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)slot * h->slot_stride, h->pool[key], h->blob_bytes,
-                                   cudaMemcpyHostToDevice, h->copy_stream));
+                                   cudaMemcpyHostToDevice, (i & 1) ? h->copy_stream2 : h->copy_stream));
+      }
+      if (n_miss > 1) {
+        FT_CUDA(h, cudaEventRecord(h->ev_copy2, h->copy_stream2));
+        FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_copy2, 0));
       }
       prof_end(h, FT_PROF_MISS_COPY, h->copy_stream);
       FT_CUDA(h, cudaEventRecord(h->ev_copy, h->copy_stream));

@@ -3,24 +3,25 @@
 //
 // Per distinct expert u of a call (blob in slot u_slot[u]; its tokens sit at
 // permuted positions offsets[e] .. offsets[e+1]):
-//   gate/up:  [g | u] = x_rows . W_gu^T   (fp32 accumulators in TMEM)
+//   gate/up:  [g | u] = xp_rows . W_gu^T  (fp32 accumulators in TMEM)
 //             h = bf16( silu(g) * u )     (epilogue)
 //   down:     y = h . W_d^T               (fp32)
-// The pages say only that cached experts run "at GPU speed" ("Why a Huge MoE
-// Model Fits on One Consumer GPU"); SwiGLU and this kernel design are ours.
+// xp is x gathered into permuted order (one row per (token, rank) pair) by a
+// small kernel first, so that both GEMMs read their token rows as plain
+// 128-row boxes.  The pages say only that cached experts run "at GPU speed"
+// ("Why a Huge MoE Model Fits on One Consumer GPU"); SwiGLU and this kernel
+// design are ours.
 //
 // One persistent CTA per SM walks the call's output tiles.  A tile is 128
 // token rows x 256 weight rows (gate/up: 128 gate rows + the 128 matching up
 // rows, so the SiLU*mul epilogue sees both halves; down: 256 rows of H).
 // K advances in blocks of 64 through a ring of shared-memory stages:
-//   - A (token rows, bf16) is gathered row by row with cp.async into the
-//     128-byte-swizzled K-major layout (gate/up rows come from x through the
-//     permutation; down rows are the contiguous h rows of the group);
-//   - B (weights) comes by TMA from the slot bank.  BF16 weights land directly
-//     in the swizzled layout.  NVFP4 / MXFP4 codes land raw; the loader warps
-//     dequantise them to bf16 (e2m1 x block scale, exact in bf16) into the
-//     swizzled B tile.  The NVFP4 per-matrix global scale is applied to the
-//     fp32 accumulator in the epilogue.
+//   - one producer thread issues, per stage, the TMA load of the A box (128
+//     token rows x 64, 128-byte swizzle) and of the weights: BF16 weights land
+//     directly in the swizzled layout; NVFP4 / MXFP4 codes land raw in a
+//     separate ring, and eight converter warps dequantise them to bf16
+//     (e2m1 x block scale, exact in bf16) into the swizzled B tile.  The NVFP4
+//     per-matrix global scale is applied to the fp32 accumulator in the epilogue.
 //   - one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> f32)
 //     into one of two TMEM accumulators (2 x 256 columns), so the epilogue of
 //     a tile overlaps the MMAs of the next;
@@ -56,25 +57,18 @@ struct Cfg {
   // stages of A + (bf16) B; FP4 also has a ring of raw-code stages
   static constexpr int kNS = kFp4 ? 3 : 4;
   static constexpr int kNR = kFp4 ? 4 : 0;
-  static constexpr int kLoadWarps = kFp4 ? 8 : 4;
-  static constexpr int kLoadThreads = kLoadWarps * 32;
-  static constexpr int kEpiWarp0 = kLoadWarps;               // multiple of 4: TMEM lane quarter = warp % 4
-  static constexpr int kMmaWarp = kLoadWarps + kEpiWarps;
-  static constexpr int kTmaWarp = kFp4 ? kMmaWarp + 1 : -1;  // FP4: raw-code TMA producer
-  static constexpr int kThreads = (kMmaWarp + 1 + (kFp4 ? 1 : 0)) * 32;
-  static constexpr int kChunksA = 8 * BM / kLoadThreads;    // 16-byte chunks of A per loader thread
-  // A stage is published (one FULL arrival per loader thread) kLag stages
-  // after its loads were issued, once the thread's own cp.async group has
-  // landed and been fenced for the tensor core's (async-proxy) reads.
-  static constexpr int kLag = kNS - 1;
-  static constexpr int kFullCount = kLoadThreads;
+  // warp roles: 0 producer, 1 MMA, 2-3 idle, 4-7 epilogue, 8-15 converters (FP4)
+  static constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 4, kConvWarp0 = 8;
+  static constexpr int kConvThreads = kFp4 ? 256 : 0;
+  static constexpr int kThreads = kFp4 ? 512 : 256;
+  // FULL arrivals per stage: the producer's expect_tx, plus (FP4) one per converter thread
+  static constexpr int kFullCount = 1 + kConvThreads;
   // shared memory: [A x kNS][B x kNS][RAW x kNR] then barriers and tables
   static constexpr int kOffB = kNS * A_STAGE;
   static constexpr int kOffRaw = kOffB + kNS * B_STAGE;
   static constexpr int kOffBar = kOffRaw + kNR * RAW_STAGE;
-  // barriers: FULL, BFULL, EMPTY (kNS each), RAWFULL, RAWEMPTY (kNR each),
-  // TFULL x2, TEMPTY x2, DRAIN
-  static constexpr int kBars = 3 * kNS + 2 * kNR + 5;
+  // barriers: FULL, EMPTY (kNS each), RAWFULL, RAWEMPTY (kNR each), TFULL x2, TEMPTY x2, DRAIN
+  static constexpr int kBars = 2 * kNS + 2 * kNR + 5;
   static constexpr int kOffTab = kOffBar + kBars * 8 + 16;
   static constexpr int kSmem = kOffTab + 4 * (2 * (kMaxU + 1)) + 64;
   static constexpr int kSmemAlloc = kSmem + 1024;             // room to align the base to 1024
@@ -149,15 +143,6 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
@@ -166,6 +151,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
       "[%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -307,7 +300,7 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int *s_start, const
 
 template <int FMT, bool DOWN>
 __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
-    gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmB) {
+    gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
   using C = Cfg<FMT>;
   constexpr int NS = C::kNS, NR = C::kNR;
   extern __shared__ unsigned char smem_raw[];
@@ -316,14 +309,13 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
   unsigned char *sm = smem_raw + (base - raw_base);
   const uint32_t sA = base, sB = base + C::kOffB, sRaw = base + C::kOffRaw;
   const uint32_t bar0 = base + C::kOffBar;
-  auto FULL = [&](int s) { return bar0 + 8u * s; };                    // A (and converted B) landed
-  auto BFULL = [&](int s) { return bar0 + 8u * (NS + s); };            // bf16 B landed (TMA)
-  auto EMPTY = [&](int s) { return bar0 + 8u * (2 * NS + s); };        // stage consumed by the MMAs
-  auto RAWFULL = [&](int r) { return bar0 + 8u * (3 * NS + r); };      // FP4 codes landed (TMA)
-  auto RAWEMPTY = [&](int r) { return bar0 + 8u * (3 * NS + NR + r); };  // FP4 codes converted
-  auto TFULL = [&](int b) { return bar0 + 8u * (3 * NS + 2 * NR + b); };
-  auto TEMPTY = [&](int b) { return bar0 + 8u * (3 * NS + 2 * NR + 2 + b); };
-  const uint32_t DRAIN = bar0 + 8u * (3 * NS + 2 * NR + 4);
+  auto FULL = [&](int s) { return bar0 + 8u * s; };                    // A (and B) of a stage landed
+  auto EMPTY = [&](int s) { return bar0 + 8u * (NS + s); };            // stage consumed by the MMAs
+  auto RAWFULL = [&](int r) { return bar0 + 8u * (2 * NS + r); };      // FP4 codes landed
+  auto RAWEMPTY = [&](int r) { return bar0 + 8u * (2 * NS + NR + r); };  // FP4 codes converted
+  auto TFULL = [&](int b) { return bar0 + 8u * (2 * NS + 2 * NR + b); };
+  auto TEMPTY = [&](int b) { return bar0 + 8u * (2 * NS + 2 * NR + 2 + b); };
+  const uint32_t DRAIN = bar0 + 8u * (2 * NS + 2 * NR + 4);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + C::kOffBar + C::kBars * 8);
   volatile int *s_abort = reinterpret_cast<volatile int *>(sm + C::kOffBar + C::kBars * 8 + 4);
   int *s_start = reinterpret_cast<int *>(sm + C::kOffTab);
@@ -338,12 +330,11 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(FULL(s), C::kFullCount);
-      mbar_init(BFULL(s), 1);
       mbar_init(EMPTY(s), 1);
     }
     for (int r = 0; r < NR; ++r) {
       mbar_init(RAWFULL(r), 1);
-      mbar_init(RAWEMPTY(r), C::kLoadThreads);
+      mbar_init(RAWEMPTY(r), C::kConvThreads);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(TFULL(b), 1);
@@ -355,7 +346,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
   }
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(s_tmem), kTmemCols);
   const int nU = a.plan.n[0];
-  if (warp == 0) {
+  if (warp == C::kEpiWarp0) {
     // per distinct expert: M tiles (0 when filtered out); exclusive prefix in s_start
     int run = 0;
     for (int u0 = 0; u0 < nU; u0 += 32) {
@@ -386,168 +377,127 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
   const uint32_t tmem_base = *s_tmem;
   const int n_tiles = s_start[nU] * NTN;
 
-  if (warp < C::kLoadWarps) {
-    // ================================================================ loaders
-    // Stage j: publish stage j - kLag (this thread's A chunks for it have
-    // landed: cp.async.wait_group; fence for the async proxy; arrive on FULL),
-    // then wait for slot j, issue its A row chunks by cp.async, and (BF16)
-    // thread 0 issues its B tile by TMA, or (FP4) every thread dequantises one
-    // B row from the raw codes into the swizzled bf16 tile right away.
-    // Publishing before the slot wait keeps the MMA fed: slot j frees when the
-    // MMA finishes stage j - kNS, which was published kNS - kLag >= 1 stages ago.
-    constexpr int LAG = C::kLag;
-    const int t = tid;
-    const int arow = t % BM;
-    const int achunk0 = (t / BM) * C::kChunksA;
-    const BlobLayout L = blob_layout(FMT, a.H, a.I);
-    uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_nxt = make_uint4(0, 0, 0, 0);
-    int j = 0;  // stage counter across tiles
-    bool ok = true;
-    auto publish = [&](int jj) {
-      fence_proxy_async();
-      mbar_arrive(FULL(jj % NS));
-    };
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
-      // this thread's A source row (rows past the group repeat its last row;
-      // their results are never stored)
-      const int r = ti.row0 + min(arow, ti.rows - 1);
-      const __nv_bfloat16 *asrc;
-      if constexpr (DOWN) asrc = a.h + (size_t)r * a.I;
-      else asrc = a.x + (size_t)(a.plan.perm[r] / a.k) * a.H;
-      // FP4: this thread's B row in the blob (gate/up: 128 gate rows, then the 128 matching up rows)
-      const uint8_t *sf_row = nullptr;
-      if constexpr (C::kFp4) {
-        const int brow =
-            DOWN ? ti.n * BN + t : (t < BN / 2 ? ti.n * (BN / 2) + t : a.I + ti.n * (BN / 2) + (t - BN / 2));
-        const int sf_per_row = K / (FMT == FMT_NVFP4 ? 16 : 32);
-        sf_row = a.slot_bank + (size_t)ti.slot * a.slot_stride + (DOWN ? L.d_sf : L.gu_sf) +
-                 (size_t)brow * sf_per_row;
-      }
-      for (int kb = 0; kb < nk; ++kb, ++j) {
-        if (j >= LAG) {
-          cp_async_wait<LAG - 1>();   // groups j-LAG+1 .. j-1 may still be in flight
-          publish(j - LAG);
-        }
-        const int s = j % NS;
-        if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 10)) { ok = false; break; }
-        if constexpr (!C::kFp4) {
-          if (t == 0) {
-            mbar_arrive_expect_tx(BFULL(s), B_STAGE);
-            const uint32_t dst = sB + s * B_STAGE;
-            if (DOWN) {
-              tma_load_3d(dst, &tmB, BFULL(s), kb * BK, ti.n * BN, ti.slot);
-              tma_load_3d(dst + B_STAGE / 2, &tmB, BFULL(s), kb * BK, ti.n * BN + BN / 2, ti.slot);
-            } else {
-              tma_load_3d(dst, &tmB, BFULL(s), kb * BK, ti.n * (BN / 2), ti.slot);
-              tma_load_3d(dst + B_STAGE / 2, &tmB, BFULL(s), kb * BK, a.I + ti.n * (BN / 2), ti.slot);
-            }
-          }
-        }
-        // A: this thread's chunks of its row, swizzled (chunk c of row r at c ^ (r & 7))
-        const uint32_t adst = sA + s * A_STAGE + arow * 128;
-        const char *src = reinterpret_cast<const char *>(asrc + (size_t)kb * BK);
-#pragma unroll
-        for (int c = 0; c < C::kChunksA; ++c) {
-          const int cc = achunk0 + c;
-          cp_async16(adst + ((cc ^ (arow & 7)) << 4), src + cc * 16);
-        }
-        cp_async_commit();
-        if constexpr (C::kFp4) {
-          // block scales of the 4 stages of group kb/4 (NVFP4: 16 bytes, MXFP4:
-          // 8 bytes), loaded one group ahead
-          constexpr int per = FMT == FMT_NVFP4 ? 4 : 2;   // scale bytes per stage
-          auto load_group = [&](int g) -> uint4 {
-            if (FMT == FMT_NVFP4) return __ldg(reinterpret_cast<const uint4 *>(sf_row + g * 4 * per));
-            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(sf_row + g * 4 * per));
-            return make_uint4(v.x, v.y, 0, 0);
-          };
-          if (kb == 0) sc_nxt = load_group(0);
-          if ((kb & 3) == 0) {
-            sc_cur = sc_nxt;
-            if (kb + 4 < nk) sc_nxt = load_group(kb / 4 + 1);
-          }
-          const int sub = kb & 3;
-          float sc[4];
-          if constexpr (FMT == FMT_NVFP4) {
-            const uint32_t word = sub == 0 ? sc_cur.x : sub == 1 ? sc_cur.y : sub == 2 ? sc_cur.z : sc_cur.w;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) sc[i] = e4m3_to_float((word >> (8 * i)) & 0xFFu);
-          } else {
-            const uint32_t word = (sub >> 1) == 0 ? sc_cur.x : sc_cur.y;
-            const uint32_t pair = (word >> (16 * (sub & 1))) & 0xFFFFu;
-            sc[0] = sc[1] = e8m0_to_float(pair & 0xFFu);
-            sc[2] = sc[3] = e8m0_to_float(pair >> 8);
-          }
-          const int rs = j % NR;
-          if (!mbar_wait(RAWFULL(rs), (j / NR) & 1, s_abort, a.err, 11)) { ok = false; ++j; break; }
-          const uint32_t raw = sRaw + rs * RAW_STAGE + t * 32;
-          uint4 q0, q1;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(q0.x), "=r"(q0.y), "=r"(q0.z), "=r"(q0.w)
-                       : "r"(raw)
-                       : "memory");
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(q1.x), "=r"(q1.y), "=r"(q1.z), "=r"(q1.w)
-                       : "r"(raw + 16)
-                       : "memory");
-          const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          const uint32_t bdst = sB + s * B_STAGE + t * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = dequant8(w[c], sc[c >> 1]);
-            const uint32_t d = bdst + ((c ^ (t & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v.x), "r"(v.y), "r"(v.z),
-                         "r"(v.w)
-                         : "memory");
-          }
-          // the raw codes have been consumed (the stores above depend on them):
-          // the producer may now refill this raw slot
-          mbar_arrive(RAWEMPTY(rs));
-        }
-      }
-    }
-    // publish the stages still pending, and exit with no copy of ours in flight
-    cp_async_wait_all();
-    if (ok)
-      for (int jj = max(0, j - LAG); jj < j; ++jj) publish(jj);
-    if (!C::kFp4 && t == 0) {
-      for (int jj = max(0, j - NS); jj < j; ++jj) {
-        const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(BFULL(jj % NS), (jj / NS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
-        }
-      }
-    }
-  } else if (C::kFp4 && warp == C::kTmaWarp) {
-    // ================================================================ FP4 code producer
+  if (warp == C::kProdWarp) {
+    // ================================================================ producer
+    // Per stage: wait for the slot; one expect_tx for the stage's TMA bytes;
+    // A box (128 permuted rows x 64 K) and, for BF16, the two halves of the
+    // weight tile; for FP4, the raw codes into their own ring.
     if (lane == 0) {
       int j = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
+        const int r0 = DOWN ? ti.n * BN : ti.n * (BN / 2);            // first weight row (gate rows for gate/up)
+        const int r1 = DOWN ? ti.n * BN + BN / 2 : a.I + ti.n * (BN / 2);  // second half (up rows)
         for (int kb = 0; kb < nk; ++kb, ++j) {
-          const int rs = j % NR;
-          if (!mbar_wait(RAWEMPTY(rs), ((j / NR) & 1) ^ 1, s_abort, a.err, 40)) { ok = false; break; }
-          fence_proxy_async();   // the converters' reads of this slot precede the TMA's writes
-          mbar_arrive_expect_tx(RAWFULL(rs), RAW_STAGE);
-          const uint32_t dst = sRaw + rs * RAW_STAGE;
-          if (DOWN) {
-            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * (BK / 2), ti.n * BN, ti.slot);
-            tma_load_3d(dst + RAW_STAGE / 2, &tmB, RAWFULL(rs), kb * (BK / 2), ti.n * BN + BN / 2, ti.slot);
+          const int s = j % NS;
+          if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 10)) { ok = false; break; }
+          mbar_arrive_expect_tx(FULL(s), A_STAGE + (C::kFp4 ? 0 : B_STAGE));
+          tma_load_2d(sA + s * A_STAGE, &tmA, FULL(s), kb * BK, ti.row0);
+          if constexpr (!C::kFp4) {
+            const uint32_t dst = sB + s * B_STAGE;
+            tma_load_3d(dst, &tmB, FULL(s), kb * BK, r0, ti.slot);
+            tma_load_3d(dst + B_STAGE / 2, &tmB, FULL(s), kb * BK, r1, ti.slot);
           } else {
-            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * (BK / 2), ti.n * (BN / 2), ti.slot);
-            tma_load_3d(dst + RAW_STAGE / 2, &tmB, RAWFULL(rs), kb * (BK / 2), a.I + ti.n * (BN / 2), ti.slot);
+            const int rs = j % NR;
+            if (!mbar_wait(RAWEMPTY(rs), ((j / NR) & 1) ^ 1, s_abort, a.err, 11)) { ok = false; ++j; break; }
+            fence_proxy_async();   // the converters' reads of this slot precede the TMA's writes
+            mbar_arrive_expect_tx(RAWFULL(rs), RAW_STAGE);
+            const uint32_t dst = sRaw + rs * RAW_STAGE;
+            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * (BK / 2), r0, ti.slot);
+            tma_load_3d(dst + RAW_STAGE / 2, &tmB, RAWFULL(rs), kb * (BK / 2), r1, ti.slot);
           }
         }
       }
       // every TMA this CTA issued must land before the CTA exits
-      for (int jj = max(0, j - NR); jj < j; ++jj) {
+      for (int jj = max(0, j - NS); jj < j; ++jj) {
         const unsigned long long t0 = globaltimer();
-        while (!mbar_try_wait(RAWFULL(jj % NR), (jj / NR) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(FULL(jj % NS), (jj / NS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
+      }
+      if constexpr (C::kFp4) {
+        for (int jj = max(0, j - NR); jj < j; ++jj) {
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait(RAWFULL(jj % NR), (jj / NR) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+          }
         }
       }
     }
     __syncwarp();
+  } else if (C::kFp4 && warp >= C::kConvWarp0) {
+    // ================================================================ FP4 converters
+    // Each thread dequantises one B row per stage from the raw codes into the
+    // swizzled bf16 tile (chunk c of row t at c ^ (t & 7)).
+    const int t = tid - C::kConvWarp0 * 32;
+    const BlobLayout L = blob_layout(FMT, a.H, a.I);
+    uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_nxt = make_uint4(0, 0, 0, 0);
+    int j = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
+      // this thread's B row in the blob (gate/up: 128 gate rows, then the 128 matching up rows)
+      const int brow =
+          DOWN ? ti.n * BN + t : (t < BN / 2 ? ti.n * (BN / 2) + t : a.I + ti.n * (BN / 2) + (t - BN / 2));
+      const int sf_per_row = K / (FMT == FMT_NVFP4 ? 16 : 32);
+      const uint8_t *sf_row = a.slot_bank + (size_t)ti.slot * a.slot_stride + (DOWN ? L.d_sf : L.gu_sf) +
+                              (size_t)brow * sf_per_row;
+      for (int kb = 0; kb < nk; ++kb, ++j) {
+        const int s = j % NS;
+        // block scales of the 4 stages of group kb/4 (NVFP4: 16 bytes, MXFP4:
+        // 8 bytes), loaded one group ahead
+        constexpr int per = FMT == FMT_NVFP4 ? 4 : 2;   // scale bytes per stage
+        auto load_group = [&](int g) -> uint4 {
+          if (FMT == FMT_NVFP4) return __ldg(reinterpret_cast<const uint4 *>(sf_row + g * 4 * per));
+          const uint2 v = __ldg(reinterpret_cast<const uint2 *>(sf_row + g * 4 * per));
+          return make_uint4(v.x, v.y, 0, 0);
+        };
+        if (kb == 0) sc_nxt = load_group(0);
+        if ((kb & 3) == 0) {
+          sc_cur = sc_nxt;
+          if (kb + 4 < nk) sc_nxt = load_group(kb / 4 + 1);
+        }
+        const int sub = kb & 3;
+        float sc[4];
+        if constexpr (FMT == FMT_NVFP4) {
+          const uint32_t word = sub == 0 ? sc_cur.x : sub == 1 ? sc_cur.y : sub == 2 ? sc_cur.z : sc_cur.w;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sc[i] = e4m3_to_float((word >> (8 * i)) & 0xFFu);
+        } else {
+          const uint32_t word = (sub >> 1) == 0 ? sc_cur.x : sc_cur.y;
+          const uint32_t pair = (word >> (16 * (sub & 1))) & 0xFFFFu;
+          sc[0] = sc[1] = e8m0_to_float(pair & 0xFFu);
+          sc[2] = sc[3] = e8m0_to_float(pair >> 8);
+        }
+        // the B slot is free once the MMAs of stage j - NS are done
+        if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 12)) { ok = false; break; }
+        const int rs = j % NR;
+        if (!mbar_wait(RAWFULL(rs), (j / NR) & 1, s_abort, a.err, 13)) { ok = false; break; }
+        const uint32_t raw = sRaw + rs * RAW_STAGE + t * 32;
+        uint4 q0, q1;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(q0.x), "=r"(q0.y), "=r"(q0.z), "=r"(q0.w)
+                     : "r"(raw)
+                     : "memory");
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(q1.x), "=r"(q1.y), "=r"(q1.z), "=r"(q1.w)
+                     : "r"(raw + 16)
+                     : "memory");
+        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint32_t bdst = sB + s * B_STAGE + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = dequant8(w[c], sc[c >> 1]);
+          const uint32_t d = bdst + ((c ^ (t & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+        // the raw codes have been consumed (the stores above depend on them):
+        // the producer may refill this raw slot
+        mbar_arrive(RAWEMPTY(rs));
+        fence_proxy_async();   // this thread's B row is visible to the tensor core's reads
+        mbar_arrive(FULL(s));
+      }
+    }
   } else if (warp == C::kMmaWarp) {
     // ================================================================ MMA issuer
     if (lane == 0) {
@@ -560,8 +510,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         const uint32_t d = tmem_base + b * BN;
         for (int kb = 0; kb < nk; ++kb, ++j) {
           const int s = j % NS;
-          if (!mbar_wait(FULL(s), (j / NS) & 1, s_abort, a.err, 21) ||
-              (!C::kFp4 && !mbar_wait(BFULL(s), (j / NS) & 1, s_abort, a.err, 22))) {
+          if (!mbar_wait(FULL(s), (j / NS) & 1, s_abort, a.err, 21)) {
             ok = false;
             break;
           }
@@ -674,16 +623,30 @@ void set_attr() {
 }
 
 template <int FMT, bool DOWN>
-cudaError_t launch(const GemmArgs &a, const CUtensorMap &map, int grid, cudaStream_t s) {
-  gemm_kernel<FMT, DOWN><<<grid, Cfg<FMT>::kThreads, Cfg<FMT>::kSmemAlloc, s>>>(a, map);
+cudaError_t launch(const GemmArgs &a, const CUtensorMap &mapA, const CUtensorMap &mapB, int grid, cudaStream_t s) {
+  gemm_kernel<FMT, DOWN><<<grid, Cfg<FMT>::kThreads, Cfg<FMT>::kSmemAlloc, s>>>(a, mapA, mapB);
   return cudaGetLastError();
+}
+
+// xp[i] = x[perm[i] / k] for the n permuted rows (bf16 rows of H).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                          const int32_t *__restrict__ perm, int k, int H, int n,
+                                                          __nv_bfloat16 *__restrict__ xp) {
+  const int vec = H / 8;
+  const long long total = (long long)n * vec;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i / vec), v = (int)(i - (long long)r * vec);
+    const uint4 val = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(perm[r] / k) * H) + v);
+    reinterpret_cast<uint4 *>(xp + (size_t)r * H)[v] = val;
+  }
 }
 
 }  // namespace
 
 static_assert(Cfg<FMT_BF16>::kSmemAlloc <= 227 * 1024, "bf16 smem");
 static_assert(Cfg<FMT_NVFP4>::kSmemAlloc <= 227 * 1024, "fp4 smem");
-static_assert(Cfg<FMT_NVFP4>::kThreads == 448 && Cfg<FMT_BF16>::kThreads == 288, "warp roles");
+static_assert(Cfg<FMT_NVFP4>::kThreads == 512 && Cfg<FMT_BF16>::kThreads == 256, "warp roles");
 
 int tc_num_sms() {
   static int n = 0;
@@ -703,6 +666,19 @@ void gemm_init_attributes() {
   set_attr<FMT_NVFP4, true>();
   set_attr<FMT_MXFP4, false>();
   set_attr<FMT_MXFP4, true>();
+}
+
+// Tensor map over a bf16 activation matrix [rows][K] (the permuted x rows,
+// or h): box of 64 K x 128 rows with the 128-byte swizzle.
+int make_act_map(const void *base, int64_t rows, int K, void *map) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return -1;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows}, strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {BK, BM}, estr[2] = {1, 1};
+  CUresult r = enc(reinterpret_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
 // Tensor maps over the slot bank: 3-D (K, rows, slot).  BF16: box 64 x 128
@@ -742,10 +718,21 @@ int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, 
   return 0;
 }
 
+// Gathers x into permuted order for the gate/up GEMM (rows = T*k pairs).
+cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, int k, int H, int n, __nv_bfloat16 *xp,
+                               cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const long long total = (long long)n * (H / 8);
+  const int grid = (int)std::min<long long>((total + 255) / 256, 148LL * 16);
+  gather_rows_kernel<<<grid, 256, 0, s>>>(x, perm, k, H, n, xp);
+  return cudaGetLastError();
+}
+
 // Grouped gate/up (down=false) or down (down=true) FFN of the call's experts on
-// the tensor cores.  `max_tiles` bounds the CTAs launched.
-cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_gu, const void *map_d, int *err,
-                          int64_t max_rows, cudaStream_t s) {
+// the tensor cores.  map_xp / map_h: activation maps (make_act_map) over the
+// permuted x rows and over h; map_gu / map_d: the slot-bank weight maps.
+cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const void *map_h, const void *map_gu,
+                          const void *map_d, int *err, int64_t max_rows, cudaStream_t s) {
   GemmArgs a{};
   a.slot_bank = f.slot_bank;
   a.slot_stride = f.slot_stride;
@@ -759,11 +746,13 @@ cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_gu, const
   // M tiles <= ceil(rows / BM) + distinct experts
   const int64_t mtiles = (max_rows + BM - 1) / BM + f.umax;
   const int grid = (int)std::min<int64_t>(tc_num_sms(), std::max<int64_t>(1, mtiles * NTN));
-  const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(down ? map_d : map_gu);
+  const CUtensorMap &mA = *reinterpret_cast<const CUtensorMap *>(down ? map_h : map_xp);
+  const CUtensorMap &mB = *reinterpret_cast<const CUtensorMap *>(down ? map_d : map_gu);
   switch (f.fmt) {
-    case FMT_BF16: return down ? launch<FMT_BF16, true>(a, m, grid, s) : launch<FMT_BF16, false>(a, m, grid, s);
-    case FMT_NVFP4: return down ? launch<FMT_NVFP4, true>(a, m, grid, s) : launch<FMT_NVFP4, false>(a, m, grid, s);
-    default: return down ? launch<FMT_MXFP4, true>(a, m, grid, s) : launch<FMT_MXFP4, false>(a, m, grid, s);
+    case FMT_BF16: return down ? launch<FMT_BF16, true>(a, mA, mB, grid, s) : launch<FMT_BF16, false>(a, mA, mB, grid, s);
+    case FMT_NVFP4:
+      return down ? launch<FMT_NVFP4, true>(a, mA, mB, grid, s) : launch<FMT_NVFP4, false>(a, mA, mB, grid, s);
+    default: return down ? launch<FMT_MXFP4, true>(a, mA, mB, grid, s) : launch<FMT_MXFP4, false>(a, mA, mB, grid, s);
   }
 }
 

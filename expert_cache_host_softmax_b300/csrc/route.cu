@@ -63,50 +63,66 @@ __device__ int block_excl_scan(int v, int *s_warp, int *total) {
   return base + x - v;
 }
 
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key); +0 and -0 map to the same key.  key_of(-inf) = 0x007FFFFF > 0, so a
+// key of 0 marks "taken or padding".
+__device__ __forceinline__ uint32_t key_of(float x) {
+  if (x == 0.0f) x = 0.0f;
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float float_of(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // One warp selects the k largest logits of one token (ties to the lower id,
-// NaN treated as -inf) and writes their ids and softmax gates.  Returns, in
-// lanes 0..k-1, the selected expert of rank `lane` (else -1).
-__device__ int warp_topk_softmax(const float *__restrict__ row, int E, int k, int32_t *out_idx,
-                                 float *out_gate) {
+// NaN treated as -inf) and writes their ids and softmax gates.  Lane l holds
+// experts l, l+32, ..; each round takes the warp-wide largest key (redux.sync)
+// and, among lanes holding it, the lowest expert id (a second redux).
+// Returns, in lanes 0..k-1, the selected expert of rank `lane` (else -1).
+template <int NV>
+__device__ int warp_topk_softmax_t(const float *__restrict__ row, int E, int k, int32_t *out_idx, float *out_gate) {
   const int lane = threadIdx.x & 31;
-  float v[kMaxExperts / 32];
+  uint32_t key[NV];
 #pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
     float x = e < E ? __ldg(row + e) : -INFINITY;
-    v[i] = isnan(x) ? -INFINITY : x;
+    if (isnan(x)) x = -INFINITY;
+    key[i] = e < E ? key_of(x) : 0u;
   }
-  unsigned taken = 0;
+  auto local_best = [&](uint32_t &bk, int &bi) {
+    bk = 0u;
+    bi = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (key[i] > bk) {   // strict: the lowest i (lowest id) keeps a tie
+        bk = key[i];
+        bi = i;
+      }
+  };
+  uint32_t bk;
+  int bi;
+  local_best(bk, bi);
   float my_v = -INFINITY;
   int my_i = -1;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = bk == m ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    if (lane == (int)(win & 31u)) {
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
-      }
+      for (int i = 0; i < NV; ++i)
+        if (i == (int)(win >> 5)) key[i] = 0u;
+      local_best(bk, bi);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == j) {
-      my_v = bv;
-      my_i = bi;
+      my_v = float_of(m);
+      my_i = (int)win;
     }
   }
-  const float m = __shfl_sync(0xffffffffu, my_v, 0);
-  float z = lane < k ? expf(my_v - m) : 0.0f;
+  const float mx = __shfl_sync(0xffffffffu, my_v, 0);
+  float z = lane < k ? expf(my_v - mx) : 0.0f;
   float sum = z;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -117,11 +133,39 @@ __device__ int warp_topk_softmax(const float *__restrict__ row, int E, int k, in
   return lane < k ? my_i : -1;
 }
 
+__device__ __forceinline__ int warp_topk_softmax(const float *__restrict__ row, int E, int k, int32_t *out_idx,
+                                                 float *out_gate) {
+  if (E <= 32) return warp_topk_softmax_t<1>(row, E, k, out_idx, out_gate);
+  if (E <= 64) return warp_topk_softmax_t<2>(row, E, k, out_idx, out_gate);
+  if (E <= 128) return warp_topk_softmax_t<4>(row, E, k, out_idx, out_gate);
+  if (E <= 256) return warp_topk_softmax_t<8>(row, E, k, out_idx, out_gate);
+  return warp_topk_softmax_t<kMaxExperts / 32>(row, E, k, out_idx, out_gate);
+}
+
 // Stable scatter of pairs [p0, p1) by expert.  s_base[e] is the next free
 // permuted position of expert e and is advanced.  s_wcnt holds nwarps*E ints.
 __device__ void block_rank_scatter(const int32_t *__restrict__ idx, int p0, int p1, int E, int *s_base,
                                    int *s_wcnt, int32_t *__restrict__ perm, int32_t *__restrict__ inv) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
+  if (p1 - p0 <= 32) {
+    // one warp: rank among equal ids by lane order
+    if (w == 0) {
+      const int p = p0 + lane;
+      int e = p < p1 ? idx[p] : -1;
+      const bool valid = e >= 0 && e < E;
+      if (!valid) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (valid) {
+        const int pos = s_base[e] + __popc(peers & lanemask_lt());
+        perm[pos] = p;
+        inv[p] = pos;
+      }
+      __syncwarp();
+      if (valid && lane == __ffs(peers) - 1) s_base[e] += __popc(peers);
+    }
+    __syncthreads();
+    return;
+  }
   for (int r0 = p0; r0 < p1; r0 += blockDim.x) {
     for (int i = tid; i < nw * E; i += blockDim.x) s_wcnt[i] = 0;
     __syncthreads();
@@ -157,7 +201,7 @@ struct PlanSmem {
   int *s_uexp;    // [E]
   int *s_victim;  // [E]
   unsigned *s_bits;  // [(S+31)/32]
-  int *s_warp;    // [32]
+  int *s_warp;    // [33]: scan partials, [32] a counter
   int *s_keyslot;    // [E] this layer's key -> slot, loaded up front (or null)
   int *s_victim_key; // [E] key held by each victim slot (with s_keyslot)
 };
@@ -169,11 +213,14 @@ constexpr int kPre = 8;
 struct Prefetch {
   int n;              // entries held, or -1 (range longer than kPre: read in place)
   int ord[kPre], key[kPre];
+  unsigned long long st[5];   // thread 0: the cumulative counters
 };
 
 __device__ __forceinline__ void prefetch_tables(const RouteArgs &a, int *s_keyslot, Prefetch &pf) {
   const int tid = threadIdx.x, NT = blockDim.x;
   pf.n = -1;
+  if (tid == 0)
+    for (int i = 0; i < 5; ++i) pf.st[i] = a.cache.stats[i];
   if (a.mode != MODE_LRU) return;
   for (int e = tid; e < a.E; e += NT) s_keyslot[e] = a.cache.key_slot[a.layer * a.E + e];
   const int per = (a.S + NT - 1) / NT;
@@ -279,8 +326,12 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm, const Prefetc
       }
     }
   }
-  int nEv;
-  block_excl_scan(evicted >= 0, sm.s_warp, &nEv);
+  // evictions of this call: a count in shared memory (no order needed)
+  if (tid == 0) sm.s_warp[32] = 0;
+  __syncthreads();
+  if (evicted >= 0) atomicAdd(&sm.s_warp[32], 1);
+  __syncthreads();
+  const int nEv = sm.s_warp[32];
   if (tid < nU) {
     a.plan.u_expert[tid] = sm.s_uexp[tid];
     a.plan.u_slot[tid] = slot;
@@ -299,7 +350,6 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm, const Prefetc
       a.mirror[1] = nM;
       __threadfence_system();
       *(volatile int32_t *)&a.mirror[0] = (int32_t)a.seq;
-      __threadfence_system();
     }
     a.plan.n[0] = nU;
     a.plan.n[1] = nH;
@@ -308,7 +358,8 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm, const Prefetc
     unsigned long long *st = a.cache.stats;
     const unsigned long long bytes = a.mode == MODE_LRU ? (unsigned long long)nM * a.blob_bytes : 0ull;
     const unsigned long long hits_ = a.mode == MODE_LRU ? nH : 0, miss_ = a.mode == MODE_LRU ? nM : 0;
-    st[0] += nU; st[1] += hits_; st[2] += miss_; st[3] += nEv; st[4] += bytes;
+    st[0] = pf.st[0] + nU; st[1] = pf.st[1] + hits_; st[2] = pf.st[2] + miss_; st[3] = pf.st[3] + nEv;
+    st[4] = pf.st[4] + bytes;
     st[8] = nU; st[9] = hits_; st[10] = miss_; st[11] = nEv; st[12] = bytes;
   }
 }
@@ -327,8 +378,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
   int *s_victim = s_uexp + E;          // E
   int *s_keyslot = s_victim + E;       // E
   int *s_victim_key = s_keyslot + E;   // E
-  int *s_warp = s_victim_key + E;      // 32
-  int *s_wcnt = s_warp + 32;           // nw*E
+  int *s_warp = s_victim_key + E;      // 33
+  int *s_wcnt = s_warp + 33;           // nw*E
   unsigned *s_bits = (unsigned *)(s_wcnt + nw * E);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   Prefetch pf;
@@ -396,8 +447,8 @@ __global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int wi
   int *s_count = smem;
   int *s_uexp = s_count + E;
   int *s_victim = s_uexp + E;
-  int *s_warp = s_victim + E;
-  unsigned *s_bits = (unsigned *)(s_warp + 32);
+  int *s_warp = s_victim + E;          // 33
+  unsigned *s_bits = (unsigned *)(s_warp + 33);
   const int tid = threadIdx.x;
   int cnt = 0;
   if (tid < E)
@@ -419,6 +470,8 @@ __global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int wi
     PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, nullptr, nullptr};
     Prefetch pf;
     pf.n = -1;
+    if (tid == 0)
+      for (int i = 0; i < 5; ++i) pf.st[i] = a.cache.stats[i];
     block_plan(a, sm, pf);
   }
 }
@@ -442,10 +495,10 @@ int small_threads(int E) { return std::min(kRouteThreads, std::max(256, (E + 31)
 
 size_t small_smem_bytes(int E, int S) {
   const size_t nw = small_threads(E) / 32;
-  return sizeof(int) * (6 * (size_t)E + 32 + nw * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
+  return sizeof(int) * (6 * (size_t)E + 33 + nw * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
 }
 size_t plan_smem_bytes(int E, int S) {
-  return sizeof(int) * (3 * (size_t)E + 32) + sizeof(unsigned) * (((size_t)S + 31) / 32);
+  return sizeof(int) * (3 * (size_t)E + 33) + sizeof(unsigned) * (((size_t)S + 31) / 32);
 }
 
 }  // namespace
