@@ -308,6 +308,8 @@ def run_ours(args, cfg):
         stack.set_mode(F.FT_MODE_STREAM)
     if args.ffn != "auto":
         stack.set_ffn_kernel(args.ffn)
+    if args.miss_path != "copy":
+        stack.set_miss_path(args.miss_path)
 
     W, K = args.warmup, args.steps
     n_prof = min(args.profile_steps, K)
@@ -507,7 +509,7 @@ def run_ours(args, cfg):
         "data": "synthetic",
         "config": {"workload": cfg["name"], "layers": L, "hidden": H, "experts": E, "top_k": k, "inter": I,
                    "weight_fmt": fmt, "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
-                   "mode": cfg["mode"], "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
+                   "mode": cfg["mode"], "miss_path": args.miss_path, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
                    "pool": f"{n_keys} logical experts over {n_phys} distinct pinned blobs ({n_phys * nb / 1e9:.2f} GB)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": L * T * (H * 2 + E * 4),
                 "d2h_bytes_per_step": L * T * H * 2},
@@ -543,6 +545,8 @@ def main():
     ap.add_argument("--fmt", choices=("bf16", "nvfp4", "mxfp4"), default=None,
                     help="weight format (default: the workload's)")
     ap.add_argument("--ffn", choices=("auto", "gemv", "tc"), default="auto", help="FFN kernel")
+    ap.add_argument("--miss-path", choices=("copy", "pull"), default="copy",
+                    help="LRU misses: cudaMemcpyAsync on copy streams, or read over PCIe by the FFN kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -177,10 +177,26 @@ __device__ __forceinline__ RowPtrs row_ptrs(const uint8_t *blob, const BlobLayou
 // Dot products of NROWS weight rows (gate/up: 2, down: 1) with NT staged
 // activation rows, over this lane's chunks l, l+LPR, l+2 LPR, ... of K.  Loads
 // of a batch of chunks are all issued before any of them is used.
+// Writes a chunk's raw bytes (codes and its block-scale bytes) to row `dst`.
+template <int FMT>
+__device__ __forceinline__ void store_chunk(const RowPtrs &dst, int c, const Chunk<FMT> &ch) {
+  if constexpr (FMT == FMT_BF16) {
+    uint4 *p = reinterpret_cast<uint4 *>(const_cast<uint8_t *>(dst.codes)) + 4 * c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = ch.q[i];
+  } else {
+    reinterpret_cast<uint4 *>(const_cast<uint8_t *>(dst.codes))[c] = ch.q[0];
+    if constexpr (FMT == FMT_NVFP4) reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(dst.sf))[c] = (uint16_t)ch.sf;
+    else const_cast<uint8_t *>(dst.sf)[c] = (uint8_t)ch.sf;
+  }
+}
+
+// With `dst` set (a miss read from host memory), every chunk read is also
+// written to the same place in the expert's GPU slot.
 template <int FMT, int NT, int NROWS, int LPR>
-__device__ __forceinline__ void rows_dot(const RowPtrs *rp, int K, const __nv_bfloat16 *xs, int l8,
-                                         float (&acc)[NROWS][NT]) {
-  constexpr int kBatch = FMT == FMT_BF16 ? 2 : 4;
+__device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, int K, const __nv_bfloat16 *xs,
+                                         int l8, float (&acc)[NROWS][NT]) {
+  constexpr int kBatch = 2;   // the whole row was prefetched into L2 at kernel start
   const int cpl = K / (32 * LPR);  // chunks per lane
 #pragma unroll 1
   for (int i0 = 0; i0 < cpl; i0 += kBatch) {
@@ -190,6 +206,13 @@ __device__ __forceinline__ void rows_dot(const RowPtrs *rp, int K, const __nv_bf
       if (i0 + b < cpl)
 #pragma unroll
         for (int r = 0; r < NROWS; ++r) load_chunk<FMT>(rp[r].codes, rp[r].sf, l8 + LPR * (i0 + b), ch[r][b]);
+    if (dst) {
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b)
+        if (i0 + b < cpl)
+#pragma unroll
+          for (int r = 0; r < NROWS; ++r) store_chunk<FMT>(dst[r], l8 + LPR * (i0 + b), ch[r][b]);
+    }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b)
       if (i0 + b < cpl)
@@ -199,15 +222,21 @@ __device__ __forceinline__ void rows_dot(const RowPtrs *rp, int K, const __nv_bf
 }
 
 template <int FMT, bool DOWN, int NT, int LPR>
-__device__ __forceinline__ void ffn_rows(const uint8_t *blob, const BlobLayout &L, const FfnArgs &a, int feat,
-                                         const __nv_bfloat16 *xs, int nt, int p0, float gs0, float gs1, int l8) {
+__device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst, const BlobLayout &L, const FfnArgs &a,
+                                         int feat, const __nv_bfloat16 *xs, int nt, int p0, float gs0, float gs1,
+                                         int l8) {
   if constexpr (!DOWN) {
     if (feat >= a.I) return;
     const RowPtrs rp[2] = {row_ptrs<FMT>(blob, L, false, feat, a.H), row_ptrs<FMT>(blob, L, false, a.I + feat, a.H)};
+    RowPtrs dp[2];
+    if (slot_dst) {
+      dp[0] = row_ptrs<FMT>(slot_dst, L, false, feat, a.H);
+      dp[1] = row_ptrs<FMT>(slot_dst, L, false, a.I + feat, a.H);
+    }
     float acc[2][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.0f;
-    rows_dot<FMT, NT, 2, LPR>(rp, a.H, xs, l8, acc);
+    rows_dot<FMT, NT, 2, LPR>(rp, slot_dst ? dp : nullptr, a.H, xs, l8, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const float g = group_sum<LPR>(acc[0][t]) * gs0;
@@ -217,10 +246,12 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, const BlobLayout &
   } else {
     if (feat >= a.H) return;
     const RowPtrs rp[1] = {row_ptrs<FMT>(blob, L, true, feat, a.I)};
+    RowPtrs dp[1];
+    if (slot_dst) dp[0] = row_ptrs<FMT>(slot_dst, L, true, feat, a.I);
     float acc[1][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = 0.0f;
-    rows_dot<FMT, NT, 1, LPR>(rp, a.I, xs, l8, acc);
+    rows_dot<FMT, NT, 1, LPR>(rp, slot_dst ? dp : nullptr, a.I, xs, l8, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const float v = group_sum<LPR>(acc[0][t]) * gs0;
@@ -242,8 +273,10 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
   const int u = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l8 = lane & (LPR - 1);
+  pdl_wait();      // the plan, activations and slots come from earlier kernels
+  pdl_trigger();
   bool work = u < a.plan.n[0];
-  int hit = 0;
+  int hit = 1;
   if (work) {
     hit = a.plan.u_hit[u];
     if ((a.only == 1 && !hit) || (a.only == 2 && hit)) work = false;
@@ -252,7 +285,15 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
     const int e = a.plan.u_expert[u];
     const int off = a.plan.offsets[e];
     const int n = a.plan.offsets[e + 1] - off;
-    const uint8_t *blob = a.slot_bank + (size_t)a.plan.u_slot[u] * a.slot_stride;
+    uint8_t *slot = const_cast<uint8_t *>(a.slot_bank) + (size_t)a.plan.u_slot[u] * a.slot_stride;
+    const uint8_t *blob = slot;
+    uint8_t *pull_dst = nullptr;
+    if (a.pull && !hit) {
+      // a miss read straight from pinned host memory over PCIe; the bytes read
+      // are also written into its slot, so later calls hit
+      blob = reinterpret_cast<const uint8_t *>(a.pool_dev[(size_t)a.layer * a.E + e]);
+      pull_dst = slot;
+    }
     const BlobLayout L = blob_layout(FMT, a.H, a.I);
     const int K = DOWN ? a.I : a.H;
     float gs0 = 1.0f, gs1 = 1.0f;
@@ -260,8 +301,28 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
       const float *gs = reinterpret_cast<const float *>(blob + L.gscale);
       gs0 = DOWN ? gs[2] : gs[0];
       gs1 = gs[1];
+      if (DOWN && pull_dst && blockIdx.x == 0 && threadIdx.x == 0)
+        *reinterpret_cast<uint4 *>(pull_dst + L.gscale) = *reinterpret_cast<const uint4 *>(blob + L.gscale);
     }
     const int feat0 = blockIdx.x * kFeatPerCta + warp * (32 / LPR) + lane / LPR;
+    {
+      // ask L2 for this lane's weight chunks now, so that their DRAM latency
+      // overlaps the activation staging below
+      const int cpl = K / (32 * LPR);
+      const int cbytes = FMT == FMT_BF16 ? 64 : 16;
+      for (int fp = 0; fp < fpw; ++fp) {
+        const int feat = feat0 + fp * kWarps * (32 / LPR);
+        if (feat >= (DOWN ? a.H : a.I)) break;
+#pragma unroll
+        for (int r = 0; r < (DOWN ? 1 : 2); ++r) {
+          const RowPtrs rp = row_ptrs<FMT>(blob, L, DOWN, DOWN ? feat : (r == 0 ? feat : a.I + feat), K);
+          for (int i = 0; i < cpl; ++i) {
+            const uint8_t *p = rp.codes + (size_t)(l8 + LPR * i) * cbytes;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+          }
+        }
+      }
+    }
     for (int c0 = 0; c0 < n; c0 += kTokChunk) {
       const int nt = min(kTokChunk, n - c0);
       // stage the chunk's activations (bf16 rows of K) in shared memory
@@ -280,7 +341,8 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
       __syncthreads();
       // rows nt..NT-1 of xs may hold stale data: their dot products are computed and dropped
       for (int fp = 0; fp < fpw; ++fp)
-        ffn_rows<FMT, DOWN, NT, LPR>(blob, L, a, feat0 + fp * kWarps * (32 / LPR), xs, nt, off + c0, gs0, gs1, l8);
+        ffn_rows<FMT, DOWN, NT, LPR>(blob, c0 == 0 ? pull_dst : nullptr, L, a, feat0 + fp * kWarps * (32 / LPR), xs,
+                                     nt, off + c0, gs0, gs1, l8);
       __syncthreads();
     }
   }
@@ -353,8 +415,7 @@ cudaError_t launch_t(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
   const int fpc = kWarps * (32 / LPR) * fpw;
   dim3 grid((feats + fpc - 1) / fpc, a.umax);
   const size_t smem = (size_t)NT * K * sizeof(__nv_bfloat16);
-  ffn_gemv_kernel<FMT, DOWN, NT, LPR><<<grid, kWarps * 32, smem, s>>>(a, cb, fpw);
-  return cudaGetLastError();
+  return launch_k(ffn_gemv_kernel<FMT, DOWN, NT, LPR>, grid, dim3(kWarps * 32), smem, s, a.pdl != 0, a, cb, fpw);
 }
 
 template <int FMT, bool DOWN, int NT>

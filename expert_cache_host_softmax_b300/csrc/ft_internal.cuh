@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "../../include/ft_moe.h"
 
@@ -76,6 +77,7 @@ struct RouteArgs {
   int32_t *chunk_counts;    // [n_chunks][E]
   int32_t *chunk_base;      // [n_chunks][E]
   int n_chunks;
+  int pdl;                  // single-CTA route kernel launched with programmatic dependent launch
 };
 
 // Launchers (route.cu)
@@ -102,6 +104,12 @@ struct FfnArgs {
   int only;                   // 0 all, 1 hits only, 2 misses only
   int max_tokens;             // tokens of the call (no expert sees more)
   int *err;                   // device error word: a bounded wait that gave up records its site
+  // misses read from host memory (FT_MISS_PULL): device-visible addresses of
+  // the pool's blobs [L*E], the call's layer, and the switch
+  const uint64_t *pool_dev;
+  int layer;
+  int pull;
+  int pdl;                    // launch with programmatic dependent launch (follows a kernel directly)
 };
 // Combine fused into the down GEMV (small calls): out[t] = sum_j gates[t][j] *
 // y[inv[t*k+j]], written by the last CTA of each feature tile.  counters: one
@@ -131,6 +139,32 @@ cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, int 
                                cudaStream_t s);
 cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const void *map_h, const void *map_gu,
                           const void *map_d, int *err, int64_t max_rows, cudaStream_t s);
+
+// Programmatic dependent launch.  A kernel launched with `pdl` may start
+// while the previous kernel on its stream is still running; it must execute
+// pdl_wait() before touching anything that kernel writes (pdl_wait returns
+// once it has completed and its memory is visible; without the launch
+// attribute it returns at once).  pdl_trigger() lets the next kernel launch;
+// every kernel here triggers only after its own pdl_wait, so when kernel n
+// starts, kernel n-2 has completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Sets the message ft_last_error(NULL) returns on this thread.
 void set_stateless_error(const std::string &msg);

@@ -57,6 +57,7 @@ struct ft_moe {
   int last_T = 0;
   bool any_call = false;
   bool last_tc = false;
+  bool captured = false;   // a forward was captured into a graph since the last synchronising call
   uint64_t host_warm = 0, host_streamed = 0, host_bytes = 0;
   uint64_t last_streamed = 0, last_stream_bytes = 0;
   // optional per-step timing (ft_moe_set_profiling)
@@ -75,6 +76,8 @@ struct ft_moe {
   int ffn_kernel = FT_FFN_AUTO;
   int *err_dev = nullptr;
   int *combine_counters = nullptr;   // per feature tile, for the combine fused into the down GEMV
+  uint64_t *pool_dev = nullptr;      // device-visible addresses of the pool's blobs [L*E] (FT_MISS_PULL)
+  int miss_path = FT_MISS_COPY;
   std::string err;
 };
 
@@ -139,6 +142,7 @@ void free_all(ft_moe *h) {
   cudaFree(h->err_dev);
   cudaFree(h->xpbuf);
   cudaFree(h->combine_counters);
+  cudaFree(h->pool_dev);
   if (h->mirror_host) cudaFreeHost(h->mirror_host);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   if (h->copy_stream2) cudaStreamDestroy(h->copy_stream2);
@@ -175,7 +179,12 @@ void prof_collect(ft_moe *h) {
 // Waits for everything the handle has issued, then checks the device error
 // word (set by a kernel whose bounded wait gave up).
 int sync_handle(ft_moe *h) {
-  if (h->any_call) FT_CUDA(h, cudaEventSynchronize(h->ev_done));
+  if (h->captured) {
+    FT_CUDA(h, cudaDeviceSynchronize());
+    h->captured = false;
+  } else if (h->any_call) {
+    FT_CUDA(h, cudaEventSynchronize(h->ev_done));
+  }
   FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
   FT_CUDA(h, cudaStreamSynchronize(h->copy_stream2));
   int code = 0;
@@ -386,6 +395,19 @@ int ft_moe_load_pool(ft_moe *h, const void *const *host_experts) {
       return fail(h, FT_ERR_NOT_PINNED, "expert " + std::to_string(i) + " is not in page-locked host memory");
     }
   }
+  // device-visible address of every blob, for misses read over PCIe by the kernels
+  std::vector<uint64_t> dev_ptrs(n);
+  for (size_t i = 0; i < n; ++i) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, host_experts[i]) != cudaSuccess || at.devicePointer == nullptr) {
+      cudaGetLastError();
+      return fail(h, FT_ERR_NOT_PINNED, "expert " + std::to_string(i) + " has no device-visible mapping");
+    }
+    dev_ptrs[i] = reinterpret_cast<uint64_t>(at.devicePointer);
+  }
+  FT_CUDA(h, cudaSetDevice(h->device));
+  if (!h->pool_dev) FT_CUDA(h, cudaMalloc(&h->pool_dev, n * sizeof(uint64_t)));
+  FT_CUDA(h, cudaMemcpy(h->pool_dev, dev_ptrs.data(), n * sizeof(uint64_t), cudaMemcpyHostToDevice));
   h->pool.assign(host_experts, host_experts + n);
   h->pool_loaded = true;
   return reset_tables(h, true);
@@ -419,12 +441,15 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
     return fail(h, FT_ERR_ARG, "x, router_logits and out must be 16-byte aligned");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   FT_CUDA(h, cudaSetDevice(h->device));
-  if (h->mode == MODE_LRU) {
-    cudaStreamCaptureStatus cs;
-    FT_CUDA(h, cudaStreamIsCapturing(stream, &cs));
-    if (cs != cudaStreamCaptureStatusNone)
-      return fail(h, FT_ERR_STATE, "LRU-mode forward waits on the host and cannot be captured");
-  }
+  const bool tc = use_tc(h, n_tokens);
+  // misses read by the kernels over PCIe: no host round trip (GEMV calls only)
+  const bool pull = h->mode == MODE_LRU && h->miss_path == FT_MISS_PULL && !tc;
+  cudaStreamCaptureStatus cs;
+  FT_CUDA(h, cudaStreamIsCapturing(stream, &cs));
+  const bool capturing = cs != cudaStreamCaptureStatusNone;
+  if (capturing && (h->mode != MODE_LRU || !pull))
+    return fail(h, FT_ERR_STATE, "only LRU-mode forward with FT_MISS_PULL on the GEMV can be captured");
+  if (capturing && h->prof) return fail(h, FT_ERR_STATE, "profiling is on: forward cannot be captured");
   const int bank = layer & 1;
   if (h->mode == MODE_STREAM) {
     if (int rc = stage_layer(h, layer)) return rc;
@@ -445,17 +470,19 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   ra.cache.order_in = h->order[h->order_cur];
   ra.cache.order_out = h->order[h->order_cur ^ 1];
   ra.cache.stats = h->stats_dev;
-  ra.mirror = h->mode == MODE_LRU ? h->mirror_dev : nullptr;
+  ra.mirror = (h->mode == MODE_LRU && !pull) ? h->mirror_dev : nullptr;
   ra.umax = h->umax;
   ra.seq = h->seq;
   ra.chunk_counts = h->chunk_counts;
   ra.chunk_base = h->chunk_base;
+  // follows the previous call's last kernel directly (STREAM mode waits on a copy event first)
+  ra.pdl = h->mode == MODE_LRU && !h->prof && !capturing;
   prof_begin(h, FT_PROF_ROUTE, stream);
   FT_CUDA(h, launch_route(ra, stream));
   prof_end(h, FT_PROF_ROUTE, stream);
   h->kernel_launches += route_kernel_count(n_tokens, h->k) + 2;  // + gate/up, down (+ combine below)
   if (h->mode == MODE_LRU) h->order_cur ^= 1;
-  FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
+  if (!capturing) FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
 
   FfnArgs fa{};
   fa.slot_bank = h->slots;
@@ -468,9 +495,11 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
   fa.max_tokens = n_tokens;
   fa.err = h->err_dev;
-  const bool tc = use_tc(h, n_tokens);
+  fa.pool_dev = h->pool_dev;
+  fa.layer = layer;
+  fa.pull = pull ? 1 : 0;
   h->last_tc = tc;
-  if (h->mode == MODE_LRU) {
+  if (h->mode == MODE_LRU && !pull) {
     fa.only = 1;
     prof_begin(h, FT_PROF_GATEUP_HIT, stream);
     FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
@@ -510,6 +539,7 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
     prof_end(h, FT_PROF_GATEUP_HIT, stream);
   }
   fa.only = 0;
+  fa.pdl = !tc && !h->prof && !capturing;   // the down kernel follows the gate/up kernel directly
   // small calls on the GEMV: the combine runs inside the down kernel
   const bool fused = !tc && gemv_fuses_combine(n_tokens);
   CombineArgs cb{};
@@ -531,7 +561,10 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
     prof_end(h, FT_PROF_COMBINE, stream);
   }
   if (h->mode == MODE_STREAM) FT_CUDA(h, cudaEventRecord(h->ev_bank_free[bank], stream));
-  FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
+  // a captured call runs when its graph is launched: the next synchronising
+  // call waits for the device instead of the handle's event
+  if (capturing) h->captured = true;
+  else FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
   h->host_streamed += h->last_streamed;
   h->host_bytes += h->last_stream_bytes;
   if (h->prof) prof_collect(h);
@@ -626,6 +659,13 @@ int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
 }
 
 int ft_moe_last_ffn_kernel(const ft_moe *h) { return h ? (h->last_tc ? FT_FFN_TC : FT_FFN_GEMV) : -1; }
+
+int ft_moe_set_miss_path(ft_moe *h, int path) {
+  if (!h || (path != FT_MISS_COPY && path != FT_MISS_PULL)) return fail(h, FT_ERR_ARG, "bad miss path");
+  if (int rc = sync_handle(h)) return rc;
+  h->miss_path = path;
+  return FT_OK;
+}
 
 int64_t ft_moe_slot_stride(const ft_moe *h) { return h ? h->slot_stride : -1; }
 

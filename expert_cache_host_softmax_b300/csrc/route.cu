@@ -382,8 +382,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
   int *s_wcnt = s_warp + 33;           // nw*E
   unsigned *s_bits = (unsigned *)(s_wcnt + nw * E);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  // the cache tables were last written by the previous call's route kernel,
+  // which has completed (see pdl_trigger); everything else waits for the
+  // kernel before this one
   Prefetch pf;
   prefetch_tables(a, s_keyslot, pf);
+  pdl_wait();
+  pdl_trigger();
   for (int i = tid; i < E; i += blockDim.x) s_count[i] = 0;
   __syncthreads();
   for (int t = w; t < a.T; t += nw) {
@@ -449,22 +454,42 @@ __global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int wi
   int *s_victim = s_uexp + E;
   int *s_warp = s_victim + E;          // 33
   unsigned *s_bits = (unsigned *)(s_warp + 33);
+  int *s_part = (int *)(s_bits + ((a.S + 31) >> 5));   // [G][E]
   const int tid = threadIdx.x;
+  // G groups of threads per expert, each summing a contiguous range of chunks
+  const int G = max(1, (int)blockDim.x / E);
+  const int e = tid % E, g = tid / E;
+  const int per = (a.n_chunks + G - 1) / G;
+  const int c0 = min(a.n_chunks, g * per), c1 = min(a.n_chunks, c0 + per);
+  if (g < G) {
+    int part = 0;
+    for (int c = c0; c < c1; ++c) part += a.chunk_counts[(size_t)c * E + e];
+    s_part[g * E + e] = part;
+  }
+  __syncthreads();
   int cnt = 0;
   if (tid < E)
-    for (int c = 0; c < a.n_chunks; ++c) cnt += a.chunk_counts[(size_t)c * E + tid];
+    for (int gg = 0; gg < G; ++gg) {   // exclusive prefix over the groups, per expert
+      const int p = s_part[gg * E + tid];
+      s_part[gg * E + tid] = cnt;
+      cnt += p;
+    }
   int total;
   const int off = block_excl_scan(tid < E ? cnt : 0, s_warp, &total);
   if (tid < E) {
     s_count[tid] = cnt;
     a.plan.offsets[tid] = off;
-    int run = off;
-    for (int c = 0; c < a.n_chunks; ++c) {
-      a.chunk_base[(size_t)c * E + tid] = run;
-      run += a.chunk_counts[(size_t)c * E + tid];
-    }
+    s_uexp[tid] = off;   // expert offsets for the chunk bases below (s_uexp is rewritten by the plan)
   }
   if (tid == 0) a.plan.offsets[E] = total;
+  __syncthreads();
+  if (g < G) {
+    int run = s_uexp[e] + s_part[g * E + e];
+    for (int c = c0; c < c1; ++c) {
+      a.chunk_base[(size_t)c * E + e] = run;
+      run += a.chunk_counts[(size_t)c * E + e];
+    }
+  }
   __syncthreads();
   if (with_plan) {
     PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, nullptr, nullptr};
@@ -490,15 +515,16 @@ __global__ void __launch_bounds__(256) scatter_chunk_kernel(const int32_t *__res
 }
 
 // Threads of the single-CTA routing kernel: at least E (one per expert in
-// the plan), at least 256, a whole number of warps.
-int small_threads(int E) { return std::min(kRouteThreads, std::max(256, (E + 31) / 32 * 32)); }
+// the plan), at least 128, a whole number of warps.
+int small_threads(int E) { return std::min(kRouteThreads, std::max(128, (E + 31) / 32 * 32)); }
 
 size_t small_smem_bytes(int E, int S) {
   const size_t nw = small_threads(E) / 32;
   return sizeof(int) * (6 * (size_t)E + 33 + nw * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
 }
 size_t plan_smem_bytes(int E, int S) {
-  return sizeof(int) * (3 * (size_t)E + 33) + sizeof(unsigned) * (((size_t)S + 31) / 32);
+  return sizeof(int) * (3 * (size_t)E + 33) + sizeof(unsigned) * (((size_t)S + 31) / 32) +
+         sizeof(int) * (size_t)kRouteThreads;   // per-group chunk partials
 }
 
 }  // namespace
@@ -522,8 +548,8 @@ int route_kernel_count(int T, int k) { return T * k <= kSmallRoutePairs ? 1 : 3;
 // three kernels over kChunkTokens-token chunks.
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s) {
   if (a.T * a.k <= kSmallRoutePairs || a.chunk_counts == nullptr) {
-    route_small_kernel<<<1, small_threads(a.E), small_smem_bytes(a.E, a.S), s>>>(a);
-    return cudaGetLastError();
+    return launch_k(route_small_kernel, dim3(1), dim3(small_threads(a.E)), small_smem_bytes(a.E, a.S), s, a.pdl != 0,
+                    a);
   }
   RouteArgs b = a;
   b.n_chunks = n_chunks_of(a.T);

@@ -132,10 +132,15 @@ int ft_moe_set_mode(ft_moe *h, int mode);
  * table.  Hits move to MRU in ascending expert id.  Then misses, in ascending
  * id, take the lowest free slot or evict the LRU expert.  All of this is
  * decided on the GPU.  Miss blobs are copied by cudaMemcpyAsync on the
- * handle's copy stream, overlapping the FFN of the hits.  The call blocks the
+ * handle's copy streams, overlapping the FFN of the hits.  The call blocks the
  * host until the GPU's miss list is known: a bounded wait, FT_ERR_TIMEOUT
  * after FT_WAIT_TIMEOUT_MS (default 20000).  It cannot run under stream
- * capture (FT_ERR_STATE).
+ * capture (FT_ERR_STATE).  With FT_MISS_PULL (ft_moe_set_miss_path) on a GEMV
+ * call, the kernels read the misses from host memory instead: no host wait,
+ * and the call can be captured in a CUDA graph (not while profiling).  Each
+ * launch of such a graph is one more call: it advances the cache state.
+ * After a captured call, the synchronising calls (ft_cache_stats and others)
+ * wait for the whole device.
  * STREAM mode: bank (layer mod 2) receives all E experts of `layer` before
  * its FFN.  The copy of the next layer starts in this call and overlaps this
  * layer's compute.
@@ -216,6 +221,21 @@ int ft_moe_set_ffn_kernel(ft_moe *h, int which);
 /* The FFN kernel the last forward call used: FT_FFN_GEMV or FT_FFN_TC
  * (-1 for NULL). */
 int ft_moe_last_ffn_kernel(const ft_moe *h);
+
+/* How LRU-mode misses reach their slots. */
+enum ft_miss_path {
+  FT_MISS_COPY = 0, /* default: cudaMemcpyAsync per miss on the handle's copy streams, issued by the host
+                       once it has read the GPU's miss list; the hits' FFN overlaps the copies */
+  FT_MISS_PULL = 1  /* the FFN kernels read a missed expert's weights straight from pinned host
+                       memory over PCIe and write the same bytes into its slot; no host round
+                       trip, so forward returns without waiting and can be captured in a CUDA
+                       graph.  Applies to calls on the GEMV kernel; tensor-core calls still copy. */
+};
+
+/* Selects the miss path for later forward calls (default FT_MISS_COPY).  The
+ * cache decisions, counters and results are the same on both paths.  Waits for
+ * the handle's outstanding work.  Errors: FT_ERR_ARG. */
+int ft_moe_set_miss_path(ft_moe *h, int path);
 
 /* Bytes between consecutive slots in the device slot bank. */
 int64_t ft_moe_slot_stride(const ft_moe *h);

@@ -62,9 +62,11 @@ def test_permute_matches_oracle(T, E, k):
 
 # ------------------------------------------------------------ whole layer
 
-def _check_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=False, fmt=None):
+def _check_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=False, fmt=None, outs=None):
     xd, lgd = Hn.to_dev(x, lg)
     out = gpu.forward(layer, xd, lgd)
+    if outs is not None:
+        outs.append(out)
     torch.cuda.synchronize()
     ref = orc.forward(layer, x, lg, tokens=tokens)
     r = gpu.last_routing()
@@ -272,6 +274,59 @@ def test_auto_picks_gemv_for_decode():
         xd, lgd = Hn.to_dev(x, lg)
         gpu.forward(0, xd, lgd)
         assert gpu.last_ffn_kernel == want
+    gpu.close()
+
+
+# ------------------------------------------------------------ misses read over PCIe by the kernels
+
+@pytest.mark.parametrize("fmt,T", [("nvfp4", 1), ("mxfp4", 2), ("bf16", 3), ("nvfp4", 6)])
+def test_pull_misses_match_oracle_and_copy_path(fmt, T):
+    # same decisions and counters as the oracle; outputs bit-identical to the
+    # copy-engine path (the same kernels read the same bytes, from host memory
+    # instead of the slot); later calls hit on the slots the pull filled
+    H, I, E, k, L, S = 256, 512, 16, 2, 3, min(16, 8 + 2 * T)
+    seed = 101 + T
+    pull, orc, pool = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed)
+    pull.set_miss_path("pull")
+    copy = F.MoELayerStack(H, E, k, I, fmt, S, L, T)
+    copy.load_pool(pool.pointers, keepalive=pool)
+    for step in range(12):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, T, H, E, step, layer, zipf=0.7)
+            xd, lgd = Hn.to_dev(x, lg)
+            b = copy.forward(layer, xd, lgd)
+            outs = []
+            _check_call(pull, orc, layer, x, lg, gemm_check=(step % 5 == 0), outs=outs)
+            torch.cuda.synchronize()
+            assert copy.trace() == pull.trace()
+            assert torch.equal(outs[0].view(torch.int16), b.view(torch.int16))
+    cum_p, _ = pull.stats()
+    cum_c, _ = copy.stats()
+    assert cum_p == cum_c
+    assert cum_p["misses"] == orc.stats["misses"] > 0 and cum_p["hits"] > 0
+    pull.close()
+    copy.close()
+
+
+def test_pull_forward_is_capturable():
+    H, I, E, k, L, T = 256, 256, 8, 2, 2, 4
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, L, T, 111, warm=False)
+    gpu.set_miss_path("pull")
+    x, lg = Hn.inputs(111, T, H, E, 0, 1)
+    xd, lgd = Hn.to_dev(x, lg)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        gpu.forward(1, xd, lgd, out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    ref = orc.forward(1, x, lg)
+    assert gpu.trace() == [tuple(p) for p in ref["plan"]]
+    assert Hn.rel_err(Hn.out_to_f64(out), ref["out"]) <= OUT_TOL
+    _, last = gpu.stats()
+    assert last["misses"] == ref["last"]["misses"] > 0
     gpu.close()
 
 
