@@ -310,6 +310,8 @@ def run_ours(args, cfg):
         stack.set_ffn_kernel(args.ffn)
     if args.miss_path != "copy":
         stack.set_miss_path(args.miss_path)
+    if args.fused_decode:
+        stack.set_decode_fusion(True)
 
     W, K = args.warmup, args.steps
     n_prof = min(args.profile_steps, K)
@@ -457,6 +459,11 @@ def run_ours(args, cfg):
         "route": (toks_p * E * 4, prof["route"][0], 0),
         "combine": (toks_p * (k * H * 4 + H * 2), prof["combine"][0], 0),
     }
+    if prof.get("layer", (0.0, 0))[1] > 0:
+        # decode calls ran as the fused layer kernel: routing, FFN and combine in one launch
+        # (its duration includes waiting for the misses' copies)
+        kern["decode_layer"] = (pd["lookups"] * (gu_bytes + d_bytes) + act_gu + act_dn + toks_p * (E * 4 + H * 2),
+                                prof["layer"][0], fl_gu + fl_dn)
     dom = max(kern, key=lambda n: kern[n][1])
     b_dom, ms_dom, f_dom = kern[dom]
     share = {n: round(kern[n][1] / max(1e-9, sum(v[1] for v in kern.values())), 4) for n in kern}
@@ -509,7 +516,8 @@ def run_ours(args, cfg):
         "data": "synthetic",
         "config": {"workload": cfg["name"], "layers": L, "hidden": H, "experts": E, "top_k": k, "inter": I,
                    "weight_fmt": fmt, "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
-                   "mode": cfg["mode"], "miss_path": args.miss_path, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
+                   "mode": cfg["mode"], "miss_path": args.miss_path,
+                   "decode_kernels": "fused" if args.fused_decode else "split", "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
                    "pool": f"{n_keys} logical experts over {n_phys} distinct pinned blobs ({n_phys * nb / 1e9:.2f} GB)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": L * T * (H * 2 + E * 4),
                 "d2h_bytes_per_step": L * T * H * 2},
@@ -547,6 +555,9 @@ def main():
     ap.add_argument("--ffn", choices=("auto", "gemv", "tc"), default="auto", help="FFN kernel")
     ap.add_argument("--miss-path", choices=("copy", "pull"), default="copy",
                     help="LRU misses: cudaMemcpyAsync on copy streams, or read over PCIe by the FFN kernels")
+    ap.add_argument("--fused-decode", action="store_true",
+                    help="decode calls as one cooperative kernel instead of separate kernels (its copy-flag "
+                         "wait needs the copy stream to progress alongside it: profile it with --miss-path pull)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

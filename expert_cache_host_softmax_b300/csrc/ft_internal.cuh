@@ -166,6 +166,12 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Fused decode layer (decode_layer.cu): one cooperative kernel per call.
+bool mega_supported(int E, int T, int k);
+cudaError_t launch_decode_layer(const RouteArgs &route, const FfnArgs &ffn, const CombineArgs &cb, int *sync,
+                                bool wait_copies, size_t route_smem, cudaStream_t s);
+size_t route_small_smem(int E, int S);
+
 // Sets the message ft_last_error(NULL) returns on this thread.
 void set_stateless_error(const std::string &msg);
 

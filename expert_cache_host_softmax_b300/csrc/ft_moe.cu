@@ -77,6 +77,9 @@ struct ft_moe {
   int *err_dev = nullptr;
   int *combine_counters = nullptr;   // per feature tile, for the combine fused into the down GEMV
   uint64_t *pool_dev = nullptr;      // device-visible addresses of the pool's blobs [L*E] (FT_MISS_PULL)
+  int *mega_sync = nullptr;          // fused decode layer: plan flag, copy flag, grid barrier count and generation
+  int32_t *seq_ring = nullptr;       // pinned: seq_ring[seq % 64] = seq, the source of the copy-flag write
+  bool decode_fused = false;   // ft_moe_set_decode_fusion
   int miss_path = FT_MISS_COPY;
   std::string err;
 };
@@ -143,7 +146,9 @@ void free_all(ft_moe *h) {
   cudaFree(h->xpbuf);
   cudaFree(h->combine_counters);
   cudaFree(h->pool_dev);
+  cudaFree(h->mega_sync);
   if (h->mirror_host) cudaFreeHost(h->mirror_host);
+  if (h->seq_ring) cudaFreeHost(h->seq_ring);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   if (h->copy_stream2) cudaStreamDestroy(h->copy_stream2);
   for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_copy2, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
@@ -191,6 +196,9 @@ int sync_handle(ft_moe *h) {
   FT_CUDA(h, cudaMemcpy(&code, h->err_dev, sizeof code, cudaMemcpyDeviceToHost));
   if (code != 0) {
     FT_CUDA(h, cudaMemset(h->err_dev, 0, sizeof(int)));
+    // an aborted kernel may have left its flags or counters mid-way
+    FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
+    FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
     return fail(h, FT_ERR_DEVICE, "a tensor-core FFN kernel gave up waiting (site " + std::to_string(code) + ")");
   }
   return FT_OK;
@@ -241,6 +249,8 @@ int reset_tables(ft_moe *h, bool warm) {
   FT_CUDA(h, cudaMemcpy(h->order[0], order.data(), order.size() * 4, cudaMemcpyHostToDevice));
   h->order_cur = 0;
   FT_CUDA(h, cudaMemset(h->stats_dev, 0, 16 * sizeof(unsigned long long)));
+  FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
+  FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
   h->host_warm = h->host_streamed = h->host_bytes = 0;
   h->last_streamed = h->last_stream_bytes = 0;
   h->bank_layer[0] = h->bank_layer[1] = -1;
@@ -302,6 +312,84 @@ int wait_plan(ft_moe *h) {
   return FT_OK;
 }
 
+// Issues the call's miss copies (after the GPU's miss list is known): one
+// cudaMemcpyAsync per miss, alternating between the two copy streams, joined
+// on copy_stream.  Returns the number of misses, or a negative status.
+int issue_miss_copies(ft_moe *h) {
+  if (int rc = wait_plan(h)) return rc;
+  const int n_miss = h->mirror_host[1];
+  if (n_miss <= 0) return 0;
+  prof_begin(h, FT_PROF_MISS_COPY, h->copy_stream);
+  for (int i = 0; i < n_miss; ++i) {
+    const int key = h->mirror_host[2 + i], slot = h->mirror_host[2 + h->umax + i];
+    if (key < 0 || key >= h->L * h->E || slot < 0 || slot >= h->S)
+      return fail(h, FT_ERR_DEVICE, "miss list entry out of range");
+    FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)slot * h->slot_stride, h->pool[key], h->blob_bytes,
+                               cudaMemcpyHostToDevice, (i & 1) ? h->copy_stream2 : h->copy_stream));
+  }
+  if (n_miss > 1) {
+    FT_CUDA(h, cudaEventRecord(h->ev_copy2, h->copy_stream2));
+    FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_copy2, 0));
+  }
+  prof_end(h, FT_PROF_MISS_COPY, h->copy_stream);
+  return n_miss;
+}
+
+// A decode call (LRU mode, GEMV, few tokens) as one cooperative kernel: route,
+// gate/up of the hits, [the copies land] gate/up of the misses, down and
+// combine.  The copy stream tells the kernel that the misses have landed by
+// writing the call's sequence number (the mirror's first word) into a device
+// flag after the expert copies.
+int forward_fused(ft_moe *h, RouteArgs &ra, int layer, int n_tokens, const void *x, void *out, bool pull,
+                  cudaStream_t stream) {
+  FfnArgs fa{};
+  fa.slot_bank = h->slots;
+  fa.slot_stride = h->slot_stride;
+  fa.H = h->H; fa.I = h->I; fa.E = h->E; fa.k = h->k; fa.fmt = h->fmt;
+  fa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+  fa.h = h->hbuf;
+  fa.y = h->ybuf;
+  fa.plan = h->plan;
+  fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
+  fa.max_tokens = n_tokens;
+  fa.err = h->err_dev;
+  fa.pool_dev = h->pool_dev;
+  fa.layer = layer;
+  fa.pull = pull ? 1 : 0;
+  CombineArgs cb{};
+  cb.gates = h->plan.gates;
+  cb.inv = h->plan.inv;
+  cb.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  cb.counters = h->combine_counters;
+  cb.T = n_tokens;
+  h->last_tc = false;
+  // the value the copy stream writes into the kernel's copy flag; a ring, so
+  // that a later call cannot overwrite it before the copy engine reads it
+  int32_t *release = h->seq_ring + (h->seq % 64);
+  *release = (int32_t)h->seq;
+  prof_begin(h, FT_PROF_LAYER, stream);
+  FT_CUDA(h, launch_decode_layer(ra, fa, cb, h->mega_sync, !pull, route_small_smem(h->E, h->S), stream));
+  prof_end(h, FT_PROF_LAYER, stream);
+  // the host's wait for the miss list polls this: it completes when the kernel does
+  FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
+  h->kernel_launches += 1;
+  h->order_cur ^= 1;
+  if (!pull) {
+    const int n_miss = issue_miss_copies(h);
+    if (n_miss != 0) {
+      // after the copies, or at once if the host side failed: the kernel must
+      // not wait out its time limit (its results are then undefined)
+      cudaError_t e = cudaMemcpyAsync(h->mega_sync + 1, release, sizeof(int32_t), cudaMemcpyHostToDevice,
+                                      h->copy_stream);
+      if (n_miss < 0) return n_miss;
+      if (e != cudaSuccess) return cuda_fail(h, e, "copy-flag write");
+    }
+  }
+  FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
+  if (h->prof) prof_collect(h);
+  return FT_OK;
+}
+
 }  // namespace
 
 void ftmoe::set_stateless_error(const std::string &msg) { g_create_err = msg; }
@@ -350,6 +438,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
             dev_alloc(&h->xpbuf, TK * hidden) == cudaSuccess &&
+            dev_alloc(&h->mega_sync, 4) == cudaSuccess && cudaMemset(h->mega_sync, 0, 16) == cudaSuccess &&
             dev_alloc(&h->combine_counters, combine_tiles(hidden)) == cudaSuccess &&
             cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(hidden)) == cudaSuccess;
   if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
@@ -360,6 +449,11 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
     return bail(FT_ERR_OOM);
   }
   std::memset(h->mirror_host, 0, sizeof(int32_t) * (2 + 2 * (size_t)umax));
+  if (cudaHostAlloc(&h->seq_ring, sizeof(int32_t) * 64, cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    fail(nullptr, FT_ERR_OOM, "pinned allocation failed");
+    return bail(FT_ERR_OOM);
+  }
   ok = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) == cudaSuccess &&
        cudaStreamCreateWithFlags(&h->copy_stream2, cudaStreamNonBlocking) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_route, cudaEventDisableTiming) == cudaSuccess &&
@@ -477,6 +571,8 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   ra.chunk_base = h->chunk_base;
   // follows the previous call's last kernel directly (STREAM mode waits on a copy event first)
   ra.pdl = h->mode == MODE_LRU && !h->prof && !capturing;
+  if (h->decode_fused && h->mode == MODE_LRU && !tc && !capturing && mega_supported(h->E, n_tokens, h->k))
+    return forward_fused(h, ra, layer, n_tokens, x, out, pull, stream);
   prof_begin(h, FT_PROF_ROUTE, stream);
   FT_CUDA(h, launch_route(ra, stream));
   prof_end(h, FT_PROF_ROUTE, stream);
@@ -659,6 +755,13 @@ int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
 }
 
 int ft_moe_last_ffn_kernel(const ft_moe *h) { return h ? (h->last_tc ? FT_FFN_TC : FT_FFN_GEMV) : -1; }
+
+int ft_moe_set_decode_fusion(ft_moe *h, int on) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  h->decode_fused = on != 0;
+  return FT_OK;
+}
 
 int ft_moe_set_miss_path(ft_moe *h, int path) {
   if (!h || (path != FT_MISS_COPY && path != FT_MISS_PULL)) return fail(h, FT_ERR_ARG, "bad miss path");

@@ -1,0 +1,382 @@
+// gemv_dev.cuh -- device code of the decode expert FFN (dequant-fused GEMV)
+// and of the combine fused into it, shared by the GEMV kernels and the fused
+// decode layer kernel.  See ffn_gemv.cu for the design.
+#pragma once
+#include "ft_internal.cuh"
+
+namespace ftmoe {
+namespace {
+
+
+constexpr int kWarps = 4;                       // per CTA
+constexpr int kTokChunk = 4;                    // tokens per pass over the weights
+constexpr int kMinFeatPerCta = kWarps;          // LPR = 32: one feature per warp
+constexpr int kFusedCombineMaxT = 16;
+
+// Two e2m1 codes (one byte) -> two halves, via the sm_100-family conversion.
+__device__ __forceinline__ __half2 e2m1x2_to_half2(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+      : "=r"(out)
+      : "r"(byte));
+  return *reinterpret_cast<__half2 *>(&out);
+}
+
+// Two E4M3 bytes (low byte first) -> two halves.
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two_bytes) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(out)
+      : "r"(two_bytes));
+  return *reinterpret_cast<__half2 *>(&out);
+}
+
+// E8M0 scale byte -> 2^(byte-127) (0xFF is NaN).
+__device__ __forceinline__ float e8m0_to_float(uint32_t b) {
+  if (b == 0xFFu) return __int_as_float(0x7fc00000);
+  return __uint_as_float(b ? (b << 23) : 0x00400000u);
+}
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float *f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// Raw bytes of one 32-element chunk of a weight row: FP4 = 16 code bytes +
+// scale bits; BF16 = 64 bytes.
+template <int FMT>
+struct Chunk {
+  uint4 q[FMT == FMT_BF16 ? 4 : 1];
+  uint32_t sf;
+};
+
+template <int FMT>
+__device__ __forceinline__ void load_chunk(const uint8_t *__restrict__ codes_row,
+                                           const uint8_t *__restrict__ sf_row, int c, Chunk<FMT> &ch) {
+  if constexpr (FMT == FMT_BF16) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(codes_row) + 4 * c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ch.q[i] = __ldg(p + i);
+    ch.sf = 0;
+  } else {
+    ch.q[0] = __ldg(reinterpret_cast<const uint4 *>(codes_row) + c);
+    if constexpr (FMT == FMT_NVFP4) ch.sf = __ldg(reinterpret_cast<const uint16_t *>(sf_row) + c);
+    else ch.sf = __ldg(sf_row + c);
+  }
+}
+
+// Decodes 8 weights (elements 8i .. 8i+7) of a chunk into w[8]: BF16 values,
+// or the bare e2m1 values of FP4 codes (block scales are applied per 8-element
+// partial sum, see chunk_fma).
+template <int FMT>
+__device__ __forceinline__ void decode8(const Chunk<FMT> &ch, int i, float *w) {
+  if constexpr (FMT == FMT_BF16) {
+    bf16x8_to_float(ch.q[i], w);
+  } else {
+    const uint32_t word = i == 0 ? ch.q[0].x : i == 1 ? ch.q[0].y : i == 2 ? ch.q[0].z : ch.q[0].w;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 v = __half22float2(e2m1x2_to_half2(word >> (8 * b)));
+      w[2 * b] = v.x;
+      w[2 * b + 1] = v.y;
+    }
+  }
+}
+
+// acc[t] += chunk . xs[t][32c .. 32c+31].  FP4: each 8-element partial sum of
+// e2m1 value x activation (every product exact in fp32) is multiplied by its
+// block scale once (NVFP4: elements 0..15 and 16..31 have one E4M3 scale
+// each; MXFP4: one E8M0 scale for all 32); the NVFP4 global scale is applied
+// to the finished dot product.
+template <int FMT, int NT>
+__device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloat16 *xs, int K, int c, float *acc) {
+  float s0 = 1.0f, s1 = 1.0f;
+  if constexpr (FMT == FMT_NVFP4) {
+    const float2 s = __half22float2(e4m3x2_to_half2(ch.sf));
+    s0 = s.x;
+    s1 = s.y;
+  } else if constexpr (FMT == FMT_MXFP4) {
+    s0 = s1 = e8m0_to_float(ch.sf);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float w[8];
+    decode8<FMT>(ch, i, w);
+    const float s = i < 2 ? s0 : s1;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)t * K + 32 * c)[i];
+      float xf[8];
+      bf16x8_to_float(xv, xf);
+      float p = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) p = fmaf(w[q], xf[q], p);
+      acc[t] = FMT == FMT_BF16 ? acc[t] + p : fmaf(s, p, acc[t]);
+    }
+  }
+}
+
+// Sum over the LPR lanes of this lane's row group (xor stays inside the group).
+template <int LPR>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+struct RowPtrs {
+  const uint8_t *codes, *sf;
+};
+
+// Row r of W_gu (r < 2I) or of W_d, inside one blob.
+template <int FMT>
+__device__ __forceinline__ RowPtrs row_ptrs(const uint8_t *blob, const BlobLayout &L, bool down, int r, int K) {
+  RowPtrs p;
+  if constexpr (FMT == FMT_BF16) {
+    p.codes = blob + (down ? L.d_codes : L.gu_codes) + (size_t)r * K * 2;
+    p.sf = nullptr;
+  } else if constexpr (FMT == FMT_NVFP4) {
+    p.codes = blob + (down ? L.d_codes : L.gu_codes) + (size_t)r * (K / 2);
+    p.sf = blob + (down ? L.d_sf : L.gu_sf) + (size_t)r * (K / 16);
+  } else {
+    p.codes = blob + (down ? L.d_codes : L.gu_codes) + (size_t)r * (K / 2);
+    p.sf = blob + (down ? L.d_sf : L.gu_sf) + (size_t)r * (K / 32);
+  }
+  return p;
+}
+
+// Dot products of NROWS weight rows (gate/up: 2, down: 1) with NT staged
+// activation rows, over this lane's chunks l, l+LPR, l+2 LPR, ... of K.  Loads
+// of a batch of chunks are all issued before any of them is used.
+// Writes a chunk's raw bytes (codes and its block-scale bytes) to row `dst`.
+template <int FMT>
+__device__ __forceinline__ void store_chunk(const RowPtrs &dst, int c, const Chunk<FMT> &ch) {
+  if constexpr (FMT == FMT_BF16) {
+    uint4 *p = reinterpret_cast<uint4 *>(const_cast<uint8_t *>(dst.codes)) + 4 * c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = ch.q[i];
+  } else {
+    reinterpret_cast<uint4 *>(const_cast<uint8_t *>(dst.codes))[c] = ch.q[0];
+    if constexpr (FMT == FMT_NVFP4) reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(dst.sf))[c] = (uint16_t)ch.sf;
+    else const_cast<uint8_t *>(dst.sf)[c] = (uint8_t)ch.sf;
+  }
+}
+
+// With `dst` set (a miss read from host memory), every chunk read is also
+// written to the same place in the expert's GPU slot.
+template <int FMT, int NT, int NROWS, int LPR>
+__device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, int K, const __nv_bfloat16 *xs,
+                                         int l8, float (&acc)[NROWS][NT]) {
+  constexpr int kBatch = 2;   // the whole row was prefetched into L2 at kernel start
+  const int cpl = K / (32 * LPR);  // chunks per lane
+#pragma unroll 1
+  for (int i0 = 0; i0 < cpl; i0 += kBatch) {
+    Chunk<FMT> ch[NROWS][kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+      if (i0 + b < cpl)
+#pragma unroll
+        for (int r = 0; r < NROWS; ++r) load_chunk<FMT>(rp[r].codes, rp[r].sf, l8 + LPR * (i0 + b), ch[r][b]);
+    if (dst) {
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b)
+        if (i0 + b < cpl)
+#pragma unroll
+          for (int r = 0; r < NROWS; ++r) store_chunk<FMT>(dst[r], l8 + LPR * (i0 + b), ch[r][b]);
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+      if (i0 + b < cpl)
+#pragma unroll
+        for (int r = 0; r < NROWS; ++r) chunk_fma<FMT, NT>(ch[r][b], xs, K, l8 + LPR * (i0 + b), acc[r]);
+  }
+}
+
+template <int FMT, bool DOWN, int NT, int LPR>
+__device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst, const BlobLayout &L, const FfnArgs &a,
+                                         int feat, const __nv_bfloat16 *xs, int nt, int p0, float gs0, float gs1,
+                                         int l8) {
+  if constexpr (!DOWN) {
+    if (feat >= a.I) return;
+    const RowPtrs rp[2] = {row_ptrs<FMT>(blob, L, false, feat, a.H), row_ptrs<FMT>(blob, L, false, a.I + feat, a.H)};
+    RowPtrs dp[2];
+    if (slot_dst) {
+      dp[0] = row_ptrs<FMT>(slot_dst, L, false, feat, a.H);
+      dp[1] = row_ptrs<FMT>(slot_dst, L, false, a.I + feat, a.H);
+    }
+    float acc[2][NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.0f;
+    rows_dot<FMT, NT, 2, LPR>(rp, slot_dst ? dp : nullptr, a.H, xs, l8, acc);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float g = group_sum<LPR>(acc[0][t]) * gs0;
+      const float u = group_sum<LPR>(acc[1][t]) * gs1;
+      if (l8 == t && t < nt) a.h[(size_t)(p0 + t) * a.I + feat] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+    }
+  } else {
+    if (feat >= a.H) return;
+    const RowPtrs rp[1] = {row_ptrs<FMT>(blob, L, true, feat, a.I)};
+    RowPtrs dp[1];
+    if (slot_dst) dp[0] = row_ptrs<FMT>(slot_dst, L, true, feat, a.I);
+    float acc[1][NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[0][t] = 0.0f;
+    rows_dot<FMT, NT, 1, LPR>(rp, slot_dst ? dp : nullptr, a.I, xs, l8, acc);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float v = group_sum<LPR>(acc[0][t]) * gs0;
+      if (l8 == t && t < nt) a.y[(size_t)(p0 + t) * a.H + feat] = v;
+    }
+  }
+}
+
+// Work of one CTA (KW warps) on one (distinct expert u, feature block bx):
+// KW * 32 / LPR * fpw output features, all of the expert's tokens, NT (>= the
+// tokens any expert of the call has, up to kTokChunk) token rows per pass.
+// xs: shared memory for NT activation rows of K.
+template <int FMT, bool DOWN, int NT, int LPR, int KW>
+__device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int fpw, __nv_bfloat16 *xs) {
+  // fpw passes per warp over feature groups: long rows (large K) give each CTA
+  // more features, so that the staged activations serve more weight bytes
+  const int kFeatPerCta = KW * (32 / LPR) * fpw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l8 = lane & (LPR - 1);
+  bool work = u < a.plan.n[0];
+  int hit = 1;
+  if (work) {
+    hit = a.plan.u_hit[u];
+    if ((a.only == 1 && !hit) || (a.only == 2 && hit)) work = false;
+  }
+  if (work) {
+    const int e = a.plan.u_expert[u];
+    const int off = a.plan.offsets[e];
+    const int n = a.plan.offsets[e + 1] - off;
+    uint8_t *slot = const_cast<uint8_t *>(a.slot_bank) + (size_t)a.plan.u_slot[u] * a.slot_stride;
+    const uint8_t *blob = slot;
+    uint8_t *pull_dst = nullptr;
+    if (a.pull && !hit) {
+      // a miss read straight from pinned host memory over PCIe; the bytes read
+      // are also written into its slot, so later calls hit
+      blob = reinterpret_cast<const uint8_t *>(a.pool_dev[(size_t)a.layer * a.E + e]);
+      pull_dst = slot;
+    }
+    const BlobLayout L = blob_layout(FMT, a.H, a.I);
+    const int K = DOWN ? a.I : a.H;
+    float gs0 = 1.0f, gs1 = 1.0f;
+    if constexpr (FMT == FMT_NVFP4) {
+      const float *gs = reinterpret_cast<const float *>(blob + L.gscale);
+      gs0 = DOWN ? gs[2] : gs[0];
+      gs1 = gs[1];
+      if (DOWN && pull_dst && bx == 0 && threadIdx.x == 0)
+        *reinterpret_cast<uint4 *>(pull_dst + L.gscale) = *reinterpret_cast<const uint4 *>(blob + L.gscale);
+    }
+    const int feat0 = bx * kFeatPerCta + warp * (32 / LPR) + lane / LPR;
+    {
+      // ask L2 for this lane's weight chunks now, so that their DRAM latency
+      // overlaps the activation staging below
+      const int cpl = K / (32 * LPR);
+      const int cbytes = FMT == FMT_BF16 ? 64 : 16;
+      for (int fp = 0; fp < fpw; ++fp) {
+        const int feat = feat0 + fp * KW * (32 / LPR);
+        if (feat >= (DOWN ? a.H : a.I)) break;
+#pragma unroll
+        for (int r = 0; r < (DOWN ? 1 : 2); ++r) {
+          const RowPtrs rp = row_ptrs<FMT>(blob, L, DOWN, DOWN ? feat : (r == 0 ? feat : a.I + feat), K);
+          for (int i = 0; i < cpl; ++i) {
+            const uint8_t *p = rp.codes + (size_t)(l8 + LPR * i) * cbytes;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+          }
+        }
+      }
+    }
+    for (int c0 = 0; c0 < n; c0 += kTokChunk) {
+      const int nt = min(kTokChunk, n - c0);
+      // stage the chunk's activations (bf16 rows of K) in shared memory
+      const int vec_per_row = K / 8;
+      for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) {
+        const int t = i / vec_per_row, v = i - t * vec_per_row;
+        const __nv_bfloat16 *src;
+        if (DOWN) {
+          src = a.h + (size_t)(off + c0 + t) * a.I;
+        } else {
+          const int pair = a.plan.perm[off + c0 + t];
+          src = a.x + (size_t)(pair / a.k) * a.H;
+        }
+        reinterpret_cast<uint4 *>(xs + (size_t)t * K)[v] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+      }
+      __syncthreads();
+      // rows nt..NT-1 of xs may hold stale data: their dot products are computed and dropped
+      for (int fp = 0; fp < fpw; ++fp)
+        ffn_rows<FMT, DOWN, NT, LPR>(blob, c0 == 0 ? pull_dst : nullptr, L, a, feat0 + fp * KW * (32 / LPR), xs,
+                                     nt, off + c0, gs0, gs1, l8);
+      __syncthreads();
+    }
+  }
+}
+
+// L2 prefetch of the weight rows of work item (u, bx) (a hit, or every
+// expert when `any`): lets a CTA request all of its items' rows up front.
+template <int FMT, bool DOWN, int LPR, int KW>
+__device__ __forceinline__ void gemv_prefetch(const FfnArgs &a, int u, int bx, int fpw, bool any) {
+  if (u >= a.plan.n[0] || (!any && !a.plan.u_hit[u])) return;
+  const uint8_t *blob = a.slot_bank + (size_t)a.plan.u_slot[u] * a.slot_stride;
+  const BlobLayout L = blob_layout(FMT, a.H, a.I);
+  const int K = DOWN ? a.I : a.H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, l8 = lane & (LPR - 1);
+  const int kFeatPerCta = KW * (32 / LPR) * fpw;
+  const int feat0 = bx * kFeatPerCta + warp * (32 / LPR) + lane / LPR;
+  const int cpl = K / (32 * LPR);
+  const int cbytes = FMT == FMT_BF16 ? 64 : 16;
+  for (int fp = 0; fp < fpw; ++fp) {
+    const int feat = feat0 + fp * KW * (32 / LPR);
+    if (feat >= (DOWN ? a.H : a.I)) break;
+#pragma unroll
+    for (int r = 0; r < (DOWN ? 1 : 2); ++r) {
+      const RowPtrs rp = row_ptrs<FMT>(blob, L, DOWN, DOWN ? feat : (r == 0 ? feat : a.I + feat), K);
+      for (int i = 0; i < cpl; ++i) {
+        const uint8_t *p = rp.codes + (size_t)(l8 + LPR * i) * cbytes;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+      }
+    }
+  }
+}
+
+// Combine fused into the down projection: after its down work on feature
+// block bx, a CTA counts itself done; the CTA that brings the count to
+// `expected` writes out[t][f] = sum_j gates[t][j] * y[inv[t*k+j]][f] for the
+// block's features (rank order j ascending) and resets the counter.
+__device__ __forceinline__ void combine_block(const FfnArgs &a, const CombineArgs &cb, int bx, int feat_per_cta,
+                                              int expected, int *s_flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(cb.counters + bx, 1);
+    *s_flag = prev == expected - 1;
+  }
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  const int f0 = bx * feat_per_cta;
+  for (int i = threadIdx.x; i < cb.T * feat_per_cta; i += blockDim.x) {
+    const int t = i / feat_per_cta, f = f0 + (i - t * feat_per_cta);
+    if (f >= a.H) continue;
+    float acc = 0.0f;
+    for (int j = 0; j < a.k; ++j) {
+      const float g = cb.gates[(size_t)t * a.k + j];
+      acc = fmaf(g, __ldcg(a.y + (size_t)cb.inv[(size_t)t * a.k + j] * a.H + f), acc);
+    }
+    cb.out[(size_t)t * a.H + f] = __float2bfloat16_rn(acc);
+  }
+  if (threadIdx.x == 0) cb.counters[bx] = 0;
+}
+
+}  // namespace
+}  // namespace ftmoe

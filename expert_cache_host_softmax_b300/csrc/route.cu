@@ -25,389 +25,18 @@
 
 #include "ft_internal.cuh"
 
+#include "route_dev.cuh"
+
 namespace ftmoe {
 
 namespace {
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// Exclusive block-wide prefix sum of v; *total receives the block sum.
-// All threads of the block must call it.  s_warp holds >= 32 ints.
-__device__ int block_excl_scan(int v, int *s_warp, int *total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int t = lane < nw ? s_warp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    s_warp[lane] = t;
-  }
-  __syncthreads();
-  const int base = w ? s_warp[w - 1] : 0;
-  *total = s_warp[nw - 1];
-  __syncthreads();
-  return base + x - v;
-}
-
-// Order-preserving map of a float to an unsigned key (larger float, larger
-// key); +0 and -0 map to the same key.  key_of(-inf) = 0x007FFFFF > 0, so a
-// key of 0 marks "taken or padding".
-__device__ __forceinline__ uint32_t key_of(float x) {
-  if (x == 0.0f) x = 0.0f;
-  const uint32_t u = __float_as_uint(x);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float float_of(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// One warp selects the k largest logits of one token (ties to the lower id,
-// NaN treated as -inf) and writes their ids and softmax gates.  Lane l holds
-// experts l, l+32, ..; each round takes the warp-wide largest key (redux.sync)
-// and, among lanes holding it, the lowest expert id (a second redux).
-// Returns, in lanes 0..k-1, the selected expert of rank `lane` (else -1).
-template <int NV>
-__device__ int warp_topk_softmax_t(const float *__restrict__ row, int E, int k, int32_t *out_idx, float *out_gate) {
-  const int lane = threadIdx.x & 31;
-  uint32_t key[NV];
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = lane + 32 * i;
-    float x = e < E ? __ldg(row + e) : -INFINITY;
-    if (isnan(x)) x = -INFINITY;
-    key[i] = e < E ? key_of(x) : 0u;
-  }
-  auto local_best = [&](uint32_t &bk, int &bi) {
-    bk = 0u;
-    bi = 0;
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (key[i] > bk) {   // strict: the lowest i (lowest id) keeps a tie
-        bk = key[i];
-        bi = i;
-      }
-  };
-  uint32_t bk;
-  int bi;
-  local_best(bk, bi);
-  float my_v = -INFINITY;
-  int my_i = -1;
-  for (int j = 0; j < k; ++j) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-    const uint32_t cand = bk == m ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
-    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-    if (lane == (int)(win & 31u)) {
-#pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if (i == (int)(win >> 5)) key[i] = 0u;
-      local_best(bk, bi);
-    }
-    if (lane == j) {
-      my_v = float_of(m);
-      my_i = (int)win;
-    }
-  }
-  const float mx = __shfl_sync(0xffffffffu, my_v, 0);
-  float z = lane < k ? expf(my_v - mx) : 0.0f;
-  float sum = z;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < k) {
-    out_idx[lane] = my_i;
-    out_gate[lane] = z / sum;
-  }
-  return lane < k ? my_i : -1;
-}
-
-__device__ __forceinline__ int warp_topk_softmax(const float *__restrict__ row, int E, int k, int32_t *out_idx,
-                                                 float *out_gate) {
-  if (E <= 32) return warp_topk_softmax_t<1>(row, E, k, out_idx, out_gate);
-  if (E <= 64) return warp_topk_softmax_t<2>(row, E, k, out_idx, out_gate);
-  if (E <= 128) return warp_topk_softmax_t<4>(row, E, k, out_idx, out_gate);
-  if (E <= 256) return warp_topk_softmax_t<8>(row, E, k, out_idx, out_gate);
-  return warp_topk_softmax_t<kMaxExperts / 32>(row, E, k, out_idx, out_gate);
-}
-
-// Stable scatter of pairs [p0, p1) by expert.  s_base[e] is the next free
-// permuted position of expert e and is advanced.  s_wcnt holds nwarps*E ints.
-__device__ void block_rank_scatter(const int32_t *__restrict__ idx, int p0, int p1, int E, int *s_base,
-                                   int *s_wcnt, int32_t *__restrict__ perm, int32_t *__restrict__ inv) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
-  if (p1 - p0 <= 32) {
-    // one warp: rank among equal ids by lane order
-    if (w == 0) {
-      const int p = p0 + lane;
-      int e = p < p1 ? idx[p] : -1;
-      const bool valid = e >= 0 && e < E;
-      if (!valid) e = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (valid) {
-        const int pos = s_base[e] + __popc(peers & lanemask_lt());
-        perm[pos] = p;
-        inv[p] = pos;
-      }
-      __syncwarp();
-      if (valid && lane == __ffs(peers) - 1) s_base[e] += __popc(peers);
-    }
-    __syncthreads();
-    return;
-  }
-  for (int r0 = p0; r0 < p1; r0 += blockDim.x) {
-    for (int i = tid; i < nw * E; i += blockDim.x) s_wcnt[i] = 0;
-    __syncthreads();
-    const int p = r0 + tid;
-    int e = p < p1 ? idx[p] : -1;
-    const bool valid = e >= 0 && e < E;   // out-of-range ids are not placed
-    if (!valid) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank_w = __popc(peers & lanemask_lt());
-    if (valid && lane == __ffs(peers) - 1) s_wcnt[w * E + e] = __popc(peers);
-    __syncthreads();
-    for (int e2 = tid; e2 < E; e2 += blockDim.x) {
-      int run = s_base[e2];
-      for (int ww = 0; ww < nw; ++ww) {
-        const int c = s_wcnt[ww * E + e2];
-        s_wcnt[ww * E + e2] = run;
-        run += c;
-      }
-      s_base[e2] = run;
-    }
-    __syncthreads();
-    if (valid) {
-      const int pos = s_wcnt[w * E + e] + rank_w;
-      perm[pos] = p;
-      inv[p] = pos;
-    }
-    __syncthreads();
-  }
-}
-
-struct PlanSmem {
-  int *s_count;   // [E] tokens per expert in this call
-  int *s_uexp;    // [E]
-  int *s_victim;  // [E]
-  unsigned *s_bits;  // [(S+31)/32]
-  int *s_warp;    // [33]: scan partials, [32] a counter
-  int *s_keyslot;    // [E] this layer's key -> slot, loaded up front (or null)
-  int *s_victim_key; // [E] key held by each victim slot (with s_keyslot)
-};
-
-// The cache-table entries a thread needs, loaded at kernel start so that the
-// plan itself waits on no global memory: its range of the recency list and the
-// key held by each of those slots.
-constexpr int kPre = 8;
-struct Prefetch {
-  int n;              // entries held, or -1 (range longer than kPre: read in place)
-  int ord[kPre], key[kPre];
-  unsigned long long st[5];   // thread 0: the cumulative counters
-};
-
-__device__ __forceinline__ void prefetch_tables(const RouteArgs &a, int *s_keyslot, Prefetch &pf) {
-  const int tid = threadIdx.x, NT = blockDim.x;
-  pf.n = -1;
-  if (tid == 0)
-    for (int i = 0; i < 5; ++i) pf.st[i] = a.cache.stats[i];
-  if (a.mode != MODE_LRU) return;
-  for (int e = tid; e < a.E; e += NT) s_keyslot[e] = a.cache.key_slot[a.layer * a.E + e];
-  const int per = (a.S + NT - 1) / NT;
-  if (per > kPre) return;
-  const int i0 = min(a.S, tid * per), i1 = min(a.S, i0 + per);
-  pf.n = i1 - i0;
-#pragma unroll
-  for (int q = 0; q < kPre; ++q)
-    if (q < pf.n) pf.ord[q] = a.cache.order_in[i0 + q];
-#pragma unroll
-  for (int q = 0; q < kPre; ++q)
-    if (q < pf.n) pf.key[q] = a.cache.slot_key[pf.ord[q]];
-}
-
-// Distinct experts of the call, slot lookup, LRU update, plan and stats.
-// One CTA.  Needs blockDim.x >= E.  With a prefetch (pf.n >= 0 and
-// sm.s_keyslot set), the tables are read from what prefetch_tables loaded.
-// The miss list is published to the host before the statistics are updated.
-__device__ void block_plan(const RouteArgs &a, const PlanSmem &sm, const Prefetch &pf) {
-  const int tid = threadIdx.x, NT = blockDim.x, E = a.E, S = a.S;
-  const int flag = (tid < E) && sm.s_count[tid] > 0;
-  int nU;
-  const int u = block_excl_scan(flag, sm.s_warp, &nU);
-  if (flag) sm.s_uexp[u] = tid;
-  __syncthreads();
-
-  int key = -1, slot = -1, hit = 0;
-  if (tid < nU) {
-    const int e = sm.s_uexp[tid];
-    key = a.layer * E + e;
-    if (a.mode == MODE_LRU) {
-      slot = sm.s_keyslot ? sm.s_keyslot[e] : a.cache.key_slot[key];
-      hit = slot >= 0;
-    } else {
-      slot = a.bank * E + e;
-      hit = 1;
-    }
-  }
-  int nH;
-  const int hrank = block_excl_scan(tid < nU && hit, sm.s_warp, &nH);
-  const int nM = nU - nH;
-  const int mrank = tid - hrank;
-  int evicted = -1;
-
-  if (a.mode == MODE_LRU) {
-    const int nwords = (S + 31) >> 5;
-    for (int i = tid; i < nwords; i += NT) sm.s_bits[i] = 0u;
-    __syncthreads();
-    if (tid < nU && hit) atomicOr(&sm.s_bits[slot >> 5], 1u << (slot & 31));
-    __syncthreads();
-    const int per = (S + NT - 1) / NT;
-    const int i0 = min(S, tid * per), i1 = min(S, i0 + per);
-    int cnt = 0, r;
-    if (pf.n >= 0) {
-#pragma unroll
-      for (int q = 0; q < kPre; ++q)
-        if (q < pf.n) cnt += !((sm.s_bits[pf.ord[q] >> 5] >> (pf.ord[q] & 31)) & 1u);
-      int nonhit;
-      r = block_excl_scan(cnt, sm.s_warp, &nonhit);
-#pragma unroll
-      for (int q = 0; q < kPre; ++q) {
-        if (q >= pf.n) continue;
-        const int s = pf.ord[q];
-        if ((sm.s_bits[s >> 5] >> (s & 31)) & 1u) continue;
-        if (r < nM) {
-          sm.s_victim[r] = s;
-          sm.s_victim_key[r] = pf.key[q];
-        } else {
-          a.cache.order_out[r - nM] = s;
-        }
-        ++r;
-      }
-    } else {
-      for (int i = i0; i < i1; ++i) {
-        const int s = a.cache.order_in[i];
-        cnt += !((sm.s_bits[s >> 5] >> (s & 31)) & 1u);
-      }
-      int nonhit;
-      r = block_excl_scan(cnt, sm.s_warp, &nonhit);
-      for (int i = i0; i < i1; ++i) {
-        const int s = a.cache.order_in[i];
-        if ((sm.s_bits[s >> 5] >> (s & 31)) & 1u) continue;
-        if (r < nM) sm.s_victim[r] = s;
-        else a.cache.order_out[r - nM] = s;
-        ++r;
-      }
-    }
-    __syncthreads();
-    if (tid < nU) {
-      if (hit) {
-        a.cache.order_out[S - nH - nM + hrank] = slot;
-      } else {
-        const int v = sm.s_victim[mrank];
-        a.cache.order_out[S - nM + mrank] = v;
-        const int ek = pf.n >= 0 ? sm.s_victim_key[mrank] : a.cache.slot_key[v];
-        if (ek >= 0) {
-          a.cache.key_slot[ek] = -1;
-          evicted = ek;
-        }
-        a.cache.slot_key[v] = key;
-        a.cache.key_slot[key] = v;
-        slot = v;
-      }
-    }
-  }
-  // evictions of this call: a count in shared memory (no order needed)
-  if (tid == 0) sm.s_warp[32] = 0;
-  __syncthreads();
-  if (evicted >= 0) atomicAdd(&sm.s_warp[32], 1);
-  __syncthreads();
-  const int nEv = sm.s_warp[32];
-  if (tid < nU) {
-    a.plan.u_expert[tid] = sm.s_uexp[tid];
-    a.plan.u_slot[tid] = slot;
-    a.plan.u_hit[tid] = hit;
-    a.plan.u_evicted[tid] = evicted;
-    if (a.mirror && !hit) {
-      a.mirror[2 + mrank] = key;
-      a.mirror[2 + a.umax + mrank] = slot;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    if (a.mirror) {
-      // the block's miss-list writes precede this fence (barrier above), and
-      // the host reads the list only after it sees the new sequence number
-      a.mirror[1] = nM;
-      __threadfence_system();
-      *(volatile int32_t *)&a.mirror[0] = (int32_t)a.seq;
-    }
-    a.plan.n[0] = nU;
-    a.plan.n[1] = nH;
-    a.plan.n[2] = nM;
-    a.plan.n[3] = nEv;
-    unsigned long long *st = a.cache.stats;
-    const unsigned long long bytes = a.mode == MODE_LRU ? (unsigned long long)nM * a.blob_bytes : 0ull;
-    const unsigned long long hits_ = a.mode == MODE_LRU ? nH : 0, miss_ = a.mode == MODE_LRU ? nM : 0;
-    st[0] = pf.st[0] + nU; st[1] = pf.st[1] + hits_; st[2] = pf.st[2] + miss_; st[3] = pf.st[3] + nEv;
-    st[4] = pf.st[4] + bytes;
-    st[8] = nU; st[9] = hits_; st[10] = miss_; st[11] = nEv; st[12] = bytes;
-  }
-}
-
 // ---------------------------------------------------------------- kernels
 
-// Whole routing of a small call in one CTA: top-k + gates, histogram,
-// offsets, plan, stable scatter.  The cache tables are read at the start,
-// alongside the logits, so the plan waits on no further global loads.
+// Whole routing of a small call in one CTA (see route_small_body).
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
   extern __shared__ int smem[];
-  const int E = a.E, nw = blockDim.x >> 5;
-  int *s_count = smem;                 // E
-  int *s_base = s_count + E;           // E
-  int *s_uexp = s_base + E;            // E
-  int *s_victim = s_uexp + E;          // E
-  int *s_keyslot = s_victim + E;       // E
-  int *s_victim_key = s_keyslot + E;   // E
-  int *s_warp = s_victim_key + E;      // 33
-  int *s_wcnt = s_warp + 33;           // nw*E
-  unsigned *s_bits = (unsigned *)(s_wcnt + nw * E);
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  // the cache tables were last written by the previous call's route kernel,
-  // which has completed (see pdl_trigger); everything else waits for the
-  // kernel before this one
-  Prefetch pf;
-  prefetch_tables(a, s_keyslot, pf);
-  pdl_wait();
-  pdl_trigger();
-  for (int i = tid; i < E; i += blockDim.x) s_count[i] = 0;
-  __syncthreads();
-  for (int t = w; t < a.T; t += nw) {
-    const int e = warp_topk_softmax(a.logits + (size_t)t * E, E, a.k, a.plan.topk_idx + (size_t)t * a.k,
-                                    a.plan.gates + (size_t)t * a.k);
-    if (lane < a.k) atomicAdd(&s_count[e], 1);
-  }
-  __syncthreads();
-  int total;
-  const int off = block_excl_scan(tid < E ? s_count[tid] : 0, s_warp, &total);
-  if (tid < E) {
-    a.plan.offsets[tid] = off;
-    s_base[tid] = off;
-  }
-  if (tid == 0) a.plan.offsets[E] = total;
-  PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, a.mode == MODE_LRU ? s_keyslot : nullptr, s_victim_key};
-  block_plan(a, sm, pf);
-  __syncthreads();
-  block_rank_scatter(a.plan.topk_idx, 0, a.T * a.k, E, s_base, s_wcnt, a.plan.perm, a.plan.inv);
+  route_small_body(a, smem, true);
 }
 
 // Multi-CTA path, step 1: top-k + gates for kChunkTokens tokens per CTA
@@ -515,8 +144,8 @@ __global__ void __launch_bounds__(256) scatter_chunk_kernel(const int32_t *__res
 }
 
 // Threads of the single-CTA routing kernel: at least E (one per expert in
-// the plan), at least 128, a whole number of warps.
-int small_threads(int E) { return std::min(kRouteThreads, std::max(128, (E + 31) / 32 * 32)); }
+// the plan), at least 256, a whole number of warps.
+int small_threads(int E) { return std::min(kRouteThreads, std::max(256, (E + 31) / 32 * 32)); }
 
 size_t small_smem_bytes(int E, int S) {
   const size_t nw = small_threads(E) / 32;
@@ -528,6 +157,8 @@ size_t plan_smem_bytes(int E, int S) {
 }
 
 }  // namespace
+
+size_t route_small_smem(int E, int S) { return small_smem_bytes(E, S); }
 
 void route_init_attributes() {
   cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);

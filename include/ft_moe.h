@@ -192,7 +192,8 @@ enum ft_prof_class {
   FT_PROF_COMBINE = 4,     /* gate-weighted combine */
   FT_PROF_MISS_COPY = 5,   /* the misses' host->device copies of one call (copy stream) */
   FT_PROF_STREAM_COPY = 6, /* one layer's staging copies in STREAM mode (copy stream) */
-  FT_PROF_CLASSES = 7
+  FT_PROF_LAYER = 7,       /* the fused decode-layer kernel (routing, FFN and combine of one call) */
+  FT_PROF_CLASSES = 8
 };
 
 /* Profiling: while enabled, every forward brackets each step class with CUDA
@@ -236,6 +237,17 @@ enum ft_miss_path {
  * cache decisions, counters and results are the same on both paths.  Waits for
  * the handle's outstanding work.  Errors: FT_ERR_ARG. */
 int ft_moe_set_miss_path(ft_moe *h, int path);
+
+/* on != 0: decode calls (LRU mode, GEMV kernel, at most 16 tokens, E <= 256,
+ * not under capture) run as one cooperative kernel: routing and the LRU plan,
+ * the hits' gate/up, then (once the copy stream has written a flag after the
+ * misses' copies) the misses' gate/up, a grid barrier, and the down projection
+ * with the combine.  Default off (separate kernels); the results are identical
+ * bit for bit.  The fused kernel waits on the copy stream, so tools that
+ * serialise all GPU work (profilers) see it wait out its time limit unless the
+ * misses are pulled (FT_MISS_PULL).  Waits for the handle's outstanding work.
+ * Errors: FT_ERR_ARG. */
+int ft_moe_set_decode_fusion(ft_moe *h, int on);
 
 /* Bytes between consecutive slots in the device slot bank. */
 int64_t ft_moe_slot_stride(const ft_moe *h);

@@ -277,6 +277,39 @@ def test_auto_picks_gemv_for_decode():
     gpu.close()
 
 
+# ------------------------------------------------------------ fused decode-layer kernel
+
+@pytest.mark.parametrize("fmt,T,path", [("nvfp4", 1, "copy"), ("mxfp4", 3, "copy"), ("bf16", 8, "copy"),
+                                        ("nvfp4", 2, "pull")])
+def test_fused_decode_matches_split_kernels(fmt, T, path):
+    # the one-kernel decode call and the separate kernels compute every value
+    # the same way: outputs, traces and counters are identical bit for bit
+    H, I, E, k, L, S = 512, 768, 16, 2, 3, 10 + 2 * T
+    seed = 131 + T
+    fused, orc, pool = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed)
+    fused.set_decode_fusion(True)
+    split = F.MoELayerStack(H, E, k, I, fmt, S, L, T)
+    split.load_pool(pool.pointers, keepalive=pool)
+    split.set_decode_fusion(False)
+    for g in (fused, split):
+        g.set_miss_path(path)
+    for step in range(10):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, T, H, E, step, layer, zipf=0.6)
+            xd, lgd = Hn.to_dev(x, lg)
+            b = split.forward(layer, xd, lgd)
+            outs = []
+            _check_call(fused, orc, layer, x, lg, gemm_check=(step % 4 == 0), outs=outs)
+            torch.cuda.synchronize()
+            assert fused.trace() == split.trace()
+            assert torch.equal(outs[0].view(torch.int16), b.view(torch.int16))
+    cf, _ = fused.stats()
+    cs, _ = split.stats()
+    assert cf == cs and cf["misses"] > 0
+    fused.close()
+    split.close()
+
+
 # ------------------------------------------------------------ misses read over PCIe by the kernels
 
 @pytest.mark.parametrize("fmt,T", [("nvfp4", 1), ("mxfp4", 2), ("bf16", 3), ("nvfp4", 6)])
