@@ -22,8 +22,8 @@ FMT = {"bf16": FT_FMT_BF16, "nvfp4": FT_FMT_NVFP4, "mxfp4": FT_FMT_MXFP4}
 FT_MODE_LRU, FT_MODE_STREAM = 0, 1
 FT_FFN_AUTO, FT_FFN_GEMV, FT_FFN_TC = 0, 1, 2
 FFN_KERNEL = {"auto": FT_FFN_AUTO, "gemv": FT_FFN_GEMV, "tc": FT_FFN_TC}
-FT_MISS_COPY, FT_MISS_PULL = 0, 1
-MISS_PATH = {"copy": FT_MISS_COPY, "pull": FT_MISS_PULL}
+FT_MISS_COPY, FT_MISS_PULL, FT_MISS_KERNEL, FT_MISS_AUTO = 0, 1, 2, 3
+MISS_PATH = {"copy": FT_MISS_COPY, "pull": FT_MISS_PULL, "kernel": FT_MISS_KERNEL, "auto": FT_MISS_AUTO}
 FT_OK, FT_ERR_ARG, FT_ERR_CUDA, FT_ERR_OOM, FT_ERR_NOT_PINNED = 0, -1, -2, -3, -4
 FT_ERR_CACHE_TOO_SMALL, FT_ERR_STATE, FT_ERR_TIMEOUT, FT_ERR_DEVICE = -5, -6, -7, -8
 STATUS_NAMES = {0: "FT_OK", -1: "FT_ERR_ARG", -2: "FT_ERR_CUDA", -3: "FT_ERR_OOM", -4: "FT_ERR_NOT_PINNED",
@@ -32,7 +32,7 @@ STATUS_NAMES = {0: "FT_OK", -1: "FT_ERR_ARG", -2: "FT_ERR_CUDA", -3: "FT_ERR_OOM
 #: every symbol include/ft_moe.h declares
 EXPORTED = ("ft_moe_blob_bytes", "ft_moe_create", "ft_moe_load_pool", "ft_moe_set_mode", "ft_moe_forward",
             "ft_cache_stats", "ft_cache_reset", "ft_cache_trace", "ft_moe_last_routing", "ft_moe_last_activations",
-            "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_set_ffn_kernel", "ft_moe_last_ffn_kernel", "ft_moe_set_miss_path", "ft_moe_set_decode_fusion",
+            "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_set_ffn_kernel", "ft_moe_last_ffn_kernel", "ft_moe_set_miss_path", "ft_moe_miss_path", "ft_moe_set_decode_fusion",
             "ft_moe_slot_stride", "ft_moe_kernel_launches",
             "ft_last_error", "ft_moe_destroy", "ft_topk_softmax", "ft_permute_workspace_bytes", "ft_permute", "ft_permute_noalloc")
 
@@ -79,6 +79,7 @@ def lib():
         L.ft_moe_profile_read.argtypes = [vp, vp, vp, i32]
         L.ft_moe_set_ffn_kernel.argtypes = [vp, i32]
         L.ft_moe_last_ffn_kernel.argtypes = [vp]
+        L.ft_moe_miss_path.argtypes = [vp]
         L.ft_moe_set_miss_path.argtypes = [vp, i32]
         L.ft_moe_set_decode_fusion.argtypes = [vp, i32]
         L.ft_moe_kernel_launches.restype = i64
@@ -222,13 +223,21 @@ class MoELayerStack:
         _check(lib().ft_moe_set_ffn_kernel(self._h, w), self._h)
 
     def set_decode_fusion(self, on=True):
-        """One cooperative kernel per decode call (default) or separate kernels."""
+        """One cooperative kernel per decode call, or separate kernels (default)."""
         _check(lib().ft_moe_set_decode_fusion(self._h, 1 if on else 0), self._h)
 
     def set_miss_path(self, path):
-        """"copy" (cudaMemcpyAsync, default) or "pull" (kernels read misses over PCIe)."""
+        """"copy" (cudaMemcpyAsync issued by the host), "pull" (the FFN kernels read misses over
+        PCIe), "kernel" (the GPU copies them; no host round trip) or "auto" (default: "kernel"
+        for experts up to 8 MiB, else "copy")."""
         w = MISS_PATH[path] if isinstance(path, str) else int(path)
         _check(lib().ft_moe_set_miss_path(self._h, w), self._h)
+
+    @property
+    def miss_path(self):
+        """The miss path LRU calls take ("auto" resolved): "copy", "pull" or "kernel"."""
+        inv = {v: k_ for k_, v in MISS_PATH.items()}
+        return inv.get(int(lib().ft_moe_miss_path(self._h)))
 
     @property
     def last_ffn_kernel(self):

@@ -21,6 +21,7 @@
 // copies).
 #include "gemv_dev.cuh"
 #include "route_dev.cuh"
+#include "wait_dev.cuh"
 
 namespace ftmoe {
 
@@ -28,36 +29,6 @@ namespace {
 
 constexpr int kMegaWarps = 8;
 constexpr int kMegaThreads = kMegaWarps * 32;
-constexpr unsigned long long kMegaWaitNs = 2000000000ull;   // 2 s per wait
-
-__device__ __forceinline__ unsigned long long mega_timer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Thread 0 waits until *flag == want (bounded); the whole CTA learns the outcome.
-__device__ __forceinline__ bool cta_wait_flag(const int *flag, int want, int *err, int site, int *s_ok) {
-  if (threadIdx.x == 0) {
-    const volatile int *vf = flag;
-    bool ok = true;
-    if (*vf != want) {
-      const unsigned long long t0 = mega_timer();
-      while (*vf != want) {
-        if (mega_timer() - t0 > kMegaWaitNs) {
-          atomicCAS(err, 0, site);
-          ok = false;
-          break;
-        }
-      }
-    }
-    __threadfence();
-    *s_ok = ok;
-  }
-  __syncthreads();
-  return *s_ok != 0;
-}
-
 // Grid-wide barrier over G resident CTAs (bounded).  count returns to 0 after
 // each use; gen only grows.
 __device__ __forceinline__ bool grid_barrier(int *count, int *gen, int G, int *err, int site, int *s_ok) {
@@ -72,9 +43,9 @@ __device__ __forceinline__ bool grid_barrier(int *count, int *gen, int G, int *e
       __threadfence();
       atomicAdd(gen, 1);
     } else {
-      const unsigned long long t0 = mega_timer();
+      const unsigned long long t0 = dev_timer_ns();
       while (*vg == g) {
-        if (mega_timer() - t0 > kMegaWaitNs) {
+        if (dev_timer_ns() - t0 > kWaitNs) {
           atomicCAS(err, 0, site);
           ok = false;
           break;

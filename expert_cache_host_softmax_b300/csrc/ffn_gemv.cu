@@ -40,7 +40,20 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
   pdl_wait();      // the plan, activations and slots come from earlier kernels
   pdl_trigger();
-  gemv_block<FMT, DOWN, NT, LPR, kWarps>(a, blockIdx.y, blockIdx.x, fpw, xs);
+  if constexpr (!DOWN) {
+    if ((int)blockIdx.y < a.copy_rows) {
+      // a copying CTA (the grid's first rows, so dispatched before any CTA
+      // that waits for them): gate/up bytes of every miss, the flag, then
+      // the down bytes
+      const long long nct = (long long)a.copy_rows * gridDim.x;
+      const long long t = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+      copy_misses(a.mc, 0, 2, t, nct * blockDim.x);
+      cta_arrive_last_sets(a.copy_sync + 1, a.copy_sync, (int)nct, a.seq_raised);
+      copy_misses(a.mc, 2, 3, t, nct * blockDim.x);
+      return;
+    }
+  }
+  gemv_block<FMT, DOWN, NT, LPR, kWarps>(a, blockIdx.y - (DOWN ? 0 : a.copy_rows), blockIdx.x, fpw, xs);
   if constexpr (DOWN) {
     if (cb.counters == nullptr) return;
     __shared__ int s_last;
@@ -87,7 +100,7 @@ cudaError_t launch_t(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
   const int K = DOWN ? a.I : a.H;
   const int fpw = K >= 4096 ? 4 : 1;
   const int fpc = kWarps * (32 / LPR) * fpw;
-  dim3 grid((feats + fpc - 1) / fpc, a.umax);
+  dim3 grid((feats + fpc - 1) / fpc, a.umax + (DOWN ? 0 : a.copy_rows));
   const size_t smem = (size_t)NT * K * sizeof(__nv_bfloat16);
   return launch_k(ffn_gemv_kernel<FMT, DOWN, NT, LPR>, grid, dim3(kWarps * 32), smem, s, a.pdl != 0, a, cb, fpw);
 }
@@ -140,6 +153,11 @@ void ffn_init_attributes() {
 }
 
 int combine_tiles(int H) { return (H + kMinFeatPerCta - 1) / kMinFeatPerCta; }
+
+int gateup_feature_blocks(int H, int I) {
+  const int fpc = kWarps * (32 / lanes_per_row(H)) * (H >= 4096 ? 4 : 1);
+  return (I + fpc - 1) / fpc;
+}
 
 bool gemv_fuses_combine(int T) { return T <= kFusedCombineMaxT; }
 

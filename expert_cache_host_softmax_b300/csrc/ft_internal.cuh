@@ -17,6 +17,7 @@ enum { MODE_LRU = 0, MODE_STREAM = 1 };
 
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
+constexpr int kMissScaleArgs = 64;   // misses whose global scales travel as kernel arguments
 constexpr int kRouteThreads = 1024;       // single-CTA routing / plan kernels
 constexpr int kChunkTokens = 32;          // tokens per CTA in the multi-CTA routing path
 constexpr int kSmallRoutePairs = 2048;    // calls with T*k up to this route in one CTA
@@ -52,6 +53,8 @@ struct PlanBufs {
   int32_t *u_slot;     // [Umax]
   int32_t *u_hit;      // [Umax]
   int32_t *u_evicted;  // [Umax]
+  int4 *u_info;        // [Umax]  {expert, slot, first permuted position, (tokens << 1) | hit}, hits first
+  int2 *miss;          // [Umax]  {key, slot} of each miss, ascending expert id (count: n[2])
   int32_t *n;          // [4]: n_unique, n_hit, n_miss, n_evicted
 };
 
@@ -92,6 +95,20 @@ size_t permute_scratch_ints(int T, int k, int E);
 void route_init_attributes();
 
 // Expert FFN (ffn_gemv.cu)
+// Misses copied on the device: byte ranges of every miss's blob (seg[r] =
+// [begin, end), 16-byte aligned; empty ranges allowed) from its pinned host
+// blob (device-visible address pool_dev[key]) into its slot.  Ranges 0-1 hold
+// what the gate/up projection reads (its rows and scales, and the NVFP4
+// global scales at the blob's end), range 2 the down rows and scales.
+struct MissCopyArgs {
+  const int2 *miss;          // plan.miss
+  const int32_t *n;          // plan counts: n[2] = misses
+  const uint64_t *pool_dev;
+  uint8_t *slots;
+  long long slot_stride;
+  long long seg[3][2];
+};
+
 struct FfnArgs {
   const uint8_t *slot_bank;
   long long slot_stride;
@@ -110,6 +127,23 @@ struct FfnArgs {
   int layer;
   int pull;
   int pdl;                    // launch with programmatic dependent launch (follows a kernel directly)
+  // misses copied inside the gate/up kernel (GEMV calls with FT_MISS_KERNEL):
+  // the first copy_rows rows of its grid copy ranges 0-1 of every miss, raise
+  // copy_sync[0] = seq, then copy range 2; the misses' CTAs wait for the flag.
+  // The down kernel starts after the whole gate/up grid (and so after range 2).
+  MissCopyArgs mc;
+  int copy_rows;
+  int *copy_sync;             // [0] flag, [1] arrival count
+  int seq;                    // the flag value this call's miss CTAs wait for
+  int seq_raised;             // the value its copying CTAs raise (seq, unless a fault is injected)
+  // NVFP4 gate/up of misses whose copies are still landing their down part
+  // (which holds the global scales): the scales, read by the host from the
+  // pool, for each missed expert; n = 0 reads them from the slot
+  struct {
+    int n;
+    int expert[kMissScaleArgs];
+    float gate[kMissScaleArgs], up[kMissScaleArgs];
+  } ms;
 };
 // Combine fused into the down GEMV (small calls): out[t] = sum_j gates[t][j] *
 // y[inv[t*k+j]], written by the last CTA of each feature tile.  counters: one
@@ -123,12 +157,17 @@ struct CombineArgs {
   int T;
 };
 int combine_tiles(int H);
+int gateup_feature_blocks(int H, int I);   // grid.x of the gate/up GEMV
 bool gemv_fuses_combine(int T);
 cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *gates, const int32_t *inv, int T, int k, int H,
                            __nv_bfloat16 *out, cudaStream_t s);
 void ffn_init_attributes();
+
+// Ranges [seg0, seg1) of a.seg, of every miss, by a kernel on stream s.
+cudaError_t launch_miss_copy(const MissCopyArgs &a, int seg0, int seg1, cudaStream_t s);
+int tc_num_sms();   // SMs of the current device
 
 // Expert FFN on the tensor cores (grouped_gemm.cu)
 void gemm_init_attributes();

@@ -32,6 +32,11 @@
 
 using namespace ftmoe;
 
+constexpr int kProfRing = 64;   // event pairs per profiled step class
+// CTAs (of 128 threads) that copy the misses inside the gate/up GEMV kernel:
+// two per SM, 8 KB of 16-byte loads in flight each
+constexpr int kCopyCtas = 296;
+
 struct ft_moe {
   int H = 0, E = 0, k = 0, I = 0, fmt = 0, S = 0, L = 0, Tmax = 0, umax = 0, mode = MODE_LRU;
   int64_t blob_bytes = 0, slot_stride = 0;
@@ -62,8 +67,12 @@ struct ft_moe {
   uint64_t last_streamed = 0, last_stream_bytes = 0;
   // optional per-step timing (ft_moe_set_profiling)
   bool prof = false;
-  cudaEvent_t prof_ev[2 * FT_PROF_CLASSES] = {};
-  bool prof_pending[FT_PROF_CLASSES] = {};
+  // a ring of event pairs per class, folded into the totals only when the
+  // ring wraps or the totals are read: timing does not stall the host, so the
+  // GPU stays ahead of it and a pair spans its kernels, not launch gaps
+  cudaEvent_t prof_ev[FT_PROF_CLASSES][kProfRing][2] = {};
+  int prof_head[FT_PROF_CLASSES] = {};
+  int prof_count[FT_PROF_CLASSES] = {};
   double prof_ms[FT_PROF_CLASSES] = {};
   int64_t prof_launches[FT_PROF_CLASSES] = {};
   int64_t kernel_launches = 0;
@@ -78,9 +87,10 @@ struct ft_moe {
   int *combine_counters = nullptr;   // per feature tile, for the combine fused into the down GEMV
   uint64_t *pool_dev = nullptr;      // device-visible addresses of the pool's blobs [L*E] (FT_MISS_PULL)
   int *mega_sync = nullptr;          // fused decode layer: plan flag, copy flag, grid barrier count and generation
+  int *copy_sync = nullptr;          // misses copied inside the gate/up kernel: flag, arrival count
   int32_t *seq_ring = nullptr;       // pinned: seq_ring[seq % 64] = seq, the source of the copy-flag write
   bool decode_fused = false;   // ft_moe_set_decode_fusion
-  int miss_path = FT_MISS_COPY;
+  int miss_path = FT_MISS_AUTO;
   std::string err;
 };
 
@@ -137,6 +147,8 @@ void free_all(ft_moe *h) {
   cudaFree(h->plan.u_slot);
   cudaFree(h->plan.u_hit);
   cudaFree(h->plan.u_evicted);
+  cudaFree(h->plan.u_info);
+  cudaFree(h->plan.miss);
   cudaFree(h->plan.n);
   cudaFree(h->chunk_counts);
   cudaFree(h->chunk_base);
@@ -147,6 +159,7 @@ void free_all(ft_moe *h) {
   cudaFree(h->combine_counters);
   cudaFree(h->pool_dev);
   cudaFree(h->mega_sync);
+  cudaFree(h->copy_sync);
   if (h->mirror_host) cudaFreeHost(h->mirror_host);
   if (h->seq_ring) cudaFreeHost(h->seq_ring);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
@@ -154,31 +167,39 @@ void free_all(ft_moe *h) {
   for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_copy2, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
                          h->ev_bank_free[0], h->ev_bank_free[1]})
     if (ev) cudaEventDestroy(ev);
-  for (cudaEvent_t ev : h->prof_ev)
-    if (ev) cudaEventDestroy(ev);
+  for (auto &cls : h->prof_ev)
+    for (auto &pair : cls)
+      for (cudaEvent_t ev : pair)
+        if (ev) cudaEventDestroy(ev);
 }
 
 // Profiling: events around one step class on the stream it runs on.
+// Folds the oldest recorded pair of class c into the totals (waits for it).
+void prof_fold_oldest(ft_moe *h, int c) {
+  const int i = (h->prof_head[c] - h->prof_count[c] + kProfRing) % kProfRing;
+  float ms = 0.f;
+  if (cudaEventSynchronize(h->prof_ev[c][i][1]) == cudaSuccess &&
+      cudaEventElapsedTime(&ms, h->prof_ev[c][i][0], h->prof_ev[c][i][1]) == cudaSuccess) {
+    h->prof_ms[c] += ms;
+    h->prof_launches[c] += 1;
+  }
+  --h->prof_count[c];
+}
 void prof_begin(ft_moe *h, int cls, cudaStream_t s) {
-  if (h->prof) cudaEventRecord(h->prof_ev[2 * cls], s);
+  if (!h->prof) return;
+  if (h->prof_count[cls] == kProfRing) prof_fold_oldest(h, cls);
+  cudaEventRecord(h->prof_ev[cls][h->prof_head[cls]][0], s);
 }
 void prof_end(ft_moe *h, int cls, cudaStream_t s) {
   if (!h->prof) return;
-  cudaEventRecord(h->prof_ev[2 * cls + 1], s);
-  h->prof_pending[cls] = true;
+  cudaEventRecord(h->prof_ev[cls][h->prof_head[cls]][1], s);
+  h->prof_head[cls] = (h->prof_head[cls] + 1) % kProfRing;
+  ++h->prof_count[cls];
 }
-// Folds the recorded pairs into the totals (waits for them).
+// Folds every recorded pair into the totals (waits for them).
 void prof_collect(ft_moe *h) {
-  for (int c = 0; c < FT_PROF_CLASSES; ++c) {
-    if (!h->prof_pending[c]) continue;
-    float ms = 0.f;
-    if (cudaEventSynchronize(h->prof_ev[2 * c + 1]) == cudaSuccess &&
-        cudaEventElapsedTime(&ms, h->prof_ev[2 * c], h->prof_ev[2 * c + 1]) == cudaSuccess) {
-      h->prof_ms[c] += ms;
-      h->prof_launches[c] += 1;
-    }
-    h->prof_pending[c] = false;
-  }
+  for (int c = 0; c < FT_PROF_CLASSES; ++c)
+    while (h->prof_count[c] > 0) prof_fold_oldest(h, c);
 }
 
 // Waits for everything the handle has issued, then checks the device error
@@ -198,8 +219,9 @@ int sync_handle(ft_moe *h) {
     FT_CUDA(h, cudaMemset(h->err_dev, 0, sizeof(int)));
     // an aborted kernel may have left its flags or counters mid-way
     FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
+    FT_CUDA(h, cudaMemset(h->copy_sync, 0, 2 * sizeof(int)));
     FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
-    return fail(h, FT_ERR_DEVICE, "a tensor-core FFN kernel gave up waiting (site " + std::to_string(code) + ")");
+    return fail(h, FT_ERR_DEVICE, "a kernel gave up a bounded wait (site " + std::to_string(code) + ")");
   }
   return FT_OK;
 }
@@ -250,6 +272,7 @@ int reset_tables(ft_moe *h, bool warm) {
   h->order_cur = 0;
   FT_CUDA(h, cudaMemset(h->stats_dev, 0, 16 * sizeof(unsigned long long)));
   FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
+  FT_CUDA(h, cudaMemset(h->copy_sync, 0, 2 * sizeof(int)));
   FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
   h->host_warm = h->host_streamed = h->host_bytes = 0;
   h->last_streamed = h->last_stream_bytes = 0;
@@ -272,7 +295,6 @@ int stage_layer(ft_moe *h, int layer) {
   const int b = layer & 1;
   if (h->bank_layer[b] == layer) return FT_OK;
   FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_bank_free[b], 0));
-  if (h->prof && h->prof_pending[FT_PROF_STREAM_COPY]) prof_collect(h);
   prof_begin(h, FT_PROF_STREAM_COPY, h->copy_stream);
   for (int e = 0; e < h->E; ++e)
     FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)(b * h->E + e) * h->slot_stride,
@@ -284,6 +306,15 @@ int stage_layer(ft_moe *h, int layer) {
   h->last_streamed += h->E;
   h->last_stream_bytes += (uint64_t)h->E * h->blob_bytes;
   return FT_OK;
+}
+
+// FT_MISS_AUTO: the copy engine (host round trip, full PCIe rate) for large
+// experts, the device copy (no round trip, ~10 % lower PCIe rate, shared SMs)
+// for small ones, where the round trip's ~12 us weighs more
+constexpr int64_t kAutoDeviceCopyMaxBytes = 8ll << 20;
+int effective_miss_path(const ft_moe *h) {
+  if (h->miss_path != FT_MISS_AUTO) return h->miss_path;
+  return h->blob_bytes <= kAutoDeviceCopyMaxBytes ? FT_MISS_KERNEL : FT_MISS_COPY;
 }
 
 int64_t wait_timeout_ms() {
@@ -386,7 +417,6 @@ int forward_fused(ft_moe *h, RouteArgs &ra, int layer, int n_tokens, const void 
     }
   }
   FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
-  if (h->prof) prof_collect(h);
   return FT_OK;
 }
 
@@ -433,12 +463,15 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->plan.inv, TK) == cudaSuccess && dev_alloc(&h->plan.u_expert, umax) == cudaSuccess &&
             dev_alloc(&h->plan.u_slot, umax) == cudaSuccess && dev_alloc(&h->plan.u_hit, umax) == cudaSuccess &&
             dev_alloc(&h->plan.u_evicted, umax) == cudaSuccess && dev_alloc(&h->plan.n, 4) == cudaSuccess &&
+            cudaMalloc(&h->plan.u_info, sizeof(int4) * (size_t)umax) == cudaSuccess &&
+            cudaMalloc(&h->plan.miss, sizeof(int2) * (size_t)umax) == cudaSuccess &&
             dev_alloc(&h->chunk_counts, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->chunk_base, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
             dev_alloc(&h->xpbuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->mega_sync, 4) == cudaSuccess && cudaMemset(h->mega_sync, 0, 16) == cudaSuccess &&
+            dev_alloc(&h->copy_sync, 2) == cudaSuccess && cudaMemset(h->copy_sync, 0, 8) == cudaSuccess &&
             dev_alloc(&h->combine_counters, combine_tiles(hidden)) == cudaSuccess &&
             cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(hidden)) == cudaSuccess;
   if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
@@ -536,13 +569,17 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   FT_CUDA(h, cudaSetDevice(h->device));
   const bool tc = use_tc(h, n_tokens);
+  const int miss_path = effective_miss_path(h);
   // misses read by the kernels over PCIe: no host round trip (GEMV calls only)
-  const bool pull = h->mode == MODE_LRU && h->miss_path == FT_MISS_PULL && !tc;
+  const bool pull = h->mode == MODE_LRU && miss_path == FT_MISS_PULL && !tc;
+  // misses copied on the device: no host round trip either
+  const bool kcopy = h->mode == MODE_LRU && miss_path == FT_MISS_KERNEL;
   cudaStreamCaptureStatus cs;
   FT_CUDA(h, cudaStreamIsCapturing(stream, &cs));
   const bool capturing = cs != cudaStreamCaptureStatusNone;
-  if (capturing && (h->mode != MODE_LRU || !pull))
-    return fail(h, FT_ERR_STATE, "only LRU-mode forward with FT_MISS_PULL on the GEMV can be captured");
+  if (capturing && (h->mode != MODE_LRU || !(pull || kcopy)))
+    return fail(h, FT_ERR_STATE,
+                "only LRU-mode forward with FT_MISS_KERNEL (or FT_MISS_PULL on the GEMV) can be captured");
   if (capturing && h->prof) return fail(h, FT_ERR_STATE, "profiling is on: forward cannot be captured");
   const int bank = layer & 1;
   if (h->mode == MODE_STREAM) {
@@ -564,21 +601,22 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   ra.cache.order_in = h->order[h->order_cur];
   ra.cache.order_out = h->order[h->order_cur ^ 1];
   ra.cache.stats = h->stats_dev;
-  ra.mirror = (h->mode == MODE_LRU && !pull) ? h->mirror_dev : nullptr;
+  ra.mirror = (h->mode == MODE_LRU && !pull && !kcopy) ? h->mirror_dev : nullptr;
   ra.umax = h->umax;
   ra.seq = h->seq;
   ra.chunk_counts = h->chunk_counts;
   ra.chunk_base = h->chunk_base;
   // follows the previous call's last kernel directly (STREAM mode waits on a copy event first)
   ra.pdl = h->mode == MODE_LRU && !h->prof && !capturing;
-  if (h->decode_fused && h->mode == MODE_LRU && !tc && !capturing && mega_supported(h->E, n_tokens, h->k))
+  if (h->decode_fused && h->mode == MODE_LRU && !tc && !kcopy && !capturing && mega_supported(h->E, n_tokens, h->k))
     return forward_fused(h, ra, layer, n_tokens, x, out, pull, stream);
   prof_begin(h, FT_PROF_ROUTE, stream);
   FT_CUDA(h, launch_route(ra, stream));
   prof_end(h, FT_PROF_ROUTE, stream);
   h->kernel_launches += route_kernel_count(n_tokens, h->k) + 2;  // + gate/up, down (+ combine below)
   if (h->mode == MODE_LRU) h->order_cur ^= 1;
-  if (!capturing) FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
+  // the copy stream forks from here (also under capture: the copies join back below)
+  if (!capturing || kcopy) FT_CUDA(h, cudaEventRecord(h->ev_route, stream));
 
   FfnArgs fa{};
   fa.slot_bank = h->slots;
@@ -595,38 +633,127 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.layer = layer;
   fa.pull = pull ? 1 : 0;
   h->last_tc = tc;
-  if (h->mode == MODE_LRU && !pull) {
+  bool copies_before_down = false;
+  // the first gate/up kernel follows the route kernel directly
+  fa.pdl = !tc && !h->prof && !capturing;
+  if (kcopy) {
+    // misses copied on the device from the GPU's miss list (no host round
+    // trip): ranges 0-1 = what the gate/up projection reads, range 2 = the rest
+    const BlobLayout bl = blob_layout(h->fmt, h->H, h->I);
+    MissCopyArgs &mc = fa.mc;
+    mc.miss = h->plan.miss;
+    mc.n = h->plan.n;
+    mc.pool_dev = h->pool_dev;
+    mc.slots = h->slots;
+    mc.slot_stride = h->slot_stride;
+    mc.seg[0][0] = 0;
+    mc.seg[0][1] = bl.d_codes;
+    mc.seg[1][0] = bl.gscale >= 0 ? bl.gscale : 0;
+    mc.seg[1][1] = bl.gscale >= 0 ? h->blob_bytes : 0;
+    mc.seg[2][0] = bl.d_codes;
+    mc.seg[2][1] = bl.gscale >= 0 ? bl.gscale : h->blob_bytes;
+    if (!tc) {
+      // GEMV: the gate/up kernel's first grid rows copy; its miss CTAs wait
+      // for their flag and the down kernel follows the whole grid
+      fa.only = 0;
+      const int fb = gateup_feature_blocks(h->H, h->I);
+      fa.copy_rows = std::max(1, (kCopyCtas + fb - 1) / fb);
+      fa.copy_sync = h->copy_sync;
+      fa.seq = (int)h->seq;
+      // FT_FAULT=devwait: the flag is raised with a value nobody waits for, so
+      // the misses' CTAs run out their bounded wait (FT_ERR_DEVICE at the next
+      // synchronising call)
+      fa.seq_raised = fault("devwait") ? fa.seq ^ 0x40000000 : fa.seq;
+      prof_begin(h, FT_PROF_GATEUP_HIT, stream);
+      FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
+      prof_end(h, FT_PROF_GATEUP_HIT, stream);
+      fa.copy_rows = 0;
+    } else {
+      // tensor cores: copy kernels on the copy stream; the misses' gate/up
+      // waits for the first, the down kernel for the second
+      FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_route, 0));
+      prof_begin(h, FT_PROF_MISS_COPY, h->copy_stream);
+      FT_CUDA(h, launch_miss_copy(mc, 0, 2, h->copy_stream));
+      FT_CUDA(h, cudaEventRecord(h->ev_copy, h->copy_stream));
+      FT_CUDA(h, launch_miss_copy(mc, 2, 3, h->copy_stream));
+      prof_end(h, FT_PROF_MISS_COPY, h->copy_stream);
+      FT_CUDA(h, cudaEventRecord(h->ev_copy2, h->copy_stream));
+      h->kernel_launches += 3;   // two copies, the misses' gate/up
+      fa.only = 1;
+      prof_begin(h, FT_PROF_GATEUP_HIT, stream);
+      FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
+      prof_end(h, FT_PROF_GATEUP_HIT, stream);
+      FT_CUDA(h, cudaStreamWaitEvent(stream, h->ev_copy, 0));
+      fa.only = 2;
+      prof_begin(h, FT_PROF_GATEUP_MISS, stream);
+      FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
+      prof_end(h, FT_PROF_GATEUP_MISS, stream);
+      FT_CUDA(h, cudaStreamWaitEvent(stream, h->ev_copy2, 0));
+      copies_before_down = true;
+    }
+    fa.pdl = 0;
+  } else if (h->mode == MODE_LRU && !pull) {
     fa.only = 1;
     prof_begin(h, FT_PROF_GATEUP_HIT, stream);
     FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
     prof_end(h, FT_PROF_GATEUP_HIT, stream);
+    fa.pdl = 0;
     if (int rc = wait_plan(h)) return rc;
     const int n_miss = h->mirror_host[1];
+    // GEMV calls copy each miss in two parts, the gate/up rows first: the
+    // misses' gate/up kernel starts once those have landed and runs while the
+    // down rows are still crossing PCIe (it reads the NVFP4 global scales,
+    // which sit in the down part, from the host blob)
+    const bool two_part = !tc && n_miss <= kMissScaleArgs;
+    const BlobLayout bl = blob_layout(h->fmt, h->H, h->I);
+    const int64_t split = two_part ? bl.d_codes : h->blob_bytes;
     if (n_miss > 0) {
       // both copy streams start after the route kernel (every earlier reader
       // of an evicted slot has finished by then); misses alternate between them
       FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_route, 0));
       if (n_miss > 1) FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream2, h->ev_route, 0));
-      prof_begin(h, FT_PROF_MISS_COPY, h->copy_stream);
       for (int i = 0; i < n_miss; ++i) {
         const int key = h->mirror_host[2 + i], slot = h->mirror_host[2 + h->umax + i];
         if (key < 0 || key >= h->L * h->E || slot < 0 || slot >= h->S)
           return fail(h, FT_ERR_DEVICE, "miss list entry out of range");
-        FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)slot * h->slot_stride, h->pool[key], h->blob_bytes,
-                                   cudaMemcpyHostToDevice, (i & 1) ? h->copy_stream2 : h->copy_stream));
       }
-      if (n_miss > 1) {
-        FT_CUDA(h, cudaEventRecord(h->ev_copy2, h->copy_stream2));
-        FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_copy2, 0));
+      // part 0: [0, split) of every miss; part 1: the rest
+      for (int part = 0; part < (two_part ? 2 : 1); ++part) {
+        const int64_t b0 = part == 0 ? 0 : split, nb = part == 0 ? split : h->blob_bytes - split;
+        if (part == 0) prof_begin(h, FT_PROF_MISS_COPY, h->copy_stream);
+        for (int i = 0; i < n_miss; ++i) {
+          const int key = h->mirror_host[2 + i], slot = h->mirror_host[2 + h->umax + i];
+          FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)slot * h->slot_stride + b0,
+                                     static_cast<const uint8_t *>(h->pool[key]) + b0, nb, cudaMemcpyHostToDevice,
+                                     (i & 1) ? h->copy_stream2 : h->copy_stream));
+        }
+        if (n_miss > 1) {
+          FT_CUDA(h, cudaEventRecord(h->ev_copy2, h->copy_stream2));
+          FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_copy2, 0));
+        }
+        if (part == (two_part ? 1 : 0)) prof_end(h, FT_PROF_MISS_COPY, h->copy_stream);
+        FT_CUDA(h, cudaEventRecord(h->ev_copy, h->copy_stream));
+        FT_CUDA(h, cudaStreamWaitEvent(stream, h->ev_copy, 0));
+        if (part == 0) {
+          fa.only = 2;
+          if (two_part && h->fmt == FMT_NVFP4) {
+            fa.ms.n = n_miss;
+            for (int i = 0; i < n_miss; ++i) {
+              const int key = h->mirror_host[2 + i];
+              const float *g = reinterpret_cast<const float *>(static_cast<const uint8_t *>(h->pool[key]) + bl.gscale);
+              fa.ms.expert[i] = key % h->E;
+              fa.ms.gate[i] = g[0];
+              fa.ms.up[i] = g[1];
+            }
+          }
+          h->kernel_launches += 1;
+          prof_begin(h, FT_PROF_GATEUP_MISS, stream);
+          FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
+          prof_end(h, FT_PROF_GATEUP_MISS, stream);
+          fa.ms.n = 0;
+        }
       }
-      prof_end(h, FT_PROF_MISS_COPY, h->copy_stream);
-      FT_CUDA(h, cudaEventRecord(h->ev_copy, h->copy_stream));
-      FT_CUDA(h, cudaStreamWaitEvent(stream, h->ev_copy, 0));
-      fa.only = 2;
-      h->kernel_launches += 1;
-      prof_begin(h, FT_PROF_GATEUP_MISS, stream);
-      FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
-      prof_end(h, FT_PROF_GATEUP_MISS, stream);
+      copies_before_down = two_part;
     }
   } else {
     fa.only = 0;
@@ -635,7 +762,8 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
     prof_end(h, FT_PROF_GATEUP_HIT, stream);
   }
   fa.only = 0;
-  fa.pdl = !tc && !h->prof && !capturing;   // the down kernel follows the gate/up kernel directly
+  // the down kernel follows the gate/up kernel directly (unless it waits for copies)
+  fa.pdl = !tc && !h->prof && !capturing && !copies_before_down;
   // small calls on the GEMV: the combine runs inside the down kernel
   const bool fused = !tc && gemv_fuses_combine(n_tokens);
   CombineArgs cb{};
@@ -663,19 +791,22 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   else FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
   h->host_streamed += h->last_streamed;
   h->host_bytes += h->last_stream_bytes;
-  if (h->prof) prof_collect(h);
   return FT_OK;
 }
 
 int ft_moe_set_profiling(ft_moe *h, int enable) {
   if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
   if (int rc = sync_handle(h)) return rc;
-  for (int i = 0; i < 2 * FT_PROF_CLASSES; ++i)
-    if (!h->prof_ev[i]) FT_CUDA(h, cudaEventCreate(&h->prof_ev[i]));
+  if (enable)
+    for (auto &cls : h->prof_ev)
+      for (auto &pair : cls)
+        for (cudaEvent_t &ev : pair)
+          if (!ev) FT_CUDA(h, cudaEventCreate(&ev));
   for (int c = 0; c < FT_PROF_CLASSES; ++c) {
     h->prof_ms[c] = 0.0;
     h->prof_launches[c] = 0;
-    h->prof_pending[c] = false;
+    h->prof_head[c] = 0;
+    h->prof_count[c] = 0;
   }
   h->prof = enable != 0;
   return FT_OK;
@@ -756,6 +887,8 @@ int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
 
 int ft_moe_last_ffn_kernel(const ft_moe *h) { return h ? (h->last_tc ? FT_FFN_TC : FT_FFN_GEMV) : -1; }
 
+int ft_moe_miss_path(const ft_moe *h) { return h ? effective_miss_path(h) : -1; }
+
 int ft_moe_set_decode_fusion(ft_moe *h, int on) {
   if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
   if (int rc = sync_handle(h)) return rc;
@@ -764,7 +897,8 @@ int ft_moe_set_decode_fusion(ft_moe *h, int on) {
 }
 
 int ft_moe_set_miss_path(ft_moe *h, int path) {
-  if (!h || (path != FT_MISS_COPY && path != FT_MISS_PULL)) return fail(h, FT_ERR_ARG, "bad miss path");
+  if (!h || path < FT_MISS_COPY || path > FT_MISS_AUTO)
+    return fail(h, FT_ERR_ARG, "bad miss path");
   if (int rc = sync_handle(h)) return rc;
   h->miss_path = path;
   return FT_OK;

@@ -3,6 +3,7 @@
 // decode layer kernel.  See ffn_gemv.cu for the design.
 #pragma once
 #include "ft_internal.cuh"
+#include "wait_dev.cuh"
 
 namespace ftmoe {
 namespace {
@@ -249,17 +250,23 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
   // more features, so that the staged activations serve more weight bytes
   const int kFeatPerCta = KW * (32 / LPR) * fpw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l8 = lane & (LPR - 1);
-  bool work = u < a.plan.n[0];
-  int hit = 1;
-  if (work) {
-    hit = a.plan.u_hit[u];
-    if ((a.only == 1 && !hit) || (a.only == 2 && hit)) work = false;
+  // the count and this item's packed plan entry, in one round trip (entries
+  // past the count are stale and ignored)
+  const int nU = a.plan.n[0];
+  const int4 ui = a.plan.u_info[u];
+  const int hit = ui.w & 1;
+  bool work = u < nU;
+  if (work && ((a.only == 1 && !hit) || (a.only == 2 && hit))) work = false;
+  if (work && !DOWN && !hit && a.copy_rows > 0) {
+    // the copying CTAs of this grid raise the flag once every miss's gate/up bytes have landed
+    __shared__ int s_ok;
+    if (!cta_wait_flag(a.copy_sync, a.seq, a.err, 70, &s_ok)) return;
   }
   if (work) {
-    const int e = a.plan.u_expert[u];
-    const int off = a.plan.offsets[e];
-    const int n = a.plan.offsets[e + 1] - off;
-    uint8_t *slot = const_cast<uint8_t *>(a.slot_bank) + (size_t)a.plan.u_slot[u] * a.slot_stride;
+    const int e = ui.x;
+    const int off = ui.z;
+    const int n = ui.w >> 1;
+    uint8_t *slot = const_cast<uint8_t *>(a.slot_bank) + (size_t)ui.y * a.slot_stride;
     const uint8_t *blob = slot;
     uint8_t *pull_dst = nullptr;
     if (a.pull && !hit) {
@@ -273,8 +280,17 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
     float gs0 = 1.0f, gs1 = 1.0f;
     if constexpr (FMT == FMT_NVFP4) {
       const float *gs = reinterpret_cast<const float *>(blob + L.gscale);
-      gs0 = DOWN ? gs[2] : gs[0];
-      gs1 = gs[1];
+      if (!DOWN && !hit && a.ms.n > 0) {
+        // the slot still waits for its down part, which holds the global scales
+        for (int i = 0; i < a.ms.n; ++i)
+          if (a.ms.expert[i] == e) {
+            gs0 = a.ms.gate[i];
+            gs1 = a.ms.up[i];
+          }
+      } else {
+        gs0 = DOWN ? gs[2] : gs[0];
+        gs1 = gs[1];
+      }
       if (DOWN && pull_dst && bx == 0 && threadIdx.x == 0)
         *reinterpret_cast<uint4 *>(pull_dst + L.gscale) = *reinterpret_cast<const uint4 *>(blob + L.gscale);
     }
@@ -326,8 +342,10 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
 // expert when `any`): lets a CTA request all of its items' rows up front.
 template <int FMT, bool DOWN, int LPR, int KW>
 __device__ __forceinline__ void gemv_prefetch(const FfnArgs &a, int u, int bx, int fpw, bool any) {
-  if (u >= a.plan.n[0] || (!any && !a.plan.u_hit[u])) return;
-  const uint8_t *blob = a.slot_bank + (size_t)a.plan.u_slot[u] * a.slot_stride;
+  if (u >= a.plan.n[0]) return;
+  const int4 ui = a.plan.u_info[u];
+  if (!any && !(ui.w & 1)) return;
+  const uint8_t *blob = a.slot_bank + (size_t)ui.y * a.slot_stride;
   const BlobLayout L = blob_layout(FMT, a.H, a.I);
   const int K = DOWN ? a.I : a.H;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, l8 = lane & (LPR - 1);
@@ -355,6 +373,14 @@ __device__ __forceinline__ void gemv_prefetch(const FfnArgs &a, int u, int bx, i
 // block's features (rank order j ascending) and resets the counter.
 __device__ __forceinline__ void combine_block(const FfnArgs &a, const CombineArgs &cb, int bx, int feat_per_cta,
                                               int expected, int *s_flag) {
+  // gates and positions of the call's (token, rank) pairs, read by every CTA
+  // before the count so that the last one has them at hand
+  __shared__ float s_g[kFusedCombineMaxT * kMaxTopK];
+  __shared__ int s_inv[kFusedCombineMaxT * kMaxTopK];
+  for (int i = threadIdx.x; i < cb.T * a.k; i += blockDim.x) {
+    s_g[i] = cb.gates[i];
+    s_inv[i] = cb.inv[i];
+  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -369,10 +395,8 @@ __device__ __forceinline__ void combine_block(const FfnArgs &a, const CombineArg
     const int t = i / feat_per_cta, f = f0 + (i - t * feat_per_cta);
     if (f >= a.H) continue;
     float acc = 0.0f;
-    for (int j = 0; j < a.k; ++j) {
-      const float g = cb.gates[(size_t)t * a.k + j];
-      acc = fmaf(g, __ldcg(a.y + (size_t)cb.inv[(size_t)t * a.k + j] * a.H + f), acc);
-    }
+    for (int j = 0; j < a.k; ++j)
+      acc = fmaf(s_g[t * a.k + j], __ldcg(a.y + (size_t)s_inv[t * a.k + j] * a.H + f), acc);
     cb.out[(size_t)t * a.H + f] = __float2bfloat16_rn(acc);
   }
   if (threadIdx.x == 0) cb.counters[bx] = 0;

@@ -81,7 +81,8 @@ __global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int wi
   int *s_count = smem;
   int *s_uexp = s_count + E;
   int *s_victim = s_uexp + E;
-  int *s_warp = s_victim + E;          // 33
+  int *s_off = s_victim + E;
+  int *s_warp = s_off + E;             // 33
   unsigned *s_bits = (unsigned *)(s_warp + 33);
   int *s_part = (int *)(s_bits + ((a.S + 31) >> 5));   // [G][E]
   const int tid = threadIdx.x;
@@ -108,12 +109,12 @@ __global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int wi
   if (tid < E) {
     s_count[tid] = cnt;
     a.plan.offsets[tid] = off;
-    s_uexp[tid] = off;   // expert offsets for the chunk bases below (s_uexp is rewritten by the plan)
+    s_off[tid] = off;
   }
   if (tid == 0) a.plan.offsets[E] = total;
   __syncthreads();
   if (g < G) {
-    int run = s_uexp[e] + s_part[g * E + e];
+    int run = s_off[e] + s_part[g * E + e];
     for (int c = c0; c < c1; ++c) {
       a.chunk_base[(size_t)c * E + e] = run;
       run += a.chunk_counts[(size_t)c * E + e];
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kRouteThreads) plan_kernel(RouteArgs a, int wi
   }
   __syncthreads();
   if (with_plan) {
-    PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, nullptr, nullptr};
+    PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, nullptr, nullptr, s_off};
     Prefetch pf;
     pf.n = -1;
     if (tid == 0)
@@ -152,7 +153,7 @@ size_t small_smem_bytes(int E, int S) {
   return sizeof(int) * (6 * (size_t)E + 33 + nw * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
 }
 size_t plan_smem_bytes(int E, int S) {
-  return sizeof(int) * (3 * (size_t)E + 33) + sizeof(unsigned) * (((size_t)S + 31) / 32) +
+  return sizeof(int) * (4 * (size_t)E + 33) + sizeof(unsigned) * (((size_t)S + 31) / 32) +
          sizeof(int) * (size_t)kRouteThreads;   // per-group chunk partials
 }
 

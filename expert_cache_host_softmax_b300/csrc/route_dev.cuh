@@ -185,6 +185,7 @@ struct PlanSmem {
   int *s_warp;    // [33]: scan partials, [32] a counter
   int *s_keyslot;    // [E] this layer's key -> slot, loaded up front (or null)
   int *s_victim_key; // [E] key held by each victim slot (with s_keyslot)
+  const int *s_off;  // [E] first permuted position of each expert
 };
 
 // The cache-table entries a thread needs, loaded at kernel start so that the
@@ -318,9 +319,16 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm, const Prefetc
     a.plan.u_slot[tid] = slot;
     a.plan.u_hit[tid] = hit;
     a.plan.u_evicted[tid] = evicted;
-    if (a.mirror && !hit) {
-      a.mirror[2 + mrank] = key;
-      a.mirror[2 + a.umax + mrank] = slot;
+    // hits first: the GEMV grid's rows follow this order, so that CTAs that
+    // wait for a miss's bytes are dispatched after every hit's CTAs
+    const int e = sm.s_uexp[tid];
+    a.plan.u_info[hit ? hrank : nH + mrank] = make_int4(e, slot, sm.s_off[e], (sm.s_count[e] << 1) | hit);
+    if (!hit) {
+      a.plan.miss[mrank] = make_int2(key, slot);
+      if (a.mirror) {
+        a.mirror[2 + mrank] = key;
+        a.mirror[2 + a.umax + mrank] = slot;
+      }
     }
   }
   __syncthreads();
@@ -384,7 +392,8 @@ __device__ __forceinline__ void route_small_body(const RouteArgs &a, int *smem, 
     s_base[tid] = off;
   }
   if (tid == 0) a.plan.offsets[E] = total;
-  PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, a.mode == MODE_LRU ? s_keyslot : nullptr, s_victim_key};
+  PlanSmem sm{s_count, s_uexp, s_victim, s_bits, s_warp, a.mode == MODE_LRU ? s_keyslot : nullptr, s_victim_key,
+              s_base};
   block_plan(a, sm, pf);
   __syncthreads();
   block_rank_scatter(a.plan.topk_idx, 0, a.T * a.k, E, s_base, s_wcnt, a.plan.perm, a.plan.inv);

@@ -131,14 +131,15 @@ int ft_moe_set_mode(ft_moe *h, int mode);
  * LRU mode: the distinct experts of the call are looked up in the slot
  * table.  Hits move to MRU in ascending expert id.  Then misses, in ascending
  * id, take the lowest free slot or evict the LRU expert.  All of this is
- * decided on the GPU.  Miss blobs are copied by cudaMemcpyAsync on the
- * handle's copy streams, overlapping the FFN of the hits.  The call blocks the
- * host until the GPU's miss list is known: a bounded wait, FT_ERR_TIMEOUT
- * after FT_WAIT_TIMEOUT_MS (default 20000).  It cannot run under stream
- * capture (FT_ERR_STATE).  With FT_MISS_PULL (ft_moe_set_miss_path) on a GEMV
- * call, the kernels read the misses from host memory instead: no host wait,
- * and the call can be captured in a CUDA graph (not while profiling).  Each
- * launch of such a graph is one more call: it advances the cache state.
+ * decided on the GPU.  How a miss's blob reaches its slot is set by
+ * ft_moe_set_miss_path.  With FT_MISS_COPY the host issues cudaMemcpyAsync on
+ * the handle's copy streams, overlapping the FFN of the hits, and the call
+ * blocks the host until the GPU's miss list is known: a bounded wait,
+ * FT_ERR_TIMEOUT after FT_WAIT_TIMEOUT_MS (default 20000); such a call cannot
+ * run under stream capture (FT_ERR_STATE).  With FT_MISS_KERNEL (or
+ * FT_MISS_PULL on a GEMV call) the GPU fetches the misses itself: no host
+ * wait, and the call can be captured in a CUDA graph (not while profiling).
+ * Each launch of such a graph is one more call: it advances the cache state.
  * After a captured call, the synchronising calls (ft_cache_stats and others)
  * wait for the whole device.
  * STREAM mode: bank (layer mod 2) receives all E experts of `layer` before
@@ -225,18 +226,34 @@ int ft_moe_last_ffn_kernel(const ft_moe *h);
 
 /* How LRU-mode misses reach their slots. */
 enum ft_miss_path {
-  FT_MISS_COPY = 0, /* default: cudaMemcpyAsync per miss on the handle's copy streams, issued by the host
-                       once it has read the GPU's miss list; the hits' FFN overlaps the copies */
-  FT_MISS_PULL = 1  /* the FFN kernels read a missed expert's weights straight from pinned host
+  FT_MISS_COPY = 0, /* cudaMemcpyAsync on the handle's copy streams, issued by the host once it has
+                       read the GPU's miss list; the hits' FFN overlaps the copies.  GEMV calls
+                       with up to 64 misses copy the gate/up bytes of every miss first, so that
+                       the misses' gate/up overlaps the copies of their down bytes */
+  FT_MISS_PULL = 1, /* the FFN kernels read a missed expert's weights straight from pinned host
                        memory over PCIe and write the same bytes into its slot; no host round
                        trip, so forward returns without waiting and can be captured in a CUDA
                        graph.  Applies to calls on the GEMV kernel; tensor-core calls still copy. */
+  FT_MISS_KERNEL = 2, /* the GPU copies the misses from pinned host memory into their slots,
+                        reading its own miss list: on GEMV calls the first CTAs of the gate/up
+                        kernel copy (gate/up bytes first; the misses' CTAs wait for them, the
+                        down kernel for the whole grid), on tensor-core calls copy kernels on
+                        the copy stream.  No host round trip: forward returns without waiting
+                        and can be captured in a CUDA graph.  SM loads reach ~90 % of the copy
+                        engine's PCIe rate and share the SMs with the FFN. */
+  FT_MISS_AUTO = 3    /* default: FT_MISS_KERNEL for experts of at most 8 MiB (the host round trip
+                        costs more than the lower rate), FT_MISS_COPY for larger ones */
 };
 
-/* Selects the miss path for later forward calls (default FT_MISS_COPY).  The
+/* Selects the miss path for later forward calls (default FT_MISS_AUTO).  The
  * cache decisions, counters and results are the same on both paths.  Waits for
  * the handle's outstanding work.  Errors: FT_ERR_ARG. */
 int ft_moe_set_miss_path(ft_moe *h, int path);
+
+/* The miss path LRU-mode calls take: FT_MISS_COPY, FT_MISS_PULL or
+ * FT_MISS_KERNEL (FT_MISS_AUTO resolved by the handle's expert size; -1 for
+ * NULL). */
+int ft_moe_miss_path(const ft_moe *h);
 
 /* on != 0: decode calls (LRU mode, GEMV kernel, at most 16 tokens, E <= 256,
  * not under capture) run as one cooperative kernel: routing and the LRU plan,

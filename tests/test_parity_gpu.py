@@ -312,17 +312,20 @@ def test_fused_decode_matches_split_kernels(fmt, T, path):
 
 # ------------------------------------------------------------ misses read over PCIe by the kernels
 
+@pytest.mark.parametrize("path", ["pull", "kernel"])
 @pytest.mark.parametrize("fmt,T", [("nvfp4", 1), ("mxfp4", 2), ("bf16", 3), ("nvfp4", 6)])
-def test_pull_misses_match_oracle_and_copy_path(fmt, T):
+def test_device_miss_paths_match_oracle_and_copy_path(fmt, T, path):
     # same decisions and counters as the oracle; outputs bit-identical to the
-    # copy-engine path (the same kernels read the same bytes, from host memory
-    # instead of the slot); later calls hit on the slots the pull filled
+    # copy-engine path (the same kernels read the same bytes: pulled from host
+    # memory, or from the slot a copy kernel filled); later calls hit on the
+    # slots the device filled
     H, I, E, k, L, S = 256, 512, 16, 2, 3, min(16, 8 + 2 * T)
     seed = 101 + T
     pull, orc, pool = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed)
-    pull.set_miss_path("pull")
+    pull.set_miss_path(path)
     copy = F.MoELayerStack(H, E, k, I, fmt, S, L, T)
     copy.load_pool(pool.pointers, keepalive=pool)
+    copy.set_miss_path("copy")
     for step in range(12):
         for layer in range(L):
             x, lg = Hn.inputs(seed, T, H, E, step, layer, zipf=0.7)
@@ -341,10 +344,28 @@ def test_pull_misses_match_oracle_and_copy_path(fmt, T):
     copy.close()
 
 
-def test_pull_forward_is_capturable():
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_kernel_copied_misses_on_tensor_cores(fmt):
+    # prefill-sized calls (tensor-core FFN) with misses copied by the kernel
+    H, I, E, k, L, T, S = 256, 512, 8, 2, 3, 512, 10
+    seed = 131
+    gpu, orc, pool = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed)
+    gpu.set_miss_path("kernel")
+    for step in range(3):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, T, H, E, step, layer, zipf=0.7)
+            _check_call(gpu, orc, layer, x, lg, gemm_check=(step == 0))
+            assert gpu.last_ffn_kernel == "tc"
+    cum, _ = gpu.stats()
+    assert cum["misses"] == orc.stats["misses"] > 0
+    gpu.close()
+
+
+@pytest.mark.parametrize("path", ["pull", "kernel"])
+def test_device_miss_forward_is_capturable(path):
     H, I, E, k, L, T = 256, 256, 8, 2, 2, 4
     gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, L, T, 111, warm=False)
-    gpu.set_miss_path("pull")
+    gpu.set_miss_path(path)
     x, lg = Hn.inputs(111, T, H, E, 0, 1)
     xd, lgd = Hn.to_dev(x, lg)
     out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
@@ -368,6 +389,7 @@ def test_pull_forward_is_capturable():
 def test_wait_timeout_is_reported_and_reset_recovers(monkeypatch):
     H, I, E, k, T = 256, 256, 8, 2, 4
     gpu, orc, _ = Hn.make_pair(H, E, k, I, "bf16", 8, 2, T, 51)
+    gpu.set_miss_path("copy")   # the host waits for the GPU's miss list
     x, lg = Hn.inputs(51, T, H, E, 0, 0)
     xd, lgd = Hn.to_dev(x, lg)
     monkeypatch.setenv("FT_FAULT", "timeout")
@@ -376,6 +398,27 @@ def test_wait_timeout_is_reported_and_reset_recovers(monkeypatch):
     assert ei.value.code == F.FT_ERR_TIMEOUT
     monkeypatch.delenv("FT_FAULT")
     gpu.reset(warm=True)
+    _check_call(gpu, orc, 1, x, lg)
+    gpu.close()
+
+
+def test_device_wait_timeout_is_reported_and_reset_recovers(monkeypatch):
+    # the misses' CTAs wait for a flag that nothing raises: their bounded wait
+    # gives up, the kernel records it, the host reports FT_ERR_DEVICE, and a
+    # reset brings the handle back
+    H, I, E, k, T = 256, 256, 8, 2, 2
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", 8, 2, T, 53, warm=False)
+    gpu.set_miss_path("kernel")
+    x, lg = Hn.inputs(53, T, H, E, 0, 0)
+    xd, lgd = Hn.to_dev(x, lg)
+    monkeypatch.setenv("FT_FAULT", "devwait")
+    gpu.forward(1, xd, lgd)
+    monkeypatch.delenv("FT_FAULT")
+    with pytest.raises(F.FtError) as ei:
+        gpu.stats()
+    assert ei.value.code == F.FT_ERR_DEVICE
+    gpu.reset(warm=True)
+    orc.reset(warm=True)
     _check_call(gpu, orc, 1, x, lg)
     gpu.close()
 
