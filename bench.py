@@ -444,7 +444,7 @@ def run_ours(args, cfg):
     stack.set_profiling(False)
     ffn_kernel = stack.last_ffn_kernel
     # GEMV calls with FT_MISS_KERNEL copy their misses inside the gate/up kernel
-    in_kernel_copy = cfg["mode"] == "lru" and ffn_kernel == "gemv" and stack.miss_path == "kernel"
+    in_kernel_copy = cfg["mode"] == "lru" and ffn_kernel == "gemv" and stack.miss_path() == "kernel"
     pd = {key_: c1[key_] - c0[key_] for key_ in c1}
 
     # algorithmic bytes and FLOPs of the FFN kernels: each distinct expert's
@@ -494,7 +494,7 @@ def run_ours(args, cfg):
                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_src": peaks["src"],
                     "bytes_per_call": b_dom / calls_p, "ms_per_call": ms_dom / calls_p, "kernel_ms_share": share}
     copy_ms = prof["miss_copy"][0]
-    copy_gbs = pd["misses"] * nb / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 else None
+    copy_gbs = pd["misses"] * nb / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 and pd["misses"] > 0 else None
     stream_ms = prof["stream_copy"][0]
     stream_gbs = pd["streamed"] * nb / (stream_ms * 1e-3) / 1e9 if stream_ms > 0 else None
 
@@ -529,7 +529,8 @@ def run_ours(args, cfg):
         "data": "synthetic",
         "config": {"workload": cfg["name"], "layers": L, "hidden": H, "experts": E, "top_k": k, "inter": I,
                    "weight_fmt": fmt, "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
-                   "mode": cfg["mode"], "miss_path": stack.miss_path if cfg["mode"] == "lru" else None,
+                   "mode": cfg["mode"],
+                   "miss_path": stack.miss_path(ffn_kernel == "tc") if cfg["mode"] == "lru" else None,
                    "decode_kernels": "fused" if args.fused_decode else "split", "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
                    "pool": f"{n_keys} logical experts over {n_phys} distinct pinned blobs ({n_phys * nb / 1e9:.2f} GB)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": L * T * (H * 2 + E * 4),

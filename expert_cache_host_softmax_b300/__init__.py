@@ -79,7 +79,7 @@ def lib():
         L.ft_moe_profile_read.argtypes = [vp, vp, vp, i32]
         L.ft_moe_set_ffn_kernel.argtypes = [vp, i32]
         L.ft_moe_last_ffn_kernel.argtypes = [vp]
-        L.ft_moe_miss_path.argtypes = [vp]
+        L.ft_moe_miss_path.argtypes = [vp, i32]
         L.ft_moe_set_miss_path.argtypes = [vp, i32]
         L.ft_moe_set_decode_fusion.argtypes = [vp, i32]
         L.ft_moe_kernel_launches.restype = i64
@@ -233,11 +233,11 @@ class MoELayerStack:
         w = MISS_PATH[path] if isinstance(path, str) else int(path)
         _check(lib().ft_moe_set_miss_path(self._h, w), self._h)
 
-    @property
-    def miss_path(self):
-        """The miss path LRU calls take ("auto" resolved): "copy", "pull" or "kernel"."""
+    def miss_path(self, tensor_core=False):
+        """The miss path LRU calls on the GEMV (or the tensor-core FFN) take, "auto" resolved:
+        "copy", "pull" or "kernel"."""
         inv = {v: k_ for k_, v in MISS_PATH.items()}
-        return inv.get(int(lib().ft_moe_miss_path(self._h)))
+        return inv.get(int(lib().ft_moe_miss_path(self._h, 1 if tensor_core else 0)))
 
     @property
     def last_ffn_kernel(self):

@@ -308,13 +308,14 @@ int stage_layer(ft_moe *h, int layer) {
   return FT_OK;
 }
 
-// FT_MISS_AUTO: the copy engine (host round trip, full PCIe rate) for large
-// experts, the device copy (no round trip, ~10 % lower PCIe rate, shared SMs)
-// for small ones, where the round trip's ~12 us weighs more
+// FT_MISS_AUTO: the device copy (no host round trip, ~10 % lower PCIe rate,
+// shares the SMs) for decode calls (GEMV) on small experts, where the round
+// trip's ~8 us weighs more; the copy engine (full PCIe rate) for large
+// experts and for tensor-core calls, whose own run time hides the round trip
 constexpr int64_t kAutoDeviceCopyMaxBytes = 8ll << 20;
-int effective_miss_path(const ft_moe *h) {
+int effective_miss_path(const ft_moe *h, bool tc) {
   if (h->miss_path != FT_MISS_AUTO) return h->miss_path;
-  return h->blob_bytes <= kAutoDeviceCopyMaxBytes ? FT_MISS_KERNEL : FT_MISS_COPY;
+  return !tc && h->blob_bytes <= kAutoDeviceCopyMaxBytes ? FT_MISS_KERNEL : FT_MISS_COPY;
 }
 
 int64_t wait_timeout_ms() {
@@ -569,7 +570,7 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   FT_CUDA(h, cudaSetDevice(h->device));
   const bool tc = use_tc(h, n_tokens);
-  const int miss_path = effective_miss_path(h);
+  const int miss_path = effective_miss_path(h, tc);
   // misses read by the kernels over PCIe: no host round trip (GEMV calls only)
   const bool pull = h->mode == MODE_LRU && miss_path == FT_MISS_PULL && !tc;
   // misses copied on the device: no host round trip either
@@ -887,7 +888,7 @@ int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
 
 int ft_moe_last_ffn_kernel(const ft_moe *h) { return h ? (h->last_tc ? FT_FFN_TC : FT_FFN_GEMV) : -1; }
 
-int ft_moe_miss_path(const ft_moe *h) { return h ? effective_miss_path(h) : -1; }
+int ft_moe_miss_path(const ft_moe *h, int tensor_core) { return h ? effective_miss_path(h, tensor_core != 0) : -1; }
 
 int ft_moe_set_decode_fusion(ft_moe *h, int on) {
   if (!h) return fail(h, FT_ERR_ARG, "NULL handle");

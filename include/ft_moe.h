@@ -241,8 +241,9 @@ enum ft_miss_path {
                         the copy stream.  No host round trip: forward returns without waiting
                         and can be captured in a CUDA graph.  SM loads reach ~90 % of the copy
                         engine's PCIe rate and share the SMs with the FFN. */
-  FT_MISS_AUTO = 3    /* default: FT_MISS_KERNEL for experts of at most 8 MiB (the host round trip
-                        costs more than the lower rate), FT_MISS_COPY for larger ones */
+  FT_MISS_AUTO = 3    /* default: FT_MISS_KERNEL for GEMV (decode) calls on experts of at most
+                        8 MiB, where the host round trip costs more than the lower rate;
+                        FT_MISS_COPY for larger experts and for tensor-core calls */
 };
 
 /* Selects the miss path for later forward calls (default FT_MISS_AUTO).  The
@@ -250,10 +251,10 @@ enum ft_miss_path {
  * the handle's outstanding work.  Errors: FT_ERR_ARG. */
 int ft_moe_set_miss_path(ft_moe *h, int path);
 
-/* The miss path LRU-mode calls take: FT_MISS_COPY, FT_MISS_PULL or
- * FT_MISS_KERNEL (FT_MISS_AUTO resolved by the handle's expert size; -1 for
- * NULL). */
-int ft_moe_miss_path(const ft_moe *h);
+/* The miss path LRU-mode calls on the GEMV (tensor_core = 0) or on the
+ * tensor-core FFN (tensor_core != 0) take: FT_MISS_COPY, FT_MISS_PULL or
+ * FT_MISS_KERNEL, with FT_MISS_AUTO resolved (-1 for NULL). */
+int ft_moe_miss_path(const ft_moe *h, int tensor_core);
 
 /* on != 0: decode calls (LRU mode, GEMV kernel, at most 16 tokens, E <= 256,
  * not under capture) run as one cooperative kernel: routing and the LRU plan,
