@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   if constexpr (DOWN) {
     if (cb.counters == nullptr) return;
     __shared__ int s_last;
-    combine_block(a, cb, blockIdx.x, kWarps * (32 / LPR) * fpw, gridDim.y, &s_last);
+    combine_block(a, cb, blockIdx.x, kWarps * (32 / LPR) * fpw, gridDim.y * max(1, cb.launches), &s_last);
   }
 }
 

@@ -155,6 +155,7 @@ struct CombineArgs {
   __nv_bfloat16 *out;
   int *counters;
   int T;
+  int launches;               // down launches of the call that arrive on the counters (0 counts as 1)
 };
 int combine_tiles(int H);
 int gateup_feature_blocks(int H, int I);   // grid.x of the gate/up GEMV

@@ -635,6 +635,17 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.pull = pull ? 1 : 0;
   h->last_tc = tc;
   bool copies_before_down = false;
+  // small calls on the GEMV: the combine runs inside the down kernel
+  const bool fused = !tc && gemv_fuses_combine(n_tokens);
+  CombineArgs cb{};
+  if (fused) {
+    cb.gates = h->plan.gates;
+    cb.inv = h->plan.inv;
+    cb.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    cb.counters = h->combine_counters;
+    cb.T = n_tokens;
+  }
+  bool down_done = false;
   // the first gate/up kernel follows the route kernel directly
   fa.pdl = !tc && !h->prof && !capturing;
   if (kcopy) {
@@ -708,6 +719,18 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
     const bool two_part = !tc && n_miss <= kMissScaleArgs;
     const BlobLayout bl = blob_layout(h->fmt, h->H, h->I);
     const int64_t split = two_part ? bl.d_codes : h->blob_bytes;
+    if (n_miss > 0 && !tc) {
+      // the hits' down projection runs now, beside the copies; the misses'
+      // follows their down bytes.  Both launches arrive on the combine counters.
+      fa.only = 1;
+      fa.pdl = !h->prof && !capturing;
+      cb.launches = 2;
+      h->kernel_launches += 1;
+      prof_begin(h, FT_PROF_DOWN, stream);
+      FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream, cb));
+      prof_end(h, FT_PROF_DOWN, stream);
+      fa.pdl = 0;
+    }
     if (n_miss > 0) {
       // both copy streams start after the route kernel (every earlier reader
       // of an evicted slot has finished by then); misses alternate between them
@@ -755,6 +778,15 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
         }
       }
       copies_before_down = two_part;
+      if (!tc) {
+        // the misses' down projection, after the last copies (no kernel between)
+        fa.only = 2;
+        fa.pdl = 0;
+        prof_begin(h, FT_PROF_DOWN, stream);
+        FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream, cb));
+        prof_end(h, FT_PROF_DOWN, stream);
+        down_done = true;
+      }
     }
   } else {
     fa.only = 0;
@@ -765,19 +797,11 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.only = 0;
   // the down kernel follows the gate/up kernel directly (unless it waits for copies)
   fa.pdl = !tc && !h->prof && !capturing && !copies_before_down;
-  // small calls on the GEMV: the combine runs inside the down kernel
-  const bool fused = !tc && gemv_fuses_combine(n_tokens);
-  CombineArgs cb{};
-  if (fused) {
-    cb.gates = h->plan.gates;
-    cb.inv = h->plan.inv;
-    cb.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    cb.counters = h->combine_counters;
-    cb.T = n_tokens;
+  if (!down_done) {
+    prof_begin(h, FT_PROF_DOWN, stream);
+    FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream, cb));
+    prof_end(h, FT_PROF_DOWN, stream);
   }
-  prof_begin(h, FT_PROF_DOWN, stream);
-  FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream, cb));
-  prof_end(h, FT_PROF_DOWN, stream);
   if (!fused) {
     h->kernel_launches += 1;
     prof_begin(h, FT_PROF_COMBINE, stream);

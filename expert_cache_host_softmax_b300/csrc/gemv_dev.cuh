@@ -98,7 +98,8 @@ __device__ __forceinline__ void decode8(const Chunk<FMT> &ch, int i, float *w) {
 // each; MXFP4: one E8M0 scale for all 32); the NVFP4 global scale is applied
 // to the finished dot product.
 template <int FMT, int NT>
-__device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloat16 *xs, int K, int c, float *acc) {
+__device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloat16 *xs, int K, int c, int nt,
+                                          float *acc) {
   float s0 = 1.0f, s1 = 1.0f;
   if constexpr (FMT == FMT_NVFP4) {
     const float2 s = __half22float2(e4m3x2_to_half2(ch.sf));
@@ -114,6 +115,7 @@ __device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloa
     const float s = i < 2 ? s0 : s1;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
+      if (t > 0 && t >= nt) break;   // uniform across the CTA: the expert's token rows in this pass
       const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)t * K + 32 * c)[i];
       float xf[8];
       bf16x8_to_float(xv, xf);
@@ -175,7 +177,7 @@ __device__ __forceinline__ void store_chunk(const RowPtrs &dst, int c, const Chu
 // written to the same place in the expert's GPU slot.
 template <int FMT, int NT, int NROWS, int LPR>
 __device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, int K, const __nv_bfloat16 *xs,
-                                         int l8, float (&acc)[NROWS][NT]) {
+                                         int l8, int nt, float (&acc)[NROWS][NT]) {
   constexpr int kBatch = 2;   // the whole row was prefetched into L2 at kernel start
   const int cpl = K / (32 * LPR);  // chunks per lane
 #pragma unroll 1
@@ -197,7 +199,7 @@ __device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, 
     for (int b = 0; b < kBatch; ++b)
       if (i0 + b < cpl)
 #pragma unroll
-        for (int r = 0; r < NROWS; ++r) chunk_fma<FMT, NT>(ch[r][b], xs, K, l8 + LPR * (i0 + b), acc[r]);
+        for (int r = 0; r < NROWS; ++r) chunk_fma<FMT, NT>(ch[r][b], xs, K, l8 + LPR * (i0 + b), nt, acc[r]);
   }
 }
 
@@ -216,7 +218,7 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
     float acc[2][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.0f;
-    rows_dot<FMT, NT, 2, LPR>(rp, slot_dst ? dp : nullptr, a.H, xs, l8, acc);
+    rows_dot<FMT, NT, 2, LPR>(rp, slot_dst ? dp : nullptr, a.H, xs, l8, nt, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const float g = group_sum<LPR>(acc[0][t]) * gs0;
@@ -231,7 +233,7 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
     float acc[1][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = 0.0f;
-    rows_dot<FMT, NT, 1, LPR>(rp, slot_dst ? dp : nullptr, a.I, xs, l8, acc);
+    rows_dot<FMT, NT, 1, LPR>(rp, slot_dst ? dp : nullptr, a.I, xs, l8, nt, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const float v = group_sum<LPR>(acc[0][t]) * gs0;
@@ -329,7 +331,7 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
         reinterpret_cast<uint4 *>(xs + (size_t)t * K)[v] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
       }
       __syncthreads();
-      // rows nt..NT-1 of xs may hold stale data: their dot products are computed and dropped
+      // rows nt..NT-1 of xs may hold stale data: their products are skipped
       for (int fp = 0; fp < fpw; ++fp)
         ffn_rows<FMT, DOWN, NT, LPR>(blob, c0 == 0 ? pull_dst : nullptr, L, a, feat0 + fp * KW * (32 / LPR), xs,
                                      nt, off + c0, gs0, gs1, l8);
