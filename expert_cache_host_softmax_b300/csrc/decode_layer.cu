@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kMegaThreads) decode_layer_kernel(MegaArgs m) 
 
   // ---- A. routing and plan (CTA 0)
   if (blockIdx.x == 0) {
-    route_small_body(m.r, reinterpret_cast<int *>(smem_raw), false);
+    route_body(m.r, reinterpret_cast<int *>(smem_raw), false);
     __syncthreads();
     if (threadIdx.x == 0) {
       __threadfence();

@@ -38,6 +38,22 @@ template <int FMT, bool DOWN, int NT, int LPR>
 __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, CombineArgs cb, int fpw) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
+  // Before the wait for the kernel ahead: this grid starts only once that
+  // kernel is past its own wait (it triggers after it), so all work before
+  // the route kernel -- the call's x -- and the route kernel's plan (for a
+  // down grid, which starts after the gate/up grid passed its wait) are final.
+  bool x_staged = false;
+  if constexpr (!DOWN) {
+    if (a.max_tokens == 1 && (int)blockIdx.y >= a.copy_rows) {
+      // one-token call: every expert multiplies the same row
+      for (int v = threadIdx.x; v < a.H / 8; v += blockDim.x)
+        reinterpret_cast<uint4 *>(xs)[v] = __ldg(reinterpret_cast<const uint4 *>(a.x) + v);
+      __syncthreads();
+      x_staged = true;
+    }
+  } else {
+    gemv_prefetch<FMT, true, LPR, kWarps>(a, blockIdx.y, blockIdx.x, fpw, false);
+  }
   pdl_wait();      // the plan, activations and slots come from earlier kernels
   pdl_trigger();
   if constexpr (!DOWN) {
@@ -53,7 +69,7 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
       return;
     }
   }
-  gemv_block<FMT, DOWN, NT, LPR, kWarps>(a, blockIdx.y - (DOWN ? 0 : a.copy_rows), blockIdx.x, fpw, xs);
+  gemv_block<FMT, DOWN, NT, LPR, kWarps>(a, blockIdx.y - (DOWN ? 0 : a.copy_rows), blockIdx.x, fpw, xs, x_staged);
   if constexpr (DOWN) {
     if (cb.counters == nullptr) return;
     __shared__ int s_last;

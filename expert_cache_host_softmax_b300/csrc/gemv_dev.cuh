@@ -178,7 +178,7 @@ __device__ __forceinline__ void store_chunk(const RowPtrs &dst, int c, const Chu
 template <int FMT, int NT, int NROWS, int LPR>
 __device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, int K, const __nv_bfloat16 *xs,
                                          int l8, int nt, float (&acc)[NROWS][NT]) {
-  constexpr int kBatch = 2;   // the whole row was prefetched into L2 at kernel start
+  constexpr int kBatch = 4;   // a lane's chunks of a row, all in flight at once (rows of up to 4 chunks per lane)
   const int cpl = K / (32 * LPR);  // chunks per lane
 #pragma unroll 1
   for (int i0 = 0; i0 < cpl; i0 += kBatch) {
@@ -246,8 +246,10 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
 // KW * 32 / LPR * fpw output features, all of the expert's tokens, NT (>= the
 // tokens any expert of the call has, up to kTokChunk) token rows per pass.
 // xs: shared memory for NT activation rows of K.
+// x_staged (gate/up of a one-token call): xs already holds the token's row.
 template <int FMT, bool DOWN, int NT, int LPR, int KW>
-__device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int fpw, __nv_bfloat16 *xs) {
+__device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int fpw, __nv_bfloat16 *xs,
+                                           bool x_staged = false) {
   // fpw passes per warp over feature groups: long rows (large K) give each CTA
   // more features, so that the staged activations serve more weight bytes
   const int kFeatPerCta = KW * (32 / LPR) * fpw;
@@ -319,7 +321,7 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
       const int nt = min(kTokChunk, n - c0);
       // stage the chunk's activations (bf16 rows of K) in shared memory
       const int vec_per_row = K / 8;
-      for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) {
+      for (int i = threadIdx.x; i < (x_staged ? 0 : nt * vec_per_row); i += blockDim.x) {
         const int t = i / vec_per_row, v = i - t * vec_per_row;
         const __nv_bfloat16 *src;
         if (DOWN) {

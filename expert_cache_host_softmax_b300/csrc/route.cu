@@ -33,10 +33,10 @@ namespace {
 
 // ---------------------------------------------------------------- kernels
 
-// Whole routing of a small call in one CTA (see route_small_body).
+// Whole routing of a small call in one CTA (see route_body).
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a) {
   extern __shared__ int smem[];
-  route_small_body(a, smem, true);
+  route_body(a, smem, true);
 }
 
 // Multi-CTA path, step 1: top-k + gates for kChunkTokens tokens per CTA
@@ -148,9 +148,13 @@ __global__ void __launch_bounds__(256) scatter_chunk_kernel(const int32_t *__res
 // the plan), at least 256, a whole number of warps.
 int small_threads(int E) { return std::min(kRouteThreads, std::max(256, (E + 31) / 32 * 32)); }
 
+// Both single-CTA bodies: 6 E-sized arrays, 33 scan partials, the general
+// path's per-warp counts (nw*E) or the decode path's 68 pair and plan ints,
+// and the hit bitmap.
 size_t small_smem_bytes(int E, int S) {
   const size_t nw = small_threads(E) / 32;
-  return sizeof(int) * (6 * (size_t)E + 33 + nw * (size_t)E) + sizeof(unsigned) * (((size_t)S + 31) / 32);
+  return sizeof(int) * (6 * (size_t)E + 33 + std::max<size_t>(nw * (size_t)E, 68)) +
+         sizeof(unsigned) * (((size_t)S + 31) / 32);
 }
 size_t plan_smem_bytes(int E, int S) {
   return sizeof(int) * (4 * (size_t)E + 33) + sizeof(unsigned) * (((size_t)S + 31) / 32) +

@@ -399,5 +399,238 @@ __device__ __forceinline__ void route_small_body(const RouteArgs &a, int *smem, 
   block_rank_scatter(a.plan.topk_idx, 0, a.T * a.k, E, s_base, s_wcnt, a.plan.perm, a.plan.inv);
 }
 
+
+// Routing of a decode-sized call (T*k <= 32 pairs) in one CTA with four
+// block barriers instead of the general path's two dozen: the warps take one
+// token each for the top-k; warp 0 alone derives the offsets, the distinct
+// experts, the hits and the stable permute (one pair per lane); all threads
+// compact the recency list; warp 0 finishes the plan.  Same results, in the
+// same order, as route_small_body.
+constexpr int kDecodeRoutePairs = 32;
+__device__ __forceinline__ void route_decode_body(const RouteArgs &a, int *smem, bool pdl) {
+  const int E = a.E, S = a.S, P = a.T * a.k;
+  const int nw = blockDim.x >> 5;
+  const bool lru = a.mode == MODE_LRU;
+  int *s_count = smem;                 // E   tokens per expert
+  int *s_off = s_count + E;            // E   first permuted position per expert
+  int *s_uexp = s_off + E;             // E   distinct experts, ascending
+  int *s_victim = s_uexp + E;          // E
+  int *s_keyslot = s_victim + E;       // E
+  int *s_victim_key = s_keyslot + E;   // E
+  int *s_wt = s_victim_key + E;        // 33  per-warp totals
+  int *s_pe = s_wt + 33;               // 32  expert of each pair
+  int *s_uslot = s_pe + 32;            // 32  slot of each distinct expert (-1: miss)
+  int *s_sc = s_uslot + 32;            // 4   nU, nH, nM
+  unsigned *s_bits = (unsigned *)(s_sc + 4);   // [S/32] hit slots
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  Prefetch pf;
+  prefetch_tables(a, s_keyslot, pf);
+  if (pdl) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  for (int i = tid; i < E; i += blockDim.x) s_count[i] = 0;
+  if (lru)
+    for (int i = tid; i < ((S + 31) >> 5); i += blockDim.x) s_bits[i] = 0u;
+  __syncthreads();
+  for (int t = w; t < a.T; t += nw) {
+    const int e = warp_topk_softmax(a.logits + (size_t)t * E, E, a.k, a.plan.topk_idx + (size_t)t * a.k,
+                                    a.plan.gates + (size_t)t * a.k);
+    if (lane < a.k) {
+      atomicAdd(&s_count[e], 1);
+      s_pe[t * a.k + lane] = e;
+    }
+  }
+  __syncthreads();
+  if (w == 0) {
+    // offsets and distinct experts: lane l scans experts [l*per, (l+1)*per)
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int c = 0, d = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int n = s_count[e];
+      c += n;
+      d += n > 0;
+    }
+    int ci = c, di = d;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ci, o), z = __shfl_up_sync(0xffffffffu, di, o);
+      if (lane >= o) {
+        ci += y;
+        di += z;
+      }
+    }
+    const int total = __shfl_sync(0xffffffffu, ci, 31), nU = __shfl_sync(0xffffffffu, di, 31);
+    int run = ci - c, u = di - d;
+    for (int e = e0; e < e1; ++e) {
+      const int n = s_count[e];
+      a.plan.offsets[e] = run;
+      s_off[e] = run;
+      if (n > 0) s_uexp[u++] = e;
+      run += n;
+    }
+    if (lane == 0) a.plan.offsets[E] = total;
+    __syncwarp();
+    // stable permute: pair p (lane p) goes to its expert's first position
+    // plus the number of earlier pairs of the same expert
+    const int pe = lane < P ? s_pe[lane] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, pe);
+    if (lane < P) {
+      const int pos = s_off[pe] + __popc(peers & lanemask_lt());
+      a.plan.perm[pos] = lane;
+      a.plan.inv[lane] = pos;
+    }
+    // hits: the distinct experts already in a slot
+    int slot = -1, hit = 0;
+    if (lane < nU) {
+      const int eu = s_uexp[lane];
+      if (lru) {
+        slot = s_keyslot[eu];
+        hit = slot >= 0;
+      } else {
+        slot = a.bank * E + eu;
+        hit = 1;
+      }
+    }
+    const int nH = __popc(__ballot_sync(0xffffffffu, lane < nU && hit));
+    if (lru && lane < nU && hit) atomicOr(&s_bits[slot >> 5], 1u << (slot & 31));
+    s_uslot[lane] = slot;
+    if (lane == 0) {
+      s_sc[0] = nU;
+      s_sc[1] = nH;
+      s_sc[2] = nU - nH;
+    }
+  }
+  __syncthreads();
+  const int nU = s_sc[0], nH = s_sc[1], nM = s_sc[2];
+  if (lru) {
+    // recency list: the non-hit entries keep their order; the first nM of
+    // them are the victims, the rest move to the front of the new list
+    const int NT = blockDim.x;
+    const int per = (S + NT - 1) / NT;
+    const int i0 = min(S, tid * per), i1 = min(S, i0 + per);
+    int cnt = 0;
+    if (pf.n >= 0) {
+#pragma unroll
+      for (int q = 0; q < kPre; ++q)
+        if (q < pf.n) cnt += !((s_bits[pf.ord[q] >> 5] >> (pf.ord[q] & 31)) & 1u);
+    } else {
+      for (int i = i0; i < i1; ++i) {
+        const int sl = a.cache.order_in[i];
+        cnt += !((s_bits[sl >> 5] >> (sl & 31)) & 1u);
+      }
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_wt[w] = x;
+    __syncthreads();
+    int r = x - cnt;
+    for (int ww = 0; ww < w; ++ww) r += s_wt[ww];
+    if (pf.n >= 0) {
+#pragma unroll
+      for (int q = 0; q < kPre; ++q) {
+        if (q >= pf.n) continue;
+        const int sl = pf.ord[q];
+        if ((s_bits[sl >> 5] >> (sl & 31)) & 1u) continue;
+        if (r < nM) {
+          s_victim[r] = sl;
+          s_victim_key[r] = pf.key[q];
+        } else {
+          a.cache.order_out[r - nM] = sl;
+        }
+        ++r;
+      }
+    } else {
+      for (int i = i0; i < i1; ++i) {
+        const int sl = a.cache.order_in[i];
+        if ((s_bits[sl >> 5] >> (sl & 31)) & 1u) continue;
+        if (r < nM) {
+          s_victim[r] = sl;
+          s_victim_key[r] = a.cache.slot_key[sl];
+        } else {
+          a.cache.order_out[r - nM] = sl;
+        }
+        ++r;
+      }
+    }
+    __syncthreads();
+  }
+  if (w != 0) return;
+  // warp 0, lane u: distinct expert u of the call
+  const int u = lane;
+  int e = -1, key = -1, slot = -1, hit = 0, evicted = -1;
+  if (u < nU) {
+    e = s_uexp[u];
+    key = a.layer * E + e;
+    slot = s_uslot[u];
+    hit = lru ? slot >= 0 : 1;
+  }
+  const int hrank = __popc(__ballot_sync(0xffffffffu, u < nU && hit) & lanemask_lt());
+  const int mrank = u - hrank;
+  if (lru && u < nU) {
+    if (hit) {
+      a.cache.order_out[S - nH - nM + hrank] = slot;
+    } else {
+      const int v = s_victim[mrank];
+      a.cache.order_out[S - nM + mrank] = v;
+      const int ek = s_victim_key[mrank];
+      if (ek >= 0) {
+        a.cache.key_slot[ek] = -1;
+        evicted = ek;
+      }
+      a.cache.slot_key[v] = key;
+      a.cache.key_slot[key] = v;
+      slot = v;
+    }
+  }
+  const int nEv = __popc(__ballot_sync(0xffffffffu, evicted >= 0));
+  if (u < nU) {
+    a.plan.u_expert[u] = e;
+    a.plan.u_slot[u] = slot;
+    a.plan.u_hit[u] = hit;
+    a.plan.u_evicted[u] = evicted;
+    a.plan.u_info[hit ? hrank : nH + mrank] = make_int4(e, slot, s_off[e], (s_count[e] << 1) | hit);
+    if (!hit) {
+      a.plan.miss[mrank] = make_int2(key, slot);
+      if (a.mirror) {
+        a.mirror[2 + mrank] = key;
+        a.mirror[2 + a.umax + mrank] = slot;
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    if (a.mirror) {
+      // the warp's miss-list writes precede this fence, and the host reads
+      // the list only after it sees the new sequence number
+      a.mirror[1] = nM;
+      __threadfence_system();
+      *(volatile int32_t *)&a.mirror[0] = (int32_t)a.seq;
+    }
+    a.plan.n[0] = nU;
+    a.plan.n[1] = nH;
+    a.plan.n[2] = nM;
+    a.plan.n[3] = nEv;
+    unsigned long long *st = a.cache.stats;
+    const unsigned long long bytes = lru ? (unsigned long long)nM * a.blob_bytes : 0ull;
+    const unsigned long long hits_ = lru ? nH : 0, miss_ = lru ? nM : 0;
+    st[0] = pf.st[0] + nU; st[1] = pf.st[1] + hits_; st[2] = pf.st[2] + miss_; st[3] = pf.st[3] + nEv;
+    st[4] = pf.st[4] + bytes;
+    st[8] = nU; st[9] = hits_; st[10] = miss_; st[11] = nEv; st[12] = bytes;
+  }
+}
+
+// Single-CTA routing: the decode-sized path when the call has at most 32
+// (token, rank) pairs, else the general one.
+__device__ __forceinline__ void route_body(const RouteArgs &a, int *smem, bool pdl) {
+  if (a.T * a.k <= kDecodeRoutePairs) route_decode_body(a, smem, pdl);
+  else route_small_body(a, smem, pdl);
+}
+
 }  // namespace
 }  // namespace ftmoe
