@@ -34,8 +34,10 @@ using namespace ftmoe;
 
 constexpr int kProfRing = 64;   // event pairs per profiled step class
 // CTAs (of 128 threads) that copy the misses inside the gate/up GEMV kernel:
-// two per SM, 8 KB of 16-byte loads in flight each
-constexpr int kCopyCtas = 296;
+// four per SM, 8 KB of 16-byte loads in flight each (measured on decode-35B:
+// 148 / 296 / 592 / 1184 CTAs -> 53.4 / 53.4 / 52.8 / 52.1 us per miss, the
+// last with 4.6 us more per miss-free layer)
+constexpr int kCopyCtas = 592;
 
 struct ft_moe {
   int H = 0, E = 0, k = 0, I = 0, fmt = 0, S = 0, L = 0, Tmax = 0, umax = 0, mode = MODE_LRU;
