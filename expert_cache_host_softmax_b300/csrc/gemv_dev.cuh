@@ -178,7 +178,10 @@ __device__ __forceinline__ void store_chunk(const RowPtrs &dst, int c, const Chu
 template <int FMT, int NT, int NROWS, int LPR>
 __device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, int K, const __nv_bfloat16 *xs,
                                          int l8, int nt, float (&acc)[NROWS][NT]) {
-  constexpr int kBatch = 4;   // a lane's chunks of a row, all in flight at once (rows of up to 4 chunks per lane)
+  // a lane's chunks of a row in flight at once: all of them for rows of up to
+  // 4 chunks per lane on one token; 2 when several token rows already hold
+  // registers (more would cost occupancy)
+  constexpr int kBatch = NT == 1 ? 4 : 2;
   const int cpl = K / (32 * LPR);  // chunks per lane
 #pragma unroll 1
   for (int i0 = 0; i0 < cpl; i0 += kBatch) {
