@@ -277,6 +277,22 @@ def test_auto_picks_gemv_for_decode():
     gpu.close()
 
 
+def test_auto_miss_path_resolution():
+    # AUTO: the GPU copies misses for GEMV calls on experts up to 8 MiB; the
+    # copy engine serves tensor-core calls and larger experts
+    small = F.MoELayerStack(256, 8, 2, 256, "nvfp4", 8, 1, 4)
+    assert small.miss_path() == "kernel" and small.miss_path(tensor_core=True) == "copy"
+    small.set_miss_path("copy")
+    assert small.miss_path() == "copy" and small.miss_path(tensor_core=True) == "copy"
+    small.set_miss_path("pull")
+    assert small.miss_path() == "pull"
+    small.close()
+    # 4096 x 2048 BF16 = 48 MiB per expert
+    big = F.MoELayerStack(4096, 2, 1, 2048, "bf16", 2, 1, 1)
+    assert big.miss_path() == "copy"
+    big.close()
+
+
 # ------------------------------------------------------------ fused decode-layer kernel
 
 @pytest.mark.parametrize("fmt,T,path", [("nvfp4", 1, "copy"), ("mxfp4", 3, "copy"), ("bf16", 8, "copy"),
