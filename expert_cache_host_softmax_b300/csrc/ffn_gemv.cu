@@ -23,6 +23,8 @@
 // Formats: NVFP4 (e2m1 codes, E4M3 scale per 16, fp32 global scale per
 // matrix), MXFP4 (e2m1 codes, E8M0 scale per 32; OCP Microscaling v1.0),
 // BF16.  Code bytes hold element 2j in the low nibble.
+#include <algorithm>
+
 #include "ft_internal.cuh"
 
 #include "gemv_dev.cuh"
@@ -180,6 +182,26 @@ bool gemv_fuses_combine(int T) { return T <= kFusedCombineMaxT; }
 cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t s) { return launch_ffn<false>(a, CombineArgs{}, s); }
 
 cudaError_t launch_down(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) { return launch_ffn<true>(a, cb, s); }
+
+__global__ void __launch_bounds__(256) acc_to_bf16_kernel(const float4 *__restrict__ acc, uint2 *__restrict__ out,
+                                                          int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = __ldcs(acc + i);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t *>(&lo);
+    pk.y = *reinterpret_cast<uint32_t *>(&hi);
+    out[i] = pk;
+  }
+}
+
+cudaError_t launch_acc_to_bf16(const float *acc, __nv_bfloat16 *out, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int64_t n4 = n / 4;
+  const int grid = (int)std::min<int64_t>((n4 + 255) / 256, 148 * 8);
+  acc_to_bf16_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4 *>(acc), reinterpret_cast<uint2 *>(out), n4);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float *y, const float *gates, const int32_t *inv, int T, int k, int H,
                            __nv_bfloat16 *out, cudaStream_t s) {

@@ -136,6 +136,11 @@ struct FfnArgs {
   int *copy_sync;             // [0] flag, [1] arrival count
   int seq;                    // the flag value this call's miss CTAs wait for
   int seq_raised;             // the value its copying CTAs raise (seq, unless a fault is injected)
+  // tensor-core down projection: with out_acc set, each row's gate-weighted
+  // y is added into out_acc[token] (fp32, zeroed before) instead of, or with
+  // keep_y as well as, being stored to y
+  float *out_acc;             // [T][H]
+  int keep_y;
   // NVFP4 gate/up of misses whose copies are still landing their down part
   // (which holds the global scales): the scales, read by the host from the
   // pool, for each missed expert; n = 0 reads them from the slot
@@ -162,6 +167,8 @@ int gateup_feature_blocks(int H, int I);   // grid.x of the gate/up GEMV
 bool gemv_fuses_combine(int T);
 cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_down(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s);
+// out = bf16(acc) for n values (multiple of 4).
+cudaError_t launch_acc_to_bf16(const float *acc, __nv_bfloat16 *out, int64_t n, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *gates, const int32_t *inv, int T, int k, int H,
                            __nv_bfloat16 *out, cudaStream_t s);
 void ffn_init_attributes();

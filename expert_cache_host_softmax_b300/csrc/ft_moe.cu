@@ -51,6 +51,8 @@ struct ft_moe {
   int32_t *chunk_counts = nullptr, *chunk_base = nullptr;
   __nv_bfloat16 *hbuf = nullptr;
   float *ybuf = nullptr;
+  float *out_acc = nullptr;          // [Tmax][H] fp32: tensor-core calls add their gate-weighted rows here
+  bool keep_y = false;               // ft_moe_set_keep_activations
   int32_t *mirror_host = nullptr, *mirror_dev = nullptr;
   std::vector<const void *> pool;
   bool pool_loaded = false;
@@ -156,6 +158,7 @@ void free_all(ft_moe *h) {
   cudaFree(h->chunk_base);
   cudaFree(h->hbuf);
   cudaFree(h->ybuf);
+  cudaFree(h->out_acc);
   cudaFree(h->err_dev);
   cudaFree(h->xpbuf);
   cudaFree(h->combine_counters);
@@ -471,6 +474,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->chunk_counts, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->chunk_base, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
+            dev_alloc(&h->out_acc, (size_t)max_tokens * hidden) == cudaSuccess &&
             dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
             dev_alloc(&h->xpbuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->mega_sync, 4) == cudaSuccess && cudaMemset(h->mega_sync, 0, 16) == cudaSuccess &&
@@ -799,12 +803,25 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   fa.only = 0;
   // the down kernel follows the gate/up kernel directly (unless it waits for copies)
   fa.pdl = !tc && !h->prof && !capturing && !copies_before_down;
+  if (tc) {
+    // tensor cores: the down GEMM adds each row, gate-weighted, into the
+    // fp32 output rows; y reaches memory only when activations are kept
+    fa.out_acc = h->out_acc;
+    fa.keep_y = h->keep_y ? 1 : 0;
+    FT_CUDA(h, cudaMemsetAsync(h->out_acc, 0, sizeof(float) * (size_t)n_tokens * h->H, stream));
+  }
   if (!down_done) {
     prof_begin(h, FT_PROF_DOWN, stream);
     FT_CUDA(h, run_ffn(h, fa, true, tc, n_tokens, stream, cb));
     prof_end(h, FT_PROF_DOWN, stream);
   }
-  if (!fused) {
+  if (tc) {
+    h->kernel_launches += 1;
+    prof_begin(h, FT_PROF_COMBINE, stream);
+    FT_CUDA(h, launch_acc_to_bf16(h->out_acc, reinterpret_cast<__nv_bfloat16 *>(out), (int64_t)n_tokens * h->H,
+                                  stream));
+    prof_end(h, FT_PROF_COMBINE, stream);
+  } else if (!fused) {
     h->kernel_launches += 1;
     prof_begin(h, FT_PROF_COMBINE, stream);
     FT_CUDA(h, launch_combine(h->ybuf, h->plan.gates, h->plan.inv, n_tokens, h->k, h->H,
@@ -915,6 +932,13 @@ int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
 int ft_moe_last_ffn_kernel(const ft_moe *h) { return h ? (h->last_tc ? FT_FFN_TC : FT_FFN_GEMV) : -1; }
 
 int ft_moe_miss_path(const ft_moe *h, int tensor_core) { return h ? effective_miss_path(h, tensor_core != 0) : -1; }
+
+int ft_moe_set_keep_activations(ft_moe *h, int on) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  h->keep_y = on != 0;
+  return FT_OK;
+}
 
 int ft_moe_set_decode_fusion(ft_moe *h, int on) {
   if (!h) return fail(h, FT_ERR_ARG, "NULL handle");

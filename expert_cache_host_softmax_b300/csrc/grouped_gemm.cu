@@ -85,6 +85,8 @@ struct GemmArgs {
   int only;                 // 0 all, 1 hits, 2 misses
   long long gscale_off;     // byte offset of the NVFP4 global scales in a blob, else -1
   int *err;                 // device error word (first failure code)
+  float *out_acc;           // down: out_acc[token] += gate * y row (fp32 atomics), or null
+  int keep_y;               // down with out_acc: store y as well
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -575,15 +577,33 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         }
       } else {
         float *dst = a.y + (size_t)(ti.row0 + row) * a.H + ti.n * BN;
+        // the combine, fused: this row is pair (token t, rank j); its y row,
+        // times the pair's gate, goes straight into t's fp32 output row
+        float *acc = nullptr;
+        float gw = 0.0f;
+        if (a.out_acc != nullptr && valid) {
+          const int pair = a.plan.perm[ti.row0 + row];
+          acc = a.out_acc + (size_t)(pair / a.k) * a.H + ti.n * BN;
+          gw = a.plan.gates[pair] * g0;
+        }
+        const bool store_y = a.out_acc == nullptr || a.keep_y;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
           tmem_ld16(tb + c, v);
           if (valid) {
-            float4 *o = reinterpret_cast<float4 *>(dst + c);
+            if (store_y) {
+              float4 *o = reinterpret_cast<float4 *>(dst + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
+              for (int i = 0; i < 4; ++i)
+                o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
+            }
+            if (acc != nullptr) {
+              float4 *o = reinterpret_cast<float4 *>(acc + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                atomicAdd(o + i, make_float4(v[4 * i] * gw, v[4 * i + 1] * gw, v[4 * i + 2] * gw, v[4 * i + 3] * gw));
+            }
           }
         }
       }
@@ -742,6 +762,8 @@ cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const
   a.only = f.only;
   a.gscale_off = f.fmt == FMT_NVFP4 ? blob_layout(FMT_NVFP4, f.H, f.I).gscale : -1;
   a.err = err;
+  a.out_acc = down ? f.out_acc : nullptr;
+  a.keep_y = f.keep_y;
   const int NTN = down ? f.H / BN : f.I / (BN / 2);
   // M tiles <= ceil(rows / BM) + distinct experts
   const int64_t mtiles = (max_rows + BM - 1) / BM + f.umax;

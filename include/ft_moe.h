@@ -180,9 +180,18 @@ int ft_moe_last_routing(ft_moe *h, int32_t *topk_idx, float *gates, int32_t *off
 /* Diagnostics: the last forward call's intermediate activations, copied to
  * host arrays (either may be NULL), in permuted order:
  * h_act bf16 [T*k][I] (silu(gate) * up, rounded to bf16) and y f32 [T*k][H]
- * (the down projection of h_act before the gate-weighted combine).
- * Waits for the handle's work. */
+ * (the down projection of h_act before the gate-weighted combine).  On
+ * tensor-core calls y is written only while activations are kept
+ * (ft_moe_set_keep_activations).  Waits for the handle's work. */
 int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y);
+
+/* on != 0: tensor-core calls also store y for ft_moe_last_activations.
+ * Default off: the tensor-core down GEMM adds each gate-weighted row straight
+ * into an fp32 copy of the output (atomic adds, so the order of a token's k
+ * terms, and the last bits of out, may differ between runs) and y never
+ * reaches memory.  GEMV calls always store y.  Waits for the handle's work.
+ * Errors: FT_ERR_ARG. */
+int ft_moe_set_keep_activations(ft_moe *h, int on);
 
 /* Step classes timed by the profiling facility. */
 enum ft_prof_class {

@@ -28,12 +28,15 @@ class Pool:
         return self.arr[key % self.n_phys]
 
 
-def make_pair(H, E, k, I, fmt, S, L, Tmax, seed, n_phys=None, mode="lru", warm=True, flags=0):
-    """(GPU stack, oracle, pool) over the same pinned pool."""
+def make_pair(H, E, k, I, fmt, S, L, Tmax, seed, n_phys=None, mode="lru", warm=True, flags=0, keep=True):
+    """(GPU stack, oracle, pool) over the same pinned pool.  keep: tensor-core
+    calls also store y, so that the tests can check the GEMM accumulation."""
     import expert_cache_host_softmax_b300 as F
     pool = Pool(fmt, H, I, L * E, seed, n_phys, flags)
     gpu = F.MoELayerStack(H, E, k, I, fmt, S, L, Tmax)
     gpu.load_pool(pool.pointers, keepalive=pool)
+    if keep:
+        gpu.set_keep_activations(True)
     f = ftgen.FMT_NAMES[fmt]
     orc = O.MoELayerOracle(H, E, k, I, f, S, L, pool.blob, mode=O.MODE_STREAM if mode == "stream" else O.MODE_LRU)
     if mode == "stream":

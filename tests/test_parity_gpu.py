@@ -199,6 +199,20 @@ def test_tc_ffn_matches_oracle(fmt, H, I, E, k, T):
     gpu.close()
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "nvfp4"])
+def test_tc_combine_in_down_epilogue(fmt):
+    # the product setting: y is never stored, the down GEMM adds its
+    # gate-weighted rows into the fp32 output (atomics); out matches the oracle
+    H, I, E, k, T = 512, 512, 16, 4, 300
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, fmt, E, 1, T, 91, keep=False)
+    gpu.set_ffn_kernel("tc")
+    for step in range(2):
+        x, lg = Hn.inputs(91, T, H, E, step, 0)
+        _check_call(gpu, orc, 0, x, lg)
+        assert gpu.last_ffn_kernel == "tc"
+    gpu.close()
+
+
 @pytest.mark.parametrize("fmt", ["bf16", "nvfp4", "mxfp4"])
 def test_tc_and_gemv_agree(fmt):
     # the two kernels differ only in the order of the K sums
