@@ -43,15 +43,20 @@ __device__ __forceinline__ bool cta_wait_flag(const int *flag, int want, int *er
 }
 
 // Copies ranges [s0, s1) of a.seg of every miss of the call from its pinned
-// host blob into its slot.  Thread `t` of `nt` copying threads takes words t,
-// t + nt, ...: consecutive threads read consecutive 16 bytes, so each warp
-// asks PCIe for whole 128-byte lines.
+// host blob into its slot.  Thread `t` of `nt` copying threads takes slots
+// t, t + nt, ... of a padded word index: each miss's range gets a multiple of
+// 8 sixteen-byte slots, shifted so that slot 0 sits on a 128-byte boundary of
+// the host address.  A warp thus reads whole, aligned 128-byte lines over
+// PCIe (the pool's blobs need only be 16-byte aligned); slots outside the
+// range copy nothing.
 constexpr int kCopyUnroll = 4;   // 16-byte loads in flight per thread and round
 __device__ __forceinline__ void copy_misses(const MissCopyArgs &a, int s0, int s1, long long t, long long nt) {
   const int n_miss = a.n[2];
   for (int sg = s0; sg < s1; ++sg) {
     const long long per = (a.seg[sg][1] - a.seg[sg][0]) >> 4;
-    const long long total = per * n_miss;
+    if (per == 0) continue;
+    const long long per_pad = (per + 7 + 7) & ~7ll;
+    const long long total = per_pad * n_miss;
     for (long long base = t; base < total; base += nt * kCopyUnroll) {
       uint4 v[kCopyUnroll];
       uint4 *dst[kCopyUnroll];
@@ -60,11 +65,14 @@ __device__ __forceinline__ void copy_misses(const MissCopyArgs &a, int s0, int s
         const long long w = base + u * nt;
         dst[u] = nullptr;
         if (w < total) {
-          const int i = (int)(w / per);
-          const long long off = a.seg[sg][0] + ((w - (long long)i * per) << 4);
+          const int i = (int)(w / per_pad);
           const int2 m = a.miss[i];
-          dst[u] = reinterpret_cast<uint4 *>(a.slots + (size_t)m.y * a.slot_stride + off);
-          v[u] = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(a.pool_dev[m.x]) + off));
+          const uint8_t *src0 = reinterpret_cast<const uint8_t *>(a.pool_dev[m.x]) + a.seg[sg][0];
+          const long long word = (w - (long long)i * per_pad) - (long long)((reinterpret_cast<uintptr_t>(src0) >> 4) & 7);
+          if (word >= 0 && word < per) {
+            dst[u] = reinterpret_cast<uint4 *>(a.slots + (size_t)m.y * a.slot_stride + a.seg[sg][0] + (word << 4));
+            v[u] = __ldg(reinterpret_cast<const uint4 *>(src0) + word);
+          }
         }
       }
 #pragma unroll
