@@ -1,16 +1,22 @@
 // ft_moe.cu -- handle, C ABI and per-call orchestration.
 //
-// LRU mode, one forward call on the caller's stream:
-//   route (GPU: top-k, gates, permute, slot lookup, LRU update, miss list
-//          written to mapped host memory)
-//   gate/up FFN over the hits               -- starts right after route
-//   host: bounded wait for the miss list; one cudaMemcpyAsync per miss on
-//         the copy stream, ordered after route, so every earlier reader of
-//         an evicted slot has finished
-//   gate/up FFN over the misses             -- after the copies
-//   down FFN, combine
-// The misses' PCIe copies overlap the hits' FFN ("Why a Huge MoE Model Fits
-// on One Consumer GPU": a cached expert runs at GPU speed; a miss is
+// LRU mode, one forward call on the caller's stream.  The route kernel (GPU:
+// top-k, gates, permute, slot lookup, LRU update, miss list) runs first; how
+// the misses then reach their slots depends on the miss path:
+//   FT_MISS_KERNEL (AUTO's choice for GEMV calls on experts <= 8 MiB): the
+//     gate/up GEMV grid's first CTAs copy every miss from pinned host memory
+//     into its slot, gate/up bytes first; the misses' CTAs wait for them, the
+//     down kernel follows the whole grid.  No host step: forward returns at
+//     once and can be captured in a CUDA graph.
+//   FT_MISS_COPY (AUTO's choice otherwise): the hits' gate/up (and, for GEMV
+//     calls, their down projection) start right after route; the host waits
+//     (bounded) for the miss list in mapped memory and issues cudaMemcpyAsync
+//     per miss on two copy streams ordered after route, so every earlier reader
+//     of an evicted slot has finished; the misses' gate/up and down follow
+//     their bytes.
+//   FT_MISS_PULL: the GEMV kernels read misses straight from host memory.
+// The misses' PCIe transfer overlaps the hits' FFN ("Why a Huge MoE Model
+// Fits on One Consumer GPU": a cached expert runs at GPU speed; a miss is
 // streamed over PCIe).
 //
 // STREAM mode ("Long Prompts Are the Bottleneck": each MoE layer copies all of
