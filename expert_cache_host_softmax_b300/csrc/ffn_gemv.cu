@@ -10,10 +10,12 @@
 // Decode (1..4 tokens per expert) reads each weight once per call and does
 // 1..4 multiply-adds with it: bound by HBM bytes and by latency, not by the
 // contraction, so this path uses CUDA cores.  What matters is bytes in
-// flight: eight lanes share one weight row, every lane issues all of its
-// 16-byte loads for a batch of chunks before it computes, and the grid has
-// one CTA per 16 output features per expert.  Activations are staged once per
-// CTA in shared memory.
+// flight and the length of each CTA's chain of dependent loads: 8-32 lanes
+// share one weight row, every lane issues its 16-byte loads for a batch of
+// chunks before it computes, a CTA reads its plan entry in one 16-byte load,
+// and the grid has one CTA per 8-16 output features per expert.  Activations
+// are staged once per CTA in shared memory.  With FT_MISS_KERNEL the gate/up
+// grid's first rows are copying CTAs (see copy_misses).
 //
 // For small calls the combine is fused into the down projection: each CTA
 // counts itself done on a per-feature-tile counter, and the last CTA of a tile

@@ -5,7 +5,8 @@
 // permuted positions offsets[e] .. offsets[e+1]):
 //   gate/up:  [g | u] = xp_rows . W_gu^T  (fp32 accumulators in TMEM)
 //             h = bf16( silu(g) * u )     (epilogue)
-//   down:     y = h . W_d^T               (fp32)
+//   down:     y = h . W_d^T               (fp32), combined in the epilogue:
+//             out_acc[token] += gate * y row  (fp32 atomics)
 // xp is x gathered into permuted order (one row per (token, rank) pair) by a
 // small kernel first, so that both GEMMs read their token rows as plain
 // 128-row boxes.  The pages say only that cached experts run "at GPU speed"
@@ -26,7 +27,9 @@
 //     into one of two TMEM accumulators (2 x 256 columns), so the epilogue of
 //     a tile overlaps the MMAs of the next;
 //   - four epilogue warps read the accumulator with tcgen05.ld (one TMEM lane
-//     = one token row per thread) and write h (bf16) or y (f32).
+//     = one token row per thread) and write h (bf16), or add the row, times
+//     its pair's gate, into the token's fp32 output row (and store y when
+//     asked to keep it).
 // Every mbarrier wait is bounded in time.  A wait that runs out records an
 // error code, raises the CTA's abort flag, and every role drains its own
 // in-flight copies before the CTA frees its TMEM and exits.
