@@ -56,6 +56,24 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x, device=None):
+    """The largest x over the ranks of the initialised process group (x when
+    there is none): each replica's timed window ends when its slowest peer's
+    does."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world_size, ms_max):
+    """Whole-job throughput: every rank processed units_per_rank in ms_max."""
+    return units_per_rank * world_size / (ms_max * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
 
@@ -395,14 +413,9 @@ def run_ours(args, cfg):
     cum1, _ = stack.stats()
     launches = stack.kernel_launches - launches0
     d = {key_: cum1[key_] - cum0[key_] for key_ in cum1}
-    ms_max = ms
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = max_over_ranks(ms, dev)
     tokens = sum(tokens_at(cfg, s) for s in range(W, W + K))
-    value = tokens * ws / (ms_max * 1e-3)
+    value = job_rate(tokens, ws, ms_max)
 
     # ---- end to end: per step, H2D of the step's inputs from pinned host and
     # D2H of its outputs, inside the timed region
@@ -423,12 +436,8 @@ def run_ours(args, cfg):
 
     with torch.cuda.stream(stream):
         e2e_ms = timed_steps(range(W, W + K), e2e_step)
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = tokens * ws / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = job_rate(tokens, ws, e2e_ms)
 
     # ---- per-kernel timing pass (events around each step class)
     stack.set_profiling(True)
