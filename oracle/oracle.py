@@ -252,6 +252,34 @@ class ExpertSlotLRU:
             plan[e] = (e, slot, False, victim)
         return [plan[e] for e in experts]
 
+    def resize(self, n_slots: int) -> list[int]:
+        """Changes the number of slots ("Why a Huge MoE Model Fits on One
+        Consumer GPU": VRAM moves between the expert cache and the KV cache at
+        run time, without a restart).  Readings: the cache keeps its most
+        recently used keys, as many as fit, in the same recency order; the
+        others leave (not counted as evictions of a call).  A kept key stays in
+        its slot if that slot still exists, else it takes the lowest free slot,
+        least recent key first.  New slots start free.  Returns the keys that
+        left, least recent first."""
+        keep = self.recency[-n_slots:] if len(self.recency) > n_slots else list(self.recency)
+        gone = self.recency[: len(self.recency) - len(keep)]
+        slot_key = [-1] * n_slots
+        key_slot = {}
+        moved = []
+        for key in keep:
+            slot = self.key_slot[key]
+            if slot < n_slots:
+                slot_key[slot] = key
+                key_slot[key] = slot
+            else:
+                moved.append(key)
+        for key in moved:
+            slot = slot_key.index(-1)
+            slot_key[slot] = key
+            key_slot[key] = slot
+        self.S, self.slot_key, self.key_slot, self.recency = n_slots, slot_key, key_slot, keep
+        return gone
+
 
 # ----------------------------------------------------------------------------
 # Permute tokens by expert (stable counting sort of the (token, rank) pairs)
@@ -338,6 +366,16 @@ class MoELayerOracle:
             n = self.lru.warm_fill()
             self.stats["warm_loads"] += n
             self.stats["bytes_h2d"] += n * self.nbytes
+
+    def resize_slots(self, n_slots: int):
+        """The cache's slot count changes (ExpertSlotLRU.resize); in STREAM mode
+        the staging banks start empty."""
+        self.S = n_slots
+        if self.mode == MODE_LRU:
+            self.lru.resize(n_slots)
+        else:
+            self.lru = ExpertSlotLRU(n_slots, self.L, self.E)
+            self.bank_layer = [-1, -1]
 
     def weights(self, key: int):
         if key not in self._wcache:

@@ -30,6 +30,16 @@ class _MruEvictLRU(OO.ExpertSlotLRU):
             self.recency.reverse()
 
 
+class _ResizeKeepsOldestLRU(OO.ExpertSlotLRU):
+    def resize(self, n_slots):                             # keeps the least recent keys
+        self.recency.reverse()
+        try:
+            gone = super().resize(n_slots)
+        finally:
+            self.recency.reverse()
+        return gone
+
+
 def _ffn_without_up(x_rows, Wg, Wu, Wd, h_bf16=True):
     g = x_rows @ Wg.T
     h = OO.silu(g)
@@ -54,6 +64,8 @@ MUTATIONS = [
      [P.test_topk_exhaustive_tiny]),
     ("LRU evicts the MRU", "ExpertSlotLRU", _MruEvictLRU,
      [lambda: [P.test_lru_hand_worked_traces(t) for t in P._parse_traces()]]),
+    ("resize keeps the least recent keys", "ExpertSlotLRU", _ResizeKeepsOldestLRU,
+     [lambda: [P.test_lru_hand_worked_traces(t) for t in P._parse_traces()], P.test_lru_with_resizes_matches_a_list_model]),
     ("up projection dropped", "expert_ffn", _ffn_without_up,
      [lambda: P.test_layer_equals_dense_masked_mixture("bf16", 2)]),
     ("gates not normalised", "gates_of", _gates_no_max_shift_wrong,

@@ -242,6 +242,9 @@ def _parse_traces():
                 e, s, hm, ev = item.split(":")
                 plan.append((int(e), int(s), hm == "hit", -1 if ev == "-" else int(ev)))
             cur["calls"].append((layer, experts, plan))
+        elif f[0] == "resize":
+            arrow = f.index("->")
+            cur["calls"].append(("resize", int(f[1]), [-1 if v == "-" else int(v) for v in f[arrow + 1:]]))
         elif f[0] == "stats":
             cur["stats"] = tuple(int(v) for v in f[1:])
     return traces
@@ -254,6 +257,10 @@ def test_lru_hand_worked_traces(trace):
         lru.warm_fill()
     look = hits = misses = ev = 0
     for layer, experts, want in trace["calls"]:
+        if layer == "resize":
+            lru.resize(experts)
+            assert lru.slot_key == want
+            continue
         got = lru.lookup(layer, experts)
         assert got == want
         look += len(got)
@@ -313,6 +320,46 @@ def test_lru_matches_most_recent_distinct_keys_characterisation(warm):
             assert sorted(lru.key_slot.values()) == sorted(set(lru.key_slot.values()))
             for key, slot in lru.key_slot.items():
                 assert lru.slot_key[slot] == key
+
+
+def test_lru_with_resizes_matches_a_list_model():
+    """Hits, victims and contents against a bare recency list (no slots):
+    touching moves a key to the end, a miss past capacity drops the front, a
+    resize keeps the last S' keys.  Slot tables stay a bijection within range."""
+    rng = np.random.default_rng(7)
+    for trial in range(300):
+        L, E = int(rng.integers(1, 4)), int(rng.integers(1, 7))
+        umax = min(E, 3)
+        S = int(rng.integers(umax, umax + 5))
+        lru = O.ExpertSlotLRU(S, L, E)
+        model = []           # cached keys, least recent first
+        for step in range(40):
+            if rng.random() < 0.15:
+                S = int(rng.integers(umax, umax + 6))
+                gone = lru.resize(S)
+                assert gone == model[: max(0, len(model) - S)]
+                model = model[max(0, len(model) - S):]
+            else:
+                layer = int(rng.integers(0, L))
+                u = sorted(set(int(v) for v in rng.integers(0, E, int(rng.integers(1, umax + 1)))))
+                keys = [layer * E + e for e in u]
+                plan = lru.lookup(layer, u)
+                assert [p[2] for p in plan] == [k in model for k in keys]
+                hit_keys = [k for k in keys if k in model]
+                model = [k for k in model if k not in hit_keys] + hit_keys
+                for k, p in zip(keys, plan):
+                    if p[2]:
+                        continue
+                    if len(model) >= S:
+                        assert p[3] == model[0]
+                        model = model[1:]
+                    else:
+                        assert p[3] == -1
+                    model.append(k)
+            assert lru.recency == model
+            assert sorted(k for k in lru.slot_key if k >= 0) == sorted(model)
+            for key, slot in lru.key_slot.items():
+                assert 0 <= slot < S and lru.slot_key[slot] == key
 
 
 def test_lru_invariants_and_capacity_cases():
