@@ -562,6 +562,95 @@ int ft_moe_set_mode(ft_moe *h, int mode) {
   return reset_tables(h, true);
 }
 
+// Changes the slot count ("Why a Huge MoE Model Fits on One Consumer GPU":
+// VRAM moves between the expert cache and other users at run time, without a
+// restart).  The cache keeps its most recently used keys, as many as fit, in
+// the same recency order; a kept key keeps its slot if the slot still exists,
+// else takes the lowest free slot (least recent key first); new slots are
+// free.  The slot bank is reallocated at the new size and the kept blobs are
+// copied into it on the device; nothing is read from host memory.
+int ft_moe_resize_slots(ft_moe *h, int n_slots) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (n_slots < 1 || n_slots > (1 << 16)) return fail(h, FT_ERR_ARG, "n_slots must be in 1..65536");
+  if (n_slots < h->umax)
+    return fail(h, FT_ERR_CACHE_TOO_SMALL, "n_slots < min(E, max_tokens*top_k)");
+  if (h->mode == MODE_STREAM && n_slots < 2 * h->E)
+    return fail(h, FT_ERR_CACHE_TOO_SMALL, "STREAM mode needs n_slots >= 2*E (two staging layers)");
+  FT_CUDA(h, cudaSetDevice(h->device));
+  if (int rc = sync_handle(h)) return rc;
+  const int S = h->S;
+  const size_t nkeys = (size_t)h->L * h->E;
+  std::vector<int32_t> slot_key(S), key_slot(nkeys), order(S);
+  FT_CUDA(h, cudaMemcpy(slot_key.data(), h->slot_key, sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(key_slot.data(), h->key_slot, sizeof(int32_t) * nkeys, cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(order.data(), h->order[h->order_cur], sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
+  // cached keys, least recent first (free slots sit at the front of the list)
+  std::vector<int32_t> recency;
+  if (h->mode == MODE_LRU)
+    for (int s : order)
+      if (slot_key[s] >= 0) recency.push_back(slot_key[s]);
+  const size_t n_keep = std::min<size_t>(recency.size(), (size_t)n_slots);
+  const std::vector<int32_t> keep(recency.end() - n_keep, recency.end());
+  std::vector<int32_t> nslot_key(n_slots, -1), nkey_slot(nkeys, -1), from(n_slots, -1);
+  for (int32_t key : keep) {
+    const int s = key_slot[key];
+    if (s < n_slots) {
+      nslot_key[s] = key;
+      nkey_slot[key] = s;
+      from[s] = s;
+    }
+  }
+  int next_free = 0;
+  for (int32_t key : keep) {
+    if (nkey_slot[key] >= 0) continue;
+    while (nslot_key[next_free] >= 0) ++next_free;
+    nslot_key[next_free] = key;
+    nkey_slot[key] = next_free;
+    from[next_free] = key_slot[key];
+  }
+  std::vector<int32_t> norder;
+  for (int s = 0; s < n_slots; ++s)
+    if (nslot_key[s] < 0) norder.push_back(s);
+  for (int32_t key : keep) norder.push_back(nkey_slot[key]);
+  // the new bank, the kept blobs copied into it, then the tables
+  uint8_t *bank = nullptr;
+  int32_t *dslot_key = nullptr, *dorder0 = nullptr, *dorder1 = nullptr;
+  if (cudaMalloc(&bank, (size_t)n_slots * h->slot_stride) != cudaSuccess ||
+      dev_alloc(&dslot_key, n_slots) != cudaSuccess || dev_alloc(&dorder0, n_slots) != cudaSuccess ||
+      dev_alloc(&dorder1, n_slots) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(bank);
+    cudaFree(dslot_key);
+    cudaFree(dorder0);
+    cudaFree(dorder1);
+    return fail(h, FT_ERR_OOM, "device allocation for the resized cache failed");
+  }
+  for (int s = 0; s < n_slots; ++s)
+    if (from[s] >= 0)
+      FT_CUDA(h, cudaMemcpyAsync(bank + (size_t)s * h->slot_stride, h->slots + (size_t)from[s] * h->slot_stride,
+                                 h->blob_bytes, cudaMemcpyDeviceToDevice, h->copy_stream));
+  FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+  FT_CUDA(h, cudaMemcpy(dslot_key, nslot_key.data(), sizeof(int32_t) * n_slots, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(dorder0, norder.data(), sizeof(int32_t) * n_slots, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(h->key_slot, nkey_slot.data(), sizeof(int32_t) * nkeys, cudaMemcpyHostToDevice));
+  cudaFree(h->slots);
+  cudaFree(h->slot_key);
+  cudaFree(h->order[0]);
+  cudaFree(h->order[1]);
+  h->slots = bank;
+  h->slot_key = dslot_key;
+  h->order[0] = dorder0;
+  h->order[1] = dorder1;
+  h->order_cur = 0;
+  h->S = n_slots;
+  h->bank_layer[0] = h->bank_layer[1] = -1;
+  const size_t TK = (size_t)h->Tmax * h->k;
+  h->tmaps_ok = make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
+                make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
+                make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
+  return FT_OK;
+}
+
 int ft_cache_reset(ft_moe *h, int warm) {
   if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
   return reset_tables(h, warm != 0);

@@ -157,6 +157,21 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x,
  * pointer may be NULL. */
 int ft_cache_stats(ft_moe *h, ft_stats *cumulative, ft_stats *last_call);
 
+/* Changes the number of expert slots at run time, returning VRAM to (or
+ * taking it from) other users without reloading the pool ("Why a Huge MoE
+ * Model Fits on One Consumer GPU": VRAM moves between the expert cache and the
+ * KV cache at run time, without a restart).  LRU mode: the cache keeps its
+ * most recently used experts, as many as fit, in the same recency order; a
+ * kept expert keeps its slot if that slot still exists, else it moves to the
+ * lowest free slot (least recent first); new slots start free.  The experts
+ * that leave are not counted as evictions of a call; the counters are kept.
+ * STREAM mode: the staging banks start empty.  The slot bank is reallocated
+ * at the new size (old and new coexist during the call) and the kept experts
+ * are copied on the device.  Waits for the handle's work.  Errors: FT_ERR_ARG,
+ * FT_ERR_CACHE_TOO_SMALL (the rules of ft_moe_create / ft_moe_set_mode),
+ * FT_ERR_OOM (the handle is unchanged), FT_ERR_CUDA. */
+int ft_moe_resize_slots(ft_moe *h, int n_slots);
+
 /* Restores the initial cache state (warm != 0: warm fill as in load_pool;
  * warm == 0: every slot free) and clears the counters.  Synchronous. */
 int ft_cache_reset(ft_moe *h, int warm);

@@ -134,6 +134,9 @@ def test_hand_worked_lru_traces_on_gpu(trace):
     gpu, _, _ = Hn.make_pair(H, E, 1, I, "bf16", S, L, 2, 5, warm=trace["warm"])
     look = hits = misses = ev = 0
     for layer, experts, want in trace["calls"]:
+        if layer == "resize":
+            gpu.resize_slots(experts)            # the following calls show its effect
+            continue
         T = len(experts)
         lg = np.full((T, E), -5.0, np.float32)
         for t, e in enumerate(experts):
@@ -411,6 +414,33 @@ def test_device_miss_forward_is_capturable(path):
     assert Hn.rel_err(Hn.out_to_f64(out), ref["out"]) <= OUT_TOL
     _, last = gpu.stats()
     assert last["misses"] == ref["last"]["misses"] > 0
+    gpu.close()
+
+
+# ------------------------------------------------------------ resizing the slot count
+
+@pytest.mark.parametrize("path", ["copy", "kernel"])
+def test_resize_slots_matches_oracle(path):
+    # shrink and grow between calls: the kept experts' slots and bytes, and the
+    # later hits, misses and victims, match the oracle's resized LRU
+    H, I, E, k, L, T = 256, 512, 8, 2, 3, 4
+    gpu, orc, pool = Hn.make_pair(H, E, k, I, "nvfp4", 12, L, T, 141)
+    gpu.set_miss_path(path)
+    step = 0
+    for size in (12, 8, 10, 16, 9):
+        if size != 12:
+            gpu.resize_slots(size)
+            orc.resize_slots(size)
+        for _ in range(4):
+            for layer in range(L):
+                x, lg = Hn.inputs(141, T, H, E, step, layer, zipf=0.6)
+                _check_call(gpu, orc, layer, x, lg)
+            step += 1
+    cum, _ = gpu.stats()
+    assert cum["misses"] == orc.stats["misses"] > 0 and cum["evictions"] == orc.stats["evictions"]
+    with pytest.raises(F.FtError) as ei:
+        gpu.resize_slots(7)                   # below min(E, max_tokens*top_k) = 8
+    assert ei.value.code == F.FT_ERR_CACHE_TOO_SMALL
     gpu.close()
 
 
