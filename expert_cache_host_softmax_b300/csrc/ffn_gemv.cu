@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
     if (a.max_tokens == 1 && (int)blockIdx.y >= a.copy_rows) {
       // one-token call: every expert multiplies the same row
       for (int v = threadIdx.x; v < a.H / 8; v += blockDim.x)
-        reinterpret_cast<uint4 *>(xs)[v] = __ldg(reinterpret_cast<const uint4 *>(a.x) + v);
+        reinterpret_cast<uint4 *>(xs)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(a.x) + v);
       __syncthreads();
       x_staged = true;
     }

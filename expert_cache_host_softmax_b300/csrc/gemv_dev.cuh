@@ -92,6 +92,11 @@ __device__ __forceinline__ void decode8(const Chunk<FMT> &ch, int i, float *w) {
   }
 }
 
+// Position of 16-byte group q of a staged activation row: XOR-swizzled inside
+// each 128-byte block, so that the lanes of a row group (which read groups
+// 4c + i for consecutive chunks c) hit distinct banks.
+__device__ __forceinline__ int xs_pos(int q) { return q ^ ((q >> 3) & 7); }
+
 // acc[t] += chunk . xs[t][32c .. 32c+31].  FP4: each 8-element partial sum of
 // e2m1 value x activation (every product exact in fp32) is multiplied by its
 // block scale once (NVFP4: elements 0..15 and 16..31 have one E4M3 scale
@@ -116,7 +121,7 @@ __device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloa
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       if (t > 0 && t >= nt) break;   // uniform across the CTA: the expert's token rows in this pass
-      const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)t * K + 32 * c)[i];
+      const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)t * K)[xs_pos(4 * c + i)];
       float xf[8];
       bf16x8_to_float(xv, xf);
       float p = 0.0f;
@@ -333,7 +338,7 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
           const int pair = a.plan.perm[off + c0 + t];
           src = a.x + (size_t)(pair / a.k) * a.H;
         }
-        reinterpret_cast<uint4 *>(xs + (size_t)t * K)[v] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+        reinterpret_cast<uint4 *>(xs + (size_t)t * K)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
       }
       __syncthreads();
       // rows nt..NT-1 of xs may hold stale data: their products are skipped
