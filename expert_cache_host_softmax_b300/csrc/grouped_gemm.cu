@@ -477,16 +477,20 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 12)) { ok = false; break; }
         const int rs = j % NR;
         if (!mbar_wait(RAWFULL(rs), (j / NR) & 1, s_abort, a.err, 13)) { ok = false; break; }
+        // rows are 32 bytes apart: lanes 4-7 of every 8 read their second half
+        // first, so that each load instruction touches all 32 banks
         const uint32_t raw = sRaw + rs * RAW_STAGE + t * 32;
-        uint4 q0, q1;
+        const uint32_t hsw = ((t >> 2) & 1) * 16;
+        uint4 qa, qb;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(q0.x), "=r"(q0.y), "=r"(q0.z), "=r"(q0.w)
-                     : "r"(raw)
+                     : "=r"(qa.x), "=r"(qa.y), "=r"(qa.z), "=r"(qa.w)
+                     : "r"(raw + hsw)
                      : "memory");
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(q1.x), "=r"(q1.y), "=r"(q1.z), "=r"(q1.w)
-                     : "r"(raw + 16)
+                     : "=r"(qb.x), "=r"(qb.y), "=r"(qb.z), "=r"(qb.w)
+                     : "r"(raw + (hsw ^ 16))
                      : "memory");
+        const uint4 q0 = hsw ? qb : qa, q1 = hsw ? qa : qb;
         const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
         const uint32_t bdst = sB + s * B_STAGE + t * 128;
 #pragma unroll
