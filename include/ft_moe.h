@@ -167,7 +167,9 @@ int ft_cache_stats(ft_moe *h, ft_stats *cumulative, ft_stats *last_call);
  * that leave are not counted as evictions of a call; the counters are kept.
  * STREAM mode: the staging banks start empty.  The slot bank is reallocated
  * at the new size (old and new coexist during the call) and the kept experts
- * are copied on the device.  Waits for the handle's work.  Errors: FT_ERR_ARG,
+ * are copied on the device.  CUDA graphs captured from this handle before the
+ * call hold the old bank's address and must not be launched after it
+ * (capture again).  Waits for the handle's work.  Errors: FT_ERR_ARG,
  * FT_ERR_CACHE_TOO_SMALL (the rules of ft_moe_create / ft_moe_set_mode),
  * FT_ERR_OOM (the handle is unchanged), FT_ERR_CUDA. */
 int ft_moe_resize_slots(ft_moe *h, int n_slots);
