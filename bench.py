@@ -290,6 +290,24 @@ def _ffn_bytes(fmt, H, I):
     return 4 * HI, 2 * HI
 
 
+def _resize_probe(torch, dev, stack, S):
+    """After the timed runs: the slot count halved and restored
+    (ft_moe_resize_slots), wall time of each call and the device memory it
+    returned."""
+    try:
+        out = {"from": S, "to": S // 2}
+        for key, n in (("shrink", S // 2), ("grow", S)):
+            torch.cuda.synchronize(dev)
+            free0 = torch.cuda.mem_get_info(dev)[0]
+            t0 = time.perf_counter()
+            stack.resize_slots(n)
+            out[key + "_ms"] = (time.perf_counter() - t0) * 1e3
+            out[key + "_gb_freed"] = (torch.cuda.mem_get_info(dev)[0] - free0) / 1e9
+        return out
+    except Exception as e:  # reported, not fatal: the measured line stands
+        return {"error": str(e)[:200]}
+
+
 def run_ours(args, cfg):
     import torch
     import expert_cache_host_softmax_b300 as F
@@ -550,6 +568,8 @@ def run_ours(args, cfg):
         "clocks": clocks,
         "wall_s_timed": wall,
     }
+    if cfg["mode"] == "lru" and S // 2 >= min(E, T * k):
+        line["resize"] = _resize_probe(torch, dev, stack, S)
     if rank == 0 and not args.no_cpu_baseline:
         tps, desc, calls, secs = _cpu_baseline(cfg, cfg["seed"], n_phys, budget_s=args.cpu_budget, fmt=fmt)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
