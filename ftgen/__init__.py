@@ -23,8 +23,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "libftgen.so")
 _lib = None
 
-FMT_BF16, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2
-FMT_NAMES = {"bf16": FMT_BF16, "nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4}
+FMT_BF16, FMT_NVFP4, FMT_MXFP4, FMT_FP8 = 0, 1, 2, 3
+FMT_NAMES = {"bf16": FMT_BF16, "nvfp4": FMT_NVFP4, "mxfp4": FMT_MXFP4, "fp8": FMT_FP8}
 FLAG_NVFP4_UNIT_GSCALE = 1
 
 # stream kinds (high byte of the 64-bit stream id)

@@ -140,7 +140,7 @@ static float e4m3_value(uint8_t c) {
   return e4m3_pos[c & 127];
 }
 
-enum { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_MXFP4 = 2 };
+enum { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_MXFP4 = 2, FMT_FP8 = 3 };
 enum { FLAG_NVFP4_UNIT_GSCALE = 1 };
 
 int64_t ftgen_blob_bytes(int fmt, int64_t H, int64_t I) {
@@ -148,8 +148,29 @@ int64_t ftgen_blob_bytes(int fmt, int64_t H, int64_t I) {
     case FMT_BF16: return 6 * H * I;
     case FMT_NVFP4: return 27 * H * I / 16 + 16;
     case FMT_MXFP4: return 51 * H * I / 32;
+    case FMT_FP8: return 3 * H * I + 4 * (2 * I + H);
   }
   return -1;
+}
+
+/* Packs one matrix w[rows][K] into E4M3 codes[rows][K] (sign in bit 7) and one
+ * fp32 scale per row: scale = absmax(row) / 448, code = nearest E4M3 of
+ * w / scale (ties to even, saturating at 448). */
+static void pack_fp8(const float *w, int64_t rows, int64_t K, uint8_t *codes, float *scale) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const float *wr = w + r * K;
+    float amax = 0.0f;
+    for (int64_t i = 0; i < K; ++i) amax = fmaxf(amax, fabsf(wr[i]));
+    float sc = amax / 448.0f;
+    if (!(sc > 0.0f)) sc = 1.0f;
+    scale[r] = sc;
+    for (int64_t i = 0; i < K; ++i) {
+      const float v = wr[i] / sc;
+      uint8_t c = enc_e4m3_pos(fabsf(v));
+      if (v < 0 && c != 0) c |= 0x80;
+      codes[r * K + i] = c;
+    }
+  }
 }
 
 /* Packs one matrix w[rows][K] into codes[rows][K/2] and scale bytes. */
@@ -244,6 +265,17 @@ static void expert_blob(int fmt, int64_t H, int64_t I, float wstd, uint64_t seed
       else pack_nvfp4(tmp, H, I, g, d_c, d_s);
     }
     gs[3] = 0.0f;
+  } else if (fmt == FMT_FP8) {
+    /* gu codes [2I][H] | gu scales f32 [2I] | d codes [H][I] | d scales f32 [H] */
+    uint8_t *gu_c = out;
+    float *gu_s = (float *)(gu_c + 2 * HI);
+    uint8_t *d_c = (uint8_t *)(gu_s + 2 * I);
+    float *d_s = (float *)(d_c + HI);
+    for (int m = 0; m < 3; ++m) {
+      master(st, (uint64_t)(m * HI), HI, wstd, tmp);
+      if (m < 2) pack_fp8(tmp, I, H, gu_c + m * HI, gu_s + m * I);
+      else pack_fp8(tmp, H, I, d_c, d_s);
+    }
   } else {
     uint8_t *gu_c = out, *gu_s = gu_c + HI, *d_c = gu_s + HI / 16, *d_s = d_c + HI / 2;
     for (int m = 0; m < 3; ++m) {

@@ -37,8 +37,10 @@ The pages are silent on everything else.  Readings taken where they are silent:
     keys (layer, expert) in lexicographic order go to slots 0.., and slot 0 is
     the LRU.
   * formats: OCP Microscaling (MX) v1.0 for e2m1, E8M0 and MXFP4 (scale per 32).
-    NVFP4 = e2m1 x E4M3 scale per 16 x an fp32 per-matrix global scale.  The
-    blob layout is the one documented in ``ftgen/ftgen.c``.
+    NVFP4 = e2m1 x E4M3 scale per 16 x an fp32 per-matrix global scale.  FP8
+    (the pages name it among the weight formats, with no detail) = E4M3 x an
+    fp32 scale per output row.  The blob layout is the one documented in
+    ``ftgen/ftgen.c``.
 """
 from __future__ import annotations
 
@@ -46,7 +48,7 @@ import math
 
 import numpy as np
 
-FMT_BF16, FMT_NVFP4, FMT_MXFP4 = 0, 1, 2
+FMT_BF16, FMT_NVFP4, FMT_MXFP4, FMT_FP8 = 0, 1, 2, 3
 MODE_LRU, MODE_STREAM = 0, 1
 
 # ----------------------------------------------------------------------------
@@ -119,6 +121,8 @@ def blob_bytes(fmt: int, H: int, I: int) -> int:
         return n // 2 + n // 16 + 16
     if fmt == FMT_MXFP4:
         return n // 2 + n // 32
+    if fmt == FMT_FP8:
+        return n + 4 * (2 * I + H)
     raise ValueError(fmt)
 
 
@@ -166,6 +170,16 @@ def dequant_expert(blob: np.ndarray, fmt: int, H: int, I: int):
         # w = e2m1(code) * 2^(E8M0 scale of its 32-element block - 127)
         gu = _fp4_matrix(gu_c, np.repeat(_E8M0_TABLE[gu_s], 32, axis=1))
         wd = _fp4_matrix(d_c, np.repeat(_E8M0_TABLE[d_s], 32, axis=1))
+        return gu[:I], gu[I:], wd
+    if fmt == FMT_FP8:
+        o = 0
+        gu_c = blob[o:o + 2 * HI].reshape(2 * I, H); o += 2 * HI
+        gu_s = blob[o:o + 8 * I].view(np.float32).astype(np.float64); o += 8 * I
+        d_c = blob[o:o + HI].reshape(H, I); o += HI
+        d_s = blob[o:o + 4 * H].view(np.float32).astype(np.float64)
+        # w = E4M3(code) * fp32 scale of its row
+        gu = _E4M3_TABLE[gu_c] * gu_s[:, None]
+        wd = _E4M3_TABLE[d_c] * d_s[:, None]
         return gu[:I], gu[I:], wd
     raise ValueError(fmt)
 
@@ -255,7 +269,10 @@ class ExpertSlotLRU:
     def resize(self, n_slots: int) -> list[int]:
         """Changes the number of slots ("Why a Huge MoE Model Fits on One
         Consumer GPU": VRAM moves between the expert cache and the KV cache at
-        run time, without a restart).  Readings: the cache keeps its most
+        run time, without a restart; "FreeToken uses bandwidth-adaptive CPU-GPU
+        co-execution on your desktop", "Memory that moves while the engine
+        runs": VRAM is re-allocated between the expert caches and KV memory
+        without reloading weights).  Readings: the cache keeps its most
         recently used keys, as many as fit, in the same recency order; the
         others leave (not counted as evictions of a call).  A kept key stays in
         its slot if that slot still exists, else it takes the lowest free slot,

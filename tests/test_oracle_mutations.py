@@ -57,6 +57,9 @@ def _e4m3_bias8(byte):
     return v / 2.0                                           # off-by-one exponent bias
 
 
+_E4M3_UNSIGNED = np.abs(OO._E4M3_TABLE)                    # sign bit of E4M3 codes dropped
+
+
 MUTATIONS = [
     ("nibble order", "_fp4_matrix", _swapped_nibbles,
      [P.test_nvfp4_dequant_all_codes_times_all_scales, P.test_mxfp4_dequant_all_codes_times_all_scales]),
@@ -70,6 +73,8 @@ MUTATIONS = [
      [lambda: P.test_layer_equals_dense_masked_mixture("bf16", 2)]),
     ("gates not normalised", "gates_of", _gates_no_max_shift_wrong,
      [P.test_gates_closed_forms]),
+    ("E4M3 sign dropped (FP8 weights)", "_E4M3_TABLE", _E4M3_UNSIGNED,
+     [P.test_fp8_dequant_all_codes_times_row_scales]),
     ("E4M3 exponent bias", "e4m3_value", _e4m3_bias8,
      [P.test_e4m3_matches_torch_for_all_bytes]),
 ]

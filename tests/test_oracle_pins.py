@@ -120,6 +120,41 @@ def test_mxfp4_dequant_all_codes_times_all_scales():
         np.testing.assert_array_equal(Wd[r], e2m1[np.arange(I) % 16] * e8m0[(3 * r) % 255])
 
 
+def test_fp8_dequant_all_codes_times_row_scales():
+    # every E4M3 byte in every row, each row with its own fp32 scale: the oracle
+    # equals torch's E4M3 decode times the row's scale, section by section
+    H, I = 256, 256
+    HI = H * I
+    gu_c = np.tile(np.arange(256, dtype=np.uint8), (2 * I, H // 256))
+    gu_s = (np.arange(2 * I, dtype=np.float32) + 1.0) * np.float32(0.001)
+    d_c = np.tile(np.arange(256, dtype=np.uint8)[::-1].copy(), (H, I // 256))
+    d_s = (np.arange(H, dtype=np.float32) + 3.0) * np.float32(0.0007)
+    blob = np.concatenate([gu_c.ravel(), gu_s.view(np.uint8), d_c.ravel(), d_s.view(np.uint8)])
+    assert blob.size == O.blob_bytes(O.FMT_FP8, H, I) == ftgen.blob_bytes("fp8", H, I) == 3 * HI + 4 * (2 * I + H)
+    Wg, Wu, Wd = O.dequant_expert(blob, O.FMT_FP8, H, I)
+    e4m3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for r in range(2 * I):
+        W, rr = (Wg, r) if r < I else (Wu, r - I)
+        np.testing.assert_array_equal(W[rr], e4m3[gu_c[r]] * np.float64(gu_s[r]))
+    for r in range(H):
+        np.testing.assert_array_equal(Wd[r], e4m3[d_c[r]] * np.float64(d_s[r]))
+
+
+def test_dequant_fp8_is_within_half_an_e4m3_step_of_master_weights():
+    # pins the FP8 blob's section order and orientation against the master
+    # weights: each weight is the master value to within half an E4M3 step of
+    # its row's scale (3 mantissa bits: 2^-4 relative; 2^-10 x scale below 2^-6)
+    H, I = 256, 128
+    blob = ftgen.expert_blob("fp8", H, I, key=4, seed=6)
+    Ws = O.dequant_expert(blob, O.FMT_FP8, H, I)
+    Ms = ftgen.master_weights(H, I, key=4, seed=6)
+    for W, M in zip(Ws, Ms):
+        M = M.astype(np.float64)
+        scale = np.abs(M).max(axis=1, keepdims=True) / 448.0
+        bound = np.maximum(np.abs(M) * 2.0 ** -4, scale * 2.0 ** -10) * (1 + 1e-6)
+        assert np.all(np.abs(W - M) <= bound)
+
+
 def test_dequant_bf16_is_within_half_ulp_of_master_weights():
     # pins the blob section order and orientation (gate, up, down) against the
     # fp32 master weights the generator quantised
@@ -429,7 +464,7 @@ def _dense_reference(x, logits, k, weights, h_bf16=True):
     return out
 
 
-@pytest.mark.parametrize("fmt,k", [("bf16", 2), ("nvfp4", 3), ("mxfp4", 2), ("bf16", 6)])
+@pytest.mark.parametrize("fmt,k", [("bf16", 2), ("nvfp4", 3), ("mxfp4", 2), ("bf16", 6), ("fp8", 2)])
 def test_layer_equals_dense_masked_mixture(fmt, k):
     H, I, E, T, seed = 64, 96, 6, 9, 11
     f = ftgen.FMT_NAMES[fmt]
