@@ -287,6 +287,8 @@ def _ffn_bytes(fmt, H, I):
         return 2 * HI // 2 + 2 * HI // 16, HI // 2 + HI // 16
     if fmt == "mxfp4":
         return 2 * HI // 2 + 2 * HI // 32, HI // 2 + HI // 32
+    if fmt == "fp8":
+        return 2 * HI + 8 * I, HI + 4 * H
     return 4 * HI, 2 * HI
 
 
@@ -552,7 +554,8 @@ def run_ours(args, cfg):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"nvfp4": "nvfp4-w/bf16-act/f32-acc", "mxfp4": "mxfp4-w/bf16-act/f32-acc"}.get(fmt, "bf16/f32-acc"),
+        "dtype": {"nvfp4": "nvfp4-w/bf16-act/f32-acc", "mxfp4": "mxfp4-w/bf16-act/f32-acc",
+                  "fp8": "fp8-w/bf16-act/f32-acc"}.get(fmt, "bf16/f32-acc"),
         "data": "synthetic",
         "config": {"workload": cfg["name"], "layers": L, "hidden": H, "experts": E, "top_k": k, "inter": I,
                    "weight_fmt": fmt, "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
@@ -593,7 +596,7 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=32)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fmt", choices=("bf16", "nvfp4", "mxfp4"), default=None,
+    ap.add_argument("--fmt", choices=("bf16", "nvfp4", "mxfp4", "fp8"), default=None,
                     help="weight format (default: the workload's)")
     ap.add_argument("--ffn", choices=("auto", "gemv", "tc"), default="auto", help="FFN kernel")
     ap.add_argument("--miss-path", choices=("auto", "copy", "pull", "kernel"), default="auto",

@@ -17,8 +17,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libftmoe.so")
 
-FT_FMT_BF16, FT_FMT_NVFP4, FT_FMT_MXFP4 = 0, 1, 2
-FMT = {"bf16": FT_FMT_BF16, "nvfp4": FT_FMT_NVFP4, "mxfp4": FT_FMT_MXFP4}
+FT_FMT_BF16, FT_FMT_NVFP4, FT_FMT_MXFP4, FT_FMT_FP8 = 0, 1, 2, 3
+FMT = {"bf16": FT_FMT_BF16, "nvfp4": FT_FMT_NVFP4, "mxfp4": FT_FMT_MXFP4, "fp8": FT_FMT_FP8}
 FT_MODE_LRU, FT_MODE_STREAM = 0, 1
 FT_FFN_AUTO, FT_FFN_GEMV, FT_FFN_TC = 0, 1, 2
 FFN_KERNEL = {"auto": FT_FFN_AUTO, "gemv": FT_FFN_GEMV, "tc": FT_FFN_TC}

@@ -192,6 +192,7 @@ cudaError_t launch_decode_layer(const RouteArgs &route, const FfnArgs &ffn, cons
   // resident CTAs per launch configuration (cached: the query costs host time)
   static int cap[3][3] = {};
   static size_t cap_smem[3][3] = {};
+  if (ffn.fmt < FMT_BF16 || ffn.fmt > FMT_MXFP4) return cudaErrorInvalidValue;   // BF16, NVFP4, MXFP4 only
   const int fi = ffn.fmt, ni = NT == 1 ? 0 : NT == 2 ? 1 : 2;
   if (cap[fi][ni] == 0 || cap_smem[fi][ni] != smem) {
     cap_smem[fi][ni] = smem;

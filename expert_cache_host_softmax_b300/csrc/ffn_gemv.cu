@@ -24,7 +24,8 @@
 //
 // Formats: NVFP4 (e2m1 codes, E4M3 scale per 16, fp32 global scale per
 // matrix), MXFP4 (e2m1 codes, E8M0 scale per 32; OCP Microscaling v1.0),
-// BF16.  Code bytes hold element 2j in the low nibble.
+// FP8 (E4M3 codes, fp32 scale per row, applied to the finished dot product),
+// BF16.  FP4 code bytes hold element 2j in the low nibble.
 #include <algorithm>
 
 #include "ft_internal.cuh"
@@ -146,6 +147,7 @@ cudaError_t launch_ffn(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) 
   switch (a.fmt) {
     case FMT_BF16: return launch_n<FMT_BF16, DOWN>(a, cb, s);
     case FMT_NVFP4: return launch_n<FMT_NVFP4, DOWN>(a, cb, s);
+    case FMT_FP8: return launch_n<FMT_FP8, DOWN>(a, cb, s);
     default: return launch_n<FMT_MXFP4, DOWN>(a, cb, s);
   }
 }
@@ -170,6 +172,7 @@ void ffn_init_attributes() {
   attr_f<FMT_BF16>();
   attr_f<FMT_NVFP4>();
   attr_f<FMT_MXFP4>();
+  attr_f<FMT_FP8>();
 }
 
 int combine_tiles(int H) { return (H + kMinFeatPerCta - 1) / kMinFeatPerCta; }

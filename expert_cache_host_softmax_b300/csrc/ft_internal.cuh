@@ -12,7 +12,7 @@
 
 namespace ftmoe {
 
-enum { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_MXFP4 = 2 };
+enum { FMT_BF16 = 0, FMT_NVFP4 = 1, FMT_MXFP4 = 2, FMT_FP8 = 3 };
 enum { MODE_LRU = 0, MODE_STREAM = 1 };
 
 constexpr int kMaxExperts = 512;
@@ -35,6 +35,10 @@ __host__ __device__ inline BlobLayout blob_layout(int fmt, int64_t H, int64_t I)
   } else if (fmt == FMT_NVFP4) {
     b.gu_codes = 0; b.gu_sf = HI; b.d_codes = HI + HI / 8; b.d_sf = b.d_codes + HI / 2;
     b.gscale = b.d_sf + HI / 16; b.bytes = b.gscale + 16;
+  } else if (fmt == FMT_FP8) {
+    // codes, then one fp32 scale per row
+    b.gu_codes = 0; b.gu_sf = 2 * HI; b.d_codes = 2 * HI + 8 * I; b.d_sf = b.d_codes + HI;
+    b.gscale = -1; b.bytes = b.d_sf + 4 * H;
   } else {
     b.gu_codes = 0; b.gu_sf = HI; b.d_codes = HI + HI / 16; b.d_sf = b.d_codes + HI / 2;
     b.gscale = -1; b.bytes = b.d_sf + HI / 32;

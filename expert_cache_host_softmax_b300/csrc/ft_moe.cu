@@ -132,7 +132,7 @@ bool fault(const char *what) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t blob_bytes_of(int fmt, int H, int I) {
-  if (fmt < 0 || fmt > 2 || H <= 0 || I <= 0 || H % 256 || I % 256) return -1;
+  if (fmt < 0 || fmt > 3 || H <= 0 || I <= 0 || H % 256 || I % 256) return -1;
   return blob_layout(fmt, H, I).bytes;
 }
 
@@ -444,7 +444,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
                   int max_tokens, ft_moe **out) {
   if (!out) return fail(nullptr, FT_ERR_ARG, "out is NULL");
   if (blob_bytes_of(weight_fmt, hidden, inter) < 0 || hidden > 8192 || inter > 8192)
-    return fail(nullptr, FT_ERR_ARG, "hidden/inter must be multiples of 256 in 256..8192 and weight_fmt 0..2");
+    return fail(nullptr, FT_ERR_ARG, "hidden/inter must be multiples of 256 in 256..8192 and weight_fmt 0..3");
   if (n_experts < 1 || n_experts > kMaxExperts) return fail(nullptr, FT_ERR_ARG, "n_experts must be in 1..512");
   if (top_k < 1 || top_k > std::min(n_experts, kMaxTopK)) return fail(nullptr, FT_ERR_ARG, "top_k must be in 1..min(E,32)");
   if (n_layers < 1 || n_slots < 1 || max_tokens < 1 || n_slots > (1 << 16) ||
@@ -514,7 +514,9 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
   route_init_attributes();
   ffn_init_attributes();
   gemm_init_attributes();
-  h->tmaps_ok = make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
+  // the tensor-core FFN takes BF16, NVFP4 and MXFP4 (FP8 experts run on the GEMV)
+  h->tmaps_ok = h->fmt != FMT_FP8 &&
+                make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
                 make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
                 make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
   if (int rc = reset_tables(h, false)) { g_create_err = h->err; return bail(rc); }
@@ -645,7 +647,8 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
   h->S = n_slots;
   h->bank_layer[0] = h->bank_layer[1] = -1;
   const size_t TK = (size_t)h->Tmax * h->k;
-  h->tmaps_ok = make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
+  h->tmaps_ok = h->fmt != FMT_FP8 &&
+                make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
                 make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
                 make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
   return FT_OK;
@@ -673,7 +676,8 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   const bool tc = use_tc(h, n_tokens);
   const int miss_path = effective_miss_path(h, tc);
   // misses read by the kernels over PCIe: no host round trip (GEMV calls only)
-  const bool pull = h->mode == MODE_LRU && miss_path == FT_MISS_PULL && !tc;
+  // (FP8 row scales sit outside the chunks the pulling kernels copy: FP8 misses are copied)
+  const bool pull = h->mode == MODE_LRU && miss_path == FT_MISS_PULL && !tc && h->fmt != FMT_FP8;
   // misses copied on the device: no host round trip either
   const bool kcopy = h->mode == MODE_LRU && miss_path == FT_MISS_KERNEL;
   cudaStreamCaptureStatus cs;
@@ -710,7 +714,8 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   ra.chunk_base = h->chunk_base;
   // follows the previous call's last kernel directly (STREAM mode waits on a copy event first)
   ra.pdl = h->mode == MODE_LRU && !h->prof && !capturing;
-  if (h->decode_fused && h->mode == MODE_LRU && !tc && !kcopy && !capturing && mega_supported(h->E, n_tokens, h->k))
+  if (h->decode_fused && h->mode == MODE_LRU && !tc && !kcopy && !capturing && h->fmt != FMT_FP8 &&
+      mega_supported(h->E, n_tokens, h->k))
     return forward_fused(h, ra, layer, n_tokens, x, out, pull, stream);
   prof_begin(h, FT_PROF_ROUTE, stream);
   FT_CUDA(h, launch_route(ra, stream));
@@ -1018,6 +1023,8 @@ int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y) {
 
 int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
   if (!h || which < FT_FFN_AUTO || which > FT_FFN_TC) return fail(h, FT_ERR_ARG, "bad FFN kernel choice");
+  if (which == FT_FFN_TC && h->fmt == FMT_FP8)
+    return fail(h, FT_ERR_ARG, "the tensor-core FFN takes BF16, NVFP4 and MXFP4 experts; FP8 runs on the GEMV");
   if (which == FT_FFN_TC && !h->tmaps_ok)
     return fail(h, FT_ERR_CUDA, "tensor-core FFN unavailable: the TMA descriptors could not be encoded");
   h->ffn_kernel = which;

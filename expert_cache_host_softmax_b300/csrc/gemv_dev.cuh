@@ -52,20 +52,23 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float *f) {
 }
 
 // Raw bytes of one 32-element chunk of a weight row: FP4 = 16 code bytes +
-// scale bits; BF16 = 64 bytes.
+// scale bits; FP8 = 32 code bytes (its scale is per row); BF16 = 64 bytes.
+template <int FMT>
+constexpr int chunk_vecs() { return FMT == FMT_BF16 ? 4 : FMT == FMT_FP8 ? 2 : 1; }
 template <int FMT>
 struct Chunk {
-  uint4 q[FMT == FMT_BF16 ? 4 : 1];
+  uint4 q[chunk_vecs<FMT>()];
   uint32_t sf;
 };
 
 template <int FMT>
 __device__ __forceinline__ void load_chunk(const uint8_t *__restrict__ codes_row,
                                            const uint8_t *__restrict__ sf_row, int c, Chunk<FMT> &ch) {
-  if constexpr (FMT == FMT_BF16) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(codes_row) + 4 * c;
+  if constexpr (FMT == FMT_BF16 || FMT == FMT_FP8) {
+    constexpr int V = chunk_vecs<FMT>();
+    const uint4 *p = reinterpret_cast<const uint4 *>(codes_row) + V * c;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ch.q[i] = __ldg(p + i);
+    for (int i = 0; i < V; ++i) ch.q[i] = __ldg(p + i);
     ch.sf = 0;
   } else {
     ch.q[0] = __ldg(reinterpret_cast<const uint4 *>(codes_row) + c);
@@ -81,6 +84,17 @@ template <int FMT>
 __device__ __forceinline__ void decode8(const Chunk<FMT> &ch, int i, float *w) {
   if constexpr (FMT == FMT_BF16) {
     bf16x8_to_float(ch.q[i], w);
+  } else if constexpr (FMT == FMT_FP8) {
+    // eight E4M3 codes: bytes 8i .. 8i+7 of the chunk (exact in f16)
+    const uint4 &v = ch.q[i >> 1];
+    const uint32_t lo = (i & 1) ? v.z : v.x, hi = (i & 1) ? v.w : v.y;
+    const uint32_t pairs[4] = {lo & 0xFFFFu, lo >> 16, hi & 0xFFFFu, hi >> 16};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 f = __half22float2(e4m3x2_to_half2(pairs[b]));
+      w[2 * b] = f.x;
+      w[2 * b + 1] = f.y;
+    }
   } else {
     const uint32_t word = i == 0 ? ch.q[0].x : i == 1 ? ch.q[0].y : i == 2 ? ch.q[0].z : ch.q[0].w;
 #pragma unroll
@@ -127,7 +141,7 @@ __device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloa
       float p = 0.0f;
 #pragma unroll
       for (int q = 0; q < 8; ++q) p = fmaf(w[q], xf[q], p);
-      acc[t] = FMT == FMT_BF16 ? acc[t] + p : fmaf(s, p, acc[t]);
+      acc[t] = (FMT == FMT_BF16 || FMT == FMT_FP8) ? acc[t] + p : fmaf(s, p, acc[t]);
     }
   }
 }
@@ -154,6 +168,9 @@ __device__ __forceinline__ RowPtrs row_ptrs(const uint8_t *blob, const BlobLayou
   } else if constexpr (FMT == FMT_NVFP4) {
     p.codes = blob + (down ? L.d_codes : L.gu_codes) + (size_t)r * (K / 2);
     p.sf = blob + (down ? L.d_sf : L.gu_sf) + (size_t)r * (K / 16);
+  } else if constexpr (FMT == FMT_FP8) {
+    p.codes = blob + (down ? L.d_codes : L.gu_codes) + (size_t)r * K;
+    p.sf = blob + (down ? L.d_sf : L.gu_sf) + (size_t)r * 4;   // the row's fp32 scale
   } else {
     p.codes = blob + (down ? L.d_codes : L.gu_codes) + (size_t)r * (K / 2);
     p.sf = blob + (down ? L.d_sf : L.gu_sf) + (size_t)r * (K / 32);
@@ -167,10 +184,12 @@ __device__ __forceinline__ RowPtrs row_ptrs(const uint8_t *blob, const BlobLayou
 // Writes a chunk's raw bytes (codes and its block-scale bytes) to row `dst`.
 template <int FMT>
 __device__ __forceinline__ void store_chunk(const RowPtrs &dst, int c, const Chunk<FMT> &ch) {
-  if constexpr (FMT == FMT_BF16) {
-    uint4 *p = reinterpret_cast<uint4 *>(const_cast<uint8_t *>(dst.codes)) + 4 * c;
+  if constexpr (FMT == FMT_BF16 || FMT == FMT_FP8) {
+    // (FP8 row scales are not part of a chunk: FT_MISS_PULL does not take FP8)
+    constexpr int V = chunk_vecs<FMT>();
+    uint4 *p = reinterpret_cast<uint4 *>(const_cast<uint8_t *>(dst.codes)) + V * c;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) p[i] = ch.q[i];
+    for (int i = 0; i < V; ++i) p[i] = ch.q[i];
   } else {
     reinterpret_cast<uint4 *>(const_cast<uint8_t *>(dst.codes))[c] = ch.q[0];
     if constexpr (FMT == FMT_NVFP4) reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(dst.sf))[c] = (uint16_t)ch.sf;
@@ -226,6 +245,10 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
     float acc[2][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.0f;
+    if constexpr (FMT == FMT_FP8) {
+      gs0 *= __ldg(reinterpret_cast<const float *>(rp[0].sf));
+      gs1 *= __ldg(reinterpret_cast<const float *>(rp[1].sf));
+    }
     rows_dot<FMT, NT, 2, LPR>(rp, slot_dst ? dp : nullptr, a.H, xs, l8, nt, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -241,6 +264,7 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
     float acc[1][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = 0.0f;
+    if constexpr (FMT == FMT_FP8) gs0 *= __ldg(reinterpret_cast<const float *>(rp[0].sf));
     rows_dot<FMT, NT, 1, LPR>(rp, slot_dst ? dp : nullptr, a.I, xs, l8, nt, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -311,7 +335,7 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
       // ask L2 for this lane's weight chunks now, so that their DRAM latency
       // overlaps the activation staging below
       const int cpl = K / (32 * LPR);
-      const int cbytes = FMT == FMT_BF16 ? 64 : 16;
+      const int cbytes = 16 * chunk_vecs<FMT>();
       for (int fp = 0; fp < fpw; ++fp) {
         const int feat = feat0 + fp * KW * (32 / LPR);
         if (feat >= (DOWN ? a.H : a.I)) break;
@@ -364,7 +388,7 @@ __device__ __forceinline__ void gemv_prefetch(const FfnArgs &a, int u, int bx, i
   const int kFeatPerCta = KW * (32 / LPR) * fpw;
   const int feat0 = bx * kFeatPerCta + warp * (32 / LPR) + lane / LPR;
   const int cpl = K / (32 * LPR);
-  const int cbytes = FMT == FMT_BF16 ? 64 : 16;
+  const int cbytes = 16 * chunk_vecs<FMT>();
   for (int fp = 0; fp < fpw; ++fp) {
     const int feat = feat0 + fp * KW * (32 / LPR);
     if (feat >= (DOWN ? a.H : a.I)) break;

@@ -781,6 +781,7 @@ cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const
     case FMT_BF16: return down ? launch<FMT_BF16, true>(a, mA, mB, grid, s) : launch<FMT_BF16, false>(a, mA, mB, grid, s);
     case FMT_NVFP4:
       return down ? launch<FMT_NVFP4, true>(a, mA, mB, grid, s) : launch<FMT_NVFP4, false>(a, mA, mB, grid, s);
+    case FMT_FP8: return cudaErrorInvalidValue;   // FP8 experts run on the GEMV
     default: return down ? launch<FMT_MXFP4, true>(a, mA, mB, grid, s) : launch<FMT_MXFP4, false>(a, mA, mB, grid, s);
   }
 }

@@ -41,9 +41,14 @@
  *               | f32 global scale {gate, up, down, 0}          (27HI/16 + 16)
  *   FT_FMT_MXFP4: gu codes u8[2I][H/2] | gu scales e8m0[2I][H/32]
  *               | d codes u8[H][I/2]   | d scales e8m0[H][I/32]         (51HI/32)
+ *   FT_FMT_FP8  : gu codes e4m3[2I][H] | gu scales f32[2I]
+ *               | d codes e4m3[H][I]   | d scales f32[H]          (3HI + 8I + 4H)
  * FP4 code bytes hold element 2j in the low nibble and 2j+1 in the high
  * nibble.  An NVFP4 weight is e2m1(code) * e4m3(block scale) * global scale.
  * An MXFP4 weight is e2m1(code) * 2^(e8m0 - 127) (OCP Microscaling v1.0).
+ * An FP8 weight is e4m3(code) (OCP "FN") * the fp32 scale of its row.  FP8
+ * experts run on the GEMV kernel only (ft_moe_set_ffn_kernel(FT_FFN_TC) is
+ * refused) and are not pulled (FT_MISS_PULL copies them instead).
  */
 #ifndef FT_MOE_H_
 #define FT_MOE_H_
@@ -57,7 +62,7 @@ extern "C" {
 
 typedef struct ft_moe ft_moe; /* opaque handle: slot bank, cache tables, streams, events */
 
-enum ft_fmt { FT_FMT_BF16 = 0, FT_FMT_NVFP4 = 1, FT_FMT_MXFP4 = 2 };
+enum ft_fmt { FT_FMT_BF16 = 0, FT_FMT_NVFP4 = 1, FT_FMT_MXFP4 = 2, FT_FMT_FP8 = 3 };
 
 enum ft_mode {
   FT_MODE_LRU = 0,    /* decode: per-call slot lookup, LRU update, miss streaming */

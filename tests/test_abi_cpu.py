@@ -61,7 +61,7 @@ def test_create_validates_before_touching_a_device(F):
         (ok[:1] + (600,) + ok[2:], F.FT_ERR_ARG),         # more than 512 experts
         (ok[:2] + (0,) + ok[3:], F.FT_ERR_ARG),           # top_k 0
         (ok[:2] + (129,) + ok[3:], F.FT_ERR_ARG),         # top_k > E
-        (ok[:4] + (3,) + ok[5:], F.FT_ERR_ARG),           # unknown format
+        (ok[:4] + (4,) + ok[5:], F.FT_ERR_ARG),           # unknown format
         (ok[:5] + (7,) + ok[6:], F.FT_ERR_CACHE_TOO_SMALL),  # 7 slots < 8 experts of one call
         (ok[:7] + (0,), F.FT_ERR_ARG),                    # max_tokens 0
     ]

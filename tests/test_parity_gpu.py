@@ -417,6 +417,27 @@ def test_device_miss_forward_is_capturable(path):
     gpu.close()
 
 
+# ------------------------------------------------------------ FP8 experts (E4M3, scale per row)
+
+@pytest.mark.parametrize("path,T", [("kernel", 1), ("copy", 3), ("kernel", 6)])
+def test_fp8_experts_match_oracle(path, T):
+    H, I, E, k, L = 512, 768, 16, 2, 3
+    S = 10 + 2 * T
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "fp8", S, L, T, 151 + T)
+    gpu.set_miss_path(path)
+    for step in range(4):
+        for layer in range(L):
+            x, lg = Hn.inputs(151 + T, T, H, E, step, layer, zipf=0.6)
+            _check_call(gpu, orc, layer, x, lg, gemm_check=(step == 0))
+            assert gpu.last_ffn_kernel == "gemv"
+    cum, _ = gpu.stats()
+    assert cum["misses"] == orc.stats["misses"] > 0
+    with pytest.raises(F.FtError) as ei:
+        gpu.set_ffn_kernel("tc")              # FP8 experts run on the GEMV only
+    assert ei.value.code == F.FT_ERR_ARG
+    gpu.close()
+
+
 # ------------------------------------------------------------ resizing the slot count
 
 @pytest.mark.parametrize("path", ["copy", "kernel"])
