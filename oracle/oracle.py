@@ -36,6 +36,15 @@ The pages are silent on everything else.  Readings taken where they are silent:
     take the lowest free slot, or evict the LRU key.  Warm fill at load time:
     keys (layer, expert) in lexicographic order go to slots 0.., and slot 0 is
     the LRU.
+  * prefill hit-D2D ("FreeToken: Run Frontier MoE Models on Your Own GPU, and
+    the RAM It Takes", section "Long Prompts Are the Bottleneck": prefill can
+    skip the experts already in the GPU cache, so that only the others cross
+    PCIe): the staging banks are the last 2E slots and the cache keeps the
+    first S - 2E.  With the option on, a switch of mode keeps the cache under
+    the resize rules (ExpertSlotLRU.resize), and a staged expert whose key is
+    cached is copied from its slot (counted as hit_d2d), not from host memory.
+    Prefill neither fills the cache nor changes its recency: a prefill chunk
+    touches every expert of every layer, in layer order.
   * formats: OCP Microscaling (MX) v1.0 for e2m1, E8M0 and MXFP4 (scale per 32).
     NVFP4 = e2m1 x E4M3 scale per 16 x an fp32 per-matrix global scale.  FP8
     (the pages name it among the weight formats, with no detail) = E4M3 x an
@@ -278,8 +287,8 @@ class ExpertSlotLRU:
         its slot if that slot still exists, else it takes the lowest free slot,
         least recent key first.  New slots start free.  Returns the keys that
         left, least recent first."""
-        keep = self.recency[-n_slots:] if len(self.recency) > n_slots else list(self.recency)
-        gone = self.recency[: len(self.recency) - len(keep)]
+        n_gone = max(0, len(self.recency) - n_slots)
+        keep, gone = self.recency[n_gone:], self.recency[:n_gone]
         slot_key = [-1] * n_slots
         key_slot = {}
         moved = []
@@ -364,11 +373,12 @@ class MoELayerOracle:
     blob_of(key) -> uint8 blob of expert key = layer * E + e (the host pool)."""
 
     def __init__(self, H: int, E: int, k: int, I: int, fmt: int, n_slots: int, n_layers: int,
-                 blob_of, mode: int = MODE_LRU, h_bf16: bool = True):
+                 blob_of, mode: int = MODE_LRU, h_bf16: bool = True, hit_d2d: bool = False):
         self.H, self.E, self.k, self.I, self.fmt = H, E, k, I, fmt
         self.S, self.L, self.mode = n_slots, n_layers, mode
         self.blob_of = blob_of
         self.h_bf16 = h_bf16
+        self.hit_d2d = hit_d2d
         self.nbytes = blob_bytes(fmt, H, I)
         self._wcache: dict[int, tuple] = {}
         self.reset()
@@ -376,23 +386,45 @@ class MoELayerOracle:
     def reset(self, warm: bool = True):
         """Cache back to the warm-fill state (or all slots free when warm is
         False); statistics cleared."""
-        self.stats = dict(lookups=0, hits=0, misses=0, evictions=0, warm_loads=0, streamed=0, bytes_h2d=0)
-        self.lru = ExpertSlotLRU(self.S, self.L, self.E)
+        self.stats = dict(lookups=0, hits=0, misses=0, evictions=0, warm_loads=0, streamed=0, bytes_h2d=0,
+                          hit_d2d=0)
+        self.lru = ExpertSlotLRU(self.cache_slots(), self.L, self.E)
         self.bank_layer = [-1, -1]
         if self.mode == MODE_LRU and warm:
             n = self.lru.warm_fill()
             self.stats["warm_loads"] += n
             self.stats["bytes_h2d"] += n * self.nbytes
 
+    def cache_slots(self) -> int:
+        """Slots that belong to the LRU cache: all S in LRU mode; in STREAM mode
+        the last 2E are the two staging banks, so the first S - 2E."""
+        return self.S if self.mode == MODE_LRU else self.S - 2 * self.E
+
     def resize_slots(self, n_slots: int):
-        """The cache's slot count changes (ExpertSlotLRU.resize); in STREAM mode
-        the staging banks start empty."""
+        """The slot count changes: the cache follows ExpertSlotLRU.resize onto
+        its new share; in STREAM mode the staging banks start empty."""
         self.S = n_slots
-        if self.mode == MODE_LRU:
-            self.lru.resize(n_slots)
-        else:
-            self.lru = ExpertSlotLRU(n_slots, self.L, self.E)
+        if self.mode == MODE_STREAM:
             self.bank_layer = [-1, -1]
+        self.lru.resize(self.cache_slots())
+
+    def set_mode(self, mode: int):
+        """LRU (decode) or STREAM (prefill).  Without hit-D2D the cache starts
+        over in the new mode's initial state (reset: warm fill in LRU mode,
+        empty in STREAM mode).  With it the cache lives through the switch: it
+        shrinks onto the first S - 2E slots when STREAM mode begins and grows
+        back to S when it ends (ExpertSlotLRU.resize in both directions), and
+        the statistics carry on.  Setting the current mode again with hit-D2D
+        on changes nothing."""
+        if not self.hit_d2d:
+            self.mode = mode
+            self.reset()
+            return
+        if mode == self.mode:
+            return
+        self.mode = mode
+        self.bank_layer = [-1, -1]
+        self.lru.resize(self.cache_slots())
 
     def weights(self, key: int):
         if key not in self._wcache:
@@ -404,13 +436,18 @@ class MoELayerOracle:
     def _stream(self, layer: int, last: dict):
         """Full-layer streaming: bank (layer mod 2) must hold all E experts of
         `layer` before it computes; the next layer's experts are copied into the
-        other bank at the same call ("Long Prompts Are the Bottleneck")."""
+        other bank at the same call ("Long Prompts Are the Bottleneck").  With
+        hit-D2D on, an expert whose key is in the cache comes from its slot."""
         def fill(l):
             b = l % 2
             if self.bank_layer[b] != l:
                 self.bank_layer[b] = l
-                last["streamed"] += self.E
-                last["bytes_h2d"] += self.E * self.nbytes
+                for e in range(self.E):
+                    if self.hit_d2d and l * self.E + e in self.lru.key_slot:
+                        last["hit_d2d"] += 1          # from its cache slot
+                    else:
+                        last["streamed"] += 1         # from host memory
+                        last["bytes_h2d"] += self.nbytes
         fill(layer)
         nxt = layer + 1 if layer + 1 < self.L else 0
         if nxt % 2 != layer % 2:
@@ -430,7 +467,8 @@ class MoELayerOracle:
         idx = topk_experts(logits, self.k)
         gates = gates_of(logits, idx)
         experts = sorted(set(int(e) for e in idx.reshape(-1)))
-        last = dict(lookups=len(experts), hits=0, misses=0, evictions=0, warm_loads=0, streamed=0, bytes_h2d=0)
+        last = dict(lookups=len(experts), hits=0, misses=0, evictions=0, warm_loads=0, streamed=0, bytes_h2d=0,
+                    hit_d2d=0)
         if self.mode == MODE_LRU:
             plan = self.lru.lookup(layer, experts)
             for (_, _, hit, victim) in plan:
@@ -443,7 +481,7 @@ class MoELayerOracle:
                         last["evictions"] += 1
         else:
             self._stream(layer, last)
-            plan = [(e, (layer % 2) * self.E + e, True, -1) for e in experts]
+            plan = [(e, self.cache_slots() + (layer % 2) * self.E + e, True, -1) for e in experts]
         for key_, v in last.items():
             self.stats[key_] += v
         offsets, perm, inv = permute_by_expert(idx, self.E)

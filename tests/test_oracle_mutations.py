@@ -40,6 +40,30 @@ class _ResizeKeepsOldestLRU(OO.ExpertSlotLRU):
         return gone
 
 
+class _StagingIgnoresCacheOracle(OO.MoELayerOracle):
+    def _stream(self, layer, last):                        # stages every expert from host memory
+        on, self.hit_d2d = self.hit_d2d, False
+        try:
+            super()._stream(layer, last)
+        finally:
+            self.hit_d2d = on
+
+
+class _SwitchForgetsCacheOracle(OO.MoELayerOracle):
+    def set_mode(self, mode):                              # the cache starts over at every switch
+        self.mode = mode
+        self.bank_layer = [-1, -1]
+        self.lru = OO.ExpertSlotLRU(self.cache_slots(), self.L, self.E)
+
+
+def _plain_traces():
+    return [t for t in P._parse_traces() if not t["d2d"]]
+
+
+def _d2d_traces():
+    return [t for t in P._parse_traces() if t["d2d"]]
+
+
 def _ffn_without_up(x_rows, Wg, Wu, Wd, h_bf16=True):
     g = x_rows @ Wg.T
     h = OO.silu(g)
@@ -66,9 +90,15 @@ MUTATIONS = [
     ("top-k ties to the higher id", "topk_experts", _topk_high_index_ties,
      [P.test_topk_exhaustive_tiny]),
     ("LRU evicts the MRU", "ExpertSlotLRU", _MruEvictLRU,
-     [lambda: [P.test_lru_hand_worked_traces(t) for t in P._parse_traces()]]),
+     [lambda: [P.test_lru_hand_worked_traces(t) for t in _plain_traces()]]),
     ("resize keeps the least recent keys", "ExpertSlotLRU", _ResizeKeepsOldestLRU,
-     [lambda: [P.test_lru_hand_worked_traces(t) for t in P._parse_traces()], P.test_lru_with_resizes_matches_a_list_model]),
+     [lambda: [P.test_lru_hand_worked_traces(t) for t in _plain_traces()], P.test_lru_with_resizes_matches_a_list_model]),
+    ("prefill ignores the cache (hit-D2D)", "MoELayerOracle", _StagingIgnoresCacheOracle,
+     [lambda: [P.test_prefill_hit_d2d_hand_worked_traces(t) for t in _d2d_traces()],
+      P.test_prefill_hit_d2d_matches_a_list_model]),
+    ("mode switch forgets the cache (hit-D2D)", "MoELayerOracle", _SwitchForgetsCacheOracle,
+     [lambda: [P.test_prefill_hit_d2d_hand_worked_traces(t) for t in _d2d_traces()],
+      P.test_prefill_hit_d2d_matches_a_list_model]),
     ("up projection dropped", "expert_ffn", _ffn_without_up,
      [lambda: P.test_layer_equals_dense_masked_mixture("bf16", 2)]),
     ("gates not normalised", "gates_of", _gates_no_max_shift_wrong,

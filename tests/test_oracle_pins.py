@@ -267,7 +267,8 @@ def _parse_traces():
         f = line.split()
         if f[0] == "trace":
             kv = dict(x.split("=") for x in f[2:])
-            cur = dict(name=f[1], S=int(kv["S"]), L=int(kv["L"]), E=int(kv["E"]), warm=kv["warm"] == "1", calls=[])
+            cur = dict(name=f[1], S=int(kv["S"]), L=int(kv["L"]), E=int(kv["E"]), warm=kv["warm"] == "1",
+                       d2d=kv.get("d2d", "0") == "1", calls=[], copies=None)
             traces.append(cur)
         elif f[0] == "call":
             arrow = f.index("->")
@@ -280,12 +281,30 @@ def _parse_traces():
         elif f[0] == "resize":
             arrow = f.index("->")
             cur["calls"].append(("resize", int(f[1]), [-1 if v == "-" else int(v) for v in f[arrow + 1:]]))
+        elif f[0] == "mode":
+            arrow = f.index("->")
+            cur["calls"].append(("mode", f[1], [-1 if v == "-" else int(v) for v in f[arrow + 1:]]))
+        elif f[0] == "prefill":
+            arrow = f.index("->")
+            counts = dict(v.split("=") for v in f[arrow + 1:])
+            cur["calls"].append(("prefill", (int(f[1]), [int(v) for v in f[2:arrow]]),
+                                 (int(counts["d2d"]), int(counts["h2d"]))))
         elif f[0] == "stats":
             cur["stats"] = tuple(int(v) for v in f[1:])
+        elif f[0] == "copies":
+            cur["copies"] = tuple(int(v) for v in f[1:])
     return traces
 
 
-@pytest.mark.parametrize("trace", _parse_traces(), ids=lambda t: t["name"])
+def _one_hot_logits(experts, E):
+    """Logits that route token t to experts[t] alone (k = 1)."""
+    lg = np.full((len(experts), E), -5.0, np.float32)
+    for t, e in enumerate(experts):
+        lg[t, e] = 5.0
+    return lg
+
+
+@pytest.mark.parametrize("trace", [t for t in _parse_traces() if not t["d2d"]], ids=lambda t: t["name"])
 def test_lru_hand_worked_traces(trace):
     lru = O.ExpertSlotLRU(trace["S"], trace["L"], trace["E"])
     if trace["warm"]:
@@ -303,6 +322,101 @@ def test_lru_hand_worked_traces(trace):
         misses += sum(not p[2] for p in got)
         ev += sum(p[3] >= 0 for p in got)
     assert (look, hits, misses, ev) == trace["stats"]
+
+
+@pytest.mark.parametrize("trace", [t for t in _parse_traces() if t["d2d"]], ids=lambda t: t["name"])
+def test_prefill_hit_d2d_hand_worked_traces(trace):
+    """The whole layer object (modes, staging banks, copy counts) against the
+    hand-worked traces; k = 1 and one-hot logits fix the routing."""
+    H = I = 64
+    E, L, S = trace["E"], trace["L"], trace["S"]
+    blobs = ftgen.pool("bf16", H, I, list(range(L * E)), 9)
+    orc = O.MoELayerOracle(H, E, 1, I, O.FMT_BF16, S, L, lambda key: blobs[key], hit_d2d=True)
+    orc.reset(warm=trace["warm"])
+    for kind, arg, want in trace["calls"]:
+        if kind == "resize":
+            orc.resize_slots(arg)
+            assert orc.lru.slot_key == want
+        elif kind == "mode":
+            orc.set_mode(O.MODE_STREAM if arg == "stream" else O.MODE_LRU)
+            assert orc.lru.slot_key == want
+        else:
+            layer, experts = (arg if kind == "prefill" else (kind, arg))
+            lg = _one_hot_logits(experts, E)
+            res = orc.forward(layer, ftgen.x_bf16(9, len(experts), H, 0, layer), lg)
+            if kind == "prefill":
+                assert (res["last"]["hit_d2d"], res["last"]["streamed"]) == want
+                assert res["last"]["hits"] == res["last"]["misses"] == 0
+                # the staging banks are the last 2E slots
+                assert [p[1] for p in res["plan"]] == [S - 2 * E + (layer % 2) * E + e for e in experts]
+            else:
+                assert res["plan"] == want
+    st = orc.stats
+    assert (st["lookups"], st["hits"], st["misses"], st["evictions"]) == trace["stats"]
+    assert (st["hit_d2d"], st["streamed"]) == trace["copies"]
+
+
+def test_prefill_hit_d2d_matches_a_list_model():
+    """Random decode calls, mode switches and prefill calls with hit-D2D on,
+    against a bare recency list and a bank record kept here: the cache keeps
+    its last S - 2E keys into prefill and all of them out of it; each staged
+    layer's copies split into cached keys (slot -> bank) and the rest (host ->
+    bank); prefill leaves the list alone."""
+    rng = np.random.default_rng(11)
+    H = I = 64
+    for trial in range(40):
+        L, E = int(rng.integers(2, 5)), int(rng.integers(1, 4))
+        S = 2 * E + int(rng.integers(0, L * E + 2))
+        blobs = ftgen.pool("bf16", H, I, list(range(L * E)), 3)
+        orc = O.MoELayerOracle(H, E, 1, I, O.FMT_BF16, S, L, lambda key: blobs[key], hit_d2d=True)
+        model = list(range(min(S, L * E)))        # warm fill: keys in order, key 0 least recent
+        stream, banks = False, [-1, -1]
+        for step in range(30):
+            r = rng.random()
+            if r < 0.15:
+                stream = not stream
+                orc.set_mode(O.MODE_STREAM if stream else O.MODE_LRU)
+                if stream:
+                    model = model[max(0, len(model) - (S - 2 * E)):]
+                    banks = [-1, -1]
+                continue
+            layer = int(rng.integers(0, L))
+            experts = sorted(set(int(v) for v in rng.integers(0, E, int(rng.integers(1, E + 1)))))
+            res = orc.forward(layer, ftgen.x_bf16(3, len(experts), H, step, layer), _one_hot_logits(experts, E))
+            if stream:
+                staged = []
+                for l in (layer, (layer + 1) % L):
+                    if banks[l % 2] != l and (l == layer or l % 2 != layer % 2):
+                        banks[l % 2] = l
+                        staged.append(l)
+                cached = sum(1 for l in staged for e in range(E) if l * E + e in model)
+                assert res["last"]["hit_d2d"] == cached
+                assert res["last"]["streamed"] == len(staged) * E - cached
+            else:
+                keys = [layer * E + e for e in experts]
+                assert [p[2] for p in res["plan"]] == [key in model for key in keys]
+                hit_keys = [key for key in keys if key in model]
+                model = [key for key in model if key not in hit_keys] + hit_keys
+                for key, p in zip(keys, res["plan"]):
+                    if not p[2]:
+                        if len(model) >= S:
+                            model = model[1:]
+                        model.append(key)
+            assert orc.lru.recency == model
+
+
+def test_prefill_without_hit_d2d_streams_every_expert():
+    """With the option off, the switch to STREAM mode starts over and every
+    staged expert comes from host memory, whatever was cached before."""
+    H = I = 64
+    L, E, S = 3, 2, 10
+    blobs = ftgen.pool("bf16", H, I, list(range(L * E)), 5)
+    orc = O.MoELayerOracle(H, E, 1, I, O.FMT_BF16, S, L, lambda key: blobs[key])
+    orc.set_mode(O.MODE_STREAM)
+    for layer in range(L):
+        res = orc.forward(layer, ftgen.x_bf16(5, 1, H, 0, layer), _one_hot_logits([0], E))
+        assert res["last"]["hit_d2d"] == 0
+    assert orc.stats["streamed"] == E * L and orc.stats["hit_d2d"] == 0   # L odd: no wrap-around prefetch
 
 
 def _random_calls(rng, L, E, n, umax):
