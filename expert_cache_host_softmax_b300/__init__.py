@@ -33,13 +33,14 @@ STATUS_NAMES = {0: "FT_OK", -1: "FT_ERR_ARG", -2: "FT_ERR_CUDA", -3: "FT_ERR_OOM
 EXPORTED = ("ft_moe_blob_bytes", "ft_moe_create", "ft_moe_load_pool", "ft_moe_set_mode", "ft_moe_forward",
             "ft_cache_stats", "ft_cache_reset", "ft_cache_trace", "ft_moe_last_routing", "ft_moe_last_activations",
             "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_set_ffn_kernel", "ft_moe_last_ffn_kernel", "ft_moe_set_miss_path", "ft_moe_miss_path", "ft_moe_set_decode_fusion", "ft_moe_set_keep_activations", "ft_moe_resize_slots",
+            "ft_moe_set_prefill_hit_d2d", "ft_moe_prefill_hit_d2d",
             "ft_moe_slot_stride", "ft_moe_kernel_launches",
             "ft_last_error", "ft_moe_destroy", "ft_topk_softmax", "ft_permute_workspace_bytes", "ft_permute", "ft_permute_noalloc")
 
 
 class FtStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
-                ("lookups", "hits", "misses", "evictions", "warm_loads", "streamed", "bytes_h2d")]
+                ("lookups", "hits", "misses", "evictions", "warm_loads", "streamed", "bytes_h2d", "hit_d2d")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}
@@ -82,6 +83,8 @@ def lib():
         L.ft_moe_miss_path.argtypes = [vp, i32]
         L.ft_moe_set_keep_activations.argtypes = [vp, i32]
         L.ft_moe_resize_slots.argtypes = [vp, i32]
+        L.ft_moe_set_prefill_hit_d2d.argtypes = [vp, i32]
+        L.ft_moe_prefill_hit_d2d.argtypes = [vp]
         L.ft_moe_set_miss_path.argtypes = [vp, i32]
         L.ft_moe_set_decode_fusion.argtypes = [vp, i32]
         L.ft_moe_kernel_launches.restype = i64
@@ -231,6 +234,17 @@ class MoELayerStack:
     def resize_slots(self, n_slots):
         """Changes the number of expert slots (the most recently used experts stay)."""
         _check(lib().ft_moe_resize_slots(self._h, int(n_slots)), self._h)
+
+    def set_prefill_hit_d2d(self, on=True):
+        """STREAM-mode staging copies the experts the cache holds from their slots, and mode
+        switches keep the cache (off by default)."""
+        _check(lib().ft_moe_set_prefill_hit_d2d(self._h, 1 if on else 0), self._h)
+
+    def prefill_hit_d2d(self):
+        r = lib().ft_moe_prefill_hit_d2d(self._h)
+        if r < 0:
+            _check(r, self._h)
+        return r == 1
 
     def set_keep_activations(self, on):
         """Tensor-core calls also store y for last_activations (off by default)."""

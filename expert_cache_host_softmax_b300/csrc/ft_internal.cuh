@@ -73,7 +73,8 @@ struct CacheBufs {
 
 struct RouteArgs {
   const float *logits;
-  int T, E, k, layer, mode, bank, S;
+  int T, E, k, layer, mode, S;
+  int bank_slot0;           // STREAM mode: first slot of the bank that holds this layer
   long long blob_bytes;
   PlanBufs plan;
   CacheBufs cache;

@@ -65,7 +65,7 @@ struct ft_moe {
   // miss copies alternate between two copy streams, so that one copy's
   // set-up overlaps the previous copy's transfer; copy_stream joins both
   cudaStream_t copy_stream = nullptr, copy_stream2 = nullptr;
-  cudaEvent_t ev_route = nullptr, ev_copy = nullptr, ev_copy2 = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_route = nullptr, ev_copy = nullptr, ev_copy2 = nullptr, ev_done = nullptr, ev_d2d = nullptr;
   cudaEvent_t ev_bank_ready[2] = {nullptr, nullptr}, ev_bank_free[2] = {nullptr, nullptr};
   int bank_layer[2] = {-1, -1};
   uint32_t seq = 0;
@@ -73,8 +73,13 @@ struct ft_moe {
   bool any_call = false;
   bool last_tc = false;
   bool captured = false;   // a forward was captured into a graph since the last synchronising call
-  uint64_t host_warm = 0, host_streamed = 0, host_bytes = 0;
-  uint64_t last_streamed = 0, last_stream_bytes = 0;
+  uint64_t host_warm = 0, host_streamed = 0, host_bytes = 0, host_d2d = 0;
+  uint64_t last_streamed = 0, last_stream_bytes = 0, last_d2d = 0;
+  // prefill hit-D2D (ft_moe_set_prefill_hit_d2d): STREAM-mode staging copies
+  // the experts that the cache holds from their slots; the cache does not
+  // change during STREAM mode, so the host keeps its key -> slot map
+  bool hit_d2d = false;
+  std::vector<int32_t> stream_key_slot;
   // optional per-step timing (ft_moe_set_profiling)
   bool prof = false;
   // a ring of event pairs per class, folded into the totals only when the
@@ -175,7 +180,7 @@ void free_all(ft_moe *h) {
   if (h->seq_ring) cudaFreeHost(h->seq_ring);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   if (h->copy_stream2) cudaStreamDestroy(h->copy_stream2);
-  for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_copy2, h->ev_done, h->ev_bank_ready[0], h->ev_bank_ready[1],
+  for (cudaEvent_t ev : {h->ev_route, h->ev_copy, h->ev_copy2, h->ev_done, h->ev_d2d, h->ev_bank_ready[0], h->ev_bank_ready[1],
                          h->ev_bank_free[0], h->ev_bank_free[1]})
     if (ev) cudaEventDestroy(ev);
   for (auto &cls : h->prof_ev)
@@ -285,9 +290,10 @@ int reset_tables(ft_moe *h, bool warm) {
   FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
   FT_CUDA(h, cudaMemset(h->copy_sync, 0, 2 * sizeof(int)));
   FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
-  h->host_warm = h->host_streamed = h->host_bytes = 0;
-  h->last_streamed = h->last_stream_bytes = 0;
+  h->host_warm = h->host_streamed = h->host_bytes = h->host_d2d = 0;
+  h->last_streamed = h->last_stream_bytes = h->last_d2d = 0;
   h->bank_layer[0] = h->bank_layer[1] = -1;
+  h->stream_key_slot.assign(h->mode == MODE_STREAM ? key_slot.size() : 0, -1);
   h->last_T = 0;
   if (h->pool_loaded) {
     for (int s = 0; s < n; ++s)
@@ -300,23 +306,104 @@ int reset_tables(ft_moe *h, bool warm) {
   return FT_OK;
 }
 
+// Slots that belong to the LRU cache in `mode` with S slots: all of them in
+// LRU mode; in STREAM mode the last 2E slots are the two staging banks ("Long
+// Prompts Are the Bottleneck": the cache must hold the two staging layers).
+int cache_slots(const ft_moe *h, int mode, int S) { return mode == MODE_LRU ? S : S - 2 * h->E; }
+
+// First slot of staging bank b (STREAM mode).
+int64_t bank_slot0(const ft_moe *h, int b) { return (int64_t)h->S - 2 * h->E + (int64_t)b * h->E; }
+
 // STREAM mode: make bank (layer mod 2) receive all experts of `layer`, after
-// the FFN that last read that bank.
+// the FFN that last read that bank.  With prefill hit-D2D an expert that the
+// cache holds is copied from its slot on the device (second copy stream),
+// the others from host memory; copy_stream joins both.
 int stage_layer(ft_moe *h, int layer) {
   const int b = layer & 1;
   if (h->bank_layer[b] == layer) return FT_OK;
+  const int64_t bank0 = bank_slot0(h, b);
   FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_bank_free[b], 0));
   prof_begin(h, FT_PROF_STREAM_COPY, h->copy_stream);
-  for (int e = 0; e < h->E; ++e)
-    FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)(b * h->E + e) * h->slot_stride,
-                               h->pool[(size_t)layer * h->E + e], h->blob_bytes, cudaMemcpyHostToDevice,
-                               h->copy_stream));
+  int n_d2d = 0;
+  for (int e = 0; e < h->E; ++e) {
+    const size_t key = (size_t)layer * h->E + e;
+    uint8_t *dst = h->slots + (size_t)(bank0 + e) * h->slot_stride;
+    const int from = h->hit_d2d && key < h->stream_key_slot.size() ? h->stream_key_slot[key] : -1;
+    if (from < 0) {
+      FT_CUDA(h, cudaMemcpyAsync(dst, h->pool[key], h->blob_bytes, cudaMemcpyHostToDevice, h->copy_stream));
+      continue;
+    }
+    if (n_d2d++ == 0) FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream2, h->ev_bank_free[b], 0));
+    FT_CUDA(h, cudaMemcpyAsync(dst, h->slots + (size_t)from * h->slot_stride, h->blob_bytes,
+                               cudaMemcpyDeviceToDevice, h->copy_stream2));
+  }
+  if (n_d2d > 0) {
+    FT_CUDA(h, cudaEventRecord(h->ev_d2d, h->copy_stream2));
+    FT_CUDA(h, cudaStreamWaitEvent(h->copy_stream, h->ev_d2d, 0));
+  }
   prof_end(h, FT_PROF_STREAM_COPY, h->copy_stream);
   FT_CUDA(h, cudaEventRecord(h->ev_bank_ready[b], h->copy_stream));
   h->bank_layer[b] = layer;
-  h->last_streamed += h->E;
-  h->last_stream_bytes += (uint64_t)h->E * h->blob_bytes;
+  h->last_streamed += h->E - n_d2d;
+  h->last_stream_bytes += (uint64_t)(h->E - n_d2d) * h->blob_bytes;
+  h->last_d2d += n_d2d;
   return FT_OK;
+}
+
+// The cache's keys, least recent first, and its key -> slot table, read from
+// the device (the order list holds the free slots in front of the keys).
+int read_cache(ft_moe *h, std::vector<int32_t> &key_slot, std::vector<int32_t> &recency) {
+  const int S = h->S;
+  std::vector<int32_t> slot_key(S), order(S);
+  key_slot.resize((size_t)h->L * h->E);
+  FT_CUDA(h, cudaMemcpy(slot_key.data(), h->slot_key, sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(key_slot.data(), h->key_slot, sizeof(int32_t) * key_slot.size(), cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(order.data(), h->order[h->order_cur], sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
+  recency.clear();
+  for (int s : order)
+    if (s >= 0 && s < S && slot_key[s] >= 0) recency.push_back(slot_key[s]);
+  return FT_OK;
+}
+
+// The cache re-planned onto the first n_cache of n_slots slots ("Why a Huge
+// MoE Model Fits on One Consumer GPU": VRAM moves between the expert cache
+// and other users at run time).  The most recent keys that fit stay, in the
+// same recency order; a kept key keeps its slot if it is below n_cache, else
+// it takes the lowest free slot (least recent key first).  from[s] is the old
+// slot whose bytes slot s must receive (-1: none).  The order list has the
+// free slots first, by index, then the keys, least recent first.
+struct CachePlan {
+  std::vector<int32_t> slot_key, key_slot, order, from;
+};
+
+CachePlan plan_cache(const std::vector<int32_t> &key_slot, const std::vector<int32_t> &recency, int n_cache,
+                     int n_slots) {
+  CachePlan p;
+  p.slot_key.assign(n_slots, -1);
+  p.key_slot.assign(key_slot.size(), -1);
+  p.from.assign(n_slots, -1);
+  const size_t n_keep = std::min<size_t>(recency.size(), (size_t)std::max(n_cache, 0));
+  const std::vector<int32_t> keep(recency.end() - n_keep, recency.end());
+  for (int32_t key : keep) {
+    const int s = key_slot[key];
+    if (s < n_cache) {
+      p.slot_key[s] = key;
+      p.key_slot[key] = s;
+      p.from[s] = s;
+    }
+  }
+  int next_free = 0;
+  for (int32_t key : keep) {
+    if (p.key_slot[key] >= 0) continue;
+    while (p.slot_key[next_free] >= 0) ++next_free;
+    p.slot_key[next_free] = key;
+    p.key_slot[key] = next_free;
+    p.from[next_free] = key_slot[key];
+  }
+  for (int s = 0; s < n_slots; ++s)
+    if (p.slot_key[s] < 0) p.order.push_back(s);
+  for (int32_t key : keep) p.order.push_back(p.key_slot[key]);
+  return p;
 }
 
 // FT_MISS_AUTO: the device copy (no host round trip, ~10 % lower PCIe rate,
@@ -505,6 +592,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
        cudaEventCreateWithFlags(&h->ev_route, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_copy, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_copy2, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&h->ev_d2d, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_done, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_bank_ready[0], cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&h->ev_bank_ready[1], cudaEventDisableTiming) == cudaSuccess &&
@@ -559,9 +647,34 @@ int ft_moe_set_mode(ft_moe *h, int mode) {
   if (!h || (mode != MODE_LRU && mode != MODE_STREAM)) return fail(h, FT_ERR_ARG, "bad mode");
   if (mode == MODE_STREAM && h->S < 2 * h->E)
     return fail(h, FT_ERR_CACHE_TOO_SMALL, "STREAM mode needs n_slots >= 2*E (two staging layers)");
+  FT_CUDA(h, cudaSetDevice(h->device));
   if (int rc = sync_handle(h)) return rc;
+  if (!h->hit_d2d) {
+    h->mode = mode;
+    return reset_tables(h, true);
+  }
+  if (mode == h->mode) return FT_OK;
+  // prefill hit-D2D: the cache lives through the switch, shrunk onto the
+  // slots below the staging banks (or grown back to all S), in place: the
+  // keys that move go from slots >= S - 2E to free slots below it, so no copy
+  // reads a slot that another one writes
+  std::vector<int32_t> key_slot, recency;
+  if (int rc = read_cache(h, key_slot, recency)) return rc;
+  const CachePlan p = plan_cache(key_slot, recency, cache_slots(h, mode, h->S), h->S);
+  for (int s = 0; s < h->S; ++s)
+    if (p.from[s] >= 0 && p.from[s] != s)
+      FT_CUDA(h, cudaMemcpyAsync(h->slots + (size_t)s * h->slot_stride, h->slots + (size_t)p.from[s] * h->slot_stride,
+                                 h->blob_bytes, cudaMemcpyDeviceToDevice, h->copy_stream));
+  FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
+  FT_CUDA(h, cudaMemcpy(h->slot_key, p.slot_key.data(), sizeof(int32_t) * h->S, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(h->order[0], p.order.data(), sizeof(int32_t) * h->S, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(h->key_slot, p.key_slot.data(), sizeof(int32_t) * p.key_slot.size(), cudaMemcpyHostToDevice));
+  h->order_cur = 0;
   h->mode = mode;
-  return reset_tables(h, true);
+  h->bank_layer[0] = h->bank_layer[1] = -1;
+  if (mode == MODE_STREAM) h->stream_key_slot = p.key_slot;
+  else h->stream_key_slot.clear();
+  return FT_OK;
 }
 
 // Changes the slot count ("Why a Huge MoE Model Fits on One Consumer GPU":
@@ -580,40 +693,9 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
     return fail(h, FT_ERR_CACHE_TOO_SMALL, "STREAM mode needs n_slots >= 2*E (two staging layers)");
   FT_CUDA(h, cudaSetDevice(h->device));
   if (int rc = sync_handle(h)) return rc;
-  const int S = h->S;
-  const size_t nkeys = (size_t)h->L * h->E;
-  std::vector<int32_t> slot_key(S), key_slot(nkeys), order(S);
-  FT_CUDA(h, cudaMemcpy(slot_key.data(), h->slot_key, sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
-  FT_CUDA(h, cudaMemcpy(key_slot.data(), h->key_slot, sizeof(int32_t) * nkeys, cudaMemcpyDeviceToHost));
-  FT_CUDA(h, cudaMemcpy(order.data(), h->order[h->order_cur], sizeof(int32_t) * S, cudaMemcpyDeviceToHost));
-  // cached keys, least recent first (free slots sit at the front of the list)
-  std::vector<int32_t> recency;
-  if (h->mode == MODE_LRU)
-    for (int s : order)
-      if (slot_key[s] >= 0) recency.push_back(slot_key[s]);
-  const size_t n_keep = std::min<size_t>(recency.size(), (size_t)n_slots);
-  const std::vector<int32_t> keep(recency.end() - n_keep, recency.end());
-  std::vector<int32_t> nslot_key(n_slots, -1), nkey_slot(nkeys, -1), from(n_slots, -1);
-  for (int32_t key : keep) {
-    const int s = key_slot[key];
-    if (s < n_slots) {
-      nslot_key[s] = key;
-      nkey_slot[key] = s;
-      from[s] = s;
-    }
-  }
-  int next_free = 0;
-  for (int32_t key : keep) {
-    if (nkey_slot[key] >= 0) continue;
-    while (nslot_key[next_free] >= 0) ++next_free;
-    nslot_key[next_free] = key;
-    nkey_slot[key] = next_free;
-    from[next_free] = key_slot[key];
-  }
-  std::vector<int32_t> norder;
-  for (int s = 0; s < n_slots; ++s)
-    if (nslot_key[s] < 0) norder.push_back(s);
-  for (int32_t key : keep) norder.push_back(nkey_slot[key]);
+  std::vector<int32_t> key_slot, recency;
+  if (int rc = read_cache(h, key_slot, recency)) return rc;
+  const CachePlan p = plan_cache(key_slot, recency, cache_slots(h, h->mode, n_slots), n_slots);
   // the new bank, the kept blobs copied into it, then the tables
   uint8_t *bank = nullptr;
   int32_t *dslot_key = nullptr, *dorder0 = nullptr, *dorder1 = nullptr;
@@ -628,13 +710,13 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
     return fail(h, FT_ERR_OOM, "device allocation for the resized cache failed");
   }
   for (int s = 0; s < n_slots; ++s)
-    if (from[s] >= 0)
-      FT_CUDA(h, cudaMemcpyAsync(bank + (size_t)s * h->slot_stride, h->slots + (size_t)from[s] * h->slot_stride,
+    if (p.from[s] >= 0)
+      FT_CUDA(h, cudaMemcpyAsync(bank + (size_t)s * h->slot_stride, h->slots + (size_t)p.from[s] * h->slot_stride,
                                  h->blob_bytes, cudaMemcpyDeviceToDevice, h->copy_stream));
   FT_CUDA(h, cudaStreamSynchronize(h->copy_stream));
-  FT_CUDA(h, cudaMemcpy(dslot_key, nslot_key.data(), sizeof(int32_t) * n_slots, cudaMemcpyHostToDevice));
-  FT_CUDA(h, cudaMemcpy(dorder0, norder.data(), sizeof(int32_t) * n_slots, cudaMemcpyHostToDevice));
-  FT_CUDA(h, cudaMemcpy(h->key_slot, nkey_slot.data(), sizeof(int32_t) * nkeys, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(dslot_key, p.slot_key.data(), sizeof(int32_t) * n_slots, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(dorder0, p.order.data(), sizeof(int32_t) * n_slots, cudaMemcpyHostToDevice));
+  FT_CUDA(h, cudaMemcpy(h->key_slot, p.key_slot.data(), sizeof(int32_t) * p.key_slot.size(), cudaMemcpyHostToDevice));
   cudaFree(h->slots);
   cudaFree(h->slot_key);
   cudaFree(h->order[0]);
@@ -646,12 +728,24 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
   h->order_cur = 0;
   h->S = n_slots;
   h->bank_layer[0] = h->bank_layer[1] = -1;
+  if (h->mode == MODE_STREAM) h->stream_key_slot = p.key_slot;
   const size_t TK = (size_t)h->Tmax * h->k;
   h->tmaps_ok = h->fmt != FMT_FP8 &&
                 make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
                 make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
                 make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
   return FT_OK;
+}
+
+int ft_moe_set_prefill_hit_d2d(ft_moe *h, int on) {
+  if (!h || (on != 0 && on != 1)) return fail(h, FT_ERR_ARG, "NULL handle or on not 0/1");
+  h->hit_d2d = on != 0;
+  return FT_OK;
+}
+
+int ft_moe_prefill_hit_d2d(ft_moe *h) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  return h->hit_d2d ? 1 : 0;
 }
 
 int ft_cache_reset(ft_moe *h, int warm) {
@@ -665,7 +759,7 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   if (!h->pool_loaded) return fail(h, FT_ERR_STATE, "no expert pool loaded");
   if (layer < 0 || layer >= h->L) return fail(h, FT_ERR_ARG, "layer out of range");
   if (n_tokens < 0 || n_tokens > h->Tmax) return fail(h, FT_ERR_ARG, "n_tokens out of range");
-  h->last_streamed = h->last_stream_bytes = 0;
+  h->last_streamed = h->last_stream_bytes = h->last_d2d = 0;
   h->last_T = n_tokens;
   if (n_tokens == 0) return FT_OK;
   if (!x || !router_logits || !out) return fail(h, FT_ERR_ARG, "NULL x, router_logits or out");
@@ -699,7 +793,8 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   ++h->seq;
   RouteArgs ra{};
   ra.logits = router_logits;
-  ra.T = n_tokens; ra.E = h->E; ra.k = h->k; ra.layer = layer; ra.mode = h->mode; ra.bank = bank; ra.S = h->S;
+  ra.T = n_tokens; ra.E = h->E; ra.k = h->k; ra.layer = layer; ra.mode = h->mode; ra.S = h->S;
+  ra.bank_slot0 = h->mode == MODE_STREAM ? (int)bank_slot0(h, bank) : 0;
   ra.blob_bytes = h->blob_bytes;
   ra.plan = h->plan;
   ra.cache.key_slot = h->key_slot;
@@ -935,6 +1030,7 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   else FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
   h->host_streamed += h->last_streamed;
   h->host_bytes += h->last_stream_bytes;
+  h->host_d2d += h->last_d2d;
   return FT_OK;
 }
 
@@ -972,10 +1068,10 @@ int ft_cache_stats(ft_moe *h, ft_stats *cum, ft_stats *last) {
   if (int rc = sync_handle(h)) return rc;
   unsigned long long d[16];
   FT_CUDA(h, cudaMemcpy(d, h->stats_dev, sizeof d, cudaMemcpyDeviceToHost));
-  if (cum) *cum = ft_stats{d[0], d[1], d[2], d[3], h->host_warm, h->host_streamed, d[4] + h->host_bytes};
+  if (cum) *cum = ft_stats{d[0], d[1], d[2], d[3], h->host_warm, h->host_streamed, d[4] + h->host_bytes, h->host_d2d};
   if (last) {
-    if (h->last_T == 0) *last = ft_stats{0, 0, 0, 0, 0, 0, 0};
-    else *last = ft_stats{d[8], d[9], d[10], d[11], 0, h->last_streamed, d[12] + h->last_stream_bytes};
+    if (h->last_T == 0) *last = ft_stats{0, 0, 0, 0, 0, 0, 0, 0};
+    else *last = ft_stats{d[8], d[9], d[10], d[11], 0, h->last_streamed, d[12] + h->last_stream_bytes, h->last_d2d};
   }
   return FT_OK;
 }

@@ -237,7 +237,7 @@ __device__ void block_plan(const RouteArgs &a, const PlanSmem &sm, const Prefetc
       slot = sm.s_keyslot ? sm.s_keyslot[e] : a.cache.key_slot[key];
       hit = slot >= 0;
     } else {
-      slot = a.bank * E + e;
+      slot = a.bank_slot0 + e;
       hit = 1;
     }
   }
@@ -489,7 +489,7 @@ __device__ __forceinline__ void route_decode_body(const RouteArgs &a, int *smem,
         slot = s_keyslot[eu];
         hit = slot >= 0;
       } else {
-        slot = a.bank * E + eu;
+        slot = a.bank_slot0 + eu;
         hit = 1;
       }
     }

@@ -82,12 +82,14 @@ enum ft_status {
 };
 
 /* Cache counters.  A lookup is one distinct (layer, expert) of a forward call;
- * hits + misses = lookups.  evictions counts misses that displaced a resident
- * expert.  warm_loads counts experts copied by load_pool/reset.  streamed
- * counts experts copied by STREAM-mode layer staging.  bytes_h2d counts all
+ * in LRU mode hits + misses = lookups (STREAM-mode lookups are neither).
+ * evictions counts misses that displaced a resident expert.  warm_loads counts
+ * experts copied by load_pool/reset.  streamed counts experts that STREAM-mode
+ * layer staging copied from host memory, hit_d2d those it copied from a cache
+ * slot on the device (ft_moe_set_prefill_hit_d2d).  bytes_h2d counts all
  * expert bytes copied host->device. */
 typedef struct {
-  uint64_t lookups, hits, misses, evictions, warm_loads, streamed, bytes_h2d;
+  uint64_t lookups, hits, misses, evictions, warm_loads, streamed, bytes_h2d, hit_d2d;
 } ft_stats;
 
 /* Packed bytes of one expert blob in weight_fmt (layouts above), or -1 for a
@@ -119,11 +121,32 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
  * Env FT_FAULT=pin returns FT_ERR_NOT_PINNED before touching the device. */
 int ft_moe_load_pool(ft_moe *h, const void *const *host_experts);
 
-/* Selects FT_MODE_LRU or FT_MODE_STREAM and resets the cache to that mode's
- * initial state (LRU: warm fill; STREAM: both banks empty).  STREAM needs
- * S >= 2*E, room for the two staging layers ("Long Prompts Are the
- * Bottleneck"); FT_ERR_CACHE_TOO_SMALL otherwise.  Synchronous. */
+/* Selects FT_MODE_LRU or FT_MODE_STREAM.  STREAM needs S >= 2*E, room for
+ * the two staging layers ("Long Prompts Are the Bottleneck"); the banks are
+ * the last 2E slots (bank b = slots S-2E+b*E ..), and the first S-2E slots
+ * stay the LRU cache's.  FT_ERR_CACHE_TOO_SMALL otherwise.
+ * With prefill hit-D2D off (the default) the call resets the cache and the
+ * counters to the mode's initial state (LRU: warm fill; STREAM: an empty
+ * cache and both banks empty).  With it on, the cache survives the switch
+ * and the counters carry on: entering STREAM mode the cache keeps its most
+ * recent S-2E experts, a kept expert at slot >= S-2E moving to the lowest
+ * free slot below (least recent first, copied on the device); leaving it, the
+ * cache grows back to S slots, its experts where they are and the bank slots
+ * free; selecting the current mode again changes nothing.  Synchronous. */
 int ft_moe_set_mode(ft_moe *h, int mode);
+
+/* Prefill hit-D2D ("Long Prompts Are the Bottleneck": prefill can skip the
+ * experts already in the GPU cache, so that only the others cross PCIe).  on
+ * = 1: STREAM-mode staging copies each expert that the cache holds from its
+ * slot on the device (counted in hit_d2d, not streamed or bytes_h2d), and
+ * ft_moe_set_mode keeps the cache across switches (above).  STREAM mode
+ * reads the cache but changes neither its experts nor their recency.  on = 0
+ * (default): every staged expert comes from host memory.  Takes effect at the
+ * next staging or switch.  Errors: FT_ERR_ARG (NULL, on not 0/1). */
+int ft_moe_set_prefill_hit_d2d(ft_moe *h, int on);
+
+/* 1 if prefill hit-D2D is on, 0 if off, FT_ERR_ARG for NULL. */
+int ft_moe_prefill_hit_d2d(ft_moe *h);
 
 /* One MoE layer forward for n_tokens tokens (0 <= n_tokens <= max_tokens):
  *   x             device bf16 [n_tokens][H]
@@ -149,7 +172,8 @@ int ft_moe_set_mode(ft_moe *h, int mode);
  * wait for the whole device.
  * STREAM mode: bank (layer mod 2) receives all E experts of `layer` before
  * its FFN.  The copy of the next layer starts in this call and overlaps this
- * layer's compute.
+ * layer's compute.  With prefill hit-D2D on, the experts that the cache holds
+ * are copied from their slots, the others from host memory.
  * Work is ordered after earlier work on `stream`.  out is ready when `stream`
  * reaches the end of this call's work.  Errors: FT_ERR_ARG, FT_ERR_STATE (no
  * pool loaded), FT_ERR_TIMEOUT, FT_ERR_CUDA.  After FT_ERR_TIMEOUT or
@@ -170,7 +194,8 @@ int ft_cache_stats(ft_moe *h, ft_stats *cumulative, ft_stats *last_call);
  * kept expert keeps its slot if that slot still exists, else it moves to the
  * lowest free slot (least recent first); new slots start free.  The experts
  * that leave are not counted as evictions of a call; the counters are kept.
- * STREAM mode: the staging banks start empty.  The slot bank is reallocated
+ * STREAM mode: the cache (the slots below the banks) follows the same rules
+ * onto its new share, n_slots - 2E, and the banks start empty.  The slot bank is reallocated
  * at the new size (old and new coexist during the call) and the kept experts
  * are copied on the device.  CUDA graphs captured from this handle before the
  * call hold the old bank's address and must not be launched after it

@@ -28,9 +28,11 @@ class Pool:
         return self.arr[key % self.n_phys]
 
 
-def make_pair(H, E, k, I, fmt, S, L, Tmax, seed, n_phys=None, mode="lru", warm=True, flags=0, keep=True):
+def make_pair(H, E, k, I, fmt, S, L, Tmax, seed, n_phys=None, mode="lru", warm=True, flags=0, keep=True,
+              hit_d2d=False):
     """(GPU stack, oracle, pool) over the same pinned pool.  keep: tensor-core
-    calls also store y, so that the tests can check the GEMM accumulation."""
+    calls also store y, so that the tests can check the GEMM accumulation.
+    hit_d2d: prefill hit-D2D on both sides (before the switch to `mode`)."""
     import expert_cache_host_softmax_b300 as F
     pool = Pool(fmt, H, I, L * E, seed, n_phys, flags)
     gpu = F.MoELayerStack(H, E, k, I, fmt, S, L, Tmax)
@@ -38,9 +40,12 @@ def make_pair(H, E, k, I, fmt, S, L, Tmax, seed, n_phys=None, mode="lru", warm=T
     if keep:
         gpu.set_keep_activations(True)
     f = ftgen.FMT_NAMES[fmt]
-    orc = O.MoELayerOracle(H, E, k, I, f, S, L, pool.blob, mode=O.MODE_STREAM if mode == "stream" else O.MODE_LRU)
+    orc = O.MoELayerOracle(H, E, k, I, f, S, L, pool.blob, hit_d2d=hit_d2d)
+    if hit_d2d:
+        gpu.set_prefill_hit_d2d(True)
     if mode == "stream":
         gpu.set_mode(F.FT_MODE_STREAM)
+        orc.set_mode(O.MODE_STREAM)
     if not warm:
         gpu.reset(warm=False)
         orc.reset(warm=False)

@@ -77,7 +77,7 @@ def _check_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=False, fmt=None,
     assert np.array_equal(r["inv"], ref["inv"])
     assert gpu.trace() == [tuple(p) for p in ref["plan"]]
     _, last = gpu.stats()
-    for key_ in ("lookups", "hits", "misses", "evictions", "streamed", "bytes_h2d"):
+    for key_ in ("lookups", "hits", "misses", "evictions", "streamed", "bytes_h2d", "hit_d2d"):
         assert last[key_] == ref["last"][key_], key_
     got = Hn.out_to_f64(out)[ref["out_tokens"]]
     err = Hn.rel_err(got, ref["out"])
@@ -131,12 +131,18 @@ def _golden_traces():
 def test_hand_worked_lru_traces_on_gpu(trace):
     H = I = 256
     E, L, S = trace["E"], trace["L"], trace["S"]
-    gpu, _, _ = Hn.make_pair(H, E, 1, I, "bf16", S, L, 2, 5, warm=trace["warm"])
+    gpu, _, _ = Hn.make_pair(H, E, 1, I, "bf16", S, L, 2, 5, warm=trace["warm"], hit_d2d=trace["d2d"])
     look = hits = misses = ev = 0
     for layer, experts, want in trace["calls"]:
         if layer == "resize":
             gpu.resize_slots(experts)            # the following calls show its effect
             continue
+        if layer == "mode":
+            gpu.set_mode(F.FT_MODE_STREAM if experts == "stream" else F.FT_MODE_LRU)
+            continue
+        prefill = layer == "prefill"
+        if prefill:
+            layer, experts = experts
         T = len(experts)
         lg = np.full((T, E), -5.0, np.float32)
         for t, e in enumerate(experts):
@@ -144,10 +150,17 @@ def test_hand_worked_lru_traces_on_gpu(trace):
         x = ftgen.x_bf16(5, T, H, 0, layer)
         xd, lgd = Hn.to_dev(x, lg)
         gpu.forward(layer, xd, lgd)
-        assert gpu.trace() == want
         _, last = gpu.stats()
+        if prefill:
+            assert (last["hit_d2d"], last["streamed"]) == want
+            assert [p[1] for p in gpu.trace()] == [S - 2 * E + (layer % 2) * E + e for e in experts]
+        else:
+            assert gpu.trace() == want
         look += last["lookups"]; hits += last["hits"]; misses += last["misses"]; ev += last["evictions"]
     assert (look, hits, misses, ev) == trace["stats"]
+    if trace["copies"] is not None:
+        cum, _ = gpu.stats()
+        assert (cum["hit_d2d"], cum["streamed"]) == trace["copies"]
     gpu.close()
 
 
@@ -160,6 +173,45 @@ def test_stream_mode_matches_oracle():
             _check_call(gpu, orc, layer, x, lg)
     cum, _ = gpu.stats()
     assert cum["streamed"] == orc.stats["streamed"] == E * (2 * L + 1)
+    gpu.close()
+
+
+@pytest.mark.parametrize("fmt,T,ffn", [("nvfp4", 40, "gemv"), ("mxfp4", 300, "tc"), ("bf16", 300, "tc")])
+def test_prefill_hit_d2d_matches_oracle(fmt, T, ffn):
+    # decode calls fill the cache; prefill stages the cached experts from their
+    # slots and the rest from host memory; decode resumes on the kept cache
+    H, I, E, k, L = 256, 512, 8, 2, 4
+    S = 2 * E + 12                                   # 12 cache slots in STREAM mode, of 32 keys
+    seed = 131 + T
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed, hit_d2d=True)
+    for step in range(6):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, 2, H, E, step, layer, zipf=0.9)
+            _check_call(gpu, orc, layer, x, lg)
+    gpu.set_mode(F.FT_MODE_STREAM)
+    orc.set_mode(O.MODE_STREAM)
+    gpu.set_ffn_kernel(ffn)
+    for step in range(2):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, T, H, E, 10 + step, layer)
+            _check_call(gpu, orc, layer, x, lg, gemm_check=(ffn == "tc" and step == 0))
+    # a resize in STREAM mode: the cache follows onto its new share, banks restage
+    gpu.resize_slots(S - 4)
+    orc.resize_slots(S - 4)
+    for layer in (3, 0):
+        x, lg = Hn.inputs(seed, T, H, E, 20, layer)
+        _check_call(gpu, orc, layer, x, lg)
+    gpu.set_mode(F.FT_MODE_LRU)
+    orc.set_mode(O.MODE_LRU)
+    gpu.set_ffn_kernel("auto")
+    for step in range(4):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, 2, H, E, 30 + step, layer, zipf=0.9)
+            _check_call(gpu, orc, layer, x, lg)
+    cum, _ = gpu.stats()
+    for key_ in ("lookups", "hits", "misses", "evictions", "warm_loads", "streamed", "bytes_h2d", "hit_d2d"):
+        assert cum[key_] == orc.stats[key_], key_
+    assert cum["hit_d2d"] > 0 and cum["streamed"] > 0
     gpu.close()
 
 
