@@ -21,9 +21,12 @@
 //
 // STREAM mode ("Long Prompts Are the Bottleneck": each MoE layer copies all of
 // its experts for a prefill chunk, and the copy of layer N+1 overlaps the
-// compute of layer N): bank (layer mod 2) holds the layer's E experts.
+// compute of layer N): bank (layer mod 2) holds the layer's E experts; the
+// two banks are the last 2E slots, the slots below them keep the LRU cache.
 // Each call also issues the next layer's copies into the other bank, after
-// the FFN that last read that bank.
+// the FFN that last read that bank.  With prefill hit-D2D (same section:
+// experts already in the GPU cache need not cross PCIe) the cached experts
+// are copied slot -> bank on the device and mode switches keep the cache.
 #include <algorithm>
 #include <atomic>
 #include <chrono>
