@@ -86,6 +86,10 @@ def test_null_handle_and_stateless_validation(F):
     assert L.ft_cache_stats(None, None, None) == F.FT_ERR_ARG
     assert L.ft_cache_reset(None, 1) == F.FT_ERR_ARG
     assert L.ft_moe_set_mode(None, 0) == F.FT_ERR_ARG
+    assert L.ft_moe_resize_slots(None, 8) == F.FT_ERR_ARG
+    assert L.ft_moe_set_prefill_hit_d2d(None, 1) == F.FT_ERR_ARG
+    assert L.ft_moe_prefill_hit_d2d(None) == F.FT_ERR_ARG
+    assert L.ft_moe_set_keep_activations(None, 1) == F.FT_ERR_ARG
     assert L.ft_moe_destroy(None) == F.FT_OK
     assert L.ft_moe_slot_stride(None) == -1
     assert L.ft_topk_softmax(None, 4, 600, 2, None, None, None) == F.FT_ERR_ARG
