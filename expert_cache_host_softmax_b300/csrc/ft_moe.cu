@@ -606,7 +606,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
   ffn_init_attributes();
   gemm_init_attributes();
   // the tensor-core FFN takes BF16, NVFP4 and MXFP4 (FP8 experts run on the GEMV)
-  h->tmaps_ok = h->fmt != FMT_FP8 &&
+  h->tmaps_ok =
                 make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
                 make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
                 make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
@@ -733,7 +733,7 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
   h->bank_layer[0] = h->bank_layer[1] = -1;
   if (h->mode == MODE_STREAM) h->stream_key_slot = p.key_slot;
   const size_t TK = (size_t)h->Tmax * h->k;
-  h->tmaps_ok = h->fmt != FMT_FP8 &&
+  h->tmaps_ok =
                 make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
                 make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
                 make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
@@ -1122,8 +1122,6 @@ int ft_moe_last_activations(ft_moe *h, uint16_t *h_act, float *y) {
 
 int ft_moe_set_ffn_kernel(ft_moe *h, int which) {
   if (!h || which < FT_FFN_AUTO || which > FT_FFN_TC) return fail(h, FT_ERR_ARG, "bad FFN kernel choice");
-  if (which == FT_FFN_TC && h->fmt == FMT_FP8)
-    return fail(h, FT_ERR_ARG, "the tensor-core FFN takes BF16, NVFP4 and MXFP4 experts; FP8 runs on the GEMV");
   if (which == FT_FFN_TC && !h->tmaps_ok)
     return fail(h, FT_ERR_CUDA, "tensor-core FFN unavailable: the TMA descriptors could not be encoded");
   h->ffn_kernel = which;

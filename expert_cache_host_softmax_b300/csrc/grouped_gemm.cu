@@ -19,10 +19,11 @@
 // K advances in blocks of 64 through a ring of shared-memory stages:
 //   - one producer thread issues, per stage, the TMA load of the A box (128
 //     token rows x 64, 128-byte swizzle) and of the weights: BF16 weights land
-//     directly in the swizzled layout; NVFP4 / MXFP4 codes land raw in a
+//     directly in the swizzled layout; NVFP4 / MXFP4 / FP8 codes land raw in a
 //     separate ring, and eight converter warps dequantise them to bf16
-//     (e2m1 x block scale, exact in bf16) into the swizzled B tile.  The NVFP4
-//     per-matrix global scale is applied to the fp32 accumulator in the epilogue.
+//     (e2m1 x block scale, or the bare E4M3 value: exact in bf16) into the
+//     swizzled B tile.  The NVFP4 per-matrix global scale and the FP8 per-row
+//     scales are applied to the fp32 accumulator in the epilogue.
 //   - one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> f32)
 //     into one of two TMEM accumulators (2 x 256 columns), so the epilogue of
 //     a tile overlaps the MMAs of the next;
@@ -49,27 +50,31 @@ constexpr int BK = 64;           // K per stage: 128 bytes of bf16 (one swizzle 
 constexpr int kEpiWarps = 4;
 constexpr int A_STAGE = BM * BK * 2;          // 16 KB
 constexpr int B_STAGE = BN * BK * 2;          // 32 KB
-constexpr int RAW_STAGE = BN * BK / 2;        // 8 KB of e2m1 codes
 constexpr uint32_t kTmemCols = 512;           // two accumulators of BN fp32 columns
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxU = kMaxExperts;
 
 template <int FMT>
 struct Cfg {
-  static constexpr bool kFp4 = FMT != FMT_BF16;
-  // stages of A + (bf16) B; FP4 also has a ring of raw-code stages
-  static constexpr int kNS = kFp4 ? 3 : 4;
-  static constexpr int kNR = kFp4 ? 4 : 0;
-  // warp roles: 0 producer, 1 MMA, 2-3 idle, 4-7 epilogue, 8-15 converters (FP4)
+  // BF16 weights land in the B tile as they are; the other formats' codes
+  // land raw and are converted
+  static constexpr bool kConv = FMT != FMT_BF16;
+  // code bytes per stage: 64 K of each of the 256 B rows (FP4: 32 bytes a row, FP8: 64)
+  static constexpr int kRawRow = FMT == FMT_FP8 ? BK : BK / 2;
+  static constexpr int kRawStage = BN * kRawRow;
+  // stages of A + (bf16) B; the converted formats also have a ring of raw-code stages
+  static constexpr int kNS = kConv ? 3 : 4;
+  static constexpr int kNR = kConv ? 4 : 0;
+  // warp roles: 0 producer, 1 MMA, 2-3 idle, 4-7 epilogue, 8-15 converters
   static constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 4, kConvWarp0 = 8;
-  static constexpr int kConvThreads = kFp4 ? 256 : 0;
-  static constexpr int kThreads = kFp4 ? 512 : 256;
-  // FULL arrivals per stage: the producer's expect_tx, plus (FP4) one per converter thread
+  static constexpr int kConvThreads = kConv ? 256 : 0;
+  static constexpr int kThreads = kConv ? 512 : 256;
+  // FULL arrivals per stage: the producer's expect_tx, plus one per converter thread
   static constexpr int kFullCount = 1 + kConvThreads;
   // shared memory: [A x kNS][B x kNS][RAW x kNR] then barriers and tables
   static constexpr int kOffB = kNS * A_STAGE;
   static constexpr int kOffRaw = kOffB + kNS * B_STAGE;
-  static constexpr int kOffBar = kOffRaw + kNR * RAW_STAGE;
+  static constexpr int kOffBar = kOffRaw + kNR * kRawStage;
   // barriers: FULL, EMPTY (kNS each), RAWFULL, RAWEMPTY (kNR each), TFULL x2, TEMPTY x2, DRAIN
   static constexpr int kBars = 2 * kNS + 2 * kNR + 5;
   static constexpr int kOffTab = kOffBar + kBars * 8 + 16;
@@ -269,6 +274,24 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, float s) {
   return o;
 }
 
+// Eight E4M3 codes (two 32-bit words, byte j = element j) -> eight bf16
+// values (exact: E4M3 has 3 mantissa bits and an exponent range within bf16's).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(out)
+      : "r"(two_bytes));
+  const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&out));
+  return pack_bf16x2(f.x, f.y);
+}
+
+__device__ __forceinline__ uint4 dequant8_e4m3(uint32_t lo, uint32_t hi) {
+  return make_uint4(e4m3x2_to_bf16x2(lo & 0xFFFFu), e4m3x2_to_bf16x2(lo >> 16), e4m3x2_to_bf16x2(hi & 0xFFFFu),
+                    e4m3x2_to_bf16x2(hi >> 16));
+}
+
 // ------------------------------------------------------------------ tiles
 
 struct TileInfo {
@@ -276,6 +299,19 @@ struct TileInfo {
   int row0, rows;   // first permuted row of the tile, valid rows (<= BM)
   int slot;
 };
+
+// v[i] *= scale[i] for 16 consecutive weight rows (FP8 row scales; the same
+// 64 bytes for every thread of the warp).
+__device__ __forceinline__ void row_scale16(const float *scale, float *v) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 s4 = __ldg(reinterpret_cast<const float4 *>(scale) + i);
+    v[4 * i] *= s4.x;
+    v[4 * i + 1] *= s4.y;
+    v[4 * i + 2] *= s4.z;
+    v[4 * i + 3] *= s4.w;
+  }
+}
 
 // Tile t -> (u, n, m): experts in order, then N tiles, then M tiles (M fastest,
 // so the CTAs that share a weight tile run side by side).
@@ -397,9 +433,9 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         for (int kb = 0; kb < nk; ++kb, ++j) {
           const int s = j % NS;
           if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 10)) { ok = false; break; }
-          mbar_arrive_expect_tx(FULL(s), A_STAGE + (C::kFp4 ? 0 : B_STAGE));
+          mbar_arrive_expect_tx(FULL(s), A_STAGE + (C::kConv ? 0 : B_STAGE));
           tma_load_2d(sA + s * A_STAGE, &tmA, FULL(s), kb * BK, ti.row0);
-          if constexpr (!C::kFp4) {
+          if constexpr (!C::kConv) {
             const uint32_t dst = sB + s * B_STAGE;
             tma_load_3d(dst, &tmB, FULL(s), kb * BK, r0, ti.slot);
             tma_load_3d(dst + B_STAGE / 2, &tmB, FULL(s), kb * BK, r1, ti.slot);
@@ -407,10 +443,10 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
             const int rs = j % NR;
             if (!mbar_wait(RAWEMPTY(rs), ((j / NR) & 1) ^ 1, s_abort, a.err, 11)) { ok = false; ++j; break; }
             fence_proxy_async();   // the converters' reads of this slot precede the TMA's writes
-            mbar_arrive_expect_tx(RAWFULL(rs), RAW_STAGE);
-            const uint32_t dst = sRaw + rs * RAW_STAGE;
-            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * (BK / 2), r0, ti.slot);
-            tma_load_3d(dst + RAW_STAGE / 2, &tmB, RAWFULL(rs), kb * (BK / 2), r1, ti.slot);
+            mbar_arrive_expect_tx(RAWFULL(rs), C::kRawStage);
+            const uint32_t dst = sRaw + rs * C::kRawStage;
+            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * C::kRawRow, r0, ti.slot);
+            tma_load_3d(dst + C::kRawStage / 2, &tmB, RAWFULL(rs), kb * C::kRawRow, r1, ti.slot);
           }
         }
       }
@@ -420,7 +456,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         while (!mbar_try_wait(FULL(jj % NS), (jj / NS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
         }
       }
-      if constexpr (C::kFp4) {
+      if constexpr (C::kConv) {
         for (int jj = max(0, j - NR); jj < j; ++jj) {
           const unsigned long long t0 = globaltimer();
           while (!mbar_try_wait(RAWFULL(jj % NR), (jj / NR) & 1) && globaltimer() - t0 < kWaitLimitNs) {
@@ -429,7 +465,49 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (C::kFp4 && warp >= C::kConvWarp0) {
+  } else if (FMT == FMT_FP8 && warp >= C::kConvWarp0) {
+    // ================================================================ FP8 converters
+    // Each thread expands one B row per stage, 64 E4M3 codes, into the
+    // swizzled bf16 tile (chunk c of row t at c ^ (t & 7)); the row scales
+    // wait for the epilogue.  Thread t reads its four 16-byte code groups in
+    // the order g = sigma(a) ^ i (a = (t >> 1) & 3, sigma = 0 2 3 1): within
+    // each 8 lanes both the loads (rows 64 bytes apart) and the swizzled
+    // stores then touch 8 distinct 16-byte bank groups.
+    const int t = tid - C::kConvWarp0 * 32;
+    const uint32_t sig = (0x1320u >> (4 * ((t >> 1) & 3))) & 3u;
+    int j = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < nk; ++kb, ++j) {
+        const int s = j % NS;
+        if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 12)) { ok = false; break; }
+        const int rs = j % NR;
+        if (!mbar_wait(RAWFULL(rs), (j / NR) & 1, s_abort, a.err, 13)) { ok = false; break; }
+        const uint32_t raw = sRaw + rs * C::kRawStage + t * C::kRawRow;
+        const uint32_t bdst = sB + s * B_STAGE + t * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t g = sig ^ (uint32_t)i;
+          uint4 q;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                       : "r"(raw + g * 16)
+                       : "memory");
+          const uint4 v0 = dequant8_e4m3(q.x, q.y), v1 = dequant8_e4m3(q.z, q.w);
+          const uint32_t d0 = bdst + (((2 * g) ^ (t & 7)) << 4), d1 = bdst + (((2 * g + 1) ^ (t & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d0), "r"(v0.x), "r"(v0.y), "r"(v0.z),
+                       "r"(v0.w)
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d1), "r"(v1.x), "r"(v1.y), "r"(v1.z),
+                       "r"(v1.w)
+                       : "memory");
+        }
+        mbar_arrive(RAWEMPTY(rs));
+        fence_proxy_async();   // this thread's B row is visible to the tensor core's reads
+        mbar_arrive(FULL(s));
+      }
+    }
+  } else if (C::kConv && warp >= C::kConvWarp0) {
     // ================================================================ FP4 converters
     // Each thread dequantises one B row per stage from the raw codes into the
     // swizzled bf16 tile (chunk c of row t at c ^ (t & 7)).
@@ -479,7 +557,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         if (!mbar_wait(RAWFULL(rs), (j / NR) & 1, s_abort, a.err, 13)) { ok = false; break; }
         // rows are 32 bytes apart: lanes 4-7 of every 8 read their second half
         // first, so that each load instruction touches all 32 banks
-        const uint32_t raw = sRaw + rs * RAW_STAGE + t * 32;
+        const uint32_t raw = sRaw + rs * C::kRawStage + t * 32;
         const uint32_t hsw = ((t >> 2) & 1) * 16;
         uint4 qa, qb;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -557,6 +635,16 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         g0 = DOWN ? gs[2] : gs[0];
         g1 = gs[1];
       }
+      // FP8: the fp32 scales of the tile's weight rows (gate/up: the 128 gate
+      // rows and the 128 matching up rows; down: 256 rows of H)
+      const float *rs0 = nullptr, *rs1 = nullptr;
+      if constexpr (FMT == FMT_FP8) {
+        const BlobLayout L = blob_layout(FMT_FP8, a.H, a.I);
+        const float *sf = reinterpret_cast<const float *>(a.slot_bank + (size_t)ti.slot * a.slot_stride +
+                                                         (DOWN ? L.d_sf : L.gu_sf));
+        rs0 = DOWN ? sf + ti.n * BN : sf + ti.n * (BN / 2);
+        rs1 = DOWN ? nullptr : sf + a.I + ti.n * (BN / 2);
+      }
       const bool valid = row < ti.rows;
       if constexpr (!DOWN) {
         __nv_bfloat16 *dst = a.h + (size_t)(ti.row0 + row) * a.I + ti.n * (BN / 2);
@@ -565,6 +653,10 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
           float gv[16], uv[16];
           tmem_ld16(tb + c, gv);
           tmem_ld16(tb + BN / 2 + c, uv);
+          if constexpr (FMT == FMT_FP8) {
+            row_scale16(rs0 + c, gv);
+            row_scale16(rs1 + c, uv);
+          }
           if (valid) {
             uint32_t pk[8];
 #pragma unroll
@@ -598,6 +690,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         for (int c = 0; c < BN; c += 16) {
           float v[16];
           tmem_ld16(tb + c, v);
+          if constexpr (FMT == FMT_FP8) row_scale16(rs0 + c, v);
           if (valid) {
             if (store_y) {
               float4 *o = reinterpret_cast<float4 *>(dst + c);
@@ -673,6 +766,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *_
 
 static_assert(Cfg<FMT_BF16>::kSmemAlloc <= 227 * 1024, "bf16 smem");
 static_assert(Cfg<FMT_NVFP4>::kSmemAlloc <= 227 * 1024, "fp4 smem");
+static_assert(Cfg<FMT_FP8>::kSmemAlloc <= 227 * 1024, "fp8 smem");
 static_assert(Cfg<FMT_NVFP4>::kThreads == 512 && Cfg<FMT_BF16>::kThreads == 256, "warp roles");
 
 int tc_num_sms() {
@@ -693,6 +787,8 @@ void gemm_init_attributes() {
   set_attr<FMT_NVFP4, true>();
   set_attr<FMT_MXFP4, false>();
   set_attr<FMT_MXFP4, true>();
+  set_attr<FMT_FP8, false>();
+  set_attr<FMT_FP8, true>();
 }
 
 // Tensor map over a bf16 activation matrix [rows][K] (the permuted x rows,
@@ -710,6 +806,7 @@ int make_act_map(const void *base, int64_t rows, int K, void *map) {
 
 // Tensor maps over the slot bank: 3-D (K, rows, slot).  BF16: box 64 x 128
 // elements with the 128-byte swizzle.  FP4: raw code bytes, box 32 x 128.
+// FP8: raw code bytes, box 64 x 128.
 int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, int H, int I, void *map_gu,
                      void *map_d) {
   EncodeTiledFn enc = encode_fn();
@@ -729,6 +826,11 @@ int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, 
       dims[0] = K; strides[0] = K * 2;
       box[0] = BK;
       sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    } else if (fmt == FMT_FP8) {
+      dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+      dims[0] = K; strides[0] = K;
+      box[0] = BK;
+      sw = CU_TENSOR_MAP_SWIZZLE_NONE;
     } else {
       dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
       dims[0] = K / 2; strides[0] = K / 2;
@@ -781,7 +883,7 @@ cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const
     case FMT_BF16: return down ? launch<FMT_BF16, true>(a, mA, mB, grid, s) : launch<FMT_BF16, false>(a, mA, mB, grid, s);
     case FMT_NVFP4:
       return down ? launch<FMT_NVFP4, true>(a, mA, mB, grid, s) : launch<FMT_NVFP4, false>(a, mA, mB, grid, s);
-    case FMT_FP8: return cudaErrorInvalidValue;   // FP8 experts run on the GEMV
+    case FMT_FP8: return down ? launch<FMT_FP8, true>(a, mA, mB, grid, s) : launch<FMT_FP8, false>(a, mA, mB, grid, s);
     default: return down ? launch<FMT_MXFP4, true>(a, mA, mB, grid, s) : launch<FMT_MXFP4, false>(a, mA, mB, grid, s);
   }
 }

@@ -47,8 +47,7 @@
  * nibble.  An NVFP4 weight is e2m1(code) * e4m3(block scale) * global scale.
  * An MXFP4 weight is e2m1(code) * 2^(e8m0 - 127) (OCP Microscaling v1.0).
  * An FP8 weight is e4m3(code) (OCP "FN") * the fp32 scale of its row.  FP8
- * experts run on the GEMV kernel only (ft_moe_set_ffn_kernel(FT_FFN_TC) is
- * refused) and are not pulled (FT_MISS_PULL copies them instead).
+ * experts are not pulled (FT_MISS_PULL copies them instead).
  */
 #ifndef FT_MOE_H_
 #define FT_MOE_H_
