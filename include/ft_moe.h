@@ -131,7 +131,10 @@ int ft_moe_load_pool(ft_moe *h, const void *const *host_experts);
  * recent S-2E experts, a kept expert at slot >= S-2E moving to the lowest
  * free slot below (least recent first, copied on the device); leaving it, the
  * cache grows back to S slots, its experts where they are and the bank slots
- * free; selecting the current mode again changes nothing.  Synchronous. */
+ * free; selecting the current mode again changes nothing.  Synchronous.
+ * Errors: FT_ERR_ARG (NULL, bad mode), FT_ERR_CACHE_TOO_SMALL, FT_ERR_DEVICE
+ * (a kernel of an earlier call gave up a bounded wait), FT_ERR_CUDA; after
+ * FT_ERR_CUDA the cache state is undefined until ft_cache_reset. */
 int ft_moe_set_mode(ft_moe *h, int mode);
 
 /* Prefill hit-D2D ("Long Prompts Are the Bottleneck": prefill can skip the
