@@ -353,6 +353,38 @@ def test_prefill35b_full_size_sampled(fmt):
     gpu.close()
 
 
+def test_decode35b_full_size_in_bench_configuration():
+    # the decode workload at full size (48 layers, H 2048, 128 experts, top-8,
+    # I 768, NVFP4, 1024 slots, one token, Zipf(1.1) logits), launched as the
+    # bench times it (AUTO: misses copied inside the gate/up GEMV, combine fused
+    # into the down GEMV); the pool aliases 6144 keys onto 128 distinct blobs.
+    # Every call's routing and cache trace bit-exact; every 8th call's output
+    # against the oracle; the counters at the end.
+    c = CONFIGS["decode35b"]
+    T, H, E, k, I, L, S, seed = c["T"], c["H"], c["E"], c["k"], c["I"], c["L"], c["S"], c["seed"]
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, c["fmt"], S, L, T, seed, n_phys=128, keep=False)
+    assert gpu.miss_path() == "kernel"
+    n = 0
+    for step in range(2):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, T, H, E, step, layer, zipf=c["zipf"])
+            if n % 8 == 0:
+                _check_call(gpu, orc, layer, x, lg)
+            else:
+                xd, lgd = Hn.to_dev(x, lg)
+                gpu.forward(layer, xd, lgd)
+                ref = orc.forward(layer, x, lg, ffn_experts=[])   # routing and cache only
+                assert np.array_equal(gpu.last_routing()["idx"], ref["idx"])
+                assert gpu.trace() == [tuple(p) for p in ref["plan"]]
+            assert gpu.last_ffn_kernel == "gemv"
+            n += 1
+    cum, _ = gpu.stats()
+    for key_ in ("lookups", "hits", "misses", "evictions", "warm_loads", "bytes_h2d"):
+        assert cum[key_] == orc.stats[key_], key_
+    assert cum["misses"] > 0 and cum["evictions"] > 0
+    gpu.close()
+
+
 def test_auto_picks_gemv_for_decode():
     H, I, E, k = 256, 256, 16, 4
     gpu, _, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, 1, 64, 3)
