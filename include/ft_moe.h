@@ -206,8 +206,9 @@ int ft_cache_stats(ft_moe *h, ft_stats *cumulative, ft_stats *last_call);
  * FT_ERR_OOM (the handle is unchanged), FT_ERR_CUDA. */
 int ft_moe_resize_slots(ft_moe *h, int n_slots);
 
-/* Restores the initial cache state (warm != 0: warm fill as in load_pool;
- * warm == 0: every slot free) and clears the counters.  Synchronous. */
+/* Restores the initial cache state and clears the counters.  LRU mode:
+ * warm != 0 warm-fills as load_pool does, warm == 0 leaves every slot free.
+ * STREAM mode: an empty cache and both staging banks empty.  Synchronous. */
 int ft_cache_reset(ft_moe *h, int warm);
 
 /* The last forward call's cache plan, one entry per distinct expert in
@@ -273,7 +274,8 @@ enum ft_ffn_kernel {
 /* Selects the FFN kernel for later forward calls (default FT_FFN_AUTO).  Both
  * compute the same function with fp32 accumulation; they differ in the order
  * of the K-dimension sums only.  FT_FFN_TC: 128-row token tiles times 256
- * weight rows; FP4 weights are dequantised exactly to bf16 in shared memory.
+ * weight rows; FP4 and FP8 weights are dequantised exactly to bf16 in shared
+ * memory (FP8 row scales multiply the fp32 accumulators).
  * Errors: FT_ERR_ARG; FT_ERR_CUDA when the TMA descriptors of the slot bank
  * could not be encoded at create time (then only the GEMV is available). */
 int ft_moe_set_ffn_kernel(ft_moe *h, int which);
