@@ -33,10 +33,14 @@ def _compile(src, force, extra):
     obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
     if not force and os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime()):
         return obj
-    cmd = ["nvcc", *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+    # written under a private name and renamed, so that processes building at
+    # the same time (one per rank) never link a half-written object
+    tmp = obj + f".tmp{os.getpid()}"
+    cmd = ["nvcc", *ARCH, *FLAGS, *extra, "-c", src, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, obj)
     return obj
 
 
