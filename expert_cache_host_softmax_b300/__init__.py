@@ -150,7 +150,8 @@ class MoELayerStack:
     def load_pool(self, pointers, keepalive=None):
         """pointers: n_layers*n_experts addresses of pinned host blobs."""
         arr = np.ascontiguousarray(np.asarray(pointers, dtype=np.uint64))
-        assert arr.size == self.L * self.E
+        if arr.size != self.L * self.E:
+            raise ValueError(f"expected {self.L * self.E} pool pointers (n_layers * n_experts), got {arr.size}")
         self._pool_ref = (arr, keepalive)
         _check(lib().ft_moe_load_pool(self._h, ctypes.c_void_p(arr.ctypes.data)), self._h)
 
@@ -166,8 +167,10 @@ class MoELayerStack:
         T = x.shape[0]
         if out is None:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=x.device)
-        assert x.is_contiguous() and logits.is_contiguous() and out.is_contiguous()
-        assert x.dtype == torch.bfloat16 and logits.dtype == torch.float32 and out.dtype == torch.bfloat16
+        for name, t, dtype, cols in (("x", x, torch.bfloat16, self.H), ("logits", logits, torch.float32, self.E),
+                                     ("out", out, torch.bfloat16, self.H)):
+            if not t.is_cuda or t.dtype != dtype or tuple(t.shape) != (T, cols) or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous cuda {dtype} tensor of shape ({T}, {cols})")
         _check(lib().ft_moe_forward(self._h, layer, T, _ptr(x), _ptr(logits), _ptr(out), _stream_ptr(stream)),
                self._h)
         return out

@@ -104,3 +104,23 @@ def test_package_import_fails_loudly_without_library(F, tmp_path, monkeypatch):
     monkeypatch.setattr(F, "_lib", None)
     with pytest.raises(ImportError):
         F.lib()
+
+
+def test_binding_checks_tensors_before_calling_the_library(F):
+    """forward and load_pool reject wrong shapes, dtypes and devices in the
+    binding itself (a stack object without a handle stands in; nothing
+    reaches the library)."""
+    import torch
+
+    class NoHandle(F.MoELayerStack):
+        def __init__(self):
+            self.H, self.E, self.L, self._h = 256, 8, 2, None
+
+    s = NoHandle()
+    x = torch.zeros(3, 256, dtype=torch.bfloat16)
+    lg = torch.zeros(3, 8, dtype=torch.float32)
+    out = torch.zeros(3, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="x must be"):
+        s.forward(0, x, lg, out)                     # host tensors
+    with pytest.raises(ValueError, match="pool pointers"):
+        s.load_pool([1, 2, 3])
