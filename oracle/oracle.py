@@ -28,6 +28,10 @@ What the sources fix:
 The pages are silent on everything else.  Readings taken where they are silent:
   * top-k is taken on the raw logits: the k largest, ties to the lower expert
     id, in descending order.  The gates are a softmax over those k logits.
+    NaN logits count as -inf (so a row with fewer than k finite logits takes
+    the rest of its experts from the -inf ones, lowest id first); the softmax
+    runs in IEEE arithmetic, so a selected +inf or an all -inf selection gives
+    NaN gates.
   * SwiGLU expert: y = W_d (silu(W_g x) * (W_u x)).  No bias, no shared expert.
   * h is rounded to bf16 before the down projection (the GPU path stores h in
     bf16).  y and the combine stay in float64 here.
@@ -199,27 +203,42 @@ def dequant_expert(blob: np.ndarray, fmt: int, H: int, I: int):
 # to only a few experts.)
 # ----------------------------------------------------------------------------
 
+def _selection_values(logits: np.ndarray) -> np.ndarray:
+    """The values top-k compares and the gates use: the logits as float64,
+    with NaN read as -inf (the pages say nothing about non-finite logits)."""
+    v = np.asarray(logits, np.float64).copy()
+    v[np.isnan(v)] = -np.inf
+    return v
+
+
 def topk_experts(logits: np.ndarray, k: int) -> np.ndarray:
-    """[T, E] logits -> [T, k] expert ids: k rounds of "take the largest not yet
-    taken", where np.argmax returns the first (lowest) id among equal maxima."""
-    logits = np.asarray(logits, np.float64)
-    T, E = logits.shape
+    """[T, E] logits -> [T, k] expert ids: k rounds of "take the largest value
+    among the experts not yet taken, the lowest id among equal values".
+    NaN counts as -inf, so a row with fewer than k finite logits takes its
+    remaining experts from the -inf ones in ascending id."""
+    v = _selection_values(logits)
+    T, E = v.shape
     taken = np.zeros((T, E), dtype=bool)
     out = np.empty((T, k), dtype=np.int32)
     rows = np.arange(T)
     for j in range(k):
-        cand = np.where(taken, -np.inf, logits)
-        best = np.argmax(cand, axis=1)
+        best_val = np.where(taken, -np.inf, v).max(axis=1)
+        # the first untaken expert holding that value (-inf included)
+        best = np.argmax(~taken & (v == best_val[:, None]), axis=1)
         out[:, j] = best
         taken[rows, best] = True
     return out
 
 
 def gates_of(logits: np.ndarray, idx: np.ndarray) -> np.ndarray:
-    """Softmax over the k selected logits of each token (float64, returned as float32)."""
-    sel = np.take_along_axis(np.asarray(logits, np.float64), idx.astype(np.int64), axis=1)
-    z = np.exp(sel - sel.max(axis=1, keepdims=True))
-    return (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
+    """Softmax over the k selected values of each token, in IEEE float64
+    arithmetic (returned as float32): exp(l_j - max) / sum.  NaN logits are
+    read as -inf.  A token whose selected values hold +inf, or are all -inf,
+    gets NaN gates, as a library softmax gives."""
+    sel = np.take_along_axis(_selection_values(logits), idx.astype(np.int64), axis=1)
+    with np.errstate(invalid="ignore"):
+        z = np.exp(sel - sel.max(axis=1, keepdims=True))
+        return (z / z.sum(axis=1, keepdims=True)).astype(np.float32)
 
 
 # ----------------------------------------------------------------------------

@@ -64,6 +64,18 @@ def _d2d_traces():
     return [t for t in P._parse_traces() if t["d2d"]]
 
 
+def _topk_argmax_on_raw_logits(logits, k):
+    logits = np.asarray(logits, np.float64)          # NaN not read as -inf; taken ones masked by -inf
+    T, E = logits.shape
+    taken = np.zeros((T, E), dtype=bool)
+    out = np.empty((T, k), dtype=np.int32)
+    for j in range(k):
+        best = np.argmax(np.where(taken, -np.inf, logits), axis=1)
+        out[:, j] = best
+        taken[np.arange(T), best] = True
+    return out
+
+
 def _ffn_without_up(x_rows, Wg, Wu, Wd, h_bf16=True):
     g = x_rows @ Wg.T
     h = OO.silu(g)
@@ -89,6 +101,9 @@ MUTATIONS = [
      [P.test_nvfp4_dequant_all_codes_times_all_scales, P.test_mxfp4_dequant_all_codes_times_all_scales]),
     ("top-k ties to the higher id", "topk_experts", _topk_high_index_ties,
      [P.test_topk_exhaustive_tiny]),
+    ("top-k compares NaN as a value", "topk_experts", _topk_argmax_on_raw_logits,
+     [P.test_topk_and_gates_on_non_finite_logits_match_hand_worked_cases,
+      P.test_topk_on_non_finite_logits_equals_a_sort_with_nan_as_minus_inf]),
     ("LRU evicts the MRU", "ExpertSlotLRU", _MruEvictLRU,
      [lambda: [P.test_lru_hand_worked_traces(t) for t in _plain_traces()]]),
     ("resize keeps the least recent keys", "ExpertSlotLRU", _ResizeKeepsOldestLRU,

@@ -256,6 +256,53 @@ def test_gates_closed_forms():
     assert np.all(O.gates_of(lg, O.topk_experts(lg, 1)) == 1.0)
 
 
+def _parse_nonfinite_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "topk_nonfinite.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            k, lg, idx, gates = (part.split() for part in line.split("|"))
+            cases.append((int(k[0]), np.array([float(v) for v in lg], np.float32),
+                          np.array([int(v) for v in idx], np.int32), np.array([float(v) for v in gates])))
+    return cases
+
+
+def test_topk_and_gates_on_non_finite_logits_match_hand_worked_cases():
+    cases = _parse_nonfinite_cases()
+    assert len(cases) >= 6
+    for k, lg, want_idx, want_gates in cases:
+        idx = O.topk_experts(lg[None, :], k)
+        assert np.array_equal(idx[0], want_idx), (lg, idx)
+        g = O.gates_of(lg[None, :], idx)[0]
+        assert np.array_equal(np.isnan(g), np.isnan(want_gates))
+        ok = ~np.isnan(want_gates)
+        np.testing.assert_allclose(g[ok], want_gates[ok], rtol=0, atol=1e-7)
+
+
+def test_topk_on_non_finite_logits_equals_a_sort_with_nan_as_minus_inf():
+    rng = np.random.default_rng(5)
+    for E, k in ((8, 4), (16, 16), (128, 8)):
+        lg = rng.standard_normal((200, E)).astype(np.float32)
+        pick = rng.random((200, E))
+        lg[pick < 0.2] = -np.inf
+        lg[(pick >= 0.2) & (pick < 0.35)] = np.nan
+        lg[pick > 0.98] = np.inf
+        lg[:3] = np.nan                                    # rows with no finite logit
+        mapped = np.where(np.isnan(lg), -np.inf, lg)
+        assert np.array_equal(O.topk_experts(lg, k), _stable_sort_topk(mapped, k))
+        idx = O.topk_experts(lg, k)
+        assert all(len(set(r)) == k for r in idx.tolist())  # k distinct experts per token
+        # gates equal a library softmax of the selected (mapped) values
+        sel = np.take_along_axis(mapped.astype(np.float64), idx.astype(np.int64), axis=1)
+        with np.errstate(invalid="ignore"):
+            ref = scipy.special.softmax(sel, axis=1)
+        g = O.gates_of(lg, idx)
+        assert np.array_equal(np.isnan(g), np.isnan(ref))
+        np.testing.assert_allclose(g[~np.isnan(g)], ref[~np.isnan(ref)], rtol=1e-6, atol=1e-7)
+
+
 # ---------------------------------------------------------------- cache
 
 def _parse_traces():
