@@ -334,8 +334,10 @@ int64_t ft_moe_slot_stride(const ft_moe *h);
  * NULL). */
 int64_t ft_moe_kernel_launches(const ft_moe *h);
 
-/* One-line reason for the last failure on h (or of the last failed create
- * when h is NULL).  Never NULL. */
+/* One-line reason for the last failure on h.  With h == NULL: the calling
+ * thread's last failure of a call that has no handle -- ft_moe_create or a
+ * stateless step (ft_topk_softmax, ft_permute, ft_permute_noalloc).  Never
+ * NULL. */
 const char *ft_last_error(const ft_moe *h);
 
 /* Waits for outstanding work, frees every device and pinned buffer the
@@ -346,8 +348,10 @@ int ft_moe_destroy(ft_moe *h);
 
 /* Router step: for each of T tokens, the top_k largest of E logits (ties to
  * the lower id, descending) into topk_idx i32 [T][k], and their softmax into
- * gates f32 [T][k].  E in 1..512, k in 1..min(E, 32).  Errors: FT_ERR_ARG,
- * FT_ERR_CUDA. */
+ * gates f32 [T][k].  A NaN logit counts as -inf, so a token always gets k
+ * distinct experts (the -inf ones lowest id first); the softmax is plain IEEE
+ * arithmetic, so a selected +inf or an all -inf selection gives NaN gates.
+ * E in 1..512, k in 1..min(E, 32).  Errors: FT_ERR_ARG, FT_ERR_CUDA. */
 int ft_topk_softmax(const float *router_logits, int T, int E, int k, int32_t *topk_idx,
                     float *gates, void *stream);
 
@@ -377,7 +381,11 @@ int ft_permute(const int32_t *topk_idx, int T, int k, int E, int32_t *offsets, i
  *     return FT_ERR_ARG (e.g. E = 256 allows T <= 32768).
  *   - The first call made with a given device current looks up the array's
  *     device address (cudaGetSymbolAddress) once for that device.  Make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The address is kept for the
+ *     process, per device ordinal: it belongs to that device's primary
+ *     context and is not looked up again, so after cudaDeviceReset (or under
+ *     another context on the same device) this entry point must not be
+ *     called.
  *   - Every call shares the one array and overwrites it.  Calls whose work
  *     overlaps on the GPU (other streams, other threads) race on it; serialise
  *     them, e.g. on one stream.  Nothing in the array needs to start at zero:

@@ -5,7 +5,8 @@ own pool allocator.  The entry point keeps its scratch in a fixed device array
 inside the library, so it allocates nothing and takes no workspace.
 
 Checked through the C ABI against the existing entry point ft_permute (which
-uses a caller workspace), bit-exactly, on two calls in a row.  The second
+uses a caller workspace) and against the oracle's stable counting sort,
+bit-exactly, on two calls in a row.  The second
 call uses other sizes, so stale scratch from the first call would show.
 This file is collected last, and it passes both alone and after the other
 tests.
@@ -22,6 +23,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
 import expert_cache_host_softmax_b300 as F  # noqa: E402
+import oracle as O  # noqa: E402
 
 
 def _ptr(t):
@@ -75,6 +77,8 @@ def test_noalloc_permute_matches_workspace_permute_twice():
         torch.cuda.synchronize()
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+        for a, b in zip(got, O.permute_by_expert(idx.cpu().numpy(), E)):
+            assert np.array_equal(a.cpu().numpy(), b)
         assert int(got[0][-1]) == T * k
 
 
