@@ -311,9 +311,33 @@ def _resize_probe(torch, dev, stack, S):
         return {"error": str(e)[:200]}
 
 
+def _host_cpu():
+    """The host's CPU model and logical core count."""
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model}
+
+
+# Further workloads measured after the headline one by the default run (one
+# GPU): the prefill layer of the same 35B-A3B shape with BF16 and NVFP4 experts
+# (all resident: tensor-core bound), and the 753B-shaped whole-layer streaming
+# prefill (PCIe bound).  Each gets its own device time, end-to-end time and
+# rooflines, under "workloads" in the same JSON line.
+EXTRA_WORKLOADS = (
+    ("prefill35b_bf16", "prefill35b", dict(fmt="bf16", steps=5, warmup=3, profile_steps=2, n_phys=128)),
+    ("prefill35b_nvfp4", "prefill35b", dict(fmt="nvfp4", steps=5, warmup=3, profile_steps=2, n_phys=128)),
+    ("stream753b", "stream753b", dict(fmt=None, steps=2, warmup=3, profile_steps=1, n_phys=512)),
+)
+
+
 def run_ours(args, cfg):
     import torch
-    import expert_cache_host_softmax_b300 as F
     from __graft_entry__ import build
     ws, rank, local = _dist()
     if ws > 1:
@@ -322,6 +346,38 @@ def run_ours(args, cfg):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     build()
+    line = _measure(args, cfg, dev, ws, rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, desc, calls, secs = _cpu_baseline(cfg, cfg["seed"], min(args.n_phys, cfg["L"] * cfg["E"]),
+                                               budget_s=args.cpu_budget, fmt=args.fmt or cfg["fmt"])
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
+                                "seconds": secs, **_host_cpu()}
+    if args.extras and ws == 1:
+        line["workloads"] = {}
+        for name, cname, opts in EXTRA_WORKLOADS:
+            sub = argparse.Namespace(**{**vars(args), **opts, "fmt": opts["fmt"], "hit_d2d_cache": 0,
+                                        "ffn": "auto", "miss_path": "auto", "fused_decode": False})
+            try:
+                w = _measure(sub, CONFIGS[cname], dev, ws, rank, resize=False)
+                keep = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "e2e",
+                        "gpu_launches", "roofline", "path_roofline", "clocks")
+                line["workloads"][name] = {key_: w[key_] for key_ in keep}
+            except Exception as e:  # reported in the line; the headline stands
+                line["workloads"][name] = {"error": str(e)[:300]}
+            torch.cuda.empty_cache()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _measure(args, cfg, dev, ws, rank, resize=True):
+    """One workload on this rank's GPU: device-resident timing, end-to-end
+    timing, the per-kernel pass and the rooflines.  Returns the JSON line
+    (without cpu_baseline)."""
+    import torch
+    import expert_cache_host_softmax_b300 as F
     peaks = _peaks()
     seed = cfg["seed"] + rank
     T, H, E, k, I, L, S = cfg["T"], cfg["H"], cfg["E"], cfg["k"], cfg["I"], cfg["L"], cfg["S"]
@@ -626,18 +682,10 @@ def run_ours(args, cfg):
         "clocks": clocks,
         "wall_s_timed": wall,
     }
-    if cfg["mode"] == "lru" and S // 2 >= min(E, T * k):
+    if resize and cfg["mode"] == "lru" and S // 2 >= min(E, T * k):
         line["resize"] = _resize_probe(torch, dev, stack, S)
-    if rank == 0 and not args.no_cpu_baseline:
-        tps, desc, calls, secs = _cpu_baseline(cfg, cfg["seed"], n_phys, budget_s=args.cpu_budget, fmt=fmt)
-        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": desc,
-                                "seconds": secs}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     stack.close()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    return line
 
 
 def main():
@@ -660,6 +708,9 @@ def main():
     ap.add_argument("--miss-path", choices=("auto", "copy", "pull", "kernel"), default="auto",
                     help="LRU misses: cudaMemcpyAsync issued by the host, read over PCIe by the FFN kernels, "
                          "copied by the GPU, or auto (the GPU for experts up to 8 MiB, else the host)")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the further workloads (prefill-35B BF16 and NVFP4, stream-753B) that a one-GPU run "
+                         "of the default workload also measures")
     ap.add_argument("--fused-decode", action="store_true",
                     help="decode calls as one cooperative kernel instead of separate kernels (its copy-flag "
                          "wait needs the copy stream to progress alongside it: profile it with --miss-path pull)")
@@ -667,6 +718,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     cfg = CONFIGS[args.config]
+    # the further workloads come with the default workload only
+    args.extras = args.extras and args.config == "decode35b" and args.fmt is None and args.ffn == "auto" \
+        and args.miss_path == "auto" and not args.fused_decode
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -69,11 +69,14 @@ struct MegaArgs {
   int wait_copies;    // misses arrive by copy: wait for the copy flag before their gate/up
 };
 
+// Every load of weights and h goes through L2 (coherent): the misses' slots
+// are written while the kernel runs (by the copy engine, or by its own CTAs
+// pulling them from host memory), and so is h.
 template <int FMT, bool DOWN, int NT>
 __device__ __forceinline__ void gemv_item(const FfnArgs &a, int lpr, int u, int bx, int fpw, __nv_bfloat16 *xs) {
-  if (lpr == 32) gemv_block<FMT, DOWN, NT, 32, kMegaWarps>(a, u, bx, fpw, xs);
-  else if (lpr == 16) gemv_block<FMT, DOWN, NT, 16, kMegaWarps>(a, u, bx, fpw, xs);
-  else gemv_block<FMT, DOWN, NT, 8, kMegaWarps>(a, u, bx, fpw, xs);
+  if (lpr == 32) gemv_block<FMT, DOWN, NT, 32, kMegaWarps, true>(a, u, bx, fpw, xs);
+  else if (lpr == 16) gemv_block<FMT, DOWN, NT, 16, kMegaWarps, true>(a, u, bx, fpw, xs);
+  else gemv_block<FMT, DOWN, NT, 8, kMegaWarps, true>(a, u, bx, fpw, xs);
 }
 
 template <int FMT, bool DOWN>
@@ -181,6 +184,7 @@ cudaError_t launch_decode_layer(const RouteArgs &route, const FfnArgs &ffn, cons
   m.cb = cb;
   m.sync = sync;
   m.wait_copies = wait_copies ? 1 : 0;
+
   m.lpr_gu = lanes_per_row_m(ffn.H);
   m.lpr_dn = lanes_per_row_m(ffn.I);
   m.fpw_gu = ffn.H >= 4096 ? 4 : 1;

@@ -39,17 +39,49 @@ namespace {
 // One CTA: kWarps * 32 / LPR * fpw output features (block blockIdx.x) of one
 // distinct expert (blockIdx.y).  With combine counters (down only), the last
 // CTA of each feature block also writes that block of the combined output.
-template <int FMT, bool DOWN, int NT, int LPR>
+// COH (gate/up grids whose own CTAs copy misses into their slots): weights
+// are loaded through L2 (ld.global.cg), not through the read-only path, which
+// is defined only for data no one writes while the kernel runs.
+template <int FMT, bool DOWN, int NT, int LPR, bool COH>
 __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, CombineArgs cb, int fpw) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
+  // Roles.  Without in-kernel copies, CTA (x, y) works on feature block x of
+  // distinct expert y.  With them (copy_rows > 0), roles go by arrival, not by
+  // block index (CUDA does not promise an order of dispatch): the first
+  // copy_rows * gridDim.x CTAs to take a ticket copy, and the others take the
+  // work items in ticket order, hits first.  The copiers are thus running
+  // before any CTA waits for them, whatever the order of dispatch.  The
+  // ticket counter was last used by the gate/up grid two kernels back, which
+  // has completed; the CTA that takes the last ticket re-arms it.
+  int item_y = blockIdx.y, item_x = blockIdx.x;
+  long long copier = -1;
+  if constexpr (!DOWN) {
+    if (a.copy_rows > 0) {
+      __shared__ int s_ticket;
+      if (threadIdx.x == 0) {
+        const int total = gridDim.x * gridDim.y;
+        const int t = atomicAdd(a.copy_sync + 2, 1);
+        if (t == total - 1) a.copy_sync[2] = 0;
+        s_ticket = t;
+      }
+      __syncthreads();
+      const int t = s_ticket, nct = a.copy_rows * gridDim.x;
+      if (t < nct) {
+        copier = t;
+      } else {
+        item_y = a.copy_rows + (t - nct) / gridDim.x;
+        item_x = (t - nct) % gridDim.x;
+      }
+    }
+  }
   // Before the wait for the kernel ahead: this grid starts only once that
   // kernel is past its own wait (it triggers after it), so all work before
   // the route kernel -- the call's x -- and the route kernel's plan (for a
   // down grid, which starts after the gate/up grid passed its wait) are final.
   bool x_staged = false;
   if constexpr (!DOWN) {
-    if (a.max_tokens == 1 && (int)blockIdx.y >= a.copy_rows) {
+    if (a.max_tokens == 1 && copier < 0) {
       // one-token call: every expert multiplies the same row
       for (int v = threadIdx.x; v < a.H / 8; v += blockDim.x)
         reinterpret_cast<uint4 *>(xs)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(a.x) + v);
@@ -62,19 +94,17 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   pdl_wait();      // the plan, activations and slots come from earlier kernels
   pdl_trigger();
   if constexpr (!DOWN) {
-    if ((int)blockIdx.y < a.copy_rows) {
-      // a copying CTA (the grid's first rows, so dispatched before any CTA
-      // that waits for them): gate/up bytes of every miss, the flag, then
-      // the down bytes
+    if (copier >= 0) {
+      // a copying CTA: gate/up bytes of every miss, the flag, then the down bytes
       const long long nct = (long long)a.copy_rows * gridDim.x;
-      const long long t = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+      const long long t = copier * blockDim.x + threadIdx.x;
       copy_misses(a.mc, 0, 2, t, nct * blockDim.x);
       cta_arrive_last_sets(a.copy_sync + 1, a.copy_sync, (int)nct, a.seq_raised);
       copy_misses(a.mc, 2, 3, t, nct * blockDim.x);
       return;
     }
   }
-  gemv_block<FMT, DOWN, NT, LPR, kWarps>(a, blockIdx.y - (DOWN ? 0 : a.copy_rows), blockIdx.x, fpw, xs, x_staged);
+  gemv_block<FMT, DOWN, NT, LPR, kWarps, COH>(a, item_y - (DOWN ? 0 : a.copy_rows), item_x, fpw, xs, x_staged);
   if constexpr (DOWN) {
     if (cb.counters == nullptr) return;
     __shared__ int s_last;
@@ -123,7 +153,12 @@ cudaError_t launch_t(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
   const int fpc = kWarps * (32 / LPR) * fpw;
   dim3 grid((feats + fpc - 1) / fpc, a.umax + (DOWN ? 0 : a.copy_rows));
   const size_t smem = (size_t)NT * K * sizeof(__nv_bfloat16);
-  return launch_k(ffn_gemv_kernel<FMT, DOWN, NT, LPR>, grid, dim3(kWarps * 32), smem, s, a.pdl != 0, a, cb, fpw);
+  if constexpr (!DOWN)
+    if (a.miss_coherent)
+      return launch_k(ffn_gemv_kernel<FMT, false, NT, LPR, true>, grid, dim3(kWarps * 32), smem, s, a.pdl != 0, a,
+                      cb, fpw);
+  return launch_k(ffn_gemv_kernel<FMT, DOWN, NT, LPR, false>, grid, dim3(kWarps * 32), smem, s, a.pdl != 0, a, cb,
+                  fpw);
 }
 
 template <int FMT, bool DOWN, int NT>
@@ -152,12 +187,18 @@ cudaError_t launch_ffn(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) 
   }
 }
 
+template <int FMT, bool DOWN, int NT, bool COH>
+void attr_c() {
+  const int max_smem = NT * 8192 * 2;   // activations of NT token rows, K <= 8192
+  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 8, COH>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 16, COH>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 32, COH>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+}
+
 template <int FMT, bool DOWN, int NT>
 void attr_l() {
-  const int max_smem = NT * 8192 * 2;   // activations of NT token rows, K <= 8192
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  attr_c<FMT, DOWN, NT, false>();
+  if constexpr (!DOWN) attr_c<FMT, DOWN, NT, true>();
 }
 
 template <int FMT>

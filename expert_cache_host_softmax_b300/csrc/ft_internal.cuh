@@ -138,9 +138,13 @@ struct FfnArgs {
   // The down kernel starts after the whole gate/up grid (and so after range 2).
   MissCopyArgs mc;
   int copy_rows;
-  int *copy_sync;             // [0] flag, [1] arrival count
+  int *copy_sync;             // [0] flag, [1] arrival count, [2] role ticket
   int seq;                    // the flag value this call's miss CTAs wait for
   int seq_raised;             // the value its copying CTAs raise (seq, unless a fault is injected)
+  // the misses' slots are written while this grid runs (its own copying
+  // CTAs): the GEMV variant that reads weights through L2 (ld.global.cg)
+  // instead of the read-only path is launched
+  int miss_coherent;
   // tensor-core down projection: with out_acc set, each row's gate-weighted
   // y is added into out_acc[token] (fp32, zeroed before) instead of, or with
   // keep_y as well as, being stored to y

@@ -105,7 +105,7 @@ struct ft_moe {
   int *combine_counters = nullptr;   // per feature tile, for the combine fused into the down GEMV
   uint64_t *pool_dev = nullptr;      // device-visible addresses of the pool's blobs [L*E] (FT_MISS_PULL)
   int *mega_sync = nullptr;          // fused decode layer: plan flag, copy flag, grid barrier count and generation
-  int *copy_sync = nullptr;          // misses copied inside the gate/up kernel: flag, arrival count
+  int *copy_sync = nullptr;          // misses copied inside the gate/up kernel: flag, arrival count, role ticket
   int32_t *seq_ring = nullptr;       // pinned: seq_ring[seq % 64] = seq, the source of the copy-flag write
   bool decode_fused = false;   // ft_moe_set_decode_fusion
   int miss_path = FT_MISS_AUTO;
@@ -238,7 +238,7 @@ int sync_handle(ft_moe *h) {
     FT_CUDA(h, cudaMemset(h->err_dev, 0, sizeof(int)));
     // an aborted kernel may have left its flags or counters mid-way
     FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
-    FT_CUDA(h, cudaMemset(h->copy_sync, 0, 2 * sizeof(int)));
+    FT_CUDA(h, cudaMemset(h->copy_sync, 0, 4 * sizeof(int)));
     FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
     return fail(h, FT_ERR_DEVICE, "a kernel gave up a bounded wait (site " + std::to_string(code) + ")");
   }
@@ -291,7 +291,7 @@ int reset_tables(ft_moe *h, bool warm) {
   h->order_cur = 0;
   FT_CUDA(h, cudaMemset(h->stats_dev, 0, 16 * sizeof(unsigned long long)));
   FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
-  FT_CUDA(h, cudaMemset(h->copy_sync, 0, 2 * sizeof(int)));
+  FT_CUDA(h, cudaMemset(h->copy_sync, 0, 4 * sizeof(int)));
   FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
   h->host_warm = h->host_streamed = h->host_bytes = h->host_d2d = 0;
   h->last_streamed = h->last_stream_bytes = h->last_d2d = 0;
@@ -574,7 +574,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
             dev_alloc(&h->xpbuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->mega_sync, 4) == cudaSuccess && cudaMemset(h->mega_sync, 0, 16) == cudaSuccess &&
-            dev_alloc(&h->copy_sync, 2) == cudaSuccess && cudaMemset(h->copy_sync, 0, 8) == cudaSuccess &&
+            dev_alloc(&h->copy_sync, 4) == cudaSuccess && cudaMemset(h->copy_sync, 0, 16) == cudaSuccess &&
             dev_alloc(&h->combine_counters, combine_tiles(hidden)) == cudaSuccess &&
             cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(hidden)) == cudaSuccess;
   if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
@@ -880,10 +880,12 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
       // the misses' CTAs run out their bounded wait (FT_ERR_DEVICE at the next
       // synchronising call)
       fa.seq_raised = fault("devwait") ? fa.seq ^ 0x40000000 : fa.seq;
+      fa.miss_coherent = 1;   // the misses' slots fill while this grid runs
       prof_begin(h, FT_PROF_GATEUP_HIT, stream);
       FT_CUDA(h, run_ffn(h, fa, false, tc, n_tokens, stream));
       prof_end(h, FT_PROF_GATEUP_HIT, stream);
       fa.copy_rows = 0;
+      fa.miss_coherent = 0;
     } else {
       // tensor cores: copy kernels on the copy stream; the misses' gate/up
       // waits for the first, the down kernel for the second

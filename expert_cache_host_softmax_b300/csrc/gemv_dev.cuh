@@ -61,19 +61,31 @@ struct Chunk {
   uint32_t sf;
 };
 
-template <int FMT>
+// Weight loads.  COH = false: the read-only path (ld.global.nc), for bytes
+// that no one writes while the kernel runs (cached experts, pinned host
+// memory).  COH = true: loads cached in L2 only (ld.global.cg), for a miss
+// whose slot is filled while the kernel runs (by copying CTAs of the same
+// grid, by the copy engine, or by CTAs that pull it from host memory); the
+// flag wait before them orders them after those writes.
+template <bool COH, typename T>
+__device__ __forceinline__ T ld_w(const T *p) {
+  if constexpr (COH) return __ldcg(p);
+  else return __ldg(p);
+}
+
+template <int FMT, bool COH>
 __device__ __forceinline__ void load_chunk(const uint8_t *__restrict__ codes_row,
                                            const uint8_t *__restrict__ sf_row, int c, Chunk<FMT> &ch) {
   if constexpr (FMT == FMT_BF16 || FMT == FMT_FP8) {
     constexpr int V = chunk_vecs<FMT>();
     const uint4 *p = reinterpret_cast<const uint4 *>(codes_row) + V * c;
 #pragma unroll
-    for (int i = 0; i < V; ++i) ch.q[i] = __ldg(p + i);
+    for (int i = 0; i < V; ++i) ch.q[i] = ld_w<COH>(p + i);
     ch.sf = 0;
   } else {
-    ch.q[0] = __ldg(reinterpret_cast<const uint4 *>(codes_row) + c);
-    if constexpr (FMT == FMT_NVFP4) ch.sf = __ldg(reinterpret_cast<const uint16_t *>(sf_row) + c);
-    else ch.sf = __ldg(sf_row + c);
+    ch.q[0] = ld_w<COH>(reinterpret_cast<const uint4 *>(codes_row) + c);
+    if constexpr (FMT == FMT_NVFP4) ch.sf = ld_w<COH>(reinterpret_cast<const uint16_t *>(sf_row) + c);
+    else ch.sf = ld_w<COH>(sf_row + c);
   }
 }
 
@@ -199,7 +211,7 @@ __device__ __forceinline__ void store_chunk(const RowPtrs &dst, int c, const Chu
 
 // With `dst` set (a miss read from host memory), every chunk read is also
 // written to the same place in the expert's GPU slot.
-template <int FMT, int NT, int NROWS, int LPR>
+template <int FMT, int NT, int NROWS, int LPR, bool COH>
 __device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, int K, const __nv_bfloat16 *xs,
                                          int l8, int nt, float (&acc)[NROWS][NT]) {
   // a lane's chunks of a row in flight at once: all of them for rows of up to
@@ -214,7 +226,7 @@ __device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, 
     for (int b = 0; b < kBatch; ++b)
       if (i0 + b < cpl)
 #pragma unroll
-        for (int r = 0; r < NROWS; ++r) load_chunk<FMT>(rp[r].codes, rp[r].sf, l8 + LPR * (i0 + b), ch[r][b]);
+        for (int r = 0; r < NROWS; ++r) load_chunk<FMT, COH>(rp[r].codes, rp[r].sf, l8 + LPR * (i0 + b), ch[r][b]);
     if (dst) {
 #pragma unroll
       for (int b = 0; b < kBatch; ++b)
@@ -230,7 +242,7 @@ __device__ __forceinline__ void rows_dot(const RowPtrs *rp, const RowPtrs *dst, 
   }
 }
 
-template <int FMT, bool DOWN, int NT, int LPR>
+template <int FMT, bool DOWN, int NT, int LPR, bool COH>
 __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst, const BlobLayout &L, const FfnArgs &a,
                                          int feat, const __nv_bfloat16 *xs, int nt, int p0, float gs0, float gs1,
                                          int l8) {
@@ -246,10 +258,10 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = acc[1][t] = 0.0f;
     if constexpr (FMT == FMT_FP8) {
-      gs0 *= __ldg(reinterpret_cast<const float *>(rp[0].sf));
-      gs1 *= __ldg(reinterpret_cast<const float *>(rp[1].sf));
+      gs0 *= ld_w<COH>(reinterpret_cast<const float *>(rp[0].sf));
+      gs1 *= ld_w<COH>(reinterpret_cast<const float *>(rp[1].sf));
     }
-    rows_dot<FMT, NT, 2, LPR>(rp, slot_dst ? dp : nullptr, a.H, xs, l8, nt, acc);
+    rows_dot<FMT, NT, 2, LPR, COH>(rp, slot_dst ? dp : nullptr, a.H, xs, l8, nt, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const float g = group_sum<LPR>(acc[0][t]) * gs0;
@@ -264,8 +276,8 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
     float acc[1][NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[0][t] = 0.0f;
-    if constexpr (FMT == FMT_FP8) gs0 *= __ldg(reinterpret_cast<const float *>(rp[0].sf));
-    rows_dot<FMT, NT, 1, LPR>(rp, slot_dst ? dp : nullptr, a.I, xs, l8, nt, acc);
+    if constexpr (FMT == FMT_FP8) gs0 *= ld_w<COH>(reinterpret_cast<const float *>(rp[0].sf));
+    rows_dot<FMT, NT, 1, LPR, COH>(rp, slot_dst ? dp : nullptr, a.I, xs, l8, nt, acc);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const float v = group_sum<LPR>(acc[0][t]) * gs0;
@@ -279,7 +291,10 @@ __device__ __forceinline__ void ffn_rows(const uint8_t *blob, uint8_t *slot_dst,
 // tokens any expert of the call has, up to kTokChunk) token rows per pass.
 // xs: shared memory for NT activation rows of K.
 // x_staged (gate/up of a one-token call): xs already holds the token's row.
-template <int FMT, bool DOWN, int NT, int LPR, int KW>
+// COH: every weight and activation load goes through L2 (ld.global.cg), for
+// grids during which slots of misses (or h) are written; otherwise weights
+// take the read-only path.
+template <int FMT, bool DOWN, int NT, int LPR, int KW, bool COH>
 __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int fpw, __nv_bfloat16 *xs,
                                            bool x_staged = false) {
   // fpw passes per warp over feature groups: long rows (large K) give each CTA
@@ -324,8 +339,8 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
             gs1 = a.ms.up[i];
           }
       } else {
-        gs0 = DOWN ? gs[2] : gs[0];
-        gs1 = gs[1];
+        gs0 = ld_w<COH>(gs + (DOWN ? 2 : 0));
+        gs1 = ld_w<COH>(gs + 1);
       }
       if (DOWN && pull_dst && bx == 0 && threadIdx.x == 0)
         *reinterpret_cast<uint4 *>(pull_dst + L.gscale) = *reinterpret_cast<const uint4 *>(blob + L.gscale);
@@ -362,13 +377,13 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
           const int pair = a.plan.perm[off + c0 + t];
           src = a.x + (size_t)(pair / a.k) * a.H;
         }
-        reinterpret_cast<uint4 *>(xs + (size_t)t * K)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(src) + v);
+        reinterpret_cast<uint4 *>(xs + (size_t)t * K)[xs_pos(v)] = ld_w<COH>(reinterpret_cast<const uint4 *>(src) + v);
       }
       __syncthreads();
       // rows nt..NT-1 of xs may hold stale data: their products are skipped
       for (int fp = 0; fp < fpw; ++fp)
-        ffn_rows<FMT, DOWN, NT, LPR>(blob, c0 == 0 ? pull_dst : nullptr, L, a, feat0 + fp * KW * (32 / LPR), xs,
-                                     nt, off + c0, gs0, gs1, l8);
+        ffn_rows<FMT, DOWN, NT, LPR, COH>(blob, c0 == 0 ? pull_dst : nullptr, L, a, feat0 + fp * KW * (32 / LPR), xs,
+                                          nt, off + c0, gs0, gs1, l8);
       __syncthreads();
     }
   }

@@ -400,6 +400,7 @@ class MoELayerOracle:
         self.hit_d2d = hit_d2d
         self.nbytes = blob_bytes(fmt, H, I)
         self._wcache: dict[int, tuple] = {}
+        self.wcache_max = 64          # decoded experts kept (memory only; no effect on results)
         self.reset()
 
     def reset(self, warm: bool = True):
@@ -447,7 +448,7 @@ class MoELayerOracle:
 
     def weights(self, key: int):
         if key not in self._wcache:
-            if len(self._wcache) > 64:
+            if len(self._wcache) >= self.wcache_max:
                 self._wcache.clear()
             self._wcache[key] = dequant_expert(self.blob_of(key), self.fmt, self.H, self.I)
         return self._wcache[key]

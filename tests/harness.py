@@ -74,3 +74,19 @@ def rel_err(got, ref):
     """max |got - ref| / max |ref| over the tensor (norm-wise)."""
     den = float(np.abs(ref).max())
     return float(np.abs(got - ref).max()) / (den if den > 0 else 1.0)
+
+
+def elem_rel_err(got, ref, floor=1e-3):
+    """max over elements of |got - ref| / max(|ref|, floor * max|ref|): the
+    element-wise relative error, with an absolute floor at `floor` of the
+    tensor's largest magnitude."""
+    ref = np.asarray(ref, np.float64)
+    den = np.maximum(np.abs(ref), floor * float(np.abs(ref).max()) if ref.size else 0.0)
+    den[den == 0] = 1.0
+    return float((np.abs(np.asarray(got, np.float64) - ref) / den).max()) if ref.size else 0.0
+
+
+def bf16_ulp(v):
+    """Spacing of bf16 values at |v| (8 significant bits): 2^(floor(log2|v|) - 7)."""
+    _, e = np.frexp(np.abs(np.asarray(v, np.float64)))
+    return np.ldexp(1.0, e - 8)
