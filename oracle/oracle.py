@@ -354,6 +354,81 @@ def permute_by_expert(idx: np.ndarray, E: int):
 
 
 # ----------------------------------------------------------------------------
+# Activation quantiser of the FP4 x FP4 variant
+# (the pages name NVFP4 as a weight format and say nothing of activation
+# precision; this variant quantises the activations too, so that both GEMM
+# operands are FP4.  Reading: the NVFP4 layout of the weights -- e2m1 codes,
+# one E4M3 scale per 16 consecutive elements of a row -- applied to x and h;
+# x rows also get an fp32 second-level scale g = amax(row) / (6 * 448), h rows
+# none.  Every quantiser decision is taken in IEEE binary32, as the kernels
+# take it.)
+# ----------------------------------------------------------------------------
+
+#: values of the non-negative finite E4M3 codes 0..126, ascending
+_E4M3_NONNEG = np.array([e4m3_value(b) for b in range(127)], dtype=np.float64)
+
+
+def e4m3_encode_nonneg(v: np.ndarray) -> np.ndarray:
+    """Non-negative values -> E4M3 codes: the nearest E4M3 value, a tie to
+    the even code, values above 448 to 448 (saturation)."""
+    v = np.asarray(v, np.float64)
+    hi = np.clip(np.searchsorted(_E4M3_NONNEG, v, side="left"), 1, 126)
+    lo = hi - 1
+    d_lo, d_hi = v - _E4M3_NONNEG[lo], _E4M3_NONNEG[hi] - v
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(v >= _E4M3_NONNEG[126], 126, code)
+    return code.astype(np.uint8)
+
+
+def e2m1_encode(v: np.ndarray) -> np.ndarray:
+    """Values -> 4-bit e2m1 codes: the nearest of the 8 magnitudes, a tie to
+    the even code, magnitudes above 6 to 6 (saturation); bit 3 is the sign
+    bit of v (so -0 and negative values that round to 0 give code 8)."""
+    v = np.asarray(v, np.float64)
+    mag = np.abs(v)
+    grid = np.array(E2M1_MAGNITUDE)
+    hi = np.clip(np.searchsorted(grid, mag, side="left"), 1, 7)
+    lo = hi - 1
+    d_lo, d_hi = mag - grid[lo], grid[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(mag >= 6.0, 7, code)
+    return (code | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
+
+
+def quantize_act_fp4(a: np.ndarray, row_scale: bool):
+    """Rows of activations a [n, K] -> (codes uint8 [n, K] one 4-bit code per
+    element, block scales uint8 [n, K/16] E4M3, g float32 [n]), all in float32:
+      g   = amax(row) / 2688 (6 * 448), or 1 for an all-zero row or without row_scale
+      s_b = E4M3( (amax(block) / 6) / g )                  (nearest, ties to even)
+      q   = e2m1( a / (value(s_b) * g) )                   (0 where that product is 0)"""
+    a = np.asarray(a, np.float32)
+    n, K = a.shape
+    f = np.float32
+    if row_scale:
+        amax = np.abs(a).max(axis=1)
+        g = (amax / f(2688.0)).astype(np.float32)
+        g[amax == 0] = f(1.0)
+    else:
+        g = np.ones(n, np.float32)
+    blocks = np.abs(a).reshape(n, K // 16, 16).max(axis=2)
+    s = ((blocks / f(6.0)).astype(np.float32) / g[:, None]).astype(np.float32)
+    sf = e4m3_encode_nonneg(s)
+    denom = (_E4M3_TABLE[sf].astype(np.float32) * g[:, None]).astype(np.float32)
+    den_e = np.repeat(denom, 16, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(den_e > 0, a / np.where(den_e > 0, den_e, f(1.0)), f(0.0)).astype(np.float32)
+    return e2m1_encode(v), sf, g
+
+
+def dequant_act_fp4(codes: np.ndarray, sf: np.ndarray, g: np.ndarray) -> np.ndarray:
+    """The values that quantize_act_fp4's output stands for (float64)."""
+    scale = np.repeat(_E4M3_TABLE[sf], 16, axis=1) * np.asarray(g, np.float64)[:, None]
+    return _E2M1_TABLE[codes] * scale
+
+
+# ----------------------------------------------------------------------------
 # Expert FFN (SwiGLU) and combine
 # ----------------------------------------------------------------------------
 
@@ -362,12 +437,20 @@ def silu(a: np.ndarray) -> np.ndarray:
 
 
 def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray,
-               h_bf16: bool = True) -> np.ndarray:
-    """x_rows [n, H] float64 -> y [n, H]:  y = W_d (silu(W_g x) * (W_u x))."""
+               h_bf16: bool = True, act_fp4: bool = False) -> np.ndarray:
+    """x_rows [n, H] float64 -> y [n, H]:  y = W_d (silu(W_g x) * (W_u x)).
+
+    act_fp4 (the FP4 x FP4 variant): x is quantised first (quantize_act_fp4
+    with its row scale), and h, taken to float32, is quantised before the down
+    projection (block scales only); otherwise h is rounded to bf16 when h_bf16."""
+    if act_fp4:
+        x_rows = dequant_act_fp4(*quantize_act_fp4(x_rows, row_scale=True))
     g = x_rows @ Wg.T
     u = x_rows @ Wu.T
     h = silu(g) * u
-    if h_bf16:
+    if act_fp4:
+        h = dequant_act_fp4(*quantize_act_fp4(h.astype(np.float32), row_scale=False))
+    elif h_bf16:
         h = round_to_bf16(h)
     return h @ Wd.T
 
@@ -392,11 +475,13 @@ class MoELayerOracle:
     blob_of(key) -> uint8 blob of expert key = layer * E + e (the host pool)."""
 
     def __init__(self, H: int, E: int, k: int, I: int, fmt: int, n_slots: int, n_layers: int,
-                 blob_of, mode: int = MODE_LRU, h_bf16: bool = True, hit_d2d: bool = False):
+                 blob_of, mode: int = MODE_LRU, h_bf16: bool = True, hit_d2d: bool = False,
+                 act_fp4: bool = False):
         self.H, self.E, self.k, self.I, self.fmt = H, E, k, I, fmt
         self.S, self.L, self.mode = n_slots, n_layers, mode
         self.blob_of = blob_of
         self.h_bf16 = h_bf16
+        self.act_fp4 = act_fp4
         self.hit_d2d = hit_d2d
         self.nbytes = blob_bytes(fmt, H, I)
         self._wcache: dict[int, tuple] = {}
@@ -518,7 +603,7 @@ class MoELayerOracle:
                 pairs = [int(p) for p in perm[lo:hi] if int(p) // self.k in want]
                 if pairs:
                     Wg, Wu, Wd = self.weights(layer * self.E + e)
-                    expert_ffn(np.stack([x[p // self.k] for p in pairs]), Wg, Wu, Wd, self.h_bf16)
+                    expert_ffn(np.stack([x[p // self.k] for p in pairs]), Wg, Wu, Wd, self.h_bf16, self.act_fp4)
             return res
         for e in experts:
             lo, hi = int(offsets[e]), int(offsets[e + 1])
@@ -527,7 +612,7 @@ class MoELayerOracle:
                 continue
             Wg, Wu, Wd = self.weights(layer * self.E + e)
             rows = np.stack([x[p // self.k] for p in pairs])
-            ys = expert_ffn(rows, Wg, Wu, Wd, self.h_bf16)
+            ys = expert_ffn(rows, Wg, Wu, Wd, self.h_bf16, self.act_fp4)
             for p, yr in zip(pairs, ys):
                 y[int(inv[p])] = yr          # y is kept in permuted order
         order = sorted(want)

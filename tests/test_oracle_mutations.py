@@ -76,7 +76,16 @@ def _topk_argmax_on_raw_logits(logits, k):
     return out
 
 
-def _ffn_without_up(x_rows, Wg, Wu, Wd, h_bf16=True):
+def _quant_amax_over_4(a, row_scale):
+    a = np.asarray(a, np.float32)                     # block scale from amax / 4 instead of amax / 6
+    return OO.__dict__["_orig_quant"](a * np.float32(1.5), row_scale)
+
+
+def _quant_no_row_scale(a, row_scale):
+    return OO.__dict__["_orig_quant"](a, False)       # the row scale never applied
+
+
+def _ffn_without_up(x_rows, Wg, Wu, Wd, h_bf16=True, act_fp4=False):
     g = x_rows @ Wg.T
     h = OO.silu(g)
     return (OO.round_to_bf16(h) if h_bf16 else h) @ Wd.T
@@ -104,6 +113,10 @@ MUTATIONS = [
     ("top-k compares NaN as a value", "topk_experts", _topk_argmax_on_raw_logits,
      [P.test_topk_and_gates_on_non_finite_logits_match_hand_worked_cases,
       P.test_topk_on_non_finite_logits_equals_a_sort_with_nan_as_minus_inf]),
+    ("activation block scale from amax/4", "quantize_act_fp4", _quant_amax_over_4,
+     [P.test_fp4_activation_quantiser_round_trips_values_on_its_grid]),
+    ("activation row scale dropped", "quantize_act_fp4", _quant_no_row_scale,
+     [P.test_fp4_activation_quantiser_round_trips_values_on_its_grid]),
     ("LRU evicts the MRU", "ExpertSlotLRU", _MruEvictLRU,
      [lambda: [P.test_lru_hand_worked_traces(t) for t in _plain_traces()]]),
     ("resize keeps the least recent keys", "ExpertSlotLRU", _ResizeKeepsOldestLRU,
@@ -129,6 +142,7 @@ MUTATIONS = [
 def test_pin_catches_planted_mistake(monkeypatch, name, attr, bad, pins):
     monkeypatch.setitem(OO.__dict__, "_orig_topk", OO.topk_experts)
     monkeypatch.setitem(OO.__dict__, "_orig_e4m3", OO.e4m3_value)
+    monkeypatch.setitem(OO.__dict__, "_orig_quant", OO.quantize_act_fp4)
     monkeypatch.setattr(OO, attr, bad)
     monkeypatch.setattr(P.O, attr, bad, raising=False)
     for pin in pins:

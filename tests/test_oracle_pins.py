@@ -605,8 +605,9 @@ def test_silu_matches_library_sigmoid():
     np.testing.assert_allclose(O.silu(a), a * scipy.special.expit(a), rtol=1e-14, atol=1e-300)
 
 
-def _dense_reference(x, logits, k, weights, h_bf16=True):
-    """All E experts on all tokens, masked by the top-k gates."""
+def _dense_reference(x, logits, k, weights, h_bf16=True, act_fp4=False):
+    """All E experts on all tokens, masked by the top-k gates.  act_fp4: x and
+    h pass through the activation quantiser (pinned on its own below)."""
     T, E = logits.shape
     p = scipy.special.softmax(logits.astype(np.float64), axis=1)
     order = np.lexsort((np.tile(np.arange(E), (T, 1)), -logits.astype(np.float64)), axis=1)[:, :k]
@@ -615,11 +616,15 @@ def _dense_reference(x, logits, k, weights, h_bf16=True):
         sel = order[t]
         G[t, sel] = p[t, sel] / p[t, sel].sum()
     out = np.zeros((T, x.shape[1]))
+    if act_fp4:
+        x = O.dequant_act_fp4(*O.quantize_act_fp4(x, row_scale=True))
     for e in range(E):
         Wg, Wu, Wd = weights[e]
         a = x @ Wg.T
         h = a * scipy.special.expit(a) * (x @ Wu.T)
-        if h_bf16:
+        if act_fp4:
+            h = O.dequant_act_fp4(*O.quantize_act_fp4(h.astype(np.float32), row_scale=False))
+        elif h_bf16:
             h = O.round_to_bf16(h)
         out += G[:, [e]] * (h @ Wd.T)
     return out
@@ -639,6 +644,96 @@ def test_layer_equals_dense_masked_mixture(fmt, k):
     # both sides round h to bf16; a last-bit difference in an fp64 sum can flip
     # one rounding, which moves an output by ~1e-7 of the largest output
     np.testing.assert_allclose(res["out"], ref, rtol=0, atol=1e-6 * np.abs(ref).max())
+
+
+def test_layer_with_fp4_activations_equals_dense_masked_mixture():
+    H, I, E, T, seed, k = 64, 96, 6, 9, 11, 3
+    pool = ftgen.pool("nvfp4", H, I, list(range(E)), seed)
+    orc = O.MoELayerOracle(H, E, k, I, O.FMT_NVFP4, n_slots=E, n_layers=1, blob_of=lambda key: pool[key], act_fp4=True)
+    x = ftgen.x_bf16(seed, T, H, 0, 0)
+    lg = ftgen.router_logits(seed, T, E, 0, 0)
+    res = orc.forward(0, x, lg)
+    weights = [O.dequant_expert(pool[e], O.FMT_NVFP4, H, I) for e in range(E)]
+    ref = _dense_reference(O.bf16_bits_to_f64(x), lg, k, weights, act_fp4=True)
+    # h is quantised from float32 on both sides: a last-bit difference in an
+    # fp64 sum can flip one code, which moves an output by ~1e-3 of the largest
+    np.testing.assert_allclose(res["out"], ref, rtol=0, atol=2e-3 * np.abs(ref).max())
+    plain = _dense_reference(O.bf16_bits_to_f64(x), lg, k, weights)
+    assert 1e-3 < np.abs(ref - plain).max() / np.abs(plain).max() < 0.2   # the quantiser is really applied
+
+
+# ---------------------------------------------------------------- activation quantiser (FP4 x FP4 variant)
+
+def test_e4m3_encoder_matches_torch():
+    vals = _E4M3_NONNEG_VALUES()
+    mids = (vals[:-1] + vals[1:]) / 2                        # every tie
+    rng = np.random.default_rng(3)
+    v = np.concatenate([vals, mids, rng.uniform(0, 448, 5000), rng.uniform(0, 2 ** -5, 2000)]).astype(np.float32)
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode_nonneg(v), want)
+    # saturation above the largest finite value
+    assert np.all(O.e4m3_encode_nonneg(np.array([448.0, 460.0, 1e6], np.float32)) == 126)
+
+
+def _E4M3_NONNEG_VALUES():
+    return np.array([O.e4m3_value(b) for b in range(127)])
+
+
+_E2M1_VALUES = np.array([O.e2m1_value(c) for c in range(16)])
+_E4M3_VALUES = np.array([O.e4m3_value(b) for b in range(256)])
+
+
+def test_e2m1_encoder_picks_the_nearest_value_ties_to_even():
+    # hand-worked ties (the midpoints of the e2m1 grid) and saturation
+    cases = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6, 6.0: 7, 7.0: 7, 100.0: 7,
+             0.26: 1, 0.74: 1, 2.49: 4, 2.51: 5, -0.25: 8, -0.76: 10, -6.5: 15, 0.0: 0}
+    v = np.array(list(cases), np.float32)
+    assert O.e2m1_encode(v).tolist() == list(cases.values())
+    # away from ties: the decoded code is the nearest grid value (brute force)
+    rng = np.random.default_rng(4)
+    v = rng.uniform(-7, 7, 20000).astype(np.float32)
+    got = _E2M1_VALUES[O.e2m1_encode(v)]
+    grid = np.array([O.e2m1_value(c) for c in range(16)])
+    clipped = np.clip(v, -6, 6)
+    best = np.abs(clipped[:, None] - grid[None, :]).min(axis=1)
+    np.testing.assert_array_equal(np.abs(clipped - got), best)
+
+
+def test_fp4_activation_quantiser_round_trips_values_on_its_grid():
+    # blocks built from e2m1 values times an E4M3 scale s, each holding a 6:
+    # amax / 6 = s exactly, so every code is recovered (no row scale)
+    rng = np.random.default_rng(6)
+    n, K = 8, 128
+    scales = _E4M3_VALUES[rng.integers(8, 120, (n, K // 16))]
+    codes = rng.integers(0, 16, (n, K)).astype(np.uint8)
+    codes[:, ::16] = 7                                       # a +6 in every block
+    a = (_E2M1_VALUES[codes] * np.repeat(scales, 16, axis=1)).astype(np.float32)
+    c, sf, g = O.quantize_act_fp4(a, row_scale=False)
+    assert np.all(g == 1.0)
+    np.testing.assert_array_equal(_E4M3_VALUES[sf], scales)
+    np.testing.assert_array_equal(O.dequant_act_fp4(c, sf, g), a.astype(np.float64))
+    # with the row scale: g = amax / 2688 exactly (float32) and a row of +-6 * 448 * g returns itself
+    row = np.full((1, 32), 5376.0, np.float32)
+    row[0, 1::2] *= -1
+    c, sf, g = O.quantize_act_fp4(row, row_scale=True)
+    assert g[0] == np.float32(2.0) and np.all(_E4M3_VALUES[sf] == 448.0)
+    np.testing.assert_array_equal(O.dequant_act_fp4(c, sf, g), row.astype(np.float64))
+
+
+def test_fp4_activation_quantiser_error_bound():
+    # each element is within the e2m1 rounding of its block's scale, or the
+    # saturation the E4M3 rounding of the scale allows: <= 0.2 of the block's amax
+    rng = np.random.default_rng(8)
+    a = (rng.standard_normal((64, 256)) * np.exp(rng.uniform(-6, 6, (64, 1)))).astype(np.float32)
+    for row_scale in (True, False):
+        c, sf, g = O.quantize_act_fp4(a, row_scale)
+        d = O.dequant_act_fp4(c, sf, g)
+        amax = np.repeat(np.abs(a).reshape(64, 16, 16).max(axis=2), 16, axis=1)
+        ok = amax > 0.094 if not row_scale else amax > 0       # without a row scale: E4M3's normal range
+        assert np.all(np.abs(d - a)[ok] <= 0.2 * amax[ok])
+    z = np.zeros((2, 32), np.float32)
+    c, sf, g = O.quantize_act_fp4(z, True)
+    assert np.all(O.dequant_act_fp4(c, sf, g) == 0) and np.all(g == 1.0)
 
 
 def test_single_expert_is_plain_swiglu_mlp():
