@@ -3,8 +3,12 @@
 Routing indices, permutations, slot plans and cache counters must match
 bit-exactly.  Gates must agree to 1e-6.  Layer outputs must be within the
 stated max relative error of 2e-2: max|out - ref| / max|ref| per call, with
-bf16 activations; the element-wise relative error, with an absolute floor at
-1e-3 of the call's largest output, is checked beside it.  The GEMM
+bf16 activations.  Beside it the element-wise relative error is checked with
+an absolute floor at 1e-2 of the call's largest output, and reported with a
+floor at 1e-3: where the GPU's fp32 h and the oracle's exact h round to
+neighbouring bf16 values, every output of that row moves by W_d * ulp(h),
+about 1e-4 of the largest output, which near a zero crossing is large
+against a 1e-3 floor.  The GEMM
 accumulation is checked on the kernel's own operands against float64
 products: the down projection y within 1e-3 (norm-wise, per expert), and the
 gate/up result h = bf16(silu(W_g x) * (W_u x)) within one bf16 ulp per element
@@ -43,8 +47,9 @@ def _report_errors():
     yield
     if ERRS:
         a = np.array(ERRS)
-        print(f"\noutput errors over {len(a)} checked calls: norm-wise max {a[:, 0].max():.3e}, "
-              f"element-wise (floor 1e-3 of max) max {a[:, 1].max():.3e}, median {np.median(a[:, 1]):.3e}")
+        print(f"\noutput errors over {len(a)} checked calls: norm-wise max {a[:, 0].max():.3e}; element-wise "
+              f"with a floor at 1e-2 of the largest output: max {a[:, 1].max():.3e}, median {np.median(a[:, 1]):.3e}; "
+              f"with a floor at 1e-3: max {a[:, 2].max():.3e}, median {np.median(a[:, 2]):.3e}")
 
 
 # ------------------------------------------------------------ stateless steps
@@ -170,9 +175,9 @@ def _check_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=False, fmt=None,
     got = Hn.out_to_f64(out)[ref["out_tokens"]]
     err = Hn.rel_err(got, ref["out"])
     assert err <= OUT_TOL, err
-    elem = Hn.elem_rel_err(got, ref["out"])
+    elem = Hn.elem_rel_err(got, ref["out"], floor=1e-2)
+    ERRS.append((err, elem, Hn.elem_rel_err(got, ref["out"], floor=1e-3)))
     assert elem <= ELEM_TOL, elem
-    ERRS.append((err, elem))
     if gateup or gemm_check:
         # the GEMM accumulation on the kernel's own operands (sampled tokens' rows only, when sampled)
         tset = None if tokens is None else set(int(t) for t in tokens)
