@@ -3,12 +3,14 @@
 Routing indices, permutations, slot plans and cache counters must match
 bit-exactly.  Gates must agree to 1e-6.  Layer outputs must be within the
 stated max relative error of 2e-2: max|out - ref| / max|ref| per call, with
-bf16 activations.  Beside it the element-wise relative error is checked with
-an absolute floor at 1e-2 of the call's largest output, and reported with a
-floor at 1e-3: where the GPU's fp32 h and the oracle's exact h round to
-neighbouring bf16 values, every output of that row moves by W_d * ulp(h),
-about 1e-4 of the largest output, which near a zero crossing is large
-against a 1e-3 floor.  The GEMM
+bf16 activations.  Beside it the element-wise relative error against the
+oracle is reported, with an absolute floor at 1e-2 and at 1e-3 of the call's
+largest output (bounded loosely at 1e-1 with the 1e-2 floor): where the GPU's
+fp32 h and the oracle's exact h round to neighbouring bf16 values, every
+output of that row moves by W_d * ulp(h), about 1e-4 of the largest output.
+The tight element-wise check takes that out: the layer output must be within
+one bf16 ulp (plus 1e-5 of the largest output, for the order of fp32 sums)
+of the float64 down projection and combine of the kernel's own h.  The GEMM
 accumulation is checked on the kernel's own operands against float64
 products: the down projection y within 1e-3 (norm-wise, per expert), and the
 gate/up result h = bf16(silu(W_g x) * (W_u x)) within one bf16 ulp per element
@@ -34,7 +36,7 @@ if not torch.cuda.is_available():
 import expert_cache_host_softmax_b300 as F  # noqa: E402
 
 OUT_TOL = 2e-2
-ELEM_TOL = 5e-2
+ELEM_TOL = 1e-1
 GEMM_TOL = 1e-3
 GATE_TOL = 1e-6
 
@@ -155,6 +157,20 @@ def _down_check(orc, layer, ref, hg, y, rows_of):
         assert Hn.rel_err(y[rows].astype(np.float64), hg[rows] @ Wd.T) <= GEMM_TOL
 
 
+def _combine_check(orc, layer, ref, hg, got):
+    """Each checked token's output against sum_j gate_j * (W_d(e_j) . h_gpu[pair j])
+    in float64 on the kernel's own bf16 h: within one bf16 ulp of that value
+    plus 1e-5 of the largest (the final rounding and the order of fp32 sums)."""
+    k = orc.k
+    want = np.zeros_like(got)
+    for r, t in enumerate(ref["out_tokens"]):
+        for j in range(k):
+            _, _, Wd = orc.weights(layer * orc.E + int(ref["idx"][t, j]))
+            want[r] += float(ref["gates"][t, j]) * (Wd @ hg[int(ref["inv"][t * k + j])])
+    tol = Hn.bf16_ulp(want) + 1e-5 * float(np.abs(want).max())
+    assert np.all(np.abs(got - want) <= tol), float((np.abs(got - want) / tol).max())
+
+
 def _check_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=False, fmt=None, outs=None, gateup=False):
     xd, lgd = Hn.to_dev(x, lg)
     out = gpu.forward(layer, xd, lgd)
@@ -191,6 +207,7 @@ def _check_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=False, fmt=None,
         _gateup_check(orc, layer, x, ref, hg, rows_of)
         if gemm_check:
             _down_check(orc, layer, ref, hg, y, rows_of)
+        _combine_check(orc, layer, ref, hg, got)
     return err
 
 
