@@ -22,6 +22,8 @@ FMT = {"bf16": FT_FMT_BF16, "nvfp4": FT_FMT_NVFP4, "mxfp4": FT_FMT_MXFP4, "fp8":
 FT_MODE_LRU, FT_MODE_STREAM = 0, 1
 FT_FFN_AUTO, FT_FFN_GEMV, FT_FFN_TC = 0, 1, 2
 FFN_KERNEL = {"auto": FT_FFN_AUTO, "gemv": FT_FFN_GEMV, "tc": FT_FFN_TC}
+FT_ACT_BF16, FT_ACT_FP4 = 0, 1
+ACT_FORMAT = {"bf16": FT_ACT_BF16, "fp4": FT_ACT_FP4}
 FT_MISS_COPY, FT_MISS_PULL, FT_MISS_KERNEL, FT_MISS_AUTO = 0, 1, 2, 3
 MISS_PATH = {"copy": FT_MISS_COPY, "pull": FT_MISS_PULL, "kernel": FT_MISS_KERNEL, "auto": FT_MISS_AUTO}
 FT_OK, FT_ERR_ARG, FT_ERR_CUDA, FT_ERR_OOM, FT_ERR_NOT_PINNED = 0, -1, -2, -3, -4
@@ -35,6 +37,7 @@ EXPORTED = ("ft_moe_blob_bytes", "ft_moe_create", "ft_moe_load_pool", "ft_moe_se
             "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_set_ffn_kernel", "ft_moe_last_ffn_kernel", "ft_moe_set_miss_path", "ft_moe_miss_path", "ft_moe_set_decode_fusion", "ft_moe_set_keep_activations", "ft_moe_resize_slots",
             "ft_moe_set_prefill_hit_d2d", "ft_moe_prefill_hit_d2d",
             "ft_moe_slot_stride", "ft_moe_kernel_launches",
+            "ft_moe_set_act_format", "ft_moe_act_format", "ft_moe_last_act_fp4", "ft_fp4_tensor_peak",
             "ft_last_error", "ft_moe_destroy", "ft_topk_softmax", "ft_permute_workspace_bytes", "ft_permute", "ft_permute_noalloc")
 
 
@@ -87,6 +90,10 @@ def lib():
         L.ft_moe_prefill_hit_d2d.argtypes = [vp]
         L.ft_moe_set_miss_path.argtypes = [vp, i32]
         L.ft_moe_set_decode_fusion.argtypes = [vp, i32]
+        L.ft_moe_set_act_format.argtypes = [vp, i32]
+        L.ft_moe_act_format.argtypes = [vp]
+        L.ft_moe_last_act_fp4.argtypes = [vp, vp, vp, vp, vp, vp]
+        L.ft_fp4_tensor_peak.argtypes = [i32, i32, P(ctypes.c_double)]
         L.ft_moe_kernel_launches.restype = i64
         L.ft_moe_kernel_launches.argtypes = [vp]
         L.ft_moe_slot_stride.restype = i64
@@ -266,6 +273,27 @@ class MoELayerStack:
         inv = {v: k_ for k_, v in MISS_PATH.items()}
         return inv.get(int(lib().ft_moe_miss_path(self._h, 1 if tensor_core else 0)))
 
+    def set_act_format(self, fmt):
+        """"bf16" (default) or "fp4": tensor-core calls quantise x and h to NVFP4 and
+        multiply FP4 x FP4 (ft_moe_set_act_format; NVFP4 weights only)."""
+        w = ACT_FORMAT[fmt] if isinstance(fmt, str) else int(fmt)
+        _check(lib().ft_moe_set_act_format(self._h, w), self._h)
+
+    @property
+    def act_format(self):
+        return {FT_ACT_BF16: "bf16", FT_ACT_FP4: "fp4"}.get(int(lib().ft_moe_act_format(self._h)))
+
+    def last_act_fp4(self, T):
+        """The last call's quantised activations, permuted order: dict of x_codes u8
+        [T*k, H/2], x_sf u8 [T*k, H/16], x_g f32 [T*k], h_codes u8 [T*k, I/2], h_sf u8 [T*k, I/16]."""
+        n = T * self.k
+        out = dict(x_codes=np.zeros((n, self.H // 2), np.uint8), x_sf=np.zeros((n, self.H // 16), np.uint8),
+                   x_g=np.zeros(n, np.float32), h_codes=np.zeros((n, self.I // 2), np.uint8),
+                   h_sf=np.zeros((n, self.I // 16), np.uint8))
+        _check(lib().ft_moe_last_act_fp4(self._h, *(ctypes.c_void_p(out[k_].ctypes.data) for k_ in
+                                                  ("x_codes", "x_sf", "x_g", "h_codes", "h_sf"))), self._h)
+        return out
+
     @property
     def last_ffn_kernel(self):
         return {FT_FFN_GEMV: "gemv", FT_FFN_TC: "tc"}.get(int(lib().ft_moe_last_ffn_kernel(self._h)))
@@ -277,6 +305,14 @@ class MoELayerStack:
     @property
     def slot_stride(self):
         return int(lib().ft_moe_slot_stride(self._h))
+
+
+def fp4_tensor_peak(n_tile=256, iters=20000):
+    """Block-scaled FP4 tensor-core rate of the current device (TFLOP/s), measured
+    by the library's one-kernel probe (ft_fp4_tensor_peak)."""
+    v = ctypes.c_double()
+    _check(lib().ft_fp4_tensor_peak(int(n_tile), int(iters), ctypes.byref(v)))
+    return v.value
 
 
 def topk_softmax(logits, k, stream=None):

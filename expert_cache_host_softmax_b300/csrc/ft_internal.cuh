@@ -196,6 +196,25 @@ cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, int 
 cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const void *map_h, const void *map_gu,
                           const void *map_d, int *err, int64_t max_rows, cudaStream_t s);
 
+// FP4 x FP4 variant of the tensor-core FFN (gemm_fp4.cu).  Buffers over
+// expert-padded rows (see fp4_padded_rows): x and h as e2m1 codes [rows][K/2],
+// their E4M3 block scales as 512-byte atoms (128 rows x 4 blocks), x's fp32
+// row scales.
+struct Fp4Bufs {
+  uint8_t *xq, *xsf;
+  float *xg;
+  uint8_t *hq, *hsf;
+};
+void fp4_init_attributes();
+int64_t fp4_padded_rows(int64_t rows, int64_t umax);
+cudaError_t launch_quant_x(const __nv_bfloat16 *x, const PlanBufs &plan, int T, int k, int H, uint8_t *xq,
+                           uint8_t *xsf, float *xg, cudaStream_t s);
+cudaError_t launch_tc_ffn_fp4(const FfnArgs &f, bool down, const Fp4Bufs &q, const void *map_a, const void *map_b,
+                              int *err, int64_t max_rows, cudaStream_t s);
+int make_fp4_maps(const uint8_t *slots, int64_t slot_stride, int S, int H, int I, const void *xq, const void *hq,
+                  int64_t rows, void *map_xq, void *map_hq, void *map_gu, void *map_d);
+double fp4_peak_ms(int n_tile, int iters, int *err, cudaStream_t s);
+
 // Programmatic dependent launch.  A kernel launched with `pdl` may start
 // while the previous kernel on its stream is still running; it must execute
 // pdl_wait() before touching anything that kernel writes (pdl_wait returns

@@ -109,6 +109,13 @@ struct ft_moe {
   int32_t *seq_ring = nullptr;       // pinned: seq_ring[seq % 64] = seq, the source of the copy-flag write
   bool decode_fused = false;   // ft_moe_set_decode_fusion
   int miss_path = FT_MISS_AUTO;
+  // FP4 x FP4 variant of the tensor-core FFN (ft_moe_set_act_format): buffers
+  // over expert-padded rows and their TMA maps (xq, hq, gate/up codes, down codes)
+  int act_fmt = FT_ACT_BF16;
+  Fp4Bufs q{};
+  int64_t q_rows = 0;
+  alignas(64) unsigned char qmap[4][128] = {};
+  bool qmaps_ok = false;
   std::string err;
 };
 
@@ -179,6 +186,11 @@ void free_all(ft_moe *h) {
   cudaFree(h->pool_dev);
   cudaFree(h->mega_sync);
   cudaFree(h->copy_sync);
+  cudaFree(h->q.xq);
+  cudaFree(h->q.xsf);
+  cudaFree(h->q.xg);
+  cudaFree(h->q.hq);
+  cudaFree(h->q.hsf);
   if (h->mirror_host) cudaFreeHost(h->mirror_host);
   if (h->seq_ring) cudaFreeHost(h->seq_ring);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
@@ -258,6 +270,16 @@ bool use_tc(const ft_moe *h, int T) {
 
 cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cudaStream_t s,
                     const CombineArgs &cb = CombineArgs{}) {
+  if (tc && h->act_fmt == FT_ACT_FP4) {
+    if (!down && fa.only != 2) {
+      // x quantised once per token into the expert-padded rows (before the first gate/up launch)
+      cudaError_t e = launch_quant_x(fa.x, fa.plan, T, h->k, h->H, h->q.xq, h->q.xsf, h->q.xg, s);
+      if (e != cudaSuccess) return e;
+      h->kernel_launches += 1;
+    }
+    return launch_tc_ffn_fp4(fa, down, h->q, h->qmap[down ? 1 : 0], h->qmap[down ? 3 : 2], h->err_dev,
+                             (int64_t)T * h->k, s);
+  }
   if (tc) {
     if (!down && fa.only != 2) {
       // the permuted x rows, once per call (before the first gate/up launch)
@@ -605,6 +627,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
   route_init_attributes();
   ffn_init_attributes();
   gemm_init_attributes();
+  fp4_init_attributes();
   // the tensor-core FFN takes BF16, NVFP4 and MXFP4 (FP8 experts run on the GEMV)
   h->tmaps_ok =
                 make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
@@ -737,6 +760,10 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
                 make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
                 make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
                 make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
+  if (h->q.xq)
+    h->qmaps_ok = make_fp4_maps(h->slots, h->slot_stride, h->S, h->H, h->I, h->q.xq, h->q.hq, h->q_rows, h->qmap[0],
+                                h->qmap[1], h->qmap[2], h->qmap[3]) == 0;
+  if (h->act_fmt == FT_ACT_FP4 && !h->qmaps_ok) h->act_fmt = FT_ACT_BF16;
   return FT_OK;
 }
 
@@ -1156,6 +1183,85 @@ int ft_moe_set_miss_path(ft_moe *h, int path) {
   return FT_OK;
 }
 
+// FP4 x FP4 variant ("The Real Requirement Is System RAM": NVFP4 = 4-bit
+// values with an 8-bit scale per 16 weights; the activations take the same
+// layout here).  Buffers over expert-padded rows are allocated on first use.
+int ft_moe_set_act_format(ft_moe *h, int act_fmt) {
+  if (!h || (act_fmt != FT_ACT_BF16 && act_fmt != FT_ACT_FP4)) return fail(h, FT_ERR_ARG, "NULL handle or bad act_fmt");
+  if (int rc = sync_handle(h)) return rc;
+  if (act_fmt == FT_ACT_BF16) {
+    h->act_fmt = act_fmt;
+    return FT_OK;
+  }
+  if (h->fmt != FMT_NVFP4) return fail(h, FT_ERR_ARG, "FP4 activations need NVFP4 weights");
+  FT_CUDA(h, cudaSetDevice(h->device));
+  if (!h->q.xq) {
+    const int64_t rows = fp4_padded_rows((int64_t)h->Tmax * h->k, h->umax);
+    Fp4Bufs q{};
+    const bool ok = cudaMalloc(&q.xq, (size_t)rows * h->H / 2) == cudaSuccess &&
+                    cudaMalloc(&q.xsf, (size_t)rows * h->H / 16) == cudaSuccess &&
+                    cudaMalloc(&q.xg, (size_t)rows * sizeof(float)) == cudaSuccess &&
+                    cudaMalloc(&q.hq, (size_t)rows * h->I / 2) == cudaSuccess &&
+                    cudaMalloc(&q.hsf, (size_t)rows * h->I / 16) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      cudaFree(q.xq);
+      cudaFree(q.xsf);
+      cudaFree(q.xg);
+      cudaFree(q.hq);
+      cudaFree(q.hsf);
+      return fail(h, FT_ERR_OOM, "device allocation of the FP4 activation buffers failed");
+    }
+    h->q = q;
+    h->q_rows = rows;
+    h->qmaps_ok = make_fp4_maps(h->slots, h->slot_stride, h->S, h->H, h->I, h->q.xq, h->q.hq, rows, h->qmap[0],
+                                h->qmap[1], h->qmap[2], h->qmap[3]) == 0;
+  }
+  if (!h->qmaps_ok) return fail(h, FT_ERR_CUDA, "FP4 TMA descriptors could not be encoded");
+  h->act_fmt = act_fmt;
+  return FT_OK;
+}
+
+int ft_moe_act_format(const ft_moe *h) { return h ? h->act_fmt : -1; }
+
+int ft_moe_last_act_fp4(ft_moe *h, uint8_t *x_codes, uint8_t *x_sf, float *x_g, uint8_t *h_codes, uint8_t *h_sf) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  if (!h->q.xq || !h->last_tc || h->act_fmt != FT_ACT_FP4)
+    return fail(h, FT_ERR_STATE, "the last forward did not run the FP4 x FP4 FFN");
+  const int T = h->last_T, k = h->k, E = h->E, H = h->H, I = h->I;
+  const size_t TK = (size_t)T * k;
+  if (TK == 0) return FT_OK;
+  std::vector<int32_t> off(E + 1);
+  FT_CUDA(h, cudaMemcpy(off.data(), h->plan.offsets, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToHost));
+  std::vector<int64_t> pad(E + 1, 0);
+  for (int e = 0; e < E; ++e) pad[e + 1] = pad[e] + (off[e + 1] - off[e] + 127) / 128 * 128;
+  const int64_t rows = pad[E];
+  std::vector<uint8_t> xq((size_t)rows * H / 2), xsf((size_t)rows * H / 16), hq((size_t)rows * I / 2),
+      hsf((size_t)rows * I / 16);
+  std::vector<float> xg(rows);
+  FT_CUDA(h, cudaMemcpy(xq.data(), h->q.xq, xq.size(), cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(xsf.data(), h->q.xsf, xsf.size(), cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(xg.data(), h->q.xg, xg.size() * sizeof(float), cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(hq.data(), h->q.hq, hq.size(), cudaMemcpyDeviceToHost));
+  FT_CUDA(h, cudaMemcpy(hsf.data(), h->q.hsf, hsf.size(), cudaMemcpyDeviceToHost));
+  auto atom = [](int64_t r, int b, int K) {
+    return ((size_t)(r >> 7) * (K >> 6) + (b >> 2)) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (b & 3);
+  };
+  for (int e = 0; e < E; ++e)
+    for (int p = off[e]; p < off[e + 1]; ++p) {
+      const int64_t r = pad[e] + (p - off[e]);
+      if (x_codes) std::memcpy(x_codes + (size_t)p * H / 2, xq.data() + (size_t)r * H / 2, H / 2);
+      if (h_codes) std::memcpy(h_codes + (size_t)p * I / 2, hq.data() + (size_t)r * I / 2, I / 2);
+      if (x_g) x_g[p] = xg[r];
+      if (x_sf)
+        for (int b = 0; b < H / 16; ++b) x_sf[(size_t)p * (H / 16) + b] = xsf[atom(r, b, H)];
+      if (h_sf)
+        for (int b = 0; b < I / 16; ++b) h_sf[(size_t)p * (I / 16) + b] = hsf[atom(r, b, I)];
+    }
+  return FT_OK;
+}
+
 int64_t ft_moe_slot_stride(const ft_moe *h) { return h ? h->slot_stride : -1; }
 
 int64_t ft_moe_kernel_launches(const ft_moe *h) { return h ? h->kernel_launches : -1; }
@@ -1177,6 +1283,27 @@ int ft_topk_softmax(const float *router_logits, int T, int E, int k, int32_t *to
   if (T > 0 && (!router_logits || !topk_idx || !gates)) return fail(nullptr, FT_ERR_ARG, "NULL pointer");
   cudaError_t e = launch_topk_only(router_logits, T, E, k, topk_idx, gates, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FT_OK : cuda_fail(nullptr, e, "topk kernel");
+}
+
+int ft_fp4_tensor_peak(int n_tile, int iters, double *tflops) {
+  if ((n_tile != 128 && n_tile != 256) || iters < 1 || !tflops)
+    return fail(nullptr, FT_ERR_ARG, "n_tile must be 128 or 256, iters >= 1, tflops not NULL");
+  int *err = nullptr;
+  if (cudaMalloc(&err, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(nullptr, FT_ERR_OOM, "device allocation failed");
+  }
+  cudaMemset(err, 0, sizeof(int));
+  fp4_init_attributes();
+  const double ms = fp4_peak_ms(n_tile, iters, err, nullptr);
+  int code = 0;
+  cudaError_t e = cudaMemcpy(&code, err, sizeof code, cudaMemcpyDeviceToHost);
+  cudaFree(err);
+  if (ms < 0 || e != cudaSuccess) return cuda_fail(nullptr, e != cudaSuccess ? e : cudaGetLastError(), "fp4 peak kernel");
+  if (code != 0) return fail(nullptr, FT_ERR_DEVICE, "fp4 peak kernel gave up its bounded wait");
+  const double flops = (double)tc_num_sms() * iters * 4 * 2.0 * 128 * n_tile * 64;
+  *tflops = flops / (ms * 1e-3) / 1e12;
+  return FT_OK;
 }
 
 size_t ft_permute_workspace_bytes(int T, int k, int E) {

@@ -39,10 +39,13 @@
 #include <algorithm>
 
 #include "ft_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace ftmoe {
 
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128;          // token rows per tile (one TMEM lane each)
 constexpr int BN = 256;          // weight rows per tile (MMA N)
@@ -51,7 +54,6 @@ constexpr int kEpiWarps = 4;
 constexpr int A_STAGE = BM * BK * 2;          // 16 KB
 constexpr int B_STAGE = BN * BK * 2;          // 32 KB
 constexpr uint32_t kTmemCols = 512;           // two accumulators of BN fp32 columns
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxU = kMaxExperts;
 
 template <int FMT>
@@ -97,200 +99,12 @@ struct GemmArgs {
   int keep_y;               // down with out_acc: store y as well
 };
 
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Waits for the phase of `bar` with the given parity to complete.  Gives up
-// after kWaitLimitNs, or as soon as the CTA's abort flag is up: returns false,
-// and on a timeout records `where` in the error word and raises the flag.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err,
-                                       int where) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicCAS(err, 0, where);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
-                                            int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-      "[%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D[tmem] (+)= A[smem] . B[smem]^T, both K-major bf16, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrives once on `bar` when every tcgen05.mma this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// 16 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (SBO), descriptor version 1 (sm_100 family).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;             // LBO (unused for swizzled K-major)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;     // SBO
-  d |= static_cast<uint64_t>(1) << 46;             // version
-  d |= static_cast<uint64_t>(2) << 61;             // SWIZZLE_128B
-  return d;
-}
+// ------------------------------------------------------------------ instruction descriptor
 
 // Instruction descriptor: kind::f16, A = B = bf16, D = f32, K-major A and B,
 // N = BN, M = BM.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                             ((uint32_t)(BM >> 4) << 24);
-
-// Two e2m1 codes (one byte) -> two halves.
-__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
-  uint32_t out;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
-      : "=r"(out)
-      : "r"(byte));
-  return __half22float2(*reinterpret_cast<__half2 *>(&out));
-}
-
-__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
-  uint32_t out;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %1;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
-      : "=r"(out)
-      : "r"(byte & 0xFFu));
-  return __low2float(*reinterpret_cast<__half2 *>(&out));
-}
-
-__device__ __forceinline__ float e8m0_to_float(uint32_t b) {
-  if (b == 0xFFu) return __int_as_float(0x7fc00000);
-  return __uint_as_float(b ? (b << 23) : 0x00400000u);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Eight e2m1 codes (one 32-bit word, element 2j in the low nibble of byte j)
-// times one block scale -> eight bf16 values (exact: at most 6 significant bits).
-__device__ __forceinline__ uint4 dequant8(uint32_t w, float s) {
-  uint4 o;
-  float2 a = e2m1x2_to_float2(w), b = e2m1x2_to_float2(w >> 8), c = e2m1x2_to_float2(w >> 16),
-         d = e2m1x2_to_float2(w >> 24);
-  o.x = pack_bf16x2(a.x * s, a.y * s);
-  o.y = pack_bf16x2(b.x * s, b.y * s);
-  o.z = pack_bf16x2(c.x * s, c.y * s);
-  o.w = pack_bf16x2(d.x * s, d.y * s);
-  return o;
-}
-
-// Eight E4M3 codes (two 32-bit words, byte j = element j) -> eight bf16
-// values (exact: E4M3 has 3 mantissa bits and an exponent range within bf16's).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
-  uint32_t out;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %1;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
-      : "=r"(out)
-      : "r"(two_bytes));
-  const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&out));
-  return pack_bf16x2(f.x, f.y);
-}
-
-__device__ __forceinline__ uint4 dequant8_e4m3(uint32_t lo, uint32_t hi) {
-  return make_uint4(e4m3x2_to_bf16x2(lo & 0xFFFFu), e4m3x2_to_bf16x2(lo >> 16), e4m3x2_to_bf16x2(hi & 0xFFFFu),
-                    e4m3x2_to_bf16x2(hi >> 16));
-}
 
 // ------------------------------------------------------------------ tiles
 
@@ -720,23 +534,6 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 template <int FMT, bool DOWN>
 void set_attr() {
   cudaFuncSetAttribute(gemm_kernel<FMT, DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<FMT>::kSmemAlloc);
@@ -763,6 +560,19 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *_
 }
 
 }  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
 
 static_assert(Cfg<FMT_BF16>::kSmemAlloc <= 227 * 1024, "bf16 smem");
 static_assert(Cfg<FMT_NVFP4>::kSmemAlloc <= 227 * 1024, "fp4 smem");
@@ -794,7 +604,7 @@ void gemm_init_attributes() {
 // Tensor map over a bf16 activation matrix [rows][K] (the permuted x rows,
 // or h): box of 64 K x 128 rows with the 128-byte swizzle.
 int make_act_map(const void *base, int64_t rows, int K, void *map) {
-  EncodeTiledFn enc = encode_fn();
+  EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return -1;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows}, strides[1] = {(cuuint64_t)K * 2};
   cuuint32_t box[2] = {BK, BM}, estr[2] = {1, 1};
@@ -809,7 +619,7 @@ int make_act_map(const void *base, int64_t rows, int K, void *map) {
 // FP8: raw code bytes, box 64 x 128.
 int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, int H, int I, void *map_gu,
                      void *map_d) {
-  EncodeTiledFn enc = encode_fn();
+  EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return -1;
   const BlobLayout L = blob_layout(fmt, H, I);
   for (int which = 0; which < 2; ++which) {

@@ -284,6 +284,56 @@ int ft_moe_set_ffn_kernel(ft_moe *h, int which);
  * (-1 for NULL). */
 int ft_moe_last_ffn_kernel(const ft_moe *h);
 
+/* ---- FP4 x FP4 tensor-core FFN ----
+ * "FreeToken: Run Frontier MoE Models on Your Own GPU, and the RAM It Takes",
+ * section "The Real Requirement Is System RAM": NVFP4 stores 4-bit values
+ * with an 8-bit scale for every 16 weights.  The pages say nothing about the
+ * precision of the activations.  With FT_ACT_FP4, tensor-core calls (FT_FFN_TC,
+ * or AUTO's choice for prefill-sized calls) also quantise the activations to
+ * that layout and multiply FP4 x FP4 on the block-scaled tensor cores
+ * (tcgen05.mma kind::mxf4nvf4, fp32 accumulation):
+ *   x (per token): g = amax(row) / (6 * 448) (1 for an all-zero row);
+ *                  scale s_b = E4M3_rn((amax(block of 16) / 6) / g);
+ *                  code q = e2m1_rn(x / (s_b * g)) (0 where s_b * g is 0);
+ *                  the GEMM multiplies its fp32 result by g (and the weights'
+ *                  global scales);
+ *   h (per row, in the gate/up epilogue, from its fp32 value): the same with
+ *                  g = 1, i.e. E4M3 block scales alone -- so h blocks whose
+ *                  largest magnitude is below 6 * 2^-6 (about 0.094) get
+ *                  subnormal scales and lose precision, and below 6 * 2^-10
+ *                  they quantise to zero.
+ * Every decision (amax, divisions, roundings: nearest, ties to even,
+ * saturating) is taken in IEEE binary32.  GEMV calls (decode) keep bf16
+ * activations.  Only NVFP4 weights: FT_ERR_ARG for other formats.  The
+ * first FT_ACT_FP4 call allocates 5 device buffers over (max_tokens * top_k
+ * + 128 * min(E, max_tokens * top_k)) rows: about 0.6 * hidden + 0.6 * inter
+ * bytes per row.  Synchronises the handle.  Errors: FT_ERR_ARG, FT_ERR_OOM,
+ * FT_ERR_CUDA, FT_ERR_DEVICE. */
+enum ft_act_format { FT_ACT_BF16 = 0, FT_ACT_FP4 = 1 };
+int ft_moe_set_act_format(ft_moe *h, int act_fmt);
+
+/* The current activation format (FT_ACT_BF16 or FT_ACT_FP4; -1 for NULL). */
+int ft_moe_act_format(const ft_moe *h);
+
+/* The quantised activations of the last forward call, which must have run
+ * the FP4 x FP4 FFN (else FT_ERR_STATE), for the T*k (token, rank) pairs in
+ * permuted order (position i of ft_moe_last_routing's perm):
+ *   x_codes u8 [T*k][hidden/2]  e2m1 codes of x (element 2j in the low nibble of byte j)
+ *   x_sf    u8 [T*k][hidden/16] E4M3 block scales of x
+ *   x_g     f32 [T*k]           x's row scale g
+ *   h_codes u8 [T*k][inter/2], h_sf u8 [T*k][inter/16]  the same for h (no row scale)
+ * Any pointer may be NULL.  Host buffers, owned by the caller.  Synchronises
+ * the handle.  Errors: FT_ERR_ARG, FT_ERR_STATE, FT_ERR_CUDA, FT_ERR_DEVICE. */
+int ft_moe_last_act_fp4(ft_moe *h, uint8_t *x_codes, uint8_t *x_sf, float *x_g, uint8_t *h_codes, uint8_t *h_sf);
+
+/* Measures the block-scaled FP4 tensor-core rate of the current device: one
+ * CTA per SM issues `iters` x 4 MMAs (tcgen05.mma kind::mxf4nvf4, M = 128,
+ * N = n_tile (128 or 256), K = 64) on operands already in shared memory;
+ * *tflops = 2 * 128 * n_tile * 64 * 4 * iters * SMs / (CUDA-event time).
+ * Synchronous (default stream).  Errors: FT_ERR_ARG, FT_ERR_OOM, FT_ERR_CUDA,
+ * FT_ERR_DEVICE (ft_last_error(NULL) says which). */
+int ft_fp4_tensor_peak(int n_tile, int iters, double *tflops);
+
 /* How LRU-mode misses reach their slots. */
 enum ft_miss_path {
   FT_MISS_COPY = 0, /* cudaMemcpyAsync on the handle's copy streams, issued by the host once it has

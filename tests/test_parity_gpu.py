@@ -548,6 +548,140 @@ def test_auto_miss_path_resolution():
     big.close()
 
 
+# ------------------------------------------------------------ FP4 x FP4 tensor-core FFN
+
+_E2M1 = np.array([O.e2m1_value(c) for c in range(16)])
+_E4M3 = np.array([O.e4m3_value(b) for b in range(256)])
+
+
+def _fp4_values(codes, sf, g=None):
+    """Packed e2m1 codes [n, K/2] (element 2j in the low nibble), E4M3 block scales
+    [n, K/16] and row scales g [n] -> float64 values [n, K]."""
+    nib = np.empty((codes.shape[0], codes.shape[1] * 2), np.uint8)
+    nib[:, 0::2], nib[:, 1::2] = codes & 0x0F, codes >> 4
+    v = _E2M1[nib] * np.repeat(_E4M3[sf], 16, axis=1)
+    return v if g is None else v * np.asarray(g, np.float64)[:, None]
+
+
+def _check_fp4_call(gpu, orc, layer, x, lg, tokens=None, gemm_check=True):
+    """One forward with FP4 activations against the oracle's FP4 x FP4 layer:
+    routing and cache bit-exact; x's codes, block scales and row scales
+    bit-exact (the quantiser decides in float32 on both sides, from the same
+    bf16 x); h within one quantisation step of the oracle's quantiser applied
+    to the float64 h of the kernel's own x, in a small fraction of elements
+    (the two sides quantise h from float32 values that differ in their last
+    bits); y and the layer output against float64 products on the kernel's own
+    quantised h.  Returns the norm-wise output error."""
+    T, k = x.shape[0], orc.k
+    xd, lgd = Hn.to_dev(x, lg)
+    out = gpu.forward(layer, xd, lgd)
+    torch.cuda.synchronize()
+    assert gpu.last_ffn_kernel == "tc"
+    ref = orc.forward(layer, x, lg, tokens=tokens)
+    r = gpu.last_routing()
+    for key_ in ("idx", "offsets", "perm", "inv"):
+        assert np.array_equal(r[key_], ref[key_]), key_
+    assert gpu.trace() == [tuple(p) for p in ref["plan"]]
+    got = Hn.out_to_f64(out)[ref["out_tokens"]]
+    err = Hn.rel_err(got, ref["out"])
+    assert err <= OUT_TOL, err
+    q = gpu.last_act_fp4(T)
+    # x: bit-exact against the oracle's quantiser on the token rows
+    c_ref, sf_ref, g_ref = O.quantize_act_fp4(O.bf16_bits_to_f64(x), row_scale=True)
+    tok = ref["perm"] // k
+    xv_ref = O.dequant_act_fp4(c_ref, sf_ref, g_ref)[tok]
+    xv = _fp4_values(q["x_codes"], q["x_sf"], q["x_g"])
+    assert np.array_equal(q["x_sf"], sf_ref[tok])
+    assert np.array_equal(q["x_g"], g_ref[tok])
+    assert np.array_equal(xv, xv_ref)
+    # h: the oracle's quantiser on float32(h) computed in float64 from the kernel's own x
+    hv = _fp4_values(q["h_codes"], q["h_sf"])
+    y = gpu.last_activations(T)[1] if gemm_check else None
+    tset = None if tokens is None else set(int(t) for t in tokens)
+    diff = total = 0
+    for e in ref["experts"]:
+        lo, hi = int(ref["offsets"][e]), int(ref["offsets"][e + 1])
+        rows = np.array([p for p in range(lo, hi) if tset is None or int(ref["perm"][p]) // k in tset], np.int64)
+        if rows.size == 0:
+            continue
+        Wg, Wu, Wd = orc.weights(layer * orc.E + e)
+        h64 = O.silu(xv[rows] @ Wg.T) * (xv[rows] @ Wu.T)
+        hc, hs, hg = O.quantize_act_fp4(h64.astype(np.float32), row_scale=False)
+        href = O.dequant_act_fp4(hc, hs, hg)
+        step = 2.0 * np.repeat(np.maximum(_E4M3[q["h_sf"][rows]], _E4M3[hs]), 16, axis=1)
+        d = np.abs(hv[rows] - href)
+        assert np.all(d <= step), float((d / step).max())
+        assert np.all(np.abs(q["h_sf"][rows].astype(int) - hs.astype(int)) <= 1)
+        diff += int((d > 0).sum())
+        total += d.size
+        if gemm_check:
+            assert Hn.rel_err(y[rows].astype(np.float64), hv[rows] @ Wd.T) <= GEMM_TOL
+    assert diff <= 0.02 * total, (diff, total)
+    _combine_check(orc, layer, ref, hv, got)
+    ERRS.append((err, Hn.elem_rel_err(got, ref["out"], floor=1e-2), Hn.elem_rel_err(got, ref["out"], floor=1e-3)))
+    return err
+
+
+def _fp4_pair(H, E, k, I, S, L, T, seed, **kw):
+    gpu, orc, pool = Hn.make_pair(H, E, k, I, "nvfp4", S, L, T, seed, **kw)
+    gpu.set_ffn_kernel("tc")
+    gpu.set_act_format("fp4")
+    assert gpu.act_format == "fp4"
+    orc.act_fp4 = True
+    return gpu, orc, pool
+
+
+@pytest.mark.parametrize("H,I,E,k,T", [(256, 256, 8, 2, 300), (512, 768, 4, 2, 333), (1024, 512, 16, 4, 97),
+                                       (2048, 768, 8, 8, 40)])
+def test_tc_fp4_activations_match_oracle(H, I, E, k, T):
+    # several padded M tiles per expert with ragged tails, 2..12 N tiles, K of 1..8 stages
+    gpu, orc, _ = _fp4_pair(H, E, k, I, E, 1, T, 171 + H + T)
+    for step in range(2):
+        x, lg = Hn.inputs(171, T, H, E, step, 0)
+        _check_fp4_call(gpu, orc, 0, x, lg)
+    gpu.close()
+
+
+@pytest.mark.parametrize("path", ["copy", "kernel"])
+def test_tc_fp4_activations_with_lru_misses(path):
+    # hits and misses in separate gate/up launches; the quantised x is shared by both
+    H, I, E, k, T, L = 512, 256, 8, 2, 200, 3
+    gpu, orc, _ = _fp4_pair(H, E, k, I, E + 2, L, T, 177)
+    gpu.set_miss_path(path)
+    for step in range(2):
+        for layer in range(L):
+            x, lg = Hn.inputs(177, T, H, E, step, layer, zipf=0.5)
+            _check_fp4_call(gpu, orc, layer, x, lg, gemm_check=(layer == 1))
+    cum, _ = gpu.stats()
+    assert cum["misses"] > 0 and cum["misses"] == orc.stats["misses"]
+    gpu.close()
+
+
+def test_prefill35b_fp4_activations_full_size_sampled():
+    # the prefill layer at full size with FP4 activations; 32 sampled tokens
+    c = CONFIGS["prefill35b"]
+    T, H, E, k, I = c["T"], c["H"], c["E"], c["k"], c["I"]
+    gpu, orc, _ = _fp4_pair(H, E, k, I, c["S"], 1, T, c["seed"])
+    gpu.set_ffn_kernel("auto")
+    x, lg = Hn.inputs(c["seed"], T, H, E, 0, 0)
+    _check_fp4_call(gpu, orc, 0, x, lg, tokens=list(range(0, T, 128)), gemm_check=False)
+    gpu.close()
+
+
+def test_fp4_act_format_needs_nvfp4_weights():
+    gpu = F.MoELayerStack(256, 4, 1, 256, "mxfp4", 4, 1, 1)
+    with pytest.raises(F.FtError) as ei:
+        gpu.set_act_format("fp4")
+    assert ei.value.code == F.FT_ERR_ARG
+    gpu.close()
+
+
+def test_fp4_tensor_peak_probe_runs():
+    for n in (128, 256):
+        v = F.fp4_tensor_peak(n, 2000)
+        assert v > 0
+
+
 # ------------------------------------------------------------ the large decode and streaming shapes
 
 @pytest.mark.parametrize("path", ["auto", "kernel"])
