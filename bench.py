@@ -330,10 +330,25 @@ def _host_cpu():
 # prefill (PCIe bound).  Each gets its own device time, end-to-end time and
 # rooflines, under "workloads" in the same JSON line.
 EXTRA_WORKLOADS = (
-    ("prefill35b_bf16", "prefill35b", dict(fmt="bf16", steps=5, warmup=3, profile_steps=2, n_phys=128)),
-    ("prefill35b_nvfp4", "prefill35b", dict(fmt="nvfp4", steps=5, warmup=3, profile_steps=2, n_phys=128)),
-    ("stream753b", "stream753b", dict(fmt=None, steps=2, warmup=3, profile_steps=1, n_phys=512)),
+    ("prefill35b_bf16", "prefill35b", dict(fmt="bf16", act="bf16", steps=5, warmup=3, profile_steps=2, n_phys=128)),
+    ("prefill35b_nvfp4", "prefill35b", dict(fmt="nvfp4", act="bf16", steps=5, warmup=3, profile_steps=2, n_phys=128)),
+    ("prefill35b_nvfp4_fp4act", "prefill35b",
+     dict(fmt="nvfp4", act="fp4", steps=5, warmup=3, profile_steps=2, n_phys=128)),
+    ("stream753b", "stream753b", dict(fmt=None, act="bf16", steps=2, warmup=3, profile_steps=1, n_phys=512)),
 )
+
+_FP4_PEAK = {}
+
+
+def fp4_peak(n_tile=256):
+    """The block-scaled FP4 tensor-core rate measured by the library's probe
+    (ft_fp4_tensor_peak: MMAs on operands already in shared memory), best of 3
+    after one warm-up launch, TFLOP/s; cached per process."""
+    if n_tile not in _FP4_PEAK:
+        import expert_cache_host_softmax_b300 as F
+        F.fp4_tensor_peak(n_tile, 2000)
+        _FP4_PEAK[n_tile] = max(F.fp4_tensor_peak(n_tile, 20000) for _ in range(3))
+    return _FP4_PEAK[n_tile]
 
 
 def run_ours(args, cfg):
@@ -347,6 +362,10 @@ def run_ours(args, cfg):
     torch.cuda.set_device(dev)
     build()
     line = _measure(args, cfg, dev, ws, rank)
+    line["fp4_tensor_peak_tflops"] = {"n256": fp4_peak(256), "n128": fp4_peak(128),
+                                      "how": "ft_fp4_tensor_peak: one CTA per SM, tcgen05.mma kind::mxf4nvf4 "
+                                             "(M=128, K=64, E4M3 scale per 16) on operands in shared memory, "
+                                             "best of 3 launches of 20000 x 4 MMAs, CUDA events"}
     if rank == 0 and not args.no_cpu_baseline:
         tps, desc, calls, secs = _cpu_baseline(cfg, cfg["seed"], min(args.n_phys, cfg["L"] * cfg["E"]),
                                                budget_s=args.cpu_budget, fmt=args.fmt or cfg["fmt"])
@@ -355,7 +374,7 @@ def run_ours(args, cfg):
     if args.extras and ws == 1:
         line["workloads"] = {}
         for name, cname, opts in EXTRA_WORKLOADS:
-            sub = argparse.Namespace(**{**vars(args), **opts, "fmt": opts["fmt"], "hit_d2d_cache": 0,
+            sub = argparse.Namespace(**{**vars(args), **opts, "fmt": opts["fmt"], "act": opts["act"], "hit_d2d_cache": 0,
                                         "ffn": "auto", "miss_path": "auto", "fused_decode": False})
             try:
                 w = _measure(sub, CONFIGS[cname], dev, ws, rank, resize=False)
@@ -414,6 +433,9 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
         stack.set_miss_path(args.miss_path)
     if args.fused_decode:
         stack.set_decode_fusion(True)
+    fp4_act = getattr(args, "act", "bf16") == "fp4"
+    if fp4_act:
+        stack.set_act_format("fp4")
 
     W, K = args.warmup, args.steps
     n_prof = min(args.profile_steps, K)
@@ -604,9 +626,15 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
     share = {n: round(kern[n][1] / max(1e-9, sum(v[1] for v in kern.values())), 4) for n in kern}
     if ffn_kernel == "tc" and f_dom > 0:
         achieved = f_dom / (ms_dom * 1e-3) / 1e12 if ms_dom > 0 else 0.0
-        roofline = {"bound": "tensor", "kernel": f"{dom} (tcgen05 grouped GEMM, bf16 operands)", "achieved": achieved,
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "traffic": None, "peak_src": peaks["src"] + " bf16 burst",
+        if fp4_act:
+            t_peak, t_src = fp4_peak(256), "measured FP4 (ft_fp4_tensor_peak, N=256)"
+            t_kern = f"{dom} (tcgen05 block-scaled grouped GEMM, FP4 x FP4 operands)"
+        else:
+            t_peak, t_src = peaks["bf16_tflops"], peaks["src"] + " bf16 burst"
+            t_kern = f"{dom} (tcgen05 grouped GEMM, bf16 operands)"
+        roofline = {"bound": "tensor", "kernel": t_kern, "achieved": achieved,
+                    "peak": t_peak, "unit": "TFLOP/s", "frac": achieved / t_peak,
+                    "traffic": None, "peak_src": t_src,
                     "flops_per_call": f_dom / calls_p, "ms_per_call": ms_dom / calls_p,
                     "hbm_gbs_achieved": b_dom / (ms_dom * 1e-3) / 1e9 if ms_dom > 0 else 0.0,
                     "kernel_ms_share": share}
@@ -638,12 +666,14 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
     flops = 2 * 3 * H * I * k * tokens / K * L
     t_hbm = w_hbm / (peaks["hbm_gbs"] * 1e9)
     t_pcie = m_pcie / (pcie_gbs * 1e9)
-    t_flop = flops / (peaks["bf16_tflops"] * 1e12)
+    tensor_peak = fp4_peak(256) if fp4_act and ffn_kernel == "tc" else peaks["bf16_tflops"]
+    t_flop = flops / (tensor_peak * 1e12)
     t_roof = max(t_hbm, t_pcie, t_flop)
     path = {"t_step_ms": t_step * 1e3, "t_roof_ms": t_roof * 1e3, "frac": t_roof / t_step,
             "bound": ("hbm", "pcie", "tensor")[int(np.argmax([t_hbm, t_pcie, t_flop]))],
             "hbm_bytes_per_step": w_hbm, "pcie_bytes_per_step": m_pcie, "flops_per_step": flops,
-            "tensor_peak": "bf16 burst (measured)", "ffn_kernel": ffn_kernel,
+            "tensor_peak": "FP4 (measured by ft_fp4_tensor_peak)" if fp4_act and ffn_kernel == "tc"
+            else "bf16 burst (measured)", "ffn_kernel": ffn_kernel,
             "pcie_h2d_gbs_measured": pcie_gbs, "miss_copy_gbs_achieved": copy_gbs,
             "stream_copy_gbs_achieved": stream_gbs,
             "hits_per_step": d["hits"] / K, "misses_per_step": d["misses"] / K,
@@ -662,11 +692,13 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": {"nvfp4": "nvfp4-w/bf16-act/f32-acc", "mxfp4": "mxfp4-w/bf16-act/f32-acc",
-                  "fp8": "fp8-w/bf16-act/f32-acc"}.get(fmt, "bf16/f32-acc"),
+        "dtype": "nvfp4-w/nvfp4-act/f32-acc" if fp4_act else
+        {"nvfp4": "nvfp4-w/bf16-act/f32-acc", "mxfp4": "mxfp4-w/bf16-act/f32-acc",
+         "fp8": "fp8-w/bf16-act/f32-acc"}.get(fmt, "bf16/f32-acc"),
         "data": "synthetic",
         "config": {"workload": cfg["name"], "layers": L, "hidden": H, "experts": E, "top_k": k, "inter": I,
-                   "weight_fmt": fmt, "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
+                   "weight_fmt": fmt, "act_fmt": "fp4 on tensor-core calls" if fp4_act else "bf16",
+                   "slots": S, "tokens_per_step": T, "zipf_s": cfg["zipf"],
                    "mode": cfg["mode"],
                    "prefill_hit_d2d": {"cache_slots": d2d_cache} if d2d_cache > 0 else None,
                    "miss_path": stack.miss_path(ffn_kernel == "tc") if cfg["mode"] == "lru" else None,
@@ -702,6 +734,9 @@ def main():
     ap.add_argument("--fmt", choices=("bf16", "nvfp4", "mxfp4", "fp8"), default=None,
                     help="weight format (default: the workload's)")
     ap.add_argument("--ffn", choices=("auto", "gemv", "tc"), default="auto", help="FFN kernel")
+    ap.add_argument("--act", choices=("bf16", "fp4"), default="bf16",
+                    help="activations of tensor-core calls: bf16, or quantised to NVFP4 (FP4 x FP4 on the "
+                         "block-scaled tensor cores; NVFP4 weights)")
     ap.add_argument("--hit-d2d-cache", type=int, default=0,
                     help="streaming workloads: this many cache slots beside the two staging banks, with prefill "
                          "hit-D2D on (cached experts are staged from their slots, the rest from host memory)")
@@ -720,7 +755,7 @@ def main():
     cfg = CONFIGS[args.config]
     # the further workloads come with the default workload only
     args.extras = args.extras and args.config == "decode35b" and args.fmt is None and args.ffn == "auto" \
-        and args.miss_path == "auto" and not args.fused_decode
+        and args.miss_path == "auto" and not args.fused_decode and args.act == "bf16"
     if args.impl == "reference":
         run_reference(args, cfg)
     else:
