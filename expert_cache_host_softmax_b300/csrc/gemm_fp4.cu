@@ -12,7 +12,8 @@
 // Activation quantiser (all decisions in IEEE binary32):
 //   x rows: g = amax(row) / (6 * 448) (1 for an all-zero row),
 //           s_b = E4M3_rn((amax(block of 16) / 6) / g),
-//           q = e2m1_rn(x / (value(s_b) * g))   (0 where that product is 0)
+//           r_b = 1 / (value(s_b) * g)  (one rounding; 0 where the product is 0),
+//           q = e2m1_rn(x * r_b)
 //   h rows: the same with g = 1 (the E4M3 block scales alone).
 // x is quantised once per token and scattered to its k (token, rank) pairs in
 // an expert-padded row order: expert e's rows start at pad_start[e] =
@@ -36,7 +37,8 @@
 //   warp 1   MMA: tcgen05.cp of the stage's scale atoms, 4 MMAs of K = 64
 //            (M = 128, N = 128) into one of two TMEM accumulators;
 //   warp 2   B scales: loads the tile rows' scale bytes and stores them as atoms;
-//   warps 4-7 epilogue, one TMEM lane (tile row) per thread: gate/up applies
+//   warps 4-11 epilogue, one TMEM lane (tile row) per thread, two warps per
+//            lane quarter (each half of the tile's columns): gate/up applies
 //            the row's x scale and the NVFP4 global scales, SiLU * up, and
 //            quantises h (block scales, codes in padded order); down applies
 //            the global scale and adds gate * y into the token's fp32 output
@@ -70,7 +72,8 @@ constexpr int Q_BARS = 2 * QNS + 5;   // FULL, EMPTY per stage; TFULL x2, TEMPTY
 constexpr int Q_OFF_TAB = Q_OFF_BAR + Q_BARS * 8 + 16;
 constexpr int Q_SMEM = Q_OFF_TAB + 4 * 3 * (kMaxExperts + 1) + 64;
 constexpr int Q_SMEM_ALLOC = Q_SMEM + 1024;
-constexpr int Q_THREADS = 256;
+constexpr int Q_EPI_WARPS = 8;        // two per TMEM lane quarter, each half of a tile's columns
+constexpr int Q_THREADS = (4 + Q_EPI_WARPS) * 32;
 constexpr int Q_PROD = 0, Q_MMA = 1, Q_SFW = 2, Q_EPI0 = 4;
 constexpr uint32_t Q_TMEM_COLS = 512;  // accumulators 0 and 128; scale buffers from 256
 constexpr uint32_t Q_SFA_COL = 256, Q_SFB_COL = 288;   // + 16 * (stage parity)
@@ -152,13 +155,10 @@ __device__ __forceinline__ uint32_t quant16(const float *v, float g, uint32_t *q
   float sval;
   const uint32_t sc = e4m3_rn(__fdiv_rn(__fdiv_rn(amax, 6.0f), g), &sval);
   const float den = __fmul_rn(sval, g);
+  const float r = den > 0.0f ? __frcp_rn(den) : 0.0f;
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a = den > 0.0f ? __fdiv_rn(v[2 * i], den) : 0.0f;
-    const float b = den > 0.0f ? __fdiv_rn(v[2 * i + 1], den) : 0.0f;
-    w[i >> 2] |= e2m1x2_rn(a, b) << (8 * (i & 3));
-  }
+  for (int i = 0; i < 8; ++i) w[i >> 2] |= e2m1x2_rn(__fmul_rn(v[2 * i], r), __fmul_rn(v[2 * i + 1], r)) << (8 * (i & 3));
   q[0] = w[0];
   q[1] = w[1];
   return sc;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(TFULL(b), 1);
-      mbar_init(TEMPTY(b), 4 * 32);
+      mbar_init(TEMPTY(b), Q_EPI_WARPS * 32);
     }
     mbar_init(DRAIN, 1);
     *s_abort = 0;
@@ -489,7 +489,8 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
     __syncwarp();
   } else if (warp >= Q_EPI0) {
     // ================================================================ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                   // TMEM lane quarter
+    const int half = (warp - Q_EPI0) >> 2;    // which half of the tile's columns
     const int row = q * 32 + lane;
     int tl = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
@@ -502,12 +503,14 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
       const bool valid = row < ti.rows;
       const int prow = ti.prow0 + row;
       if constexpr (!DOWN) {
+        // this half: h columns 32*half .. +31 of the tile's 64 (gate column c, up column 64 + c)
         const float gx = valid ? a.xg[prow] : 0.0f;
         const float g0 = gs[0] * gx, g1 = gs[1] * gx;
-        uint32_t codes[8];
+        uint32_t codes[4];
         uint32_t scw = 0;
 #pragma unroll
-        for (int c = 0; c < QBN / 2; c += 16) {
+        for (int cb = 0; cb < 2; ++cb) {
+          const int c = 32 * half + 16 * cb;
           float gv[16], uv[16];
           tmem_ld16(tb + c, gv);
           tmem_ld16(tb + QBN / 2 + c, uv);
@@ -515,37 +518,36 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float gg = gv[i] * g0, uu = uv[i] * g1;
-            hv[i] = gg / (1.0f + expf(-gg)) * uu;
+            hv[i] = gg * __frcp_rn(1.0f + __expf(-gg)) * uu;
           }
           uint32_t qq[2];
           const uint32_t sc = quant16(hv, 1.0f, qq);
-          const int cb = c >> 4;
           codes[2 * cb] = qq[0];
           codes[2 * cb + 1] = qq[1];
           scw |= sc << (8 * cb);
         }
         if (valid) {
-          // this tile's 64 h columns = 32 code bytes and one group of 4 block scales
-          uint4 *dst = reinterpret_cast<uint4 *>(a.hq + (size_t)prow * (a.I / 2) + ti.n * 32);
-          dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-          dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-          *reinterpret_cast<uint32_t *>(a.hsf + sf_atom_off(prow, 4 * ti.n, a.I)) = scw;
+          // 32 h columns = 16 code bytes and 2 block scales
+          *reinterpret_cast<uint4 *>(a.hq + (size_t)prow * (a.I / 2) + ti.n * 32 + 16 * half) =
+              make_uint4(codes[0], codes[1], codes[2], codes[3]);
+          *reinterpret_cast<uint16_t *>(a.hsf + sf_atom_off(prow, 4 * ti.n + 2 * half, a.I)) = (uint16_t)scw;
         }
       } else {
         const float g0 = gs[2];
-        float *dst = a.y + (size_t)(ti.row0 + row) * a.H + ti.n * QBN;
+        const int c0 = half * (QBN / 2);
+        float *dst = a.y + (size_t)(ti.row0 + row) * a.H + ti.n * QBN + c0;
         float *acc = nullptr;
         float gw = 0.0f;
         if (a.out_acc != nullptr && valid) {
           const int pair = a.plan.perm[ti.row0 + row];
-          acc = a.out_acc + (size_t)(pair / a.k) * a.H + ti.n * QBN;
+          acc = a.out_acc + (size_t)(pair / a.k) * a.H + ti.n * QBN + c0;
           gw = a.plan.gates[pair] * g0;
         }
         const bool store_y = a.out_acc == nullptr || a.keep_y;
 #pragma unroll 1
-        for (int c = 0; c < QBN; c += 16) {
+        for (int c = 0; c < QBN / 2; c += 16) {
           float v[16];
-          tmem_ld16(tb + c, v);
+          tmem_ld16(tb + c0 + c, v);
           if (valid) {
             if (store_y) {
               float4 *o = reinterpret_cast<float4 *>(dst + c);

@@ -294,7 +294,8 @@ int ft_moe_last_ffn_kernel(const ft_moe *h);
  * (tcgen05.mma kind::mxf4nvf4, fp32 accumulation):
  *   x (per token): g = amax(row) / (6 * 448) (1 for an all-zero row);
  *                  scale s_b = E4M3_rn((amax(block of 16) / 6) / g);
- *                  code q = e2m1_rn(x / (s_b * g)) (0 where s_b * g is 0);
+ *                  r_b = 1 / (s_b * g), rounded once (0 where s_b * g is 0);
+ *                  code q = e2m1_rn(x * r_b);
  *                  the GEMM multiplies its fp32 result by g (and the weights'
  *                  global scales);
  *   h (per row, in the gate/up epilogue, from its fp32 value): the same with

@@ -402,7 +402,8 @@ def quantize_act_fp4(a: np.ndarray, row_scale: bool):
     element, block scales uint8 [n, K/16] E4M3, g float32 [n]), all in float32:
       g   = amax(row) / 2688 (6 * 448), or 1 for an all-zero row or without row_scale
       s_b = E4M3( (amax(block) / 6) / g )                  (nearest, ties to even)
-      q   = e2m1( a / (value(s_b) * g) )                   (0 where that product is 0)"""
+      r_b = 1 / (value(s_b) * g)                           (one rounding; 0 where the product is 0)
+      q   = e2m1( a * r_b )                                (nearest, ties to even)"""
     a = np.asarray(a, np.float32)
     n, K = a.shape
     f = np.float32
@@ -416,9 +417,9 @@ def quantize_act_fp4(a: np.ndarray, row_scale: bool):
     s = ((blocks / f(6.0)).astype(np.float32) / g[:, None]).astype(np.float32)
     sf = e4m3_encode_nonneg(s)
     denom = (_E4M3_TABLE[sf].astype(np.float32) * g[:, None]).astype(np.float32)
-    den_e = np.repeat(denom, 16, axis=1)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        v = np.where(den_e > 0, a / np.where(den_e > 0, den_e, f(1.0)), f(0.0)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        recip = np.where(denom > 0, f(1.0) / np.where(denom > 0, denom, f(1.0)), f(0.0)).astype(np.float32)
+    v = (a * np.repeat(recip, 16, axis=1)).astype(np.float32)
     return e2m1_encode(v), sf, g
 
 
