@@ -210,9 +210,10 @@ int64_t fp4_padded_rows(int64_t rows, int64_t umax);
 cudaError_t launch_quant_x(const __nv_bfloat16 *x, const PlanBufs &plan, int T, int k, int H, uint8_t *xq,
                            uint8_t *xsf, float *xg, cudaStream_t s);
 cudaError_t launch_tc_ffn_fp4(const FfnArgs &f, bool down, const Fp4Bufs &q, const void *map_a, const void *map_b,
-                              int *err, int64_t max_rows, cudaStream_t s);
+                              const void *map_sfb, int *err, int64_t max_rows, cudaStream_t s);
 int make_fp4_maps(const uint8_t *slots, int64_t slot_stride, int S, int H, int I, const void *xq, const void *hq,
-                  int64_t rows, void *map_xq, void *map_hq, void *map_gu, void *map_d);
+                  int64_t rows, void *map_xq, void *map_hq, void *map_gu, void *map_d, void *map_gu_sf,
+                  void *map_d_sf);
 double fp4_peak_ms(int n_tile, int iters, int *err, cudaStream_t s);
 
 // Programmatic dependent launch.  A kernel launched with `pdl` may start

@@ -114,7 +114,7 @@ struct ft_moe {
   int act_fmt = FT_ACT_BF16;
   Fp4Bufs q{};
   int64_t q_rows = 0;
-  alignas(64) unsigned char qmap[4][128] = {};
+  alignas(64) unsigned char qmap[6][128] = {};   // xq, hq, gate/up codes, down codes, their block scales
   bool qmaps_ok = false;
   std::string err;
 };
@@ -277,8 +277,8 @@ cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cud
       if (e != cudaSuccess) return e;
       h->kernel_launches += 1;
     }
-    return launch_tc_ffn_fp4(fa, down, h->q, h->qmap[down ? 1 : 0], h->qmap[down ? 3 : 2], h->err_dev,
-                             (int64_t)T * h->k, s);
+    return launch_tc_ffn_fp4(fa, down, h->q, h->qmap[down ? 1 : 0], h->qmap[down ? 3 : 2], h->qmap[down ? 5 : 4],
+                             h->err_dev, (int64_t)T * h->k, s);
   }
   if (tc) {
     if (!down && fa.only != 2) {
@@ -762,7 +762,7 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
                 make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
   if (h->q.xq)
     h->qmaps_ok = make_fp4_maps(h->slots, h->slot_stride, h->S, h->H, h->I, h->q.xq, h->q.hq, h->q_rows, h->qmap[0],
-                                h->qmap[1], h->qmap[2], h->qmap[3]) == 0;
+                                h->qmap[1], h->qmap[2], h->qmap[3], h->qmap[4], h->qmap[5]) == 0;
   if (h->act_fmt == FT_ACT_FP4 && !h->qmaps_ok) h->act_fmt = FT_ACT_BF16;
   return FT_OK;
 }
@@ -1215,7 +1215,7 @@ int ft_moe_set_act_format(ft_moe *h, int act_fmt) {
     h->q = q;
     h->q_rows = rows;
     h->qmaps_ok = make_fp4_maps(h->slots, h->slot_stride, h->S, h->H, h->I, h->q.xq, h->q.hq, rows, h->qmap[0],
-                                h->qmap[1], h->qmap[2], h->qmap[3]) == 0;
+                                h->qmap[1], h->qmap[2], h->qmap[3], h->qmap[4], h->qmap[5]) == 0;
   }
   if (!h->qmaps_ok) return fail(h, FT_ERR_CUDA, "FP4 TMA descriptors could not be encoded");
   h->act_fmt = act_fmt;

@@ -36,7 +36,8 @@
 //            the stage's A scale atoms (2 KB);
 //   warp 1   MMA: tcgen05.cp of the stage's scale atoms, 4 MMAs of K = 64
 //            (M = 128, N = 128) into one of two TMEM accumulators;
-//   warp 2   B scales: loads the tile rows' scale bytes and stores them as atoms;
+//   warp 2   B scales: the producer's TMA lands the tile rows' scale bytes in
+//            row order (16 bytes a row per stage); this warp stores them as atoms;
 //   warps 4-11 epilogue, one TMEM lane (tile row) per thread, two warps per
 //            lane quarter (each half of the tile's columns): gate/up applies
 //            the row's x scale and the NVFP4 global scales, SiLU * up, and
@@ -67,8 +68,9 @@ constexpr int Q_SF = 128 * (QBK / 16);  // 2 KB: 4 atoms of 512 bytes
 constexpr int Q_OFF_B = QNS * Q_A;
 constexpr int Q_OFF_SFA = Q_OFF_B + QNS * Q_B;
 constexpr int Q_OFF_SFB = Q_OFF_SFA + QNS * Q_SF;
-constexpr int Q_OFF_BAR = Q_OFF_SFB + QNS * Q_SF;
-constexpr int Q_BARS = 2 * QNS + 5;   // FULL, EMPTY per stage; TFULL x2, TEMPTY x2, DRAIN
+constexpr int Q_OFF_SFR = Q_OFF_SFB + QNS * Q_SF;   // B scales as they sit in the blob (row order)
+constexpr int Q_OFF_BAR = Q_OFF_SFR + QNS * Q_SF;
+constexpr int Q_BARS = 3 * QNS + 5;   // FULL, EMPTY, SFRAW per stage; TFULL x2, TEMPTY x2, DRAIN
 constexpr int Q_OFF_TAB = Q_OFF_BAR + Q_BARS * 8 + 16;
 constexpr int Q_SMEM = Q_OFF_TAB + 4 * 3 * (kMaxExperts + 1) + 64;
 constexpr int Q_SMEM_ALLOC = Q_SMEM + 1024;
@@ -77,7 +79,6 @@ constexpr int Q_THREADS = (4 + Q_EPI_WARPS) * 32;
 constexpr int Q_PROD = 0, Q_MMA = 1, Q_SFW = 2, Q_EPI0 = 4;
 constexpr uint32_t Q_TMEM_COLS = 512;  // accumulators 0 and 128; scale buffers from 256
 constexpr uint32_t Q_SFA_COL = 256, Q_SFB_COL = 288;   // + 16 * (stage parity)
-constexpr int Q_SF_AHEAD = 3;         // stages of B scales the scale warp holds in registers
 
 // M = 128, N = 128, A and B E2M1 (format 1 of the mxf4 kinds), UE4M3 scales
 // (bit 23 clear), K-major, dense K = 64.
@@ -237,7 +238,6 @@ struct Fp4Args {
   PlanBufs plan;
   int only;                 // 0 all, 1 hits, 2 misses
   long long gscale_off;     // byte offset of the NVFP4 global scales in a blob
-  long long sf_off;         // byte offset of the B matrix's block scales in a blob
   const uint8_t *a_sf;      // A scale atoms (x or h)
   const float *xg;          // gate/up: row scale of each padded row
   uint8_t *hq;              // gate/up: h codes [rows][I/2]
@@ -280,18 +280,21 @@ __device__ __forceinline__ QTile q_decode(int t, const int *s_start, const int *
 
 template <bool DOWN>
 __global__ void __launch_bounds__(Q_THREADS, 1)
-    gemm_fp4_kernel(Fp4Args a, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+    gemm_fp4_kernel(Fp4Args a, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSB) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   unsigned char *sm = smem_raw + (base - raw_base);
   const uint32_t sA = base, sB = base + Q_OFF_B, sSFA = base + Q_OFF_SFA, sSFB = base + Q_OFF_SFB;
+  const uint32_t sSFR = base + Q_OFF_SFR;
   const uint32_t bar0 = base + Q_OFF_BAR;
   auto FULL = [&](int s) { return bar0 + 8u * s; };
   auto EMPTY = [&](int s) { return bar0 + 8u * (QNS + s); };
-  auto TFULL = [&](int b) { return bar0 + 8u * (2 * QNS + b); };
-  auto TEMPTY = [&](int b) { return bar0 + 8u * (2 * QNS + 2 + b); };
-  const uint32_t DRAIN = bar0 + 8u * (2 * QNS + 4);
+  auto SFRAW = [&](int s) { return bar0 + 8u * (2 * QNS + s); };
+  auto TFULL = [&](int b) { return bar0 + 8u * (3 * QNS + b); };
+  auto TEMPTY = [&](int b) { return bar0 + 8u * (3 * QNS + 2 + b); };
+  const uint32_t DRAIN = bar0 + 8u * (3 * QNS + 4);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sm + Q_OFF_BAR + Q_BARS * 8);
   volatile int *s_abort = reinterpret_cast<volatile int *>(sm + Q_OFF_BAR + Q_BARS * 8 + 4);
   int *s_start = reinterpret_cast<int *>(sm + Q_OFF_TAB);
@@ -307,6 +310,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
     for (int s = 0; s < QNS; ++s) {
       mbar_init(FULL(s), 1 + 32);     // the producer's expect_tx + the B-scale warp's lanes
       mbar_init(EMPTY(s), 1);
+      mbar_init(SFRAW(s), 1);         // the producer's expect_tx for the B scales in row order
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(TFULL(b), 1);
@@ -378,6 +382,14 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
             tma_load_3d(sB + s * Q_B + Q_B / 2, &tmB, FULL(s), kb * (QBK / 2), a.I + ti.n * (QBN / 2), ti.slot);
           }
           bulk_load(sSFA + s * Q_SF, sfa + (size_t)kb * Q_SF, Q_SF, FULL(s));
+          // B scales in row order: 16 bytes (the stage's 16 blocks) of each tile row
+          mbar_arrive_expect_tx(SFRAW(s), Q_SF);
+          if constexpr (DOWN) {
+            tma_load_3d(sSFR + s * Q_SF, &tmSB, SFRAW(s), kb * 16, ti.n * QBN, ti.slot);
+          } else {
+            tma_load_3d(sSFR + s * Q_SF, &tmSB, SFRAW(s), kb * 16, ti.n * (QBN / 2), ti.slot);
+            tma_load_3d(sSFR + s * Q_SF + Q_SF / 2, &tmSB, SFRAW(s), kb * 16, a.I + ti.n * (QBN / 2), ti.slot);
+          }
         }
       }
       // every copy this CTA issued must land before the CTA exits
@@ -385,66 +397,43 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
         const unsigned long long t0 = globaltimer();
         while (!mbar_try_wait(FULL(jj % QNS), (jj / QNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
         }
+        while (!mbar_try_wait(SFRAW(jj % QNS), (jj / QNS) & 1) && globaltimer() - t0 < kWaitLimitNs) {
+        }
       }
     }
     __syncwarp();
   } else if (warp == Q_SFW) {
     // ================================================================ B scales
-    // Lane l carries tile rows l, l+32, l+64, l+96: per stage 16 scale bytes
-    // each (the stage's 16 blocks), loaded Q_SF_AHEAD stages ahead, stored as
-    // atom g's line l = {row l, row l+32, row l+64, row l+96} x word g.
-    // flat list of (tile, kb) stages this CTA walks
-    int tile_of = blockIdx.x, kb_of = 0;
-    auto next_stage = [&](int &tile, int &kb) {
-      if (++kb == nk) {
-        kb = 0;
-        tile += gridDim.x;
-      }
-    };
-    auto load_stage = [&](int tile, int kb, uint4 *dst) {
-      if (tile >= n_tiles) return;
-      const QTile ti = q_decode(tile, s_start, s_mt, s_pad, nU, NTN, a);
-      const uint8_t *sf = a.slot_bank + (size_t)ti.slot * a.slot_stride + a.sf_off;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = lane + 32 * i;
-        const int brow = DOWN ? ti.n * QBN + r : (r < QBN / 2 ? ti.n * (QBN / 2) + r : a.I + ti.n * (QBN / 2) + r - QBN / 2);
-        dst[i] = __ldg(reinterpret_cast<const uint4 *>(sf + (size_t)brow * (K / 16) + kb * 16));
-      }
-    };
-    uint4 ring[Q_SF_AHEAD][4];
-    int lt = tile_of, lk = kb_of;   // next stage to load
-#pragma unroll
-    for (int d = 0; d < Q_SF_AHEAD; ++d) {
-      load_stage(lt, lk, ring[d]);
-      next_stage(lt, lk);
-    }
+    // Lane l moves tile rows l, l+32, l+64, l+96 (16 bytes each: the stage's
+    // 16 blocks) from row order into atom g's line l = {row l, row l+32,
+    // row l+64, row l+96} x word g.
     int j = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       for (int kb = 0; kb < nk; ++kb, ++j) {
         const int s = j % QNS;
-        uint4 cur[4];
+        if (!mbar_wait(SFRAW(s), (j / QNS) & 1, s_abort, a.err, 111)) { ok = false; break; }
+        uint4 r[4];
+        const uint32_t src = sSFR + s * Q_SF + 16 * lane;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cur[i] = ring[0][i];
-#pragma unroll
-        for (int d = 0; d + 1 < Q_SF_AHEAD; ++d)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) ring[d][i] = ring[d + 1][i];
-        load_stage(lt, lk, ring[Q_SF_AHEAD - 1]);
-        next_stage(lt, lk);
-        if (!mbar_wait(EMPTY(s), ((j / QNS) & 1) ^ 1, s_abort, a.err, 111)) { ok = false; break; }
-        const uint32_t dst = sSFB + s * Q_SF + 16 * lane;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t w0 = g == 0 ? cur[0].x : g == 1 ? cur[0].y : g == 2 ? cur[0].z : cur[0].w;
-          const uint32_t w1 = g == 0 ? cur[1].x : g == 1 ? cur[1].y : g == 2 ? cur[1].z : cur[1].w;
-          const uint32_t w2 = g == 0 ? cur[2].x : g == 1 ? cur[2].y : g == 2 ? cur[2].z : cur[2].w;
-          const uint32_t w3 = g == 0 ? cur[3].x : g == 1 ? cur[3].y : g == 2 ? cur[3].z : cur[3].w;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 512 * g), "r"(w0), "r"(w1), "r"(w2),
-                       "r"(w3)
+        for (int i = 0; i < 4; ++i)
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(r[i].x), "=r"(r[i].y), "=r"(r[i].z), "=r"(r[i].w)
+                       : "r"(src + 512 * i)
                        : "memory");
-        }
+        const uint32_t dst = sSFB + s * Q_SF + 16 * lane;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(r[0].x), "r"(r[1].x), "r"(r[2].x),
+                     "r"(r[3].x)
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 512), "r"(r[0].y), "r"(r[1].y),
+                     "r"(r[2].y), "r"(r[3].y)
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 1024), "r"(r[0].z), "r"(r[1].z),
+                     "r"(r[2].z), "r"(r[3].z)
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 1536), "r"(r[0].w), "r"(r[1].w),
+                     "r"(r[2].w), "r"(r[3].w)
+                     : "memory");
         fence_proxy_async();   // these stores are visible to the tensor core's copy
         mbar_arrive(FULL(s));
       }
@@ -647,7 +636,7 @@ cudaError_t launch_quant_x(const __nv_bfloat16 *x, const PlanBufs &plan, int T, 
 }
 
 cudaError_t launch_tc_ffn_fp4(const FfnArgs &f, bool down, const Fp4Bufs &q, const void *map_a, const void *map_b,
-                              int *err, int64_t max_rows, cudaStream_t s) {
+                              const void *map_sfb, int *err, int64_t max_rows, cudaStream_t s) {
   Fp4Args a{};
   a.slot_bank = f.slot_bank;
   a.slot_stride = f.slot_stride;
@@ -658,7 +647,6 @@ cudaError_t launch_tc_ffn_fp4(const FfnArgs &f, bool down, const Fp4Bufs &q, con
   a.only = f.only;
   const BlobLayout L = blob_layout(FMT_NVFP4, f.H, f.I);
   a.gscale_off = L.gscale;
-  a.sf_off = down ? L.d_sf : L.gu_sf;
   a.a_sf = down ? q.hsf : q.xsf;
   a.xg = q.xg;
   a.hq = q.hq;
@@ -672,17 +660,20 @@ cudaError_t launch_tc_ffn_fp4(const FfnArgs &f, bool down, const Fp4Bufs &q, con
   const int grid = (int)std::min<int64_t>(tc_num_sms(), std::max<int64_t>(1, mtiles * NTN));
   const CUtensorMap &mA = *reinterpret_cast<const CUtensorMap *>(map_a);
   const CUtensorMap &mB = *reinterpret_cast<const CUtensorMap *>(map_b);
-  if (down) gemm_fp4_kernel<true><<<grid, Q_THREADS, Q_SMEM_ALLOC, s>>>(a, mA, mB);
-  else gemm_fp4_kernel<false><<<grid, Q_THREADS, Q_SMEM_ALLOC, s>>>(a, mA, mB);
+  const CUtensorMap &mS = *reinterpret_cast<const CUtensorMap *>(map_sfb);
+  if (down) gemm_fp4_kernel<true><<<grid, Q_THREADS, Q_SMEM_ALLOC, s>>>(a, mA, mB, mS);
+  else gemm_fp4_kernel<false><<<grid, Q_THREADS, Q_SMEM_ALLOC, s>>>(a, mA, mB, mS);
   return cudaGetLastError();
 }
 
 // TMA maps of the FP4 x FP4 GEMMs: A = quantised activations [rows][K/2]
 // (box 128 bytes x 128 rows), B = the slot bank's e2m1 codes of one matrix,
-// 3-D (K/2, rows, slot) with a box of 128 bytes x (64 gate/up | 128 down) rows;
-// all with the 128-byte swizzle.
+// 3-D (K/2, rows, slot) with a box of 128 bytes x (64 gate/up | 128 down) rows,
+// all with the 128-byte swizzle; and the B matrices' block scales, 3-D
+// (K/16, rows, slot) with a box of 16 bytes x (64 | 128) rows, no swizzle.
 int make_fp4_maps(const uint8_t *slots, int64_t slot_stride, int S, int H, int I, const void *xq, const void *hq,
-                  int64_t rows, void *map_xq, void *map_hq, void *map_gu, void *map_d) {
+                  int64_t rows, void *map_xq, void *map_hq, void *map_gu, void *map_d, void *map_gu_sf,
+                  void *map_d_sf) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return -1;
   const BlobLayout L = blob_layout(FMT_NVFP4, H, I);
@@ -706,6 +697,14 @@ int make_fp4_maps(const uint8_t *slots, int64_t slot_stride, int S, int H, int I
                      const_cast<uint8_t *>(slots) + (down ? L.d_codes : L.gu_codes), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return (int)r;
+    cuuint64_t sdims[3] = {(cuuint64_t)(K / 16), (cuuint64_t)rows_w, (cuuint64_t)S};
+    cuuint64_t sstrides[2] = {(cuuint64_t)(K / 16), (cuuint64_t)slot_stride};
+    cuuint32_t sbox[3] = {16, (cuuint32_t)(down ? QBN : QBN / 2), 1};
+    r = enc(reinterpret_cast<CUtensorMap *>(down ? map_d_sf : map_gu_sf), CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<uint8_t *>(slots) + (down ? L.d_sf : L.gu_sf), sdims, sstrides, sbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return (int)r;
   }
   return 0;
