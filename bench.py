@@ -433,6 +433,8 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
         stack.set_miss_path(args.miss_path)
     if args.fused_decode:
         stack.set_decode_fusion(True)
+    if getattr(args, "no_decode_grid", False):
+        stack.set_decode_grid(False)
     fp4_act = getattr(args, "act", "bf16") == "fp4"
     if fp4_act:
         stack.set_act_format("fp4")
@@ -702,7 +704,8 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
                    "mode": cfg["mode"],
                    "prefill_hit_d2d": {"cache_slots": d2d_cache} if d2d_cache > 0 else None,
                    "miss_path": stack.miss_path(ffn_kernel == "tc") if cfg["mode"] == "lru" else None,
-                   "decode_kernels": "fused" if args.fused_decode else "split", "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
+                   "decode_kernels": "fused" if args.fused_decode else
+                   ("split" if getattr(args, "no_decode_grid", False) else "grid (split where not eligible)"), "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "l2": l2,
                    "pool": f"{n_keys} logical experts over {n_phys} distinct pinned blobs ({n_phys * nb / 1e9:.2f} GB)"},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": L * T * (H * 2 + E * 4),
                 "d2h_bytes_per_step": L * T * H * 2, "ms_per_step": e2e_ms / K,
@@ -746,6 +749,8 @@ def main():
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the further workloads (prefill-35B BF16 and NVFP4, stream-753B) that a one-GPU run "
                          "of the default workload also measures")
+    ap.add_argument("--no-decode-grid", action="store_true",
+                    help="decode calls as separate route, gate/up and down kernels instead of one grid")
     ap.add_argument("--fused-decode", action="store_true",
                     help="decode calls as one cooperative kernel instead of separate kernels (its copy-flag "
                          "wait needs the copy stream to progress alongside it: profile it with --miss-path pull)")

@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "FT_OK", -1: "FT_ERR_ARG", -2: "FT_ERR_CUDA", -3: "FT_ERR_OOM
 #: every symbol include/ft_moe.h declares
 EXPORTED = ("ft_moe_blob_bytes", "ft_moe_create", "ft_moe_load_pool", "ft_moe_set_mode", "ft_moe_forward",
             "ft_cache_stats", "ft_cache_reset", "ft_cache_trace", "ft_moe_last_routing", "ft_moe_last_activations",
-            "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_set_ffn_kernel", "ft_moe_last_ffn_kernel", "ft_moe_set_miss_path", "ft_moe_miss_path", "ft_moe_set_decode_fusion", "ft_moe_set_keep_activations", "ft_moe_resize_slots",
+            "ft_moe_set_profiling", "ft_moe_profile_read", "ft_moe_set_ffn_kernel", "ft_moe_last_ffn_kernel", "ft_moe_set_miss_path", "ft_moe_miss_path", "ft_moe_set_decode_fusion", "ft_moe_set_decode_grid", "ft_moe_set_keep_activations", "ft_moe_resize_slots",
             "ft_moe_set_prefill_hit_d2d", "ft_moe_prefill_hit_d2d",
             "ft_moe_slot_stride", "ft_moe_kernel_launches",
             "ft_moe_set_act_format", "ft_moe_act_format", "ft_moe_last_act_fp4", "ft_fp4_tensor_peak",
@@ -90,6 +90,7 @@ def lib():
         L.ft_moe_prefill_hit_d2d.argtypes = [vp]
         L.ft_moe_set_miss_path.argtypes = [vp, i32]
         L.ft_moe_set_decode_fusion.argtypes = [vp, i32]
+        L.ft_moe_set_decode_grid.argtypes = [vp, i32]
         L.ft_moe_set_act_format.argtypes = [vp, i32]
         L.ft_moe_act_format.argtypes = [vp]
         L.ft_moe_last_act_fp4.argtypes = [vp, vp, vp, vp, vp, vp]
@@ -240,6 +241,10 @@ class MoELayerStack:
     def set_decode_fusion(self, on=True):
         """One cooperative kernel per decode call, or separate kernels (default)."""
         _check(lib().ft_moe_set_decode_fusion(self._h, 1 if on else 0), self._h)
+
+    def set_decode_grid(self, on=True):
+        """Eligible decode calls as one grid (default on), or separate route, gate/up and down kernels."""
+        _check(lib().ft_moe_set_decode_grid(self._h, 1 if on else 0), self._h)
 
     def resize_slots(self, n_slots):
         """Changes the number of expert slots (the most recently used experts stay)."""

@@ -242,6 +242,14 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Decode call as one grid (decode_grid.cu): router, copiers, gate/up and down
+// items by arrival ticket.  sync: decode_grid_sync_ints(umax) device ints,
+// zero at create and after an error.
+bool decode_grid_supported(int T, int k, int H, int I);
+int decode_grid_sync_ints(int umax);
+cudaError_t launch_decode_grid(const RouteArgs &route, const FfnArgs &ffn, const CombineArgs &cb, int *sync,
+                               int n_copy, int seq_raised, bool pdl, cudaStream_t s);
+
 // Fused decode layer (decode_layer.cu): one cooperative kernel per call.
 bool mega_supported(int E, int T, int k);
 cudaError_t launch_decode_layer(const RouteArgs &route, const FfnArgs &ffn, const CombineArgs &cb, int *sync,

@@ -108,6 +108,8 @@ struct ft_moe {
   int *copy_sync = nullptr;          // misses copied inside the gate/up kernel: flag, arrival count, role ticket
   int32_t *seq_ring = nullptr;       // pinned: seq_ring[seq % 64] = seq, the source of the copy-flag write
   bool decode_fused = false;   // ft_moe_set_decode_fusion
+  bool decode_grid = true;     // ft_moe_set_decode_grid: eligible decode calls as one grid
+  int *grid_sync = nullptr;    // the decode grid's flags and counters
   int miss_path = FT_MISS_AUTO;
   // FP4 x FP4 variant of the tensor-core FFN (ft_moe_set_act_format): buffers
   // over expert-padded rows and their TMA maps (xq, hq, gate/up codes, down codes)
@@ -186,6 +188,7 @@ void free_all(ft_moe *h) {
   cudaFree(h->pool_dev);
   cudaFree(h->mega_sync);
   cudaFree(h->copy_sync);
+  cudaFree(h->grid_sync);
   cudaFree(h->q.xq);
   cudaFree(h->q.xsf);
   cudaFree(h->q.xg);
@@ -251,6 +254,7 @@ int sync_handle(ft_moe *h) {
     // an aborted kernel may have left its flags or counters mid-way
     FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
     FT_CUDA(h, cudaMemset(h->copy_sync, 0, 4 * sizeof(int)));
+    FT_CUDA(h, cudaMemset(h->grid_sync, 0, sizeof(int) * decode_grid_sync_ints(h->umax)));
     FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
     return fail(h, FT_ERR_DEVICE, "a kernel gave up a bounded wait (site " + std::to_string(code) + ")");
   }
@@ -314,6 +318,7 @@ int reset_tables(ft_moe *h, bool warm) {
   FT_CUDA(h, cudaMemset(h->stats_dev, 0, 16 * sizeof(unsigned long long)));
   FT_CUDA(h, cudaMemset(h->mega_sync, 0, 4 * sizeof(int)));
   FT_CUDA(h, cudaMemset(h->copy_sync, 0, 4 * sizeof(int)));
+  FT_CUDA(h, cudaMemset(h->grid_sync, 0, sizeof(int) * decode_grid_sync_ints(h->umax)));
   FT_CUDA(h, cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(h->H)));
   h->host_warm = h->host_streamed = h->host_bytes = h->host_d2d = 0;
   h->last_streamed = h->last_stream_bytes = h->last_d2d = 0;
@@ -544,6 +549,58 @@ int forward_fused(ft_moe *h, RouteArgs &ra, int layer, int n_tokens, const void 
   return FT_OK;
 }
 
+// A decode call (LRU mode, GEMV, misses copied on the GPU, <= 32 pairs) as
+// one grid: router, copiers, gate/up and down items by arrival ticket (see
+// decode_grid.cu).  No host step; capturable in a CUDA graph.
+constexpr int kGridCopyCtas = 296;
+int forward_grid(ft_moe *h, RouteArgs &ra, int layer, int n_tokens, const void *x, void *out, bool capturing,
+                 cudaStream_t stream) {
+  FfnArgs fa{};
+  fa.slot_bank = h->slots;
+  fa.slot_stride = h->slot_stride;
+  fa.H = h->H; fa.I = h->I; fa.E = h->E; fa.k = h->k; fa.fmt = h->fmt;
+  fa.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+  fa.h = h->hbuf;
+  fa.y = h->ybuf;
+  fa.plan = h->plan;
+  fa.umax = (int)std::min<int64_t>(h->E, (int64_t)n_tokens * h->k);
+  fa.max_tokens = n_tokens;
+  fa.err = h->err_dev;
+  fa.pool_dev = h->pool_dev;
+  fa.layer = layer;
+  const BlobLayout bl = blob_layout(h->fmt, h->H, h->I);
+  MissCopyArgs &mc = fa.mc;
+  mc.miss = h->plan.miss;
+  mc.n = h->plan.n;
+  mc.pool_dev = h->pool_dev;
+  mc.slots = h->slots;
+  mc.slot_stride = h->slot_stride;
+  mc.seg[0][0] = 0;
+  mc.seg[0][1] = bl.d_codes;
+  mc.seg[1][0] = bl.gscale >= 0 ? bl.gscale : 0;
+  mc.seg[1][1] = bl.gscale >= 0 ? h->blob_bytes : 0;
+  mc.seg[2][0] = bl.d_codes;
+  mc.seg[2][1] = bl.gscale >= 0 ? bl.gscale : h->blob_bytes;
+  CombineArgs cb{};
+  cb.gates = h->plan.gates;
+  cb.inv = h->plan.inv;
+  cb.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  cb.counters = h->combine_counters;
+  cb.T = n_tokens;
+  h->last_tc = false;
+  // FT_FAULT=devwait: the copy flags are raised with a value nobody waits for
+  const int seq_raised = fault("devwait") ? (int)h->seq ^ 0x40000000 : (int)h->seq;
+  const bool pdl = !h->prof && !capturing;
+  prof_begin(h, FT_PROF_LAYER, stream);
+  FT_CUDA(h, launch_decode_grid(ra, fa, cb, h->grid_sync, kGridCopyCtas, seq_raised, pdl, stream));
+  prof_end(h, FT_PROF_LAYER, stream);
+  h->kernel_launches += 1;
+  h->order_cur ^= 1;
+  if (capturing) h->captured = true;
+  else FT_CUDA(h, cudaEventRecord(h->ev_done, stream));
+  return FT_OK;
+}
+
 }  // namespace
 
 void ftmoe::set_stateless_error(const std::string &msg) { g_create_err = msg; }
@@ -597,6 +654,8 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->xpbuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->mega_sync, 4) == cudaSuccess && cudaMemset(h->mega_sync, 0, 16) == cudaSuccess &&
             dev_alloc(&h->copy_sync, 4) == cudaSuccess && cudaMemset(h->copy_sync, 0, 16) == cudaSuccess &&
+            dev_alloc(&h->grid_sync, decode_grid_sync_ints(umax)) == cudaSuccess &&
+            cudaMemset(h->grid_sync, 0, sizeof(int) * decode_grid_sync_ints(umax)) == cudaSuccess &&
             dev_alloc(&h->combine_counters, combine_tiles(hidden)) == cudaSuccess &&
             cudaMemset(h->combine_counters, 0, sizeof(int) * combine_tiles(hidden)) == cudaSuccess;
   if (!ok) { cudaGetLastError(); fail(nullptr, FT_ERR_OOM, "device allocation failed"); return bail(FT_ERR_OOM); }
@@ -842,6 +901,9 @@ int ft_moe_forward(ft_moe *h, int layer, int n_tokens, const void *x, const floa
   if (h->decode_fused && h->mode == MODE_LRU && !tc && !kcopy && !capturing && h->fmt != FMT_FP8 &&
       mega_supported(h->E, n_tokens, h->k))
     return forward_fused(h, ra, layer, n_tokens, x, out, pull, stream);
+  if (h->decode_grid && kcopy && !tc && gemv_fuses_combine(n_tokens) &&
+      decode_grid_supported(n_tokens, h->k, h->H, h->I))
+    return forward_grid(h, ra, layer, n_tokens, x, out, capturing, stream);
   prof_begin(h, FT_PROF_ROUTE, stream);
   FT_CUDA(h, launch_route(ra, stream));
   prof_end(h, FT_PROF_ROUTE, stream);
@@ -1172,6 +1234,13 @@ int ft_moe_set_decode_fusion(ft_moe *h, int on) {
   if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
   if (int rc = sync_handle(h)) return rc;
   h->decode_fused = on != 0;
+  return FT_OK;
+}
+
+int ft_moe_set_decode_grid(ft_moe *h, int on) {
+  if (!h) return fail(h, FT_ERR_ARG, "NULL handle");
+  if (int rc = sync_handle(h)) return rc;
+  h->decode_grid = on != 0;
   return FT_OK;
 }
 

@@ -303,8 +303,9 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, l8 = lane & (LPR - 1);
   // the count and this item's packed plan entry, in one round trip (entries
   // past the count are stale and ignored)
-  const int nU = a.plan.n[0];
-  const int4 ui = a.plan.u_info[u];
+  // (COH: the plan was written by a CTA of the same grid, so it is read through L2)
+  const int nU = COH ? __ldcg(a.plan.n) : a.plan.n[0];
+  const int4 ui = COH ? __ldcg(a.plan.u_info + u) : a.plan.u_info[u];
   const int hit = ui.w & 1;
   bool work = u < nU;
   if (work && ((a.only == 1 && !hit) || (a.only == 2 && hit))) work = false;
@@ -374,7 +375,7 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
         if (DOWN) {
           src = a.h + (size_t)(off + c0 + t) * a.I;
         } else {
-          const int pair = a.plan.perm[off + c0 + t];
+          const int pair = COH ? __ldcg(a.plan.perm + off + c0 + t) : a.plan.perm[off + c0 + t];
           src = a.x + (size_t)(pair / a.k) * a.H;
         }
         reinterpret_cast<uint4 *>(xs + (size_t)t * K)[xs_pos(v)] = ld_w<COH>(reinterpret_cast<const uint4 *>(src) + v);
@@ -429,8 +430,8 @@ __device__ __forceinline__ void combine_block(const FfnArgs &a, const CombineArg
   __shared__ float s_g[kFusedCombineMaxT * kMaxTopK];
   __shared__ int s_inv[kFusedCombineMaxT * kMaxTopK];
   for (int i = threadIdx.x; i < cb.T * a.k; i += blockDim.x) {
-    s_g[i] = cb.gates[i];
-    s_inv[i] = cb.inv[i];
+    s_g[i] = __ldcg(cb.gates + i);
+    s_inv[i] = __ldcg(cb.inv + i);
   }
   __threadfence();
   __syncthreads();

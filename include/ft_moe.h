@@ -252,7 +252,7 @@ enum ft_prof_class {
   FT_PROF_COMBINE = 4,     /* gate-weighted combine */
   FT_PROF_MISS_COPY = 5,   /* the misses' host->device copies of one call (copy stream) */
   FT_PROF_STREAM_COPY = 6, /* one layer's staging copies in STREAM mode (copy stream) */
-  FT_PROF_LAYER = 7,       /* the fused decode-layer kernel (routing, FFN and combine of one call) */
+  FT_PROF_LAYER = 7,       /* a decode call as one kernel (the decode grid, or the fused decode-layer kernel) */
   FT_PROF_CLASSES = 8
 };
 
@@ -377,6 +377,20 @@ int ft_moe_miss_path(const ft_moe *h, int tensor_core);
  * misses are pulled (FT_MISS_PULL).  Waits for the handle's outstanding work.
  * Errors: FT_ERR_ARG. */
 int ft_moe_set_decode_fusion(ft_moe *h, int on);
+
+/* Decode calls as one grid (on by default).  An LRU-mode call that runs the
+ * GEMV with the misses copied on the GPU (FT_MISS_KERNEL), with at most 32
+ * (token, rank) pairs and at most 4 tokens, runs as a single grid whose CTAs
+ * take their role by arrival ticket: the router (top-k, permute, LRU plan),
+ * then copiers (the misses from pinned host memory into their slots), then the
+ * gate/up GEMV items of every distinct expert (hits first), then the down GEMV
+ * items with the combine.  Every CTA waits only for CTAs with smaller tickets,
+ * so the grid progresses whatever the order of dispatch; each wait is bounded
+ * (FT_ERR_DEVICE at the next synchronising call).  The results are those of
+ * the separate route, gate/up and down kernels, bit for bit.  Off: those
+ * separate kernels.  Synchronises the handle.  Errors: FT_ERR_ARG,
+ * FT_ERR_DEVICE. */
+int ft_moe_set_decode_grid(ft_moe *h, int on);
 
 /* Bytes between consecutive slots in the device slot bank. */
 int64_t ft_moe_slot_stride(const ft_moe *h);

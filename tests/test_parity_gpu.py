@@ -804,6 +804,44 @@ def test_fused_decode_matches_split_kernels(fmt, T, path):
     split.close()
 
 
+# ------------------------------------------------------------ decode call as one grid
+
+@pytest.mark.parametrize("fmt,T,k", [("nvfp4", 1, 2), ("mxfp4", 2, 2), ("bf16", 4, 2), ("fp8", 3, 2),
+                                     ("nvfp4", 4, 8), ("nvfp4", 1, 8)])
+def test_decode_grid_matches_split_kernels(fmt, T, k):
+    # one grid per decode call (router, copiers, gate/up and down items by
+    # arrival ticket) against the separate route, gate/up and down kernels:
+    # outputs, traces and counters identical bit for bit, both matching the oracle
+    H, I, E, L = 512, 768, 16, 3
+    S = max(16, 8 + 2 * min(E, T * k))
+    seed = 191 + T + k
+    grid, orc, pool = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed)
+    grid.set_miss_path("kernel")
+    split = F.MoELayerStack(H, E, k, I, fmt, S, L, T)
+    split.load_pool(pool.pointers, keepalive=pool)
+    split.set_miss_path("kernel")
+    split.set_decode_grid(False)
+    launches = []
+    for step in range(8):
+        for layer in range(L):
+            x, lg = Hn.inputs(seed, T, H, E, step, layer, zipf=0.6)
+            xd, lgd = Hn.to_dev(x, lg)
+            b = split.forward(layer, xd, lgd)
+            outs = []
+            n0 = grid.kernel_launches
+            _check_call(grid, orc, layer, x, lg, gemm_check=(step % 3 == 0), outs=outs)
+            launches.append(grid.kernel_launches - n0)
+            torch.cuda.synchronize()
+            assert grid.trace() == split.trace()
+            assert torch.equal(outs[0].view(torch.int16), b.view(torch.int16))
+    assert set(launches) == {1}                       # one grid per call
+    cg, _ = grid.stats()
+    cs, _ = split.stats()
+    assert cg == cs and cg["misses"] > 0
+    grid.close()
+    split.close()
+
+
 # ------------------------------------------------------------ misses read over PCIe by the kernels
 
 @pytest.mark.parametrize("path", ["pull", "kernel"])
