@@ -58,6 +58,32 @@ struct GridArgs {
 // [5..6] ticket counters (by call parity), [8 + u] gate/up items done of u.
 enum { kPlanFlag = 0, kFlagA = 1, kCountA = 2, kFlagB = 3, kCountB = 4, kTicket = 5, kDone = 8 };
 
+// Bounded wait of thread 0 until *flag == want; the CTA learns the outcome.
+// Waiters back off kGridPollNs between polls: hundreds of CTAs may wait on
+// one flag, and their polls share one L2 line with the CTA that will raise it.
+constexpr unsigned kGridPollNs = 400;
+__device__ __forceinline__ bool grid_wait(const int *flag, int want, int *err, int site, int *s_ok) {
+  if (threadIdx.x == 0) {
+    const volatile int *vf = flag;
+    bool ok = true;
+    if (*vf != want) {
+      const unsigned long long t0 = dev_timer_ns();
+      while (*vf != want) {
+        if (dev_timer_ns() - t0 > kWaitNs) {
+          atomicCAS(err, 0, site);
+          ok = false;
+          break;
+        }
+        __nanosleep(kGridPollNs);
+      }
+    }
+    __threadfence();
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
 template <int FMT, bool DOWN, int NT>
 __device__ __forceinline__ void grid_gemv(const FfnArgs &a, int lpr, int u, int bx, int fpw, __nv_bfloat16 *xs,
                                           bool x_staged) {
@@ -106,7 +132,7 @@ __global__ void __launch_bounds__(kGridThreads) decode_grid_kernel(GridArgs g) {
       reinterpret_cast<uint4 *>(xs)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(g.f.x) + v);
     x_staged = true;
   }
-  if (!cta_wait_flag(sync + kPlanFlag, g.seq, g.f.err, 80, &s_ok)) return;
+  if (!grid_wait(sync + kPlanFlag, g.seq, g.f.err, 80, &s_ok)) return;
   pdl_trigger();   // this call's plan (and the cache tables) are final
   const int nU = __ldcg(g.r.plan.n), n_miss = __ldcg(g.r.plan.n + 2);
 
@@ -125,7 +151,7 @@ __global__ void __launch_bounds__(kGridThreads) decode_grid_kernel(GridArgs g) {
     const int i = t - 1 - g.n_copy, u = i / g.nb_gu, bx = i - u * g.nb_gu;
     if (u >= nU) return;
     const bool hit = __ldcg(&g.r.plan.u_info[u].w) & 1;
-    if (!hit && !cta_wait_flag(sync + kFlagA, g.seq, g.f.err, 81, &s_ok)) return;
+    if (!hit && !grid_wait(sync + kFlagA, g.seq, g.f.err, 81, &s_ok)) return;
     grid_gemv<FMT, false, NT>(g.f, g.lpr_gu, u, bx, g.fpw_gu, xs, x_staged);
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -149,7 +175,7 @@ __global__ void __launch_bounds__(kGridThreads) decode_grid_kernel(GridArgs g) {
             ok = false;
             break;
           }
-          __nanosleep(32);
+          __nanosleep(kGridPollNs);
         }
       }
       __threadfence();
@@ -158,7 +184,7 @@ __global__ void __launch_bounds__(kGridThreads) decode_grid_kernel(GridArgs g) {
     __syncthreads();
     if (!s_ok) return;
     const bool hit = __ldcg(&g.r.plan.u_info[u].w) & 1;
-    if (!hit && !cta_wait_flag(sync + kFlagB, g.seq, g.f.err, 83, &s_ok)) return;
+    if (!hit && !grid_wait(sync + kFlagB, g.seq, g.f.err, 83, &s_ok)) return;
     grid_gemv<FMT, true, NT>(g.f, g.lpr_dn, u, bx, g.fpw_dn, xs, false);
   }
   __shared__ int s_last;

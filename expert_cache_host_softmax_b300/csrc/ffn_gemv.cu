@@ -48,14 +48,17 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
   // Roles.  Without in-kernel copies, CTA (x, y) works on feature block x of
   // distinct expert y.  With them (copy_rows > 0), roles go by arrival, not by
-  // block index (CUDA does not promise an order of dispatch): the first
-  // copy_rows * gridDim.x CTAs to take a ticket copy, and the others take the
-  // work items in ticket order, hits first.  The copiers are thus running
-  // before any CTA waits for them, whatever the order of dispatch.  The
-  // ticket counter was last used by the gate/up grid two kernels back, which
-  // has completed; the CTA that takes the last ticket re-arms it.
+  // block index (CUDA does not promise an order of dispatch): when the call
+  // has misses, the first copy_rows * gridDim.x CTAs to take a ticket copy,
+  // and the others take the work items in ticket order, hits first, so the
+  // copiers are running before any CTA waits for them, whatever the order of
+  // dispatch; when it has none, the first tickets take the work items and the
+  // last copy_rows * gridDim.x CTAs have nothing to do.  The ticket counter
+  // was last used by the gate/up grid two kernels back, which has completed;
+  // the CTA that takes the last ticket re-arms it.
   int item_y = blockIdx.y, item_x = blockIdx.x;
   long long copier = -1;
+  int ticket = -1;
   if constexpr (!DOWN) {
     if (a.copy_rows > 0) {
       __shared__ int s_ticket;
@@ -66,13 +69,7 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
         s_ticket = t;
       }
       __syncthreads();
-      const int t = s_ticket, nct = a.copy_rows * gridDim.x;
-      if (t < nct) {
-        copier = t;
-      } else {
-        item_y = a.copy_rows + (t - nct) / gridDim.x;
-        item_x = (t - nct) % gridDim.x;
-      }
+      ticket = s_ticket;
     }
   }
   // Before the wait for the kernel ahead: this grid starts only once that
@@ -81,7 +78,7 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   // down grid, which starts after the gate/up grid passed its wait) are final.
   bool x_staged = false;
   if constexpr (!DOWN) {
-    if (a.max_tokens == 1 && copier < 0) {
+    if (a.max_tokens == 1) {
       // one-token call: every expert multiplies the same row
       for (int v = threadIdx.x; v < a.H / 8; v += blockDim.x)
         reinterpret_cast<uint4 *>(xs)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(a.x) + v);
@@ -93,6 +90,25 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   }
   pdl_wait();      // the plan, activations and slots come from earlier kernels
   pdl_trigger();
+  if constexpr (!DOWN) {
+    if (ticket >= 0) {
+      const int nct = a.copy_rows * gridDim.x;
+      if (__ldcg(a.mc.n + 2) > 0) {
+        if (ticket < nct) {
+          copier = ticket;
+        } else {
+          item_y = a.copy_rows + (ticket - nct) / gridDim.x;
+          item_x = (ticket - nct) % gridDim.x;
+        }
+      } else {
+        // no misses: the items take the first tickets, the last nct CTAs exit
+        const int items = ((int)gridDim.y - a.copy_rows) * gridDim.x;
+        if (ticket >= items) return;
+        item_y = a.copy_rows + ticket / gridDim.x;
+        item_x = ticket % gridDim.x;
+      }
+    }
+  }
   if constexpr (!DOWN) {
     if (copier >= 0) {
       // a copying CTA: gate/up bytes of every miss, the flag, then the down bytes

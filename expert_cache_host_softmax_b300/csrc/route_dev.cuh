@@ -425,6 +425,10 @@ __device__ __forceinline__ void route_decode_body(const RouteArgs &a, int *smem,
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   Prefetch pf;
   prefetch_tables(a, s_keyslot, pf);
+  // the call's logits (an input, final before the kernel ahead, which writes
+  // only the previous call's output) are asked into L2 before the wait
+  for (int i = tid * 32; i < a.T * E; i += blockDim.x * 32)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.logits + i));
   if (pdl) {
     pdl_wait();
     pdl_trigger();

@@ -154,6 +154,10 @@ int ft_moe_prefill_hit_d2d(ft_moe *h);
  *   x             device bf16 [n_tokens][H]
  *   router_logits device f32  [n_tokens][E]
  *   out           device bf16 [n_tokens][H]   (written; may not alias x)
+ * x and router_logits may not alias the previous call's out either: this
+ * call's kernels read them before the previous call's last kernel has
+ * completed (they must be final when this call is issued on `stream`, as any
+ * input written by earlier work on the stream is).
  * For each token, experts = the top_k largest logits (ties to the lower id),
  * gates = softmax over those top_k logits, and
  * out = sum_j gate_j * W_d (silu(W_g x) * (W_u x)) over the token's experts,
