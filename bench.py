@@ -335,6 +335,9 @@ EXTRA_WORKLOADS = (
     ("prefill35b_nvfp4_fp4act", "prefill35b",
      dict(fmt="nvfp4", act="fp4", steps=5, warmup=3, profile_steps=2, n_phys=128)),
     ("stream753b", "stream753b", dict(fmt=None, act="bf16", steps=2, warmup=3, profile_steps=1, n_phys=512)),
+    # every expert of the 48-layer stack resident (6144 slots, 16.3 GB): no misses, the GEMV's HBM rate
+    ("decode35b_resident", "decode35b",
+     dict(fmt=None, act="bf16", steps=20, warmup=5, profile_steps=8, n_phys=768, slots=6144)),
 )
 
 _FP4_PEAK = {}
@@ -377,7 +380,8 @@ def run_ours(args, cfg):
             sub = argparse.Namespace(**{**vars(args), **opts, "fmt": opts["fmt"], "act": opts["act"], "hit_d2d_cache": 0,
                                         "ffn": "auto", "miss_path": "auto", "fused_decode": False})
             try:
-                w = _measure(sub, CONFIGS[cname], dev, ws, rank, resize=False)
+                wcfg = dict(CONFIGS[cname], S=opts["slots"]) if "slots" in opts else CONFIGS[cname]
+                w = _measure(sub, wcfg, dev, ws, rank, resize=False)
                 keep = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "e2e",
                         "gpu_launches", "roofline", "path_roofline", "clocks")
                 line["workloads"][name] = {key_: w[key_] for key_ in keep}

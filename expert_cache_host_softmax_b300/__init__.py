@@ -243,7 +243,7 @@ class MoELayerStack:
         _check(lib().ft_moe_set_decode_fusion(self._h, 1 if on else 0), self._h)
 
     def set_decode_grid(self, on=True):
-        """Eligible decode calls as one grid (default on), or separate route, gate/up and down kernels."""
+        """Eligible decode calls as one grid, or separate route, gate/up and down kernels (default)."""
         _check(lib().ft_moe_set_decode_grid(self._h, 1 if on else 0), self._h)
 
     def resize_slots(self, n_slots):

@@ -108,7 +108,7 @@ struct ft_moe {
   int *copy_sync = nullptr;          // misses copied inside the gate/up kernel: flag, arrival count, role ticket
   int32_t *seq_ring = nullptr;       // pinned: seq_ring[seq % 64] = seq, the source of the copy-flag write
   bool decode_fused = false;   // ft_moe_set_decode_fusion
-  bool decode_grid = true;     // ft_moe_set_decode_grid: eligible decode calls as one grid
+  bool decode_grid = false;    // ft_moe_set_decode_grid: eligible decode calls as one grid
   int *grid_sync = nullptr;    // the decode grid's flags and counters
   int miss_path = FT_MISS_AUTO;
   // FP4 x FP4 variant of the tensor-core FFN (ft_moe_set_act_format): buffers

@@ -382,7 +382,7 @@ int ft_moe_miss_path(const ft_moe *h, int tensor_core);
  * Errors: FT_ERR_ARG. */
 int ft_moe_set_decode_fusion(ft_moe *h, int on);
 
-/* Decode calls as one grid (on by default).  An LRU-mode call that runs the
+/* Decode calls as one grid (off by default).  An LRU-mode call that runs the
  * GEMV with the misses copied on the GPU (FT_MISS_KERNEL), with at most 32
  * (token, rank) pairs and at most 4 tokens, runs as a single grid whose CTAs
  * take their role by arrival ticket: the router (top-k, permute, LRU plan),
@@ -391,9 +391,10 @@ int ft_moe_set_decode_fusion(ft_moe *h, int on);
  * items with the combine.  Every CTA waits only for CTAs with smaller tickets,
  * so the grid progresses whatever the order of dispatch; each wait is bounded
  * (FT_ERR_DEVICE at the next synchronising call).  The results are those of
- * the separate route, gate/up and down kernels, bit for bit.  Off: those
- * separate kernels.  Synchronises the handle.  Errors: FT_ERR_ARG,
- * FT_ERR_DEVICE. */
+ * the separate route, gate/up and down kernels, bit for bit.  Off (the
+ * default): those separate kernels, which measure faster on decode-sized
+ * calls (the grid's CTAs carry the registers of its largest role, so fewer
+ * fit per SM).  Synchronises the handle.  Errors: FT_ERR_ARG, FT_ERR_DEVICE. */
 int ft_moe_set_decode_grid(ft_moe *h, int on);
 
 /* Bytes between consecutive slots in the device slot bank. */

@@ -817,6 +817,7 @@ def test_decode_grid_matches_split_kernels(fmt, T, k):
     seed = 191 + T + k
     grid, orc, pool = Hn.make_pair(H, E, k, I, fmt, S, L, T, seed)
     grid.set_miss_path("kernel")
+    grid.set_decode_grid(True)
     split = F.MoELayerStack(H, E, k, I, fmt, S, L, T)
     split.load_pool(pool.pointers, keepalive=pool)
     split.set_miss_path("kernel")
