@@ -343,6 +343,32 @@ EXTRA_WORKLOADS = (
 _FP4_PEAK = {}
 
 
+def kernel_sources_sha():
+    """sha256 of the library's CUDA sources (every file under the package's
+    csrc/, in name order): the kernels that a stored ncu capture measured."""
+    import hashlib
+    d = os.path.join(ROOT, "expert_cache_host_softmax_b300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload, kernel):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    committed ncu summary table (profiles/traffic.json), or None when the table
+    has no entry or was taken on other kernel sources than these."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    t = json.load(open(p))
+    if t.get("kernel_sources_sha") != kernel_sources_sha():
+        return None
+    e = t.get("workloads", {}).get(workload, {}).get(kernel)
+    return None if e is None else float(e["dram_bytes_per_launch"])
+
+
 def fp4_peak(n_tile=256):
     """The block-scaled FP4 tensor-core rate measured by the library's probe
     (ft_fp4_tensor_peak: MMAs on operands already in shared memory), best of 3
@@ -660,6 +686,21 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_src": peaks["src"],
                     "bytes_per_call": b_dom / calls_p, "ms_per_call": ms_dom / calls_p, "kernel_ms_share": share}
+    # every FFN kernel's own rates (the dominant one above; all of them here)
+    roofline["kernels"] = {
+        n: {"ms_per_call": v[1] / calls_p, "algorithmic_bytes_per_call": v[0] / calls_p,
+            "hbm_gbs": v[0] / (v[1] * 1e-3) / 1e9 if v[1] > 0 else None,
+            "hbm_frac": v[0] / (v[1] * 1e-3) / 1e9 / peaks["hbm_gbs"] if v[1] > 0 else None,
+            "tflops": v[2] / (v[1] * 1e-3) / 1e12 if v[1] > 0 and v[2] > 0 else None}
+        for n, v in kern.items() if v[1] > 0}
+    trk = {"gateup": "gateup", "down": "down", "route": "route", "combine": "combine",
+           "decode_layer": "decode_layer"}.get(dom, dom)
+    tr = stored_traffic(cfg["name"] + ("_" + fmt if cfg["name"].startswith("prefill") else "")
+                        + ("_fp4act" if fp4_act else "") + ("_resident" if S >= L * E and cfg["mode"] == "lru"
+                                                             and not cfg["name"].startswith("prefill") else ""), trk)
+    roofline["traffic"] = tr
+    roofline["traffic_src"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, profiles/traffic.json"
+                               if tr is not None else "no ncu capture of these kernel sources")
     copy_ms = prof["miss_copy"][0]
     copy_gbs = pd["misses"] * nb / (copy_ms * 1e-3) / 1e9 if copy_ms > 0 and pd["misses"] > 0 else None
     stream_ms = prof["stream_copy"][0]

@@ -145,14 +145,19 @@ __global__ void __launch_bounds__(256) scatter_chunk_kernel(const int32_t *__res
 }
 
 // Threads of the single-CTA routing kernel: at least E (one per expert in
-// the plan), at least 256, a whole number of warps.
-int small_threads(int E) { return std::min(kRouteThreads, std::max(256, (E + 31) / 32 * 32)); }
+// the plan), at least 256, enough that each thread's share of the recency
+// list (S slots) fits the kPre entries it loads before the wait on the
+// kernel ahead (S = 6144 slots: 768 threads), a whole number of warps.
+int small_threads(int E, int S) {
+  const int for_slots = (S + kPre - 1) / kPre;
+  return std::min(kRouteThreads, std::max({256, (E + 31) / 32 * 32, (for_slots + 31) / 32 * 32}));
+}
 
 // Both single-CTA bodies: 6 E-sized arrays, 33 scan partials, the general
 // path's per-warp counts (nw*E) or the decode path's 68 pair and plan ints,
 // and the hit bitmap.
 size_t small_smem_bytes(int E, int S) {
-  const size_t nw = small_threads(E) / 32;
+  const size_t nw = small_threads(E, S) / 32;
   return sizeof(int) * (6 * (size_t)E + 33 + std::max<size_t>(nw * (size_t)E, 68)) +
          sizeof(unsigned) * (((size_t)S + 31) / 32);
 }
@@ -184,8 +189,8 @@ int route_kernel_count(int T, int k) { return T * k <= kSmallRoutePairs ? 1 : 3;
 // three kernels over kChunkTokens-token chunks.
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t s) {
   if (a.T * a.k <= kSmallRoutePairs || a.chunk_counts == nullptr) {
-    return launch_k(route_small_kernel, dim3(1), dim3(small_threads(a.E)), small_smem_bytes(a.E, a.S), s, a.pdl != 0,
-                    a);
+    return launch_k(route_small_kernel, dim3(1), dim3(small_threads(a.E, a.S)), small_smem_bytes(a.E, a.S), s,
+                    a.pdl != 0, a);
   }
   RouteArgs b = a;
   b.n_chunks = n_chunks_of(a.T);

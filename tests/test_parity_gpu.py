@@ -367,6 +367,23 @@ def test_layer_with_masked_logits_matches_oracle(T):
     gpu.close()
 
 
+@pytest.mark.parametrize("S,warm", [(2048, False), (6144, True), (8192, False)])
+def test_route_with_many_slots_matches_oracle(S, warm):
+    # the routing CTA grows with the slot count (each thread's share of the
+    # recency list loaded before the wait): decode calls on 2048..8192 slots,
+    # cold (free slots taken lowest first) or fully resident
+    H, I, E, k, L, T = 256, 256, 128, 8, 48, 1
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", S, L, T, 211, n_phys=64, warm=warm, keep=False)
+    for step in range(2):
+        for layer in range(0, L, 5):
+            x, lg = Hn.inputs(211, T, H, E, step, layer, zipf=1.1)
+            _check_call(gpu, orc, layer, x, lg)
+    cum, _ = gpu.stats()
+    for key_ in ("lookups", "hits", "misses", "evictions", "warm_loads"):
+        assert cum[key_] == orc.stats[key_], key_
+    gpu.close()
+
+
 def test_unit_global_scale_nvfp4():
     # g = 1 puts N(0, 0.02) block scales in E4M3's subnormal range
     H, I, E, k, T = 256, 256, 4, 2, 6
