@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
     if (lane == 0) {
       int j = 0;
       bool ok = true;
+      const uint64_t wpol = l2_evict_first();   // weight tiles stream through once per expert
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const QTile ti = q_decode(tile, s_start, s_mt, s_pad, nU, NTN, a);
         const uint8_t *sfa = a.a_sf + (size_t)(ti.prow0 >> 7) * (K >> 6) * 512;
@@ -376,10 +377,11 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
           mbar_arrive_expect_tx(FULL(s), Q_A + Q_B + Q_SF);
           tma_load_2d(sA + s * Q_A, &tmA, FULL(s), kb * (QBK / 2), ti.prow0);
           if constexpr (DOWN) {
-            tma_load_3d(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * QBN, ti.slot);
+            tma_load_3d_hint(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * QBN, ti.slot, wpol);
           } else {
-            tma_load_3d(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * (QBN / 2), ti.slot);
-            tma_load_3d(sB + s * Q_B + Q_B / 2, &tmB, FULL(s), kb * (QBK / 2), a.I + ti.n * (QBN / 2), ti.slot);
+            tma_load_3d_hint(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * (QBN / 2), ti.slot, wpol);
+            tma_load_3d_hint(sB + s * Q_B + Q_B / 2, &tmB, FULL(s), kb * (QBK / 2), a.I + ti.n * (QBN / 2), ti.slot,
+                             wpol);
           }
           bulk_load(sSFA + s * Q_SF, sfa + (size_t)kb * Q_SF, Q_SF, FULL(s));
           // B scales in row order: 16 bytes (the stage's 16 blocks) of each tile row
@@ -533,6 +535,7 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
           gw = a.plan.gates[pair] * g0;
         }
         const bool store_y = a.out_acc == nullptr || a.keep_y;
+        const uint64_t opol = l2_evict_last();   // the output rows stay in L2 for the other pairs' updates
 #pragma unroll 1
         for (int c = 0; c < QBN / 2; c += 16) {
           float v[16];
@@ -545,10 +548,10 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
                 o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
             }
             if (acc != nullptr) {
-              float4 *o = reinterpret_cast<float4 *>(acc + c);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                atomicAdd(o + i, make_float4(v[4 * i] * gw, v[4 * i + 1] * gw, v[4 * i + 2] * gw, v[4 * i + 3] * gw));
+                red_add_v4(acc + c + 4 * i,
+                           make_float4(v[4 * i] * gw, v[4 * i + 1] * gw, v[4 * i + 2] * gw, v[4 * i + 3] * gw), opol);
             }
           }
         }

@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
     if (lane == 0) {
       int j = 0;
       bool ok = true;
+      const uint64_t wpol = l2_evict_first();   // each weight tile is read by the M tiles of one expert, then never
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
         const int r0 = DOWN ? ti.n * BN : ti.n * (BN / 2);            // first weight row (gate rows for gate/up)
@@ -251,16 +252,16 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
           tma_load_2d(sA + s * A_STAGE, &tmA, FULL(s), kb * BK, ti.row0);
           if constexpr (!C::kConv) {
             const uint32_t dst = sB + s * B_STAGE;
-            tma_load_3d(dst, &tmB, FULL(s), kb * BK, r0, ti.slot);
-            tma_load_3d(dst + B_STAGE / 2, &tmB, FULL(s), kb * BK, r1, ti.slot);
+            tma_load_3d_hint(dst, &tmB, FULL(s), kb * BK, r0, ti.slot, wpol);
+            tma_load_3d_hint(dst + B_STAGE / 2, &tmB, FULL(s), kb * BK, r1, ti.slot, wpol);
           } else {
             const int rs = j % NR;
             if (!mbar_wait(RAWEMPTY(rs), ((j / NR) & 1) ^ 1, s_abort, a.err, 11)) { ok = false; ++j; break; }
             fence_proxy_async();   // the converters' reads of this slot precede the TMA's writes
             mbar_arrive_expect_tx(RAWFULL(rs), C::kRawStage);
             const uint32_t dst = sRaw + rs * C::kRawStage;
-            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * C::kRawRow, r0, ti.slot);
-            tma_load_3d(dst + C::kRawStage / 2, &tmB, RAWFULL(rs), kb * C::kRawRow, r1, ti.slot);
+            tma_load_3d_hint(dst, &tmB, RAWFULL(rs), kb * C::kRawRow, r0, ti.slot, wpol);
+            tma_load_3d_hint(dst + C::kRawStage / 2, &tmB, RAWFULL(rs), kb * C::kRawRow, r1, ti.slot, wpol);
           }
         }
       }
@@ -500,6 +501,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
           gw = a.plan.gates[pair] * g0;
         }
         const bool store_y = a.out_acc == nullptr || a.keep_y;
+        const uint64_t opol = l2_evict_last();   // the output rows stay in L2 for the other pairs' updates
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
@@ -513,10 +515,10 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
                 o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
             }
             if (acc != nullptr) {
-              float4 *o = reinterpret_cast<float4 *>(acc + c);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                atomicAdd(o + i, make_float4(v[4 * i] * gw, v[4 * i + 1] * gw, v[4 * i + 2] * gw, v[4 * i + 3] * gw));
+                red_add_v4(acc + c + 4 * i,
+                           make_float4(v[4 * i] * gw, v[4 * i + 1] * gw, v[4 * i + 2] * gw, v[4 * i + 3] * gw), opol);
             }
           }
         }

@@ -40,8 +40,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(RouteArgs a)
 }
 
 // Multi-CTA path, step 1: top-k + gates for kChunkTokens tokens per CTA
-// (one warp per token), and the CTA's expert histogram.
-__global__ void __launch_bounds__(256) topk_chunk_kernel(const float *__restrict__ logits, int T, int E, int k,
+// (one warp per token, all of the chunk's tokens at once), and the CTA's
+// expert histogram.
+constexpr int kTopkThreads = kChunkTokens * 32;
+__global__ void __launch_bounds__(kTopkThreads) topk_chunk_kernel(const float *__restrict__ logits, int T, int E, int k,
                                                          int32_t *idx, float *gates, int32_t *chunk_counts) {
   __shared__ int s_count[kMaxExperts];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -194,7 +196,7 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s) {
   }
   RouteArgs b = a;
   b.n_chunks = n_chunks_of(a.T);
-  topk_chunk_kernel<<<b.n_chunks, 256, 0, s>>>(a.logits, a.T, a.E, a.k, a.plan.topk_idx, a.plan.gates,
+  topk_chunk_kernel<<<b.n_chunks, kTopkThreads, 0, s>>>(a.logits, a.T, a.E, a.k, a.plan.topk_idx, a.plan.gates,
                                                b.chunk_counts);
   plan_kernel<<<1, kRouteThreads, plan_smem_bytes(a.E, a.S), s>>>(b, 1);
   scatter_chunk_kernel<<<b.n_chunks, 256, sizeof(int) * 9 * (size_t)a.E, s>>>(
@@ -205,7 +207,7 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t s) {
 cudaError_t launch_topk_only(const float *logits, int T, int E, int k, int32_t *idx, float *gates,
                              cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  topk_chunk_kernel<<<n_chunks_of(T), 256, 0, s>>>(logits, T, E, k, idx, gates, nullptr);
+  topk_chunk_kernel<<<n_chunks_of(T), kTopkThreads, 0, s>>>(logits, T, E, k, idx, gates, nullptr);
   return cudaGetLastError();
 }
 
