@@ -367,7 +367,6 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
     if (lane == 0) {
       int j = 0;
       bool ok = true;
-      const uint64_t wpol = l2_evict_first();   // weight tiles stream through once per expert
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const QTile ti = q_decode(tile, s_start, s_mt, s_pad, nU, NTN, a);
         const uint8_t *sfa = a.a_sf + (size_t)(ti.prow0 >> 7) * (K >> 6) * 512;
@@ -377,11 +376,10 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
           mbar_arrive_expect_tx(FULL(s), Q_A + Q_B + Q_SF);
           tma_load_2d(sA + s * Q_A, &tmA, FULL(s), kb * (QBK / 2), ti.prow0);
           if constexpr (DOWN) {
-            tma_load_3d_hint(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * QBN, ti.slot, wpol);
+            tma_load_3d(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * QBN, ti.slot);
           } else {
-            tma_load_3d_hint(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * (QBN / 2), ti.slot, wpol);
-            tma_load_3d_hint(sB + s * Q_B + Q_B / 2, &tmB, FULL(s), kb * (QBK / 2), a.I + ti.n * (QBN / 2), ti.slot,
-                             wpol);
+            tma_load_3d(sB + s * Q_B, &tmB, FULL(s), kb * (QBK / 2), ti.n * (QBN / 2), ti.slot);
+            tma_load_3d(sB + s * Q_B + Q_B / 2, &tmB, FULL(s), kb * (QBK / 2), a.I + ti.n * (QBN / 2), ti.slot);
           }
           bulk_load(sSFA + s * Q_SF, sfa + (size_t)kb * Q_SF, Q_SF, FULL(s));
           // B scales in row order: 16 bytes (the stage's 16 blocks) of each tile row

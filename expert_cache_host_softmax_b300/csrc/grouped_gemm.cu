@@ -240,7 +240,6 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
     if (lane == 0) {
       int j = 0;
       bool ok = true;
-      const uint64_t wpol = l2_evict_first();   // each weight tile is read by the M tiles of one expert, then never
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
         const int r0 = DOWN ? ti.n * BN : ti.n * (BN / 2);            // first weight row (gate rows for gate/up)
@@ -252,16 +251,16 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
           tma_load_2d(sA + s * A_STAGE, &tmA, FULL(s), kb * BK, ti.row0);
           if constexpr (!C::kConv) {
             const uint32_t dst = sB + s * B_STAGE;
-            tma_load_3d_hint(dst, &tmB, FULL(s), kb * BK, r0, ti.slot, wpol);
-            tma_load_3d_hint(dst + B_STAGE / 2, &tmB, FULL(s), kb * BK, r1, ti.slot, wpol);
+            tma_load_3d(dst, &tmB, FULL(s), kb * BK, r0, ti.slot);
+            tma_load_3d(dst + B_STAGE / 2, &tmB, FULL(s), kb * BK, r1, ti.slot);
           } else {
             const int rs = j % NR;
             if (!mbar_wait(RAWEMPTY(rs), ((j / NR) & 1) ^ 1, s_abort, a.err, 11)) { ok = false; ++j; break; }
             fence_proxy_async();   // the converters' reads of this slot precede the TMA's writes
             mbar_arrive_expect_tx(RAWFULL(rs), C::kRawStage);
             const uint32_t dst = sRaw + rs * C::kRawStage;
-            tma_load_3d_hint(dst, &tmB, RAWFULL(rs), kb * C::kRawRow, r0, ti.slot, wpol);
-            tma_load_3d_hint(dst + C::kRawStage / 2, &tmB, RAWFULL(rs), kb * C::kRawRow, r1, ti.slot, wpol);
+            tma_load_3d(dst, &tmB, RAWFULL(rs), kb * C::kRawRow, r0, ti.slot);
+            tma_load_3d(dst + C::kRawStage / 2, &tmB, RAWFULL(rs), kb * C::kRawRow, r1, ti.slot);
           }
         }
       }
