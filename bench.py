@@ -639,14 +639,20 @@ def _measure(args, cfg, dev, ws, rank, resize=True):
     gu_bytes, d_bytes = _ffn_bytes(fmt, H, I)
     calls_p = n_prof * L
     toks_p = sum(tokens_at(cfg, s) for s in range(W, W + n_prof)) * L
-    act_gu = toks_p * k * (H * 2 + I * 2)          # x rows read per (token, expert) + h written
-    act_dn = toks_p * k * (I * 2 + H * 4)          # h read + y written
+    # h per (token, expert) pair: bf16, or e2m1 codes plus an E4M3 scale per 16
+    h_pair = I // 2 + I // 16 if fp4_act else I * 2
+    act_gu = toks_p * H * 2 + toks_p * k * h_pair  # x read once per token (the kernels gather it per pair) + h written
+    if ffn_kernel == "tc":
+        act_dn = toks_p * k * h_pair + toks_p * H * 4   # h read + the fp32 output rows the epilogue accumulates
+    else:
+        act_dn = toks_p * k * (I * 2 + H * 4)       # h read + y written per pair
     fl_gu, fl_dn = 2 * toks_p * k * 2 * I * H, 2 * toks_p * k * H * I
     kern = {
         "gateup": (pd["lookups"] * gu_bytes + act_gu, prof["gateup_hit"][0] + prof["gateup_miss"][0], fl_gu),
         "down": (pd["lookups"] * d_bytes + act_dn, prof["down"][0], fl_dn),
         "route": (toks_p * E * 4, prof["route"][0], 0),
-        "combine": (toks_p * (k * H * 4 + H * 2), prof["combine"][0], 0),
+        # tensor cores: the fp32 output rows converted to bf16; GEMV: y rows gathered and weighted
+        "combine": (toks_p * H * 6 if ffn_kernel == "tc" else toks_p * (k * H * 4 + H * 2), prof["combine"][0], 0),
     }
     if prof.get("layer", (0.0, 0))[1] > 0:
         # decode calls ran as the fused layer kernel: routing, FFN and combine in one launch

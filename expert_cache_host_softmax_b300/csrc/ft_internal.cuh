@@ -191,10 +191,8 @@ void gemm_init_attributes();
 int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, int H, int I, void *map_gu,
                      void *map_d);
 int make_act_map(const void *base, int64_t rows, int K, void *map);
-cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, int k, int H, int n, __nv_bfloat16 *xp,
-                               cudaStream_t s);
-cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const void *map_h, const void *map_gu,
-                          const void *map_d, int *err, int64_t max_rows, cudaStream_t s);
+cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_h, const void *map_gu, const void *map_d,
+                          int *err, int64_t max_rows, cudaStream_t s);
 
 // FP4 x FP4 variant of the tensor-core FFN (gemm_fp4.cu).  Buffers over
 // expert-padded rows (see fp4_padded_rows): x and h as e2m1 codes [rows][K/2],

@@ -97,8 +97,7 @@ struct ft_moe {
   // tensor-core FFN: TMA descriptors over the slot bank, the kernel choice,
   // and a device error word that bounded waits write when they give up
   alignas(64) unsigned char tmap[2][128] = {};     // weights: gate/up, down
-  alignas(64) unsigned char amap[2][128] = {};     // activations: permuted x rows, h
-  __nv_bfloat16 *xpbuf = nullptr;                  // x gathered into permuted order [Tmax*k][H]
+  alignas(64) unsigned char amap[128] = {};        // activations: h
   bool tmaps_ok = false;
   int ffn_kernel = FT_FFN_AUTO;
   int *err_dev = nullptr;
@@ -183,7 +182,6 @@ void free_all(ft_moe *h) {
   cudaFree(h->ybuf);
   cudaFree(h->out_acc);
   cudaFree(h->err_dev);
-  cudaFree(h->xpbuf);
   cudaFree(h->combine_counters);
   cudaFree(h->pool_dev);
   cudaFree(h->mega_sync);
@@ -284,15 +282,7 @@ cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cud
     return launch_tc_ffn_fp4(fa, down, h->q, h->qmap[down ? 1 : 0], h->qmap[down ? 3 : 2], h->qmap[down ? 5 : 4],
                              h->err_dev, (int64_t)T * h->k, s);
   }
-  if (tc) {
-    if (!down && fa.only != 2) {
-      // the permuted x rows, once per call (before the first gate/up launch)
-      cudaError_t e = launch_gather_rows(fa.x, fa.plan.perm, h->k, h->H, T * h->k, h->xpbuf, s);
-      if (e != cudaSuccess) return e;
-      h->kernel_launches += 1;
-    }
-    return launch_tc_ffn(fa, down, h->amap[0], h->amap[1], h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
-  }
+  if (tc) return launch_tc_ffn(fa, down, h->amap, h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
   return down ? launch_down(fa, cb, s) : launch_gateup(fa, s);
 }
 
@@ -651,7 +641,6 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->out_acc, (size_t)max_tokens * hidden) == cudaSuccess &&
             dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
-            dev_alloc(&h->xpbuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->mega_sync, 4) == cudaSuccess && cudaMemset(h->mega_sync, 0, 16) == cudaSuccess &&
             dev_alloc(&h->copy_sync, 4) == cudaSuccess && cudaMemset(h->copy_sync, 0, 16) == cudaSuccess &&
             dev_alloc(&h->grid_sync, decode_grid_sync_ints(umax)) == cudaSuccess &&
@@ -690,8 +679,7 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
   // the tensor-core FFN takes BF16, NVFP4 and MXFP4 (FP8 experts run on the GEMV)
   h->tmaps_ok =
                 make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
-                make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
-                make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
+                make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap) == 0;
   if (int rc = reset_tables(h, false)) { g_create_err = h->err; return bail(rc); }
   *out = h;
   return FT_OK;
@@ -817,8 +805,7 @@ int ft_moe_resize_slots(ft_moe *h, int n_slots) {
   const size_t TK = (size_t)h->Tmax * h->k;
   h->tmaps_ok =
                 make_weight_maps(h->slots, h->slot_stride, h->S, h->fmt, h->H, h->I, h->tmap[0], h->tmap[1]) == 0 &&
-                make_act_map(h->xpbuf, (int64_t)TK, h->H, h->amap[0]) == 0 &&
-                make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap[1]) == 0;
+                make_act_map(h->hbuf, (int64_t)TK, h->I, h->amap) == 0;
   if (h->q.xq)
     h->qmaps_ok = make_fp4_maps(h->slots, h->slot_stride, h->S, h->H, h->I, h->q.xq, h->q.hq, h->q_rows, h->qmap[0],
                                 h->qmap[1], h->qmap[2], h->qmap[3], h->qmap[4], h->qmap[5]) == 0;

@@ -3,22 +3,25 @@
 //
 // Per distinct expert u of a call (blob in slot u_slot[u]; its tokens sit at
 // permuted positions offsets[e] .. offsets[e+1]):
-//   gate/up:  [g | u] = xp_rows . W_gu^T  (fp32 accumulators in TMEM)
+//   gate/up:  [g | u] = x_rows . W_gu^T (fp32 accumulators in TMEM; row i of
+//             the expert's tile is x[perm[i] / k], one row per (token, rank)
+//             pair)
 //             h = bf16( silu(g) * u )     (epilogue)
 //   down:     y = h . W_d^T               (fp32), combined in the epilogue:
 //             out_acc[token] += gate * y row  (fp32 atomics)
-// xp is x gathered into permuted order (one row per (token, rank) pair) by a
-// small kernel first, so that both GEMMs read their token rows as plain
-// 128-row boxes.  The pages say only that cached experts run "at GPU speed"
-// ("Why a Huge MoE Model Fits on One Consumer GPU"); SwiGLU and this kernel
-// design are ours.
+// The pages say only that cached experts run "at GPU speed" ("Why a Huge MoE
+// Model Fits on One Consumer GPU"); SwiGLU and this kernel design are ours.
 //
 // One persistent CTA per SM walks the call's output tiles.  A tile is 128
 // token rows x 256 weight rows (gate/up: 128 gate rows + the 128 matching up
 // rows, so the SiLU*mul epilogue sees both halves; down: 256 rows of H).
 // K advances in blocks of 64 through a ring of shared-memory stages:
-//   - one producer thread issues, per stage, the TMA load of the A box (128
-//     token rows x 64, 128-byte swizzle) and of the weights: BF16 weights land
+//   - gate/up: two gatherer warps copy the stage's 128 x rows (64 K each)
+//     straight from x, by token index, into the 128-byte-swizzled A layout
+//     (cp.async, 16 bytes a copy; x is small enough to stay in L2 across the
+//     N tiles that reuse it); down: the producer TMA-loads the A box of h;
+//   - one producer thread issues, per stage, the TMA load of the weights
+//     (and of the down GEMM's A box): BF16 weights land
 //     directly in the swizzled layout; NVFP4 / MXFP4 / FP8 codes land raw in a
 //     separate ring, and eight converter warps dequantise them to bf16
 //     (e2m1 x block scale, or the bare E4M3 value: exact in bf16) into the
@@ -67,12 +70,17 @@ struct Cfg {
   // stages of A + (bf16) B; the converted formats also have a ring of raw-code stages
   static constexpr int kNS = kConv ? 3 : 4;
   static constexpr int kNR = kConv ? 4 : 0;
-  // warp roles: 0 producer, 1 MMA, 2-3 idle, 4-7 epilogue, 8-15 converters
-  static constexpr int kProdWarp = 0, kMmaWarp = 1, kEpiWarp0 = 4, kConvWarp0 = 8;
+  // warp roles: 0 producer, 1 MMA, 2-3 x gatherers (gate/up; idle in down),
+  // 4-7 epilogue, 8-15 converters
+  static constexpr int kProdWarp = 0, kMmaWarp = 1, kGatherWarp0 = 2, kEpiWarp0 = 4, kConvWarp0 = 8;
+  static constexpr int kGatherThreads = 64;
   static constexpr int kConvThreads = kConv ? 256 : 0;
   static constexpr int kThreads = kConv ? 512 : 256;
-  // FULL arrivals per stage: the producer's expect_tx, plus one per converter thread
-  static constexpr int kFullCount = 1 + kConvThreads;
+  // FULL arrivals per stage: the producer's expect_tx, plus one per converter
+  // thread, plus (gate/up) one per gatherer thread
+  __host__ __device__ static constexpr int full_count(bool down) {
+    return 1 + kConvThreads + (down ? 0 : kGatherThreads);
+  }
   // shared memory: [A x kNS][B x kNS][RAW x kNR] then barriers and tables
   static constexpr int kOffB = kNS * A_STAGE;
   static constexpr int kOffRaw = kOffB + kNS * B_STAGE;
@@ -184,7 +192,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
   // ---- prologue: barriers, TMEM, tile table
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
-      mbar_init(FULL(s), C::kFullCount);
+      mbar_init(FULL(s), C::full_count(DOWN));
       mbar_init(EMPTY(s), 1);
     }
     for (int r = 0; r < NR; ++r) {
@@ -235,8 +243,9 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
   if (warp == C::kProdWarp) {
     // ================================================================ producer
     // Per stage: wait for the slot; one expect_tx for the stage's TMA bytes;
-    // A box (128 permuted rows x 64 K) and, for BF16, the two halves of the
-    // weight tile; for FP4, the raw codes into their own ring.
+    // for down, the A box (128 permuted h rows x 64 K; the gate/up A rows come
+    // from the gatherers); for BF16, the two halves of the weight tile; for
+    // FP4, the raw codes into their own ring.
     if (lane == 0) {
       int j = 0;
       bool ok = true;
@@ -247,8 +256,10 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         for (int kb = 0; kb < nk; ++kb, ++j) {
           const int s = j % NS;
           if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 10)) { ok = false; break; }
-          mbar_arrive_expect_tx(FULL(s), A_STAGE + (C::kConv ? 0 : B_STAGE));
-          tma_load_2d(sA + s * A_STAGE, &tmA, FULL(s), kb * BK, ti.row0);
+          constexpr uint32_t tx = (DOWN ? A_STAGE : 0) + (C::kConv ? 0 : B_STAGE);
+          if constexpr (tx > 0) mbar_arrive_expect_tx(FULL(s), tx);
+          else mbar_arrive(FULL(s));
+          if constexpr (DOWN) tma_load_2d(sA + s * A_STAGE, &tmA, FULL(s), kb * BK, ti.row0);
           if constexpr (!C::kConv) {
             const uint32_t dst = sB + s * B_STAGE;
             tma_load_3d(dst, &tmB, FULL(s), kb * BK, r0, ti.slot);
@@ -279,6 +290,42 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (!DOWN && warp >= C::kGatherWarp0 && warp < C::kGatherWarp0 + C::kGatherThreads / 32) {
+    // ================================================================ x gatherers
+    // The gate/up A tile holds the x rows of the tile's permuted pairs
+    // (token perm[row] / k), copied 16 bytes at a time into the swizzled
+    // stage (chunk c of row r at c ^ (r & 7)).  Eight consecutive lanes copy
+    // one 128-byte row segment, so a warp's copy reads 4 whole lines of x and
+    // fills 512 contiguous bytes of the stage; thread (w, l) copies chunk
+    // l & 7 of rows 8 i + 4 w + (l >> 3), i = 0..15.  Rows past the expert's
+    // last pair repeat its last row (their results are dropped).  Each
+    // thread's arrival on FULL fires when its copies have landed, so the
+    // gatherers run up to a whole ring ahead of the MMAs; the MMA thread makes
+    // the landed rows visible to the tensor core's proxy (a proxy fence after
+    // its FULL wait).
+    const int t = tid - C::kGatherWarp0 * 32;
+    const int rsub = 4 * (t >> 5) + (lane >> 3), c = lane & 7;
+    const uint32_t dsub = rsub * 128 + ((c ^ (rsub & 7)) << 4);
+    int j = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
+      const int last = ti.row0 + ti.rows - 1;
+      int tok[BM / 8];
+#pragma unroll
+      for (int i = 0; i < BM / 8; ++i) tok[i] = a.plan.perm[min(ti.row0 + 8 * i + rsub, last)] / a.k;
+      const __nv_bfloat16 *xc = a.x + c * 8;
+      for (int kb = 0; kb < nk; ++kb, ++j) {
+        const int s = j % NS;
+        if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 14)) { ok = false; break; }
+        const uint32_t d = sA + s * A_STAGE + dsub;
+#pragma unroll
+        for (int i = 0; i < BM / 8; ++i) cp_async16(d + i * 1024, xc + (size_t)tok[i] * a.H + kb * BK);
+        cp_async_arrive_noinc(FULL(s));
+      }
+    }
+    // every copy lands before the thread exits
+    cp_async_wait_all();
   } else if (FMT == FMT_FP8 && warp >= C::kConvWarp0) {
     // ================================================================ FP8 converters
     // Each thread expands one B row per stage, 64 E4M3 codes, into the
@@ -416,6 +463,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
             break;
           }
           tc_fence_after();
+          if constexpr (!DOWN) fence_proxy_async();   // the gatherers' x rows, written by cp.async
           const uint32_t a0 = sA + s * A_STAGE, b0 = sB + s * B_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
@@ -546,20 +594,6 @@ cudaError_t launch(const GemmArgs &a, const CUtensorMap &mapA, const CUtensorMap
   return cudaGetLastError();
 }
 
-// xp[i] = x[perm[i] / k] for the n permuted rows (bf16 rows of H).
-__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *__restrict__ x,
-                                                          const int32_t *__restrict__ perm, int k, int H, int n,
-                                                          __nv_bfloat16 *__restrict__ xp) {
-  const int vec = H / 8;
-  const long long total = (long long)n * vec;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(i / vec), v = (int)(i - (long long)r * vec);
-    const uint4 val = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(perm[r] / k) * H) + v);
-    reinterpret_cast<uint4 *>(xp + (size_t)r * H)[v] = val;
-  }
-}
-
 }  // namespace
 
 EncodeTiledFn encode_tiled_fn() {
@@ -579,6 +613,7 @@ static_assert(Cfg<FMT_BF16>::kSmemAlloc <= 227 * 1024, "bf16 smem");
 static_assert(Cfg<FMT_NVFP4>::kSmemAlloc <= 227 * 1024, "fp4 smem");
 static_assert(Cfg<FMT_FP8>::kSmemAlloc <= 227 * 1024, "fp8 smem");
 static_assert(Cfg<FMT_NVFP4>::kThreads == 512 && Cfg<FMT_BF16>::kThreads == 256, "warp roles");
+static_assert(Cfg<FMT_BF16>::kGatherThreads == 64 && BM == 128 && BK == 64, "gatherer row map: 2 warps, 8 lanes a row");
 
 int tc_num_sms() {
   static int n = 0;
@@ -602,8 +637,8 @@ void gemm_init_attributes() {
   set_attr<FMT_FP8, true>();
 }
 
-// Tensor map over a bf16 activation matrix [rows][K] (the permuted x rows,
-// or h): box of 64 K x 128 rows with the 128-byte swizzle.
+// Tensor map over the bf16 activation matrix h [rows][K]: box of 64 K x 128
+// rows with the 128-byte swizzle.
 int make_act_map(const void *base, int64_t rows, int K, void *map) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return -1;
@@ -658,21 +693,12 @@ int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, 
   return 0;
 }
 
-// Gathers x into permuted order for the gate/up GEMM (rows = T*k pairs).
-cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm, int k, int H, int n, __nv_bfloat16 *xp,
-                               cudaStream_t s) {
-  if (n == 0) return cudaSuccess;
-  const long long total = (long long)n * (H / 8);
-  const int grid = (int)std::min<long long>((total + 255) / 256, 148LL * 16);
-  gather_rows_kernel<<<grid, 256, 0, s>>>(x, perm, k, H, n, xp);
-  return cudaGetLastError();
-}
-
 // Grouped gate/up (down=false) or down (down=true) FFN of the call's experts on
-// the tensor cores.  map_xp / map_h: activation maps (make_act_map) over the
-// permuted x rows and over h; map_gu / map_d: the slot-bank weight maps.
-cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const void *map_h, const void *map_gu,
-                          const void *map_d, int *err, int64_t max_rows, cudaStream_t s) {
+// the tensor cores.  map_h: the activation map (make_act_map) over h, the
+// down GEMM's A (the gate/up GEMM gathers its x rows itself); map_gu /
+// map_d: the slot-bank weight maps.
+cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_h, const void *map_gu, const void *map_d,
+                          int *err, int64_t max_rows, cudaStream_t s) {
   GemmArgs a{};
   a.slot_bank = f.slot_bank;
   a.slot_stride = f.slot_stride;
@@ -688,7 +714,7 @@ cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_xp, const
   // M tiles <= ceil(rows / BM) + distinct experts
   const int64_t mtiles = (max_rows + BM - 1) / BM + f.umax;
   const int grid = (int)std::min<int64_t>(tc_num_sms(), std::max<int64_t>(1, mtiles * NTN));
-  const CUtensorMap &mA = *reinterpret_cast<const CUtensorMap *>(down ? map_h : map_xp);
+  const CUtensorMap &mA = *reinterpret_cast<const CUtensorMap *>(map_h);   // unused by gate/up
   const CUtensorMap &mB = *reinterpret_cast<const CUtensorMap *>(down ? map_d : map_gu);
   switch (f.fmt) {
     case FMT_BF16: return down ? launch<FMT_BF16, true>(a, mA, mB, grid, s) : launch<FMT_BF16, false>(a, mA, mB, grid, s);
