@@ -151,11 +151,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 }
 
 // Lanes per weight row: a power of two dividing the row's 32-element chunks,
-// as large as leaves each lane >= 4 chunks (fewer lanes per row for short rows).
+// as large as leaves each lane >= 8 chunks for rows shorter than 4096 (>= 4
+// for longer rows, whose CTAs already take 4 features a warp; fewer lanes per
+// row for short rows).  Eight chunks a lane halves the CTA count against
+// four: a decode gate/up grid over 8 experts of H = 2048, I = 768 is then 384
+// work CTAs, one wave at 5 CTAs per SM, where 768 left a second wave of 28.
 int lanes_per_row(int K) {
   const int chunks = K / 32;
+  const int min_per_lane = K >= 4096 ? 4 : 8;
   for (int l : {32, 16, 8})
-    if (chunks % l == 0 && chunks / l >= 4) return l;
+    if (chunks % l == 0 && chunks / l >= min_per_lane) return l;
   for (int l : {32, 16, 8})
     if (chunks % l == 0) return l;
   return 8;
