@@ -127,9 +127,8 @@ __global__ void __launch_bounds__(kGridThreads) decode_grid_kernel(GridArgs g) {
   __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
   const bool gu_item = t >= 1 + g.n_copy && t < 1 + g.n_copy + n_gu;
   bool x_staged = false;
-  if (gu_item && g.f.max_tokens == 1) {
-    for (int v = threadIdx.x; v < g.f.H / 8; v += blockDim.x)
-      reinterpret_cast<uint4 *>(xs)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(g.f.x) + v);
+  if (NT == 1 && gu_item && g.f.max_tokens == 1) {
+    stage_row1<FMT, false>(xs, g.f.x, g.f.H);
     x_staged = true;
   }
   if (!grid_wait(sync + kPlanFlag, g.seq, g.f.err, 80, &s_ok)) return;
@@ -245,7 +244,7 @@ cudaError_t launch_decode_grid(const RouteArgs &route, const FfnArgs &ffn, const
   g.seq_raised = seq_raised;
   const int NT = ffn.max_tokens <= 1 ? 1 : ffn.max_tokens == 2 ? 2 : 4;
   const size_t route_smem = sizeof(int) * (6 * (size_t)route.E + 33 + 68) + sizeof(unsigned) * (((size_t)route.S + 31) / 32);
-  const size_t smem = std::max(route_smem, (size_t)NT * std::max(ffn.H, ffn.I) * 2);
+  const size_t smem = std::max(route_smem, (size_t)NT * std::max(ffn.H, ffn.I) * 2 + 16);
   if (smem > 96 * 1024) return cudaErrorInvalidValue;
   const int grid = 1 + n_copy + ffn.umax * (g.nb_gu + g.nb_dn);
   switch (ffn.fmt) {

@@ -192,7 +192,7 @@ cudaError_t launch_decode_layer(const RouteArgs &route, const FfnArgs &ffn, cons
   m.nb_gu = ffn.I / (kMegaWarps * (32 / m.lpr_gu) * m.fpw_gu);
   m.nb_dn = ffn.H / (kMegaWarps * (32 / m.lpr_dn) * m.fpw_dn);
   const int NT = ffn.max_tokens <= 1 ? 1 : ffn.max_tokens == 2 ? 2 : 4;
-  const size_t smem = std::max(route_smem, (size_t)NT * std::max(ffn.H, ffn.I) * 2);
+  const size_t smem = std::max(route_smem, (size_t)NT * std::max(ffn.H, ffn.I) * 2 + 16);
   // resident CTAs per launch configuration (cached: the query costs host time)
   static int cap[3][3] = {};
   static size_t cap_smem[3][3] = {};

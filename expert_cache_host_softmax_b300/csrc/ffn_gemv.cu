@@ -78,10 +78,9 @@ __global__ void __launch_bounds__(kWarps * 32) ffn_gemv_kernel(FfnArgs a, Combin
   // down grid, which starts after the gate/up grid passed its wait) are final.
   bool x_staged = false;
   if constexpr (!DOWN) {
-    if (a.max_tokens == 1) {
+    if (NT == 1 && a.max_tokens == 1) {
       // one-token call: every expert multiplies the same row
-      for (int v = threadIdx.x; v < a.H / 8; v += blockDim.x)
-        reinterpret_cast<uint4 *>(xs)[xs_pos(v)] = __ldg(reinterpret_cast<const uint4 *>(a.x) + v);
+      stage_row1<FMT, false>(xs, a.x, a.H);
       __syncthreads();
       x_staged = true;
     }
@@ -173,7 +172,7 @@ cudaError_t launch_t(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) {
   const int fpw = K >= 4096 ? 4 : 1;
   const int fpc = kWarps * (32 / LPR) * fpw;
   dim3 grid((feats + fpc - 1) / fpc, a.umax + (DOWN ? 0 : a.copy_rows));
-  const size_t smem = (size_t)NT * K * sizeof(__nv_bfloat16);
+  const size_t smem = (size_t)NT * K * sizeof(__nv_bfloat16) + 16;   // + the one-token row's scale
   if constexpr (!DOWN)
     if (a.miss_coherent)
       return launch_k(ffn_gemv_kernel<FMT, false, NT, LPR, true>, grid, dim3(kWarps * 32), smem, s, a.pdl != 0, a,
@@ -210,7 +209,7 @@ cudaError_t launch_ffn(const FfnArgs &a, const CombineArgs &cb, cudaStream_t s) 
 
 template <int FMT, bool DOWN, int NT, bool COH>
 void attr_c() {
-  const int max_smem = NT * 8192 * 2;   // activations of NT token rows, K <= 8192
+  const int max_smem = NT * 8192 * 2 + 16;   // activations of NT token rows, K <= 8192
   cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 8, COH>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 16, COH>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   cudaFuncSetAttribute(ffn_gemv_kernel<FMT, DOWN, NT, 32, COH>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);

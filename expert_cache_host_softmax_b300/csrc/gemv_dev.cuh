@@ -123,11 +123,103 @@ __device__ __forceinline__ void decode8(const Chunk<FMT> &ch, int i, float *w) {
 // 4c + i for consecutive chunks c) hit distinct banks.
 __device__ __forceinline__ int xs_pos(int q) { return q ^ ((q >> 3) & 7); }
 
+// c + a.lo * b.lo, then + a.hi * b.hi, for two pairs of 16-bit operands (bf16
+// when BF, else f16) held in 32-bit words: each product is exact in fp32 and
+// rounded once with its sum, as fmaf on the widened operands would be.
+template <bool BF>
+__device__ __forceinline__ float fma2x16(uint32_t a, uint32_t b, float c) {
+  float d;
+  if constexpr (BF)
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %3;\n\tfma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Activation row of a one-token pass (NT = 1), staged for multiplies on the
+// 16-bit operands themselves (no conversion per product): BF16 weights take
+// the bf16 row as it is; the other formats, whose codes convert to f16, take
+// it as f16 scaled by a power of two s that puts the row's largest magnitude
+// in [2^14, 2^15).  Every element down to 2^-31 of that largest one converts
+// exactly, and the factor s passes exactly through every product and sum,
+// so the dot products times 1/s (stored as a float after the row's K
+// values) equal those of the unscaled fp32 arithmetic.  A row whose largest
+// magnitude is zero or not finite is not scaled.  Every thread of the CTA
+// calls this; the caller's barrier publishes the row.
+template <int FMT, bool COH>
+__device__ __forceinline__ void stage_row1(void *xs, const __nv_bfloat16 *src, int K) {
+  const int nv = K / 8;
+  uint4 *dst = reinterpret_cast<uint4 *>(xs);
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  if constexpr (FMT == FMT_BF16) {
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) dst[xs_pos(v)] = ld_w<COH>(s4 + v);
+  } else {
+    __shared__ uint32_t s_wmax[32];
+    uint32_t m = 0;   // largest |x| as fp32 bits
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      const uint4 q = ld_w<COH>(s4 + v);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = max(m, max((w[j] & 0x7FFFu) << 16, w[j] & 0x7FFF0000u));
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0) s_wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = max(m, s_wmax[i]);
+    int k = 0;
+    if (m != 0 && m < 0x7F800000u) k = min(126, max(-126, 14 - ((int)(m >> 23) - 127)));
+    const float s = __uint_as_float((uint32_t)(127 + k) << 23);
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      float f[8];
+      bf16x8_to_float(ld_w<COH>(s4 + v), f);
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h = __floats2half2_rn(f[2 * j] * s, f[2 * j + 1] * s);
+        o[j] = *reinterpret_cast<const uint32_t *>(&h);
+      }
+      dst[xs_pos(v)] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (threadIdx.x == 0)
+      *reinterpret_cast<float *>(static_cast<char *>(xs) + (size_t)K * 2) = __uint_as_float((uint32_t)(127 - k) << 23);
+  }
+}
+
+// Eight weights (elements 8i .. 8i+7 of a chunk) as four f16x2 words (FP4:
+// bare e2m1 values; FP8: E4M3 values; both exact in f16).
+template <int FMT>
+__device__ __forceinline__ void decode8h(const Chunk<FMT> &ch, int i, uint32_t *w) {
+  if constexpr (FMT == FMT_FP8) {
+    const uint4 &v = ch.q[i >> 1];
+    const uint32_t lo = (i & 1) ? v.z : v.x, hi = (i & 1) ? v.w : v.y;
+    const uint32_t pairs[4] = {lo & 0xFFFFu, lo >> 16, hi & 0xFFFFu, hi >> 16};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const __half2 h = e4m3x2_to_half2(pairs[b]);
+      w[b] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+  } else {
+    const uint32_t word = i == 0 ? ch.q[0].x : i == 1 ? ch.q[0].y : i == 2 ? ch.q[0].z : ch.q[0].w;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const __half2 h = e2m1x2_to_half2(word >> (8 * b));
+      w[b] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+  }
+}
+
 // acc[t] += chunk . xs[t][32c .. 32c+31].  FP4: each 8-element partial sum of
 // e2m1 value x activation (every product exact in fp32) is multiplied by its
 // block scale once (NVFP4: elements 0..15 and 16..31 have one E4M3 scale
 // each; MXFP4: one E8M0 scale for all 32); the NVFP4 global scale is applied
-// to the finished dot product.
+// to the finished dot product.  One-token passes (NT = 1) multiply the 16-bit
+// weights and staged activations directly (see stage_row1), in the same order.
 template <int FMT, int NT>
 __device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloat16 *xs, int K, int c, int nt,
                                           float *acc) {
@@ -141,9 +233,24 @@ __device__ __forceinline__ void chunk_fma(const Chunk<FMT> &ch, const __nv_bfloa
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
+    const float s = i < 2 ? s0 : s1;
+    if constexpr (NT == 1) {
+      const uint4 xv = reinterpret_cast<const uint4 *>(xs)[xs_pos(4 * c + i)];
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      uint32_t ww[4];
+      if constexpr (FMT == FMT_BF16) {
+        ww[0] = ch.q[i].x; ww[1] = ch.q[i].y; ww[2] = ch.q[i].z; ww[3] = ch.q[i].w;
+      } else {
+        decode8h<FMT>(ch, i, ww);
+      }
+      float p = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p = fma2x16<FMT == FMT_BF16>(ww[j], xw[j], p);
+      acc[0] = (FMT == FMT_BF16 || FMT == FMT_FP8) ? acc[0] + p : fmaf(s, p, acc[0]);
+      continue;
+    }
     float w[8];
     decode8<FMT>(ch, i, w);
-    const float s = i < 2 ? s0 : s1;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       if (t > 0 && t >= nt) break;   // uniform across the CTA: the expert's token rows in this pass
@@ -367,9 +474,20 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
     }
     for (int c0 = 0; c0 < n; c0 += kTokChunk) {
       const int nt = min(kTokChunk, n - c0);
-      // stage the chunk's activations (bf16 rows of K) in shared memory
+      // stage the chunk's activations in shared memory: one-token passes
+      // through stage_row1, else bf16 rows of K
+      if (NT == 1 && !x_staged) {
+        const __nv_bfloat16 *src;
+        if (DOWN) {
+          src = a.h + (size_t)(off + c0) * a.I;
+        } else {
+          const int pair = COH ? __ldcg(a.plan.perm + off + c0) : a.plan.perm[off + c0];
+          src = a.x + (size_t)(pair / a.k) * a.H;
+        }
+        stage_row1<FMT, COH>(xs, src, K);
+      }
       const int vec_per_row = K / 8;
-      for (int i = threadIdx.x; i < (x_staged ? 0 : nt * vec_per_row); i += blockDim.x) {
+      for (int i = threadIdx.x; i < (NT == 1 || x_staged ? 0 : nt * vec_per_row); i += blockDim.x) {
         const int t = i / vec_per_row, v = i - t * vec_per_row;
         const __nv_bfloat16 *src;
         if (DOWN) {
@@ -381,10 +499,17 @@ __device__ __forceinline__ void gemv_block(const FfnArgs &a, int u, int bx, int 
         reinterpret_cast<uint4 *>(xs + (size_t)t * K)[xs_pos(v)] = ld_w<COH>(reinterpret_cast<const uint4 *>(src) + v);
       }
       __syncthreads();
+      // one-token passes on f16 activations: their scale comes off with the weights' own
+      float g0 = gs0, g1 = gs1;
+      if constexpr (NT == 1 && FMT != FMT_BF16) {
+        const float inv = *reinterpret_cast<const float *>(reinterpret_cast<const char *>(xs) + (size_t)K * 2);
+        g0 *= inv;
+        g1 *= inv;
+      }
       // rows nt..NT-1 of xs may hold stale data: their products are skipped
       for (int fp = 0; fp < fpw; ++fp)
         ffn_rows<FMT, DOWN, NT, LPR, COH>(blob, c0 == 0 ? pull_dst : nullptr, L, a, feat0 + fp * KW * (32 / LPR), xs,
-                                          nt, off + c0, gs0, gs1, l8);
+                                          nt, off + c0, g0, g1, l8);
       __syncthreads();
     }
   }
