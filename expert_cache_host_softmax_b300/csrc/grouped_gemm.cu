@@ -19,7 +19,9 @@
 //   - gate/up: two gatherer warps copy the stage's 128 x rows (64 K each)
 //     straight from x, by token index, into the 128-byte-swizzled A layout
 //     (cp.async, 16 bytes a copy; x is small enough to stay in L2 across the
-//     N tiles that reuse it); down: the producer TMA-loads the A box of h;
+//     N tiles that reuse it), wait for their own copies and fence them into
+//     the async proxy before arriving; down: the producer TMA-loads the A box
+//     of h;
 //   - one producer thread issues, per stage, the TMA load of the weights
 //     (and of the down GEMM's A box): BF16 weights land
 //     directly in the swizzled layout; NVFP4 / MXFP4 / FP8 codes land raw in a
@@ -298,17 +300,26 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
     // one 128-byte row segment, so a warp's copy reads 4 whole lines of x and
     // fills 512 contiguous bytes of the stage; thread (w, l) copies chunk
     // l & 7 of rows 8 i + 4 w + (l >> 3), i = 0..15.  Rows past the expert's
-    // last pair repeat its last row (their results are dropped).  Each
-    // thread's arrival on FULL fires when its copies have landed, so the
-    // gatherers run up to a whole ring ahead of the MMAs; the MMA thread makes
-    // the landed rows visible to the tensor core's proxy (a proxy fence after
-    // its FULL wait).
+    // last pair repeat its last row (their results are dropped).  Stages are
+    // published LAG stages late: once a later stage's copies are issued, the
+    // thread waits for its own copies of the oldest unpublished stage, makes
+    // them visible to the tensor core's proxy and arrives on FULL; a tile's
+    // stages are all published before the next tile's token indices are
+    // loaded.  Deadlock-free for LAG < NS: the stage a gatherer waits to
+    // refill was published LAG - 1 or more iterations earlier.
+    constexpr int LAG = NS >= 4 ? 2 : 1;
     const int t = tid - C::kGatherWarp0 * 32;
     const int rsub = 4 * (t >> 5) + (lane >> 3), c = lane & 7;
     const uint32_t dsub = rsub * 128 + ((c ^ (rsub & 7)) << 4);
-    int j = 0;
+    int j = 0, p0 = 0, np = 0;   // stages p0 .. p0 + np - 1 issued, not yet published
     bool ok = true;
+    auto publish_all = [&]() {
+      cp_async_wait<0>();
+      fence_proxy_async();
+      for (; np > 0; --np, ++p0) mbar_arrive(FULL(p0 % NS));
+    };
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      if (np > 0) publish_all();
       const TileInfo ti = decode_tile(tile, s_start, s_mt, nU, NTN, a);
       const int last = ti.row0 + ti.rows - 1;
       int tok[BM / 8];
@@ -321,11 +332,19 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         const uint32_t d = sA + s * A_STAGE + dsub;
 #pragma unroll
         for (int i = 0; i < BM / 8; ++i) cp_async16(d + i * 1024, xc + (size_t)tok[i] * a.H + kb * BK);
-        cp_async_arrive_noinc(FULL(s));
+        cp_async_commit();
+        if (np == 0) p0 = j;
+        if (++np > LAG) {
+          cp_async_wait<LAG>();
+          fence_proxy_async();
+          mbar_arrive(FULL(p0 % NS));
+          ++p0;
+          --np;
+        }
       }
     }
-    // every copy lands before the thread exits
-    cp_async_wait_all();
+    // the stages still unpublished; every copy lands before the thread exits
+    publish_all();
   } else if (FMT == FMT_FP8 && warp >= C::kConvWarp0) {
     // ================================================================ FP8 converters
     // Each thread expands one B row per stage, 64 E4M3 codes, into the
@@ -463,7 +482,6 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          if constexpr (!DOWN) fence_proxy_async();   // the gatherers' x rows, written by cp.async
           const uint32_t a0 = sA + s * A_STAGE, b0 = sB + s * B_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
