@@ -348,11 +348,12 @@ def test_edge_shapes(E, k, T):
     gpu.close()
 
 
-@pytest.mark.parametrize("T", [2, 300])
+@pytest.mark.parametrize("T", [1, 2, 300])
 def test_layer_with_masked_logits_matches_oracle(T):
     # router logits with -inf (masked experts) and NaN entries, each token
     # keeping at least one finite logit: routing, cache trace and output match
-    # (the decode-sized routing body for T = 2, the multi-CTA path for T = 300)
+    # (the decode-sized routing body for T = 1 and 2, the multi-CTA path for
+    # T = 300)
     H, I, E, k, L = 256, 256, 16, 8, 2
     gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", E, L, T, 57 + T)
     rng = np.random.default_rng(T)
@@ -364,6 +365,31 @@ def test_layer_with_masked_logits_matches_oracle(T):
         lg[(pick >= 0.4) & (pick < 0.5)] = np.nan
         lg[:, 3] = 1.0                                # one finite logit per token
         _check_call(gpu, orc, layer, x, lg, gemm_check=True)
+    gpu.close()
+
+
+@pytest.mark.parametrize("E,k", [(16, 4), (128, 8), (256, 32), (260, 8), (126, 6)])
+def test_one_token_routing_ties_and_non_finite(E, k):
+    # one-token calls (the decode routing body's warp selection, E from 16 to
+    # 260, k up to 32) on logits with long runs of equal values, -inf and NaN
+    # entries, and a row of all-equal logits (the k lowest ids); indices and
+    # the plan bit-exact, gates and output against the oracle
+    H, I, L, T = 256, 256, 2, 1
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, "nvfp4", 2 * E, L, T, 300 + E)
+    rng = np.random.default_rng(E)
+    for step in range(3):
+        for layer in range(L):
+            x, lg = Hn.inputs(300 + E, T, H, E, step, layer)
+            lg = lg.copy()
+            if step == 0:
+                lg[:] = 0.25                                       # every logit equal
+            else:
+                lg = np.round(lg * 2.0) / 2.0                      # many ties
+                pick = rng.random(lg.shape)
+                lg[pick < 0.2] = -np.inf
+                lg[(pick >= 0.2) & (pick < 0.3)] = np.nan
+                lg[:, :k] = np.where(np.isfinite(lg[:, :k]), lg[:, :k], 0.0)   # k finite logits
+            _check_call(gpu, orc, layer, x, lg.astype(np.float32))
     gpu.close()
 
 
