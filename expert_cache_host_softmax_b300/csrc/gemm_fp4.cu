@@ -72,9 +72,12 @@ constexpr int Q_OFF_SFR = Q_OFF_SFB + QNS * Q_SF;   // B scales as they sit in t
 constexpr int Q_OFF_BAR = Q_OFF_SFR + QNS * Q_SF;
 constexpr int Q_BARS = 3 * QNS + 5;   // FULL, EMPTY, SFRAW per stage; TFULL x2, TEMPTY x2, DRAIN
 constexpr int Q_OFF_TAB = Q_OFF_BAR + Q_BARS * 8 + 16;
-constexpr int Q_SMEM = Q_OFF_TAB + 4 * 3 * (kMaxExperts + 1) + 64;
-constexpr int Q_SMEM_ALLOC = Q_SMEM + 1024;
 constexpr int Q_EPI_WARPS = 8;        // two per TMEM lane quarter, each half of a tile's columns
+// down epilogue: one 32 x 16 fp32 transpose block per epilogue warp (rows padded to 20)
+constexpr int Q_OFF_XP = (Q_OFF_TAB + 4 * 3 * (kMaxExperts + 1) + 64 + 15) / 16 * 16;
+constexpr int Q_XP_STRIDE = 20;
+constexpr int Q_SMEM = Q_OFF_XP + Q_EPI_WARPS * 32 * Q_XP_STRIDE * 4;
+constexpr int Q_SMEM_ALLOC = Q_SMEM + 1024;
 constexpr int Q_THREADS = (4 + Q_EPI_WARPS) * 32;
 constexpr int Q_PROD = 0, Q_MMA = 1, Q_SFW = 2, Q_EPI0 = 4;
 constexpr uint32_t Q_TMEM_COLS = 512;  // accumulators 0 and 128; scale buffers from 256
@@ -534,23 +537,42 @@ __global__ void __launch_bounds__(Q_THREADS, 1)
         }
         const bool store_y = a.out_acc == nullptr || a.keep_y;
         const uint64_t opol = l2_evict_last();   // the output rows stay in L2 for the other pairs' updates
+        // the reductions go through a per-warp transpose (as in the bf16
+        // grouped GEMM): instruction j covers rows 8 j .. 8 j + 7 of the
+        // warp, four lanes a row, 64 contiguous bytes each
+        float *xp = reinterpret_cast<float *>(sm + Q_OFF_XP) + (size_t)((warp - Q_EPI0) * 32) * Q_XP_STRIDE;
+        float *racc[4];
+        float rgw[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int src = 8 * jj + (lane >> 2);
+          racc[jj] = reinterpret_cast<float *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(acc), src));
+          rgw[jj] = __shfl_sync(0xffffffffu, gw, src);
+        }
 #pragma unroll 1
         for (int c = 0; c < QBN / 2; c += 16) {
           float v[16];
           tmem_ld16(tb + c0 + c, v);
-          if (valid) {
-            if (store_y) {
-              float4 *o = reinterpret_cast<float4 *>(dst + c);
+          if (valid && store_y) {
+            float4 *o = reinterpret_cast<float4 *>(dst + c);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
-            }
-            if (acc != nullptr) {
+            for (int i = 0; i < 4; ++i)
+              o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
+          }
+          if (a.out_acc != nullptr) {
+            float4 *w4 = reinterpret_cast<float4 *>(xp + lane * Q_XP_STRIDE);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                red_add_v4(acc + c + 4 * i,
-                           make_float4(v[4 * i] * gw, v[4 * i + 1] * gw, v[4 * i + 2] * gw, v[4 * i + 3] * gw), opol);
+            for (int i = 0; i < 4; ++i) w4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int r = 8 * jj + (lane >> 2), f4 = lane & 3;
+              const float4 t = *reinterpret_cast<const float4 *>(xp + r * Q_XP_STRIDE + 4 * f4);
+              if (racc[jj] != nullptr)
+                red_add_v4(racc[jj] + c + 4 * f4,
+                           make_float4(t.x * rgw[jj], t.y * rgw[jj], t.z * rgw[jj], t.w * rgw[jj]), opol);
             }
+            __syncwarp();
           }
         }
       }

@@ -90,7 +90,10 @@ struct Cfg {
   // barriers: FULL, EMPTY (kNS each), RAWFULL, RAWEMPTY (kNR each), TFULL x2, TEMPTY x2, DRAIN
   static constexpr int kBars = 2 * kNS + 2 * kNR + 5;
   static constexpr int kOffTab = kOffBar + kBars * 8 + 16;
-  static constexpr int kSmem = kOffTab + 4 * (2 * (kMaxU + 1)) + 64;
+  // down epilogue: one 32 x 16 fp32 transpose block per epilogue warp (rows padded to 20)
+  static constexpr int kOffXp = (kOffTab + 4 * (2 * (kMaxU + 1)) + 64 + 15) / 16 * 16;
+  static constexpr int kXpStride = 20;
+  static constexpr int kSmem = kOffXp + kEpiWarps * 32 * kXpStride * 4;
   static constexpr int kSmemAlloc = kSmem + 1024;             // room to align the base to 1024
 };
 
@@ -567,24 +570,47 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         }
         const bool store_y = a.out_acc == nullptr || a.keep_y;
         const uint64_t opol = l2_evict_last();   // the output rows stay in L2 for the other pairs' updates
+        // The reductions go through a per-warp transpose: lane l holds 16
+        // columns of its own row; after the transpose each reduction
+        // instruction j covers rows 8 j .. 8 j + 7 of the warp, four lanes a
+        // row (64 contiguous bytes), so a warp's instruction touches 8 output
+        // rows instead of 32.  Lane l then serves row 8 j + (l >> 2), float4
+        // (l & 3) of the 16 columns; that row's output pointer and gate come
+        // from its owner lane.
+        float *xp = reinterpret_cast<float *>(sm + C::kOffXp) + (size_t)(q * 32) * C::kXpStride;
+        float *racc[4];
+        float rgw[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int src = 8 * jj + (lane >> 2);
+          racc[jj] = reinterpret_cast<float *>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(acc), src));
+          rgw[jj] = __shfl_sync(0xffffffffu, gw, src);
+        }
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           float v[16];
           tmem_ld16(tb + c, v);
           if constexpr (FMT == FMT_FP8) row_scale16(rs0 + c, v);
-          if (valid) {
-            if (store_y) {
-              float4 *o = reinterpret_cast<float4 *>(dst + c);
+          if (valid && store_y) {
+            float4 *o = reinterpret_cast<float4 *>(dst + c);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
-            }
-            if (acc != nullptr) {
+            for (int i = 0; i < 4; ++i)
+              o[i] = make_float4(v[4 * i] * g0, v[4 * i + 1] * g0, v[4 * i + 2] * g0, v[4 * i + 3] * g0);
+          }
+          if (a.out_acc != nullptr) {
+            float4 *w4 = reinterpret_cast<float4 *>(xp + lane * C::kXpStride);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                red_add_v4(acc + c + 4 * i,
-                           make_float4(v[4 * i] * gw, v[4 * i + 1] * gw, v[4 * i + 2] * gw, v[4 * i + 3] * gw), opol);
+            for (int i = 0; i < 4; ++i) w4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int r = 8 * jj + (lane >> 2), f4 = lane & 3;
+              const float4 t = *reinterpret_cast<const float4 *>(xp + r * C::kXpStride + 4 * f4);
+              if (racc[jj] != nullptr)
+                red_add_v4(racc[jj] + c + 4 * f4,
+                           make_float4(t.x * rgw[jj], t.y * rgw[jj], t.z * rgw[jj], t.w * rgw[jj]), opol);
             }
+            __syncwarp();
           }
         }
       }
