@@ -150,6 +150,10 @@ struct FfnArgs {
   // keep_y as well as, being stored to y
   float *out_acc;             // [T][H]
   int keep_y;
+  // tensor-core gate/up with NVFP4 or FP8 experts: x as f16, each token row
+  // scaled by a power of two (launch_x_to_f16), and the inverse scales
+  const __half *xh;           // [T][H]
+  const float *xinv;          // [T]
   // NVFP4 gate/up of misses whose copies are still landing their down part
   // (which holds the global scales): the scales, read by the host from the
   // pool, for each missed expert; n = 0 reads them from the slot
@@ -193,6 +197,11 @@ int make_weight_maps(const uint8_t *slots, int64_t slot_stride, int S, int fmt, 
 int make_act_map(const void *base, int64_t rows, int K, void *map);
 cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_h, const void *map_gu, const void *map_d,
                           int *err, int64_t max_rows, cudaStream_t s);
+// x [T][H] bf16 -> xh f16 with each row scaled by a power of two that puts its
+// largest magnitude in [2^14, 2^15), and xinv[t] = the inverse scale
+cudaError_t launch_x_to_f16(const __nv_bfloat16 *x, int T, int H, __half *xh, float *xinv, cudaStream_t s);
+// whether the tensor-core gate/up of this weight format multiplies f16 operands
+bool tc_gateup_f16(int fmt);
 
 // FP4 x FP4 variant of the tensor-core FFN (gemm_fp4.cu).  Buffers over
 // expert-padded rows (see fp4_padded_rows): x and h as e2m1 codes [rows][K/2],

@@ -98,6 +98,8 @@ struct ft_moe {
   // and a device error word that bounded waits write when they give up
   alignas(64) unsigned char tmap[2][128] = {};     // weights: gate/up, down
   alignas(64) unsigned char amap[128] = {};        // activations: h
+  __half *xh = nullptr;                            // x as f16 rows scaled per token [Tmax][H] (f16 gate/up)
+  float *xinv = nullptr;                           // their inverse scales [Tmax]
   bool tmaps_ok = false;
   int ffn_kernel = FT_FFN_AUTO;
   int *err_dev = nullptr;
@@ -181,6 +183,8 @@ void free_all(ft_moe *h) {
   cudaFree(h->hbuf);
   cudaFree(h->ybuf);
   cudaFree(h->out_acc);
+  cudaFree(h->xh);
+  cudaFree(h->xinv);
   cudaFree(h->err_dev);
   cudaFree(h->combine_counters);
   cudaFree(h->pool_dev);
@@ -282,7 +286,20 @@ cudaError_t run_ffn(ft_moe *h, const FfnArgs &fa, bool down, bool tc, int T, cud
     return launch_tc_ffn_fp4(fa, down, h->q, h->qmap[down ? 1 : 0], h->qmap[down ? 3 : 2], h->qmap[down ? 5 : 4],
                              h->err_dev, (int64_t)T * h->k, s);
   }
-  if (tc) return launch_tc_ffn(fa, down, h->amap, h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
+  if (tc) {
+    FfnArgs f = fa;
+    if (!down && tc_gateup_f16(h->fmt)) {
+      f.xh = h->xh;
+      f.xinv = h->xinv;
+      if (fa.only != 2) {
+        // x as scaled f16 rows, once per call (before the first gate/up launch)
+        cudaError_t e = launch_x_to_f16(fa.x, T, h->H, h->xh, h->xinv, s);
+        if (e != cudaSuccess) return e;
+        h->kernel_launches += 1;
+      }
+    }
+    return launch_tc_ffn(f, down, h->amap, h->tmap[0], h->tmap[1], h->err_dev, (int64_t)T * h->k, s);
+  }
   return down ? launch_down(fa, cb, s) : launch_gateup(fa, s);
 }
 
@@ -640,6 +657,8 @@ int ft_moe_create(int hidden, int n_experts, int top_k, int inter, int weight_fm
             dev_alloc(&h->chunk_base, chunk_ints) == cudaSuccess &&
             dev_alloc(&h->hbuf, TK * inter) == cudaSuccess && dev_alloc(&h->ybuf, TK * hidden) == cudaSuccess &&
             dev_alloc(&h->out_acc, (size_t)max_tokens * hidden) == cudaSuccess &&
+            cudaMalloc(&h->xh, sizeof(__half) * (size_t)max_tokens * hidden) == cudaSuccess &&
+            dev_alloc(&h->xinv, (size_t)max_tokens) == cudaSuccess &&
             dev_alloc(&h->err_dev, 4) == cudaSuccess && cudaMemset(h->err_dev, 0, 16) == cudaSuccess &&
             dev_alloc(&h->mega_sync, 4) == cudaSuccess && cudaMemset(h->mega_sync, 0, 16) == cudaSuccess &&
             dev_alloc(&h->copy_sync, 4) == cudaSuccess && cudaMemset(h->copy_sync, 0, 16) == cudaSuccess &&

@@ -110,12 +110,22 @@ struct GemmArgs {
   int *err;                 // device error word (first failure code)
   float *out_acc;           // down: out_acc[token] += gate * y row (fp32 atomics), or null
   int keep_y;               // down with out_acc: store y as well
+  const __half *xh;         // f16 gate/up (kF16A): x rows scaled per token, and
+  const float *xinv;        // the inverse scales
 };
 
 // ------------------------------------------------------------------ instruction descriptor
 
 // Instruction descriptor: kind::f16, A = B = bf16, D = f32, K-major A and B,
 // N = BN, M = BM.
+// The gate/up of NVFP4 and FP8 experts multiplies f16 operands: their codes
+// (times an E4M3 block scale) convert to f16 exactly in one step, and x comes
+// as f16 rows scaled by a power of two (launch_x_to_f16).  MXFP4 (E8M0 block
+// scales beyond f16's range), BF16 and every down GEMM (A = h) stay bf16.
+template <int FMT, bool DOWN>
+constexpr bool kF16A = !DOWN && (FMT == FMT_NVFP4 || FMT == FMT_FP8);
+// kind::f16 with A = B = f16 (format fields 0), D = f32
+constexpr uint32_t kIdescF16 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                             ((uint32_t)(BM >> 4) << 24);
 
@@ -328,7 +338,9 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
       int tok[BM / 8];
 #pragma unroll
       for (int i = 0; i < BM / 8; ++i) tok[i] = a.plan.perm[min(ti.row0 + 8 * i + rsub, last)] / a.k;
-      const __nv_bfloat16 *xc = a.x + c * 8;
+      const uint16_t *xsrc = kF16A<FMT, DOWN> ? reinterpret_cast<const uint16_t *>(a.xh)
+                                               : reinterpret_cast<const uint16_t *>(a.x);
+      const uint16_t *xc = xsrc + c * 8;
       for (int kb = 0; kb < nk; ++kb, ++j) {
         const int s = j % NS;
         if (!mbar_wait(EMPTY(s), ((j / NS) & 1) ^ 1, s_abort, a.err, 14)) { ok = false; break; }
@@ -376,7 +388,8 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
                        : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
                        : "r"(raw + g * 16)
                        : "memory");
-          const uint4 v0 = dequant8_e4m3(q.x, q.y), v1 = dequant8_e4m3(q.z, q.w);
+          const uint4 v0 = kF16A<FMT, DOWN> ? dequant8_e4m3_f16(q.x, q.y) : dequant8_e4m3(q.x, q.y);
+          const uint4 v1 = kF16A<FMT, DOWN> ? dequant8_e4m3_f16(q.z, q.w) : dequant8_e4m3(q.z, q.w);
           const uint32_t d0 = bdst + (((2 * g) ^ (t & 7)) << 4), d1 = bdst + (((2 * g + 1) ^ (t & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d0), "r"(v0.x), "r"(v0.y), "r"(v0.z),
                        "r"(v0.w)
@@ -424,10 +437,14 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         }
         const int sub = kb & 3;
         float sc[4];
+        uint32_t sch[4];   // f16 path: the scales as f16x2 pairs
         if constexpr (FMT == FMT_NVFP4) {
           const uint32_t word = sub == 0 ? sc_cur.x : sub == 1 ? sc_cur.y : sub == 2 ? sc_cur.z : sc_cur.w;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sc[i] = e4m3_to_float((word >> (8 * i)) & 0xFFu);
+          for (int i = 0; i < 4; ++i) {
+            if constexpr (kF16A<FMT, DOWN>) sch[i] = e4m3_to_half2x(word >> (8 * i));
+            else sc[i] = e4m3_to_float((word >> (8 * i)) & 0xFFu);
+          }
         } else {
           const uint32_t word = (sub >> 1) == 0 ? sc_cur.x : sc_cur.y;
           const uint32_t pair = (word >> (16 * (sub & 1))) & 0xFFFFu;
@@ -456,7 +473,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         const uint32_t bdst = sB + s * B_STAGE + t * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = dequant8(w[c], sc[c >> 1]);
+          const uint4 v = kF16A<FMT, DOWN> ? dequant8_f16(w[c], sch[c >> 1]) : dequant8(w[c], sc[c >> 1]);
           const uint32_t d = bdst + ((c ^ (t & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                        : "memory");
@@ -488,7 +505,8 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
           const uint32_t a0 = sA + s * A_STAGE, b0 = sB + s * B_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), kIdesc, (kb | kk) != 0);
+            mma_bf16(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32),
+                     kF16A<FMT, DOWN> ? kIdescF16 : kIdesc, (kb | kk) != 0);
           mma_commit(EMPTY(s));
         }
         if (ok) mma_commit(TFULL(b));
@@ -529,6 +547,12 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         rs1 = DOWN ? nullptr : sf + a.I + ti.n * (BN / 2);
       }
       const bool valid = row < ti.rows;
+      if constexpr (kF16A<FMT, DOWN>) {
+        // the row's x came scaled by a power of two: its inverse joins the weights' scales
+        const float inv = valid ? a.xinv[a.plan.perm[ti.row0 + row] / a.k] : 1.0f;
+        g0 *= inv;
+        g1 *= inv;
+      }
       if constexpr (!DOWN) {
         __nv_bfloat16 *dst = a.h + (size_t)(ti.row0 + row) * a.I + ti.n * (BN / 2);
 #pragma unroll 1
@@ -638,7 +662,55 @@ cudaError_t launch(const GemmArgs &a, const CUtensorMap &mapA, const CUtensorMap
   return cudaGetLastError();
 }
 
+// One token row per CTA: x (bf16) -> f16 scaled by 2^k, k putting the row's
+// largest magnitude in [2^14, 2^15) (every element down to 2^-31 of it
+// converts exactly), xinv[t] = 2^-k.  A row whose largest magnitude is zero
+// or not finite is not scaled.
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const __nv_bfloat16 *__restrict__ x, int H,
+                                                       __half *__restrict__ xh, float *__restrict__ xinv) {
+  __shared__ uint32_t s_wmax[8];
+  const int t = blockIdx.x;
+  const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+  uint4 *dst = reinterpret_cast<uint4 *>(xh + (size_t)t * H);
+  const int nv = H / 8;
+  uint32_t m = 0;   // largest |x| as fp32 bits
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const uint4 q = __ldg(src + v);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = max(m, max((w[j] & 0x7FFFu) << 16, w[j] & 0x7FFF0000u));
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0) s_wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = max(m, s_wmax[i]);
+  int k = 0;
+  if (m != 0 && m < 0x7F800000u) k = min(126, max(-126, 14 - ((int)(m >> 23) - 127)));
+  const float sc = __uint_as_float((uint32_t)(127 + k) << 23);
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const uint4 q = __ldg(src + v);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h2 =
+          __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
+      o[j] = *reinterpret_cast<const uint32_t *>(&h2);
+    }
+    dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) xinv[t] = __uint_as_float((uint32_t)(127 - k) << 23);
+}
+
 }  // namespace
+
+bool tc_gateup_f16(int fmt) { return fmt == FMT_NVFP4 || fmt == FMT_FP8; }
+
+cudaError_t launch_x_to_f16(const __nv_bfloat16 *x, int T, int H, __half *xh, float *xinv, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  x_to_f16_kernel<<<T, 256, 0, s>>>(x, H, xh, xinv);
+  return cudaGetLastError();
+}
 
 EncodeTiledFn encode_tiled_fn() {
   static EncodeTiledFn fn = nullptr;
@@ -754,6 +826,8 @@ cudaError_t launch_tc_ffn(const FfnArgs &f, bool down, const void *map_h, const 
   a.err = err;
   a.out_acc = down ? f.out_acc : nullptr;
   a.keep_y = f.keep_y;
+  a.xh = f.xh;
+  a.xinv = f.xinv;
   const int NTN = down ? f.H / BN : f.I / (BN / 2);
   // M tiles <= ceil(rows / BM) + distinct experts
   const int64_t mtiles = (max_rows + BM - 1) / BM + f.umax;

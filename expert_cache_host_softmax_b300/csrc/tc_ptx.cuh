@@ -244,6 +244,43 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
   return pack_bf16x2(f.x, f.y);
 }
 
+// Eight e2m1 codes times one block scale given as an f16x2 pair (s, s) ->
+// eight f16 values.  Exact: a product has at most 6 significant bits, and
+// with an E4M3 scale its magnitude lies in [2^-10, 2688] or is 0.
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t w, uint32_t s2) {
+  uint32_t o[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    uint32_t h;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(h)
+        : "r"(w >> (8 * b)));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[b]) : "r"(h), "r"(s2));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One E4M3 scale byte -> the f16x2 pair (s, s) (exact).
+__device__ __forceinline__ uint32_t e4m3_to_half2x(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(out)
+      : "r"((byte & 0xFFu) * 0x101u));
+  return out;
+}
+
+// Eight E4M3 codes (two 32-bit words) -> eight f16 values (exact).
+__device__ __forceinline__ uint4 dequant8_e4m3_f16(uint32_t lo, uint32_t hi) {
+  uint32_t o[4];
+  const uint32_t pairs[4] = {lo & 0xFFFFu, lo >> 16, hi & 0xFFFFu, hi >> 16};
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(o[b])
+        : "r"(pairs[b]));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ uint4 dequant8_e4m3(uint32_t lo, uint32_t hi) {
   return make_uint4(e4m3x2_to_bf16x2(lo & 0xFFFFu), e4m3x2_to_bf16x2(lo >> 16), e4m3x2_to_bf16x2(hi & 0xFFFFu),
                     e4m3x2_to_bf16x2(hi >> 16));
