@@ -25,17 +25,21 @@
 //   - one producer thread issues, per stage, the TMA load of the weights
 //     (and of the down GEMM's A box): BF16 weights land
 //     directly in the swizzled layout; NVFP4 / MXFP4 / FP8 codes land raw in a
-//     separate ring, and eight converter warps dequantise them to bf16
-//     (e2m1 x block scale, or the bare E4M3 value: exact in bf16) into the
-//     swizzled B tile.  The NVFP4 per-matrix global scale and the FP8 per-row
-//     scales are applied to the fp32 accumulator in the epilogue.
-//   - one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> f32)
-//     into one of two TMEM accumulators (2 x 256 columns), so the epilogue of
-//     a tile overlaps the MMAs of the next;
+//     separate ring, and eight converter warps dequantise them (e2m1 x block
+//     scale, or the bare E4M3 value) into the swizzled B tile: to f16 for the
+//     gate/up of NVFP4 and FP8 experts (one cvt and one packed multiply a
+//     pair, exact; x then comes as f16 rows scaled per token by a power of
+//     two, see x_to_f16_kernel), to bf16 otherwise (exact too).  The NVFP4
+//     per-matrix global scale, the FP8 per-row scales and the inverse row
+//     scales of f16 x are applied to the fp32 accumulator in the epilogue.
+//   - one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 or f16 operands
+//     -> f32) into one of two TMEM accumulators (2 x 256 columns), so the
+//     epilogue of a tile overlaps the MMAs of the next;
 //   - four epilogue warps read the accumulator with tcgen05.ld (one TMEM lane
 //     = one token row per thread) and write h (bf16), or add the row, times
-//     its pair's gate, into the token's fp32 output row (and store y when
-//     asked to keep it).
+//     its pair's gate, into the token's fp32 output row (through a per-warp
+//     transpose, so each reduction covers 8 rows x 64 contiguous bytes; and
+//     store y when asked to keep it).
 // Every mbarrier wait is bounded in time.  A wait that runs out records an
 // error code, raises the CTA's abort flag, and every role drains its own
 // in-flight copies before the CTA frees its TMEM and exits.
