@@ -59,7 +59,6 @@ using namespace tc;
 constexpr int BM = 128;          // token rows per tile (one TMEM lane each)
 constexpr int BN = 256;          // weight rows per tile (MMA N)
 constexpr int BK = 64;           // K per stage: 128 bytes of bf16 (one swizzle atom)
-constexpr int kEpiWarps = 4;
 constexpr int A_STAGE = BM * BK * 2;          // 16 KB
 constexpr int B_STAGE = BN * BK * 2;          // 32 KB
 constexpr uint32_t kTmemCols = 512;           // two accumulators of BN fp32 columns
@@ -77,11 +76,14 @@ struct Cfg {
   static constexpr int kNS = kConv ? 3 : 4;
   static constexpr int kNR = kConv ? 4 : 0;
   // warp roles: 0 producer, 1 MMA, 2-3 x gatherers (gate/up; idle in down),
-  // 4-7 epilogue, 8-15 converters
+  // 4-7 epilogue, 8-15 converters (converted formats) or 8-11 epilogue (BF16)
   static constexpr int kProdWarp = 0, kMmaWarp = 1, kGatherWarp0 = 2, kEpiWarp0 = 4, kConvWarp0 = 8;
   static constexpr int kGatherThreads = 64;
   static constexpr int kConvThreads = kConv ? 256 : 0;
-  static constexpr int kThreads = kConv ? 512 : 256;
+  // epilogue warps: 8 (two per TMEM lane quarter, each half of a tile's
+  // columns) where no converter warps take the registers, else 4
+  static constexpr int kEpiW = kConv ? 4 : 8;
+  static constexpr int kThreads = kConv ? 512 : 384;
   // FULL arrivals per stage: the producer's expect_tx, plus one per converter
   // thread, plus (gate/up) one per gatherer thread
   __host__ __device__ static constexpr int full_count(bool down) {
@@ -97,7 +99,7 @@ struct Cfg {
   // down epilogue: one 32 x 16 fp32 transpose block per epilogue warp (rows padded to 20)
   static constexpr int kOffXp = (kOffTab + 4 * (2 * (kMaxU + 1)) + 64 + 15) / 16 * 16;
   static constexpr int kXpStride = 20;
-  static constexpr int kSmem = kOffXp + kEpiWarps * 32 * kXpStride * 4;
+  static constexpr int kSmem = kOffXp + kEpiW * 32 * kXpStride * 4;
   static constexpr int kSmemAlloc = kSmem + 1024;             // room to align the base to 1024
 };
 
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(TFULL(b), 1);
-      mbar_init(TEMPTY(b), kEpiWarps * 32);
+      mbar_init(TEMPTY(b), C::kEpiW * 32);
     }
     mbar_init(DRAIN, 1);
     *s_abort = 0;
@@ -522,10 +524,12 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + kEpiWarps) {
+  } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiW) {
     // ================================================================ epilogue
     const int q = warp & 3;            // TMEM lane quarter
     const int row = q * 32 + lane;     // tile row of this thread
+    constexpr int NG = C::kEpiW / 4;   // warps per lane quarter, each 1/NG of the columns
+    const int grp = (warp - C::kEpiWarp0) >> 2;
     int tl = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
       const int b = tl & 1;
@@ -560,7 +564,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
       if constexpr (!DOWN) {
         __nv_bfloat16 *dst = a.h + (size_t)(ti.row0 + row) * a.I + ti.n * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 16) {
+        for (int c = grp * (BN / 2 / NG); c < (grp + 1) * (BN / 2 / NG); c += 16) {
           float gv[16], uv[16];
           tmem_ld16(tb + c, gv);
           tmem_ld16(tb + BN / 2 + c, uv);
@@ -605,7 +609,8 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
         // rows instead of 32.  Lane l then serves row 8 j + (l >> 2), float4
         // (l & 3) of the 16 columns; that row's output pointer and gate come
         // from its owner lane.
-        float *xp = reinterpret_cast<float *>(sm + C::kOffXp) + (size_t)(q * 32) * C::kXpStride;
+        float *xp =
+            reinterpret_cast<float *>(sm + C::kOffXp) + (size_t)((warp - C::kEpiWarp0) * 32) * C::kXpStride;
         float *racc[4];
         float rgw[4];
 #pragma unroll
@@ -615,7 +620,7 @@ __global__ void __launch_bounds__(Cfg<FMT>::kThreads, 1)
           rgw[jj] = __shfl_sync(0xffffffffu, gw, src);
         }
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
+        for (int c = grp * (BN / NG); c < (grp + 1) * (BN / NG); c += 16) {
           float v[16];
           tmem_ld16(tb + c, v);
           if constexpr (FMT == FMT_FP8) row_scale16(rs0 + c, v);
@@ -732,7 +737,7 @@ EncodeTiledFn encode_tiled_fn() {
 static_assert(Cfg<FMT_BF16>::kSmemAlloc <= 227 * 1024, "bf16 smem");
 static_assert(Cfg<FMT_NVFP4>::kSmemAlloc <= 227 * 1024, "fp4 smem");
 static_assert(Cfg<FMT_FP8>::kSmemAlloc <= 227 * 1024, "fp8 smem");
-static_assert(Cfg<FMT_NVFP4>::kThreads == 512 && Cfg<FMT_BF16>::kThreads == 256, "warp roles");
+static_assert(Cfg<FMT_NVFP4>::kThreads == 512 && Cfg<FMT_BF16>::kThreads == 384, "warp roles");
 static_assert(Cfg<FMT_BF16>::kGatherThreads == 64 && BM == 128 && BK == 64, "gatherer row map: 2 warps, 8 lanes a row");
 
 int tc_num_sms() {
