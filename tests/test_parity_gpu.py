@@ -433,6 +433,38 @@ def test_tc_ffn_matches_oracle(fmt, H, I, E, k, T):
     gpu.close()
 
 
+def _scale_bf16(x_bits, scale, zero_every=0):
+    """bf16 activations (uint16 bits) times `scale`, rounded to nearest even
+    back to bf16; with zero_every > 0 every zero_every-th token row is zero."""
+    f = (x_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64) * scale
+    u = f.astype(np.float32).view(np.uint32)
+    out = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    if zero_every:
+        out[::zero_every] = 0
+    return out
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8", "bf16", "mxfp4"])
+@pytest.mark.parametrize("path", ["gemv", "tc"])
+def test_activation_rows_far_from_unit_scale(fmt, path):
+    # one-token GEMV passes stage x as f16 scaled by a power of two (bf16 for
+    # BF16 weights), and the tensor-core gate/up of NVFP4 / FP8 experts reads
+    # x as such rows: activations scaled by 1e6 and 1e-6 (out of f16's range
+    # either way without the scaling), with some all-zero rows, match the
+    # oracle, the gate/up accumulation included
+    H, I, E, k = 256, 256, 8, 2
+    T = 1 if path == "gemv" else 300
+    gpu, orc, _ = Hn.make_pair(H, E, k, I, fmt, E, 1, T, 77)
+    gpu.set_ffn_kernel(path)
+    for step, scale in enumerate((1e6, 1e-6, 3.0)):
+        x, lg = Hn.inputs(77, T, H, E, step, 0)
+        x = _scale_bf16(x, scale, zero_every=0 if path == "gemv" else 7)
+        with np.errstate(over="ignore"):   # the oracle's SiLU at -1e6 takes exp's IEEE limit
+            _check_call(gpu, orc, 0, x, lg, gemm_check=True)
+        assert gpu.last_ffn_kernel == path
+    gpu.close()
+
+
 @pytest.mark.parametrize("fmt", ["bf16", "nvfp4", "fp8"])
 def test_tc_combine_in_down_epilogue(fmt):
     # the product setting: y is never stored, the down GEMM adds its
